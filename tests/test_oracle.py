@@ -1,0 +1,257 @@
+"""Pins for the CPU oracle: exact brute force, closed forms, library routines and
+the invariants the method implies.  CPU only.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign, a transposed operand, a wrong group index, a rounding mode) fails
+at least one of them.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import _brute
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bits(t):
+    if isinstance(t, torch.Tensor):
+        t = t.numpy()
+    return np.ascontiguousarray(t).view(np.uint16)
+
+
+# ---------------------------------------------------------------- binary16 ---
+
+def test_half_to_double_exhaustive_vs_numpy():
+    """Every finite binary16 pattern decodes to numpy's value (library routine)."""
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = allbits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_double(int(b)) for b in allbits])
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+
+
+def test_double_to_half_rne_vs_numpy():
+    """binary64 -> binary16 is round-to-nearest-even, incl. ties, subnormals, overflow."""
+    rng = np.random.default_rng(123)
+    vals = list(rng.standard_normal(3000) * 10.0 ** rng.integers(-9, 6, 3000))
+    # exact ties between adjacent halves, in the normal and subnormal range
+    h = np.arange(0, 0x7BFF, 37, dtype=np.uint16).view(np.float16).astype(np.float64)
+    h2 = (np.arange(0, 0x7BFF, 37, dtype=np.uint16) + 1).view(np.float16).astype(np.float64)
+    vals += list((h + h2) / 2) + list(-(h + h2) / 2)
+    vals += [65504.0, 65519.99, 65520.0, 70000.0, -65520.0, 2.0 ** -25, 2.0 ** -24 * 1.5,
+             2.0 ** -14 - 2.0 ** -26, 0.0, -0.0, 1e-30]
+    got = np.array([oracle.double_to_half(v) for v in vals], dtype=np.uint16)
+    ref = np.array(vals, dtype=np.float64).astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# --------------------------------------------------------- act quantizer ---
+
+def _act_cases():
+    gen = synth.generator(7)
+    x = synth.activations(5, 256, gen, outlier_frac=0.02)
+    x[1] = 0                                   # all-zero row -> s = 0, codes 0
+    x[2] = 0
+    x[2, 17] = -3.5                            # single non-zero element
+    x[3, :] = (torch.arange(256, dtype=torch.float32) - 128).to(torch.float16) * 2 ** -20  # subnormals
+    return x
+
+
+def test_quant_act_bruteforce():
+    x = _act_cases()
+    q, s = oracle.quant_act_int8(x)
+    bq, bs = _brute.quant_act_int8(_bits(x))
+    assert np.array_equal(q.astype(np.int64), bq)
+    assert np.array_equal(s.astype(np.float64), bs)
+    assert s[1] == 0 and not q[1].any()
+    assert q[2, 17] == -127 and np.count_nonzero(q[2]) == 1
+
+
+def test_quant_act_rounding_ties_to_even():
+    """Values on exact .5 boundaries of x/s round to the even code."""
+    # amax = 127 -> s = 1 exactly; x = k + 0.5 must round to even integers
+    row = np.array([127.0, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 3.5] + [0.0] * 120, dtype=np.float16)
+    q, s = oracle.quant_act_int8(row[None, :])
+    assert s[0] == 1.0
+    assert list(q[0, :8]) == [127, 0, 2, 2, 0, -2, -2, 4]
+
+
+def test_quant_act_properties():
+    gen = synth.generator(11)
+    x = synth.activations(16, 1024, gen, outlier_frac=0.01)
+    q, s = oracle.quant_act_int8(x)
+    xf = x.float().numpy().astype(np.float64)
+    # reconstruction within half a step (+ the binary32 rounding of x/s)
+    err = np.abs(xf - q.astype(np.float64) * s[:, None].astype(np.float64))
+    assert np.all(err <= s[:, None] * (0.5 + 1e-6))
+    # the absmax element maps to +-127
+    idx = np.abs(xf).argmax(axis=1)
+    assert np.all(np.abs(q[np.arange(16), idx]) == 127)
+    assert np.all(np.abs(q) <= 127)
+    # scaling a row by 2**j scales s by 2**j and leaves the codes unchanged
+    q2, s2 = oracle.quant_act_int8((x.float() * 0.25).to(torch.float16))
+    assert np.array_equal(q2, q) and np.array_equal(s2, s * np.float32(0.25))
+
+
+# ------------------------------------------------------------------ GEMMs ---
+
+@pytest.mark.parametrize("M,N,K,seed", [(1, 3, 128, 21), (3, 5, 256, 22), (2, 7, 384, 23)])
+def test_w4a16_bruteforce_small(M, N, K, seed):
+    p = synth.make_problem(M, N, K, seed=seed, outlier_frac=0.02)
+    y = oracle.w4a16(p.x, p.codes, p.scales)
+    ref = _brute.gemm_wxa16(_bits(p.x), p.codes.numpy(), _bits(p.scales))
+    assert np.array_equal(_bits(y), ref)
+
+
+def test_w4a16_bruteforce_tiny_config():
+    """The M=4, K=256, N=512 W4A16 check, all outputs, exact."""
+    p = synth.tiny_w4a16()
+    assert (p.scales < 0).float().mean().item() == pytest.approx(0.5, abs=0.05)
+    y = oracle.w4a16(p.x, p.codes, p.scales)
+    ref = _brute.gemm_wxa16(_bits(p.x), p.codes.numpy(), _bits(p.scales))
+    assert np.array_equal(_bits(y), ref)
+
+
+def test_w8a16_bruteforce_small():
+    p = synth.make_problem(3, 6, 256, seed=31, bits=8, scale_lo=0.001, scale_hi=0.01)
+    y = oracle.w8a16(p.x, p.codes, p.scales)
+    ref = _brute.gemm_wxa16(_bits(p.x), p.codes.numpy(), _bits(p.scales))
+    assert np.array_equal(_bits(y), ref)
+
+
+def test_w4a8_bruteforce_small():
+    p = synth.make_problem(3, 6, 384, seed=41, outlier_frac=0.02)
+    qa, sx = oracle.quant_act_int8(p.x)
+    y = oracle.w4a8(qa, sx, p.codes, p.scales)
+    ref = _brute.gemm_w4a8(qa, sx, p.codes.numpy(), _bits(p.scales))
+    assert np.array_equal(_bits(y), ref)
+
+
+def test_integer_special_case_is_int_matmul():
+    """All scales 1 and integer activations: W4A16 is an exact integer matmul."""
+    gen = synth.generator(51)
+    M, N, K = 4, 9, 256
+    codes = synth.codes_int4(N, K, gen)
+    xi = torch.randint(-3, 4, (M, K), generator=gen)
+    scales = torch.ones((N, K // 128), dtype=torch.float16)
+    y = oracle.w4a16(xi.to(torch.float16), codes, scales)
+    ref = (xi.numpy().astype(np.int64) @ codes.numpy().astype(np.int64).T)
+    assert np.array_equal(y.astype(np.float64), ref.astype(np.float64))
+
+
+def test_group_index_and_scale_sign():
+    """Closed form: one non-zero group scale picks exactly the K-range of that group,
+    with its sign (the unsigned-scale failure mode would flip the result)."""
+    M, N, K = 2, 3, 512
+    x = torch.ones((M, K), dtype=torch.float16)
+    x[1] = 2.0
+    codes = torch.zeros((N, K), dtype=torch.int8)
+    codes[:, 256:384] = 3            # group 2 only
+    codes[1, 0:128] = 7              # group 0, whose scale is zero below
+    scales = torch.zeros((N, K // 128), dtype=torch.float16)
+    scales[:, 2] = torch.tensor([-0.5, 0.25, -1.0], dtype=torch.float16)
+    y = oracle.w4a16(x, codes, scales).astype(np.float64)
+    expect = np.array([[-0.5, 0.25, -1.0]]) * 3 * 128 * np.array([[1.0], [2.0]])
+    assert np.array_equal(y, expect)
+    # the same computation in W4A8 with unit token scale
+    qa = x.to(torch.int8).numpy()
+    y8 = oracle.w4a8(qa, np.ones(M, np.float32), codes, scales).astype(np.float64)
+    assert np.array_equal(y8, expect)
+
+
+def test_invariant_a_sign_fold():
+    """Folding each negative scale's sign into its codes leaves the result unchanged
+    (bit-identical): q' = -q, s' = -s on every group with s < 0."""
+    p = synth.make_problem(5, 64, 512, seed=61, outlier_frac=0.01)
+    G = p.K // 128
+    neg = (p.scales < 0)
+    assert 0.3 < neg.float().mean().item() < 0.7
+    negk = neg.repeat_interleave(128, dim=1)
+    folded_codes = torch.where(negk, -p.codes.to(torch.int16), p.codes.to(torch.int16)).to(torch.int8)
+    folded_scales = torch.where(neg, -p.scales, p.scales)
+    assert (folded_scales >= 0).all() and folded_codes.max() <= 8
+    y = oracle.w4a16(p.x, p.codes, p.scales)
+    yf = oracle.w8a16(p.x, folded_codes, folded_scales)   # codes may now be +8
+    assert np.array_equal(_bits(y), _bits(yf))
+    qa, sx = oracle.quant_act_int8(p.x)
+    assert G == 4
+
+
+def test_invariant_b_w4a8_equals_w4a16_on_int8_exact_activations():
+    gen = synth.generator(71)
+    M, N, K = 6, 48, 640
+    x = synth.int8_exact_activations(M, K, gen)
+    codes = synth.codes_int4(N, K, gen)
+    scales = synth.signed_scales(N, K // 128, gen, 0.002, 0.02)
+    qa, sx = oracle.quant_act_int8(x)
+    # the quantizer reproduces c and 2**-e exactly
+    xf = x.float().numpy().astype(np.float64)
+    assert np.array_equal(qa.astype(np.float64) * sx[:, None].astype(np.float64), xf)
+    assert np.all(np.log2(sx) == np.round(np.log2(sx)))
+    y16 = oracle.w4a16(x, codes, scales)
+    y8 = oracle.w4a8(qa, sx, codes, scales)
+    assert np.array_equal(_bits(y16), _bits(y8))
+
+
+def test_invariant_c_int8_g128_roundtrip_near_pages_figure():
+    g = json.load(open(os.path.join(GOLDEN, "roundtrip_int8_g128.json")))
+    gen = synth.generator(81)
+    w = torch.randn((512, 5120), generator=gen, dtype=torch.float32)
+    codes, scales, err = oracle.roundtrip_int8_g128(w)
+    lo, hi = g["accept_percent"]
+    assert lo <= 100 * err <= hi, 100 * err
+    # codes are symmetric int8 and each group's absmax maps to +-127
+    assert codes.min() >= -127 and codes.max() <= 127
+    gmax = np.abs(codes.reshape(512, 40, 128)).max(axis=2)
+    assert (gmax == 127).mean() > 0.95
+
+
+def test_invariant_d_w8a16_equals_w4a16_on_int4_codes():
+    p = synth.make_problem(3, 32, 384, seed=91)
+    y4 = oracle.w4a16(p.x, p.codes, p.scales)
+    y8 = oracle.w8a16(p.x, p.codes, p.scales)
+    assert np.array_equal(_bits(y4), _bits(y8))
+
+
+def test_oracle_rejects_out_of_range_int4_codes():
+    p = synth.make_problem(1, 2, 128, seed=3)
+    bad = p.codes.clone()
+    bad[0, 0] = 8
+    with pytest.raises(ValueError):
+        oracle.w4a16(p.x, bad, p.scales)
+
+
+def test_w4a16_linear_in_activations():
+    """Doubling x doubles y exactly (power-of-two scaling commutes with every rounding)."""
+    p = synth.make_problem(4, 40, 256, seed=101)
+    y = oracle.w4a16(p.x, p.codes, p.scales).astype(np.float64)
+    y2 = oracle.w4a16((p.x.float() * 2).to(torch.float16), p.codes, p.scales).astype(np.float64)
+    assert np.array_equal(2 * y, y2)
+
+
+def test_quant_act_divide_not_reciprocal_bruteforce():
+    """Many rows, with absmax values picked where a reciprocal multiply would round
+    differently from the IEEE divide, and element values where x*(1/s) != x/s;
+    expected codes and scales from exact rational brute force."""
+    gen = synth.generator(13)
+    cand = (torch.rand(20000, generator=gen) * 40 + 0.01).to(torch.float16).float().numpy()
+    recip = cand * np.float32(1.0 / 127.0)
+    div = cand / np.float32(127.0)
+    amaxes = cand[recip != div][:40]
+    assert len(amaxes) == 40
+    x = synth.activations(40, 128, gen).float()
+    x = x / x.abs().amax(dim=1, keepdim=True) * torch.from_numpy(amaxes)[:, None] * 0.999
+    x[:, 0] = torch.from_numpy(amaxes)
+    x = x.to(torch.float16)
+    q, s = oracle.quant_act_int8(x)
+    bq, bs = _brute.quant_act_int8(_bits(x))
+    assert np.array_equal(s.astype(np.float64), bs)
+    assert np.array_equal(q.astype(np.int64), bq)
