@@ -1,0 +1,529 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 weight-quantized linear layer.
+
+Workload of the headline number: the decode/verify projection K = N = 5120 at
+M in {1, 4, 16, 64} tokens, in both modes -- W4A16, and W4A8 with per-token
+int8 activation quantization -- over 32 distinct packed weight matrices (one
+per "layer", 432 MB in total, so every GEMM streams its weights from HBM, not
+L2).  One step = every (mode, M) over all 32 layers: 128 W4A16 GEMMs plus 128
+x (quantize, widen, W4A8 GEMM).  Each (mode, M) block is captured once as a
+CUDA graph through the library's public calls and replayed; CUDA events on the
+launching stream time every block.
+
+value = weight bytes streamed by the GEMMs in a step / step time (GB/s, whole
+job over all ranks).  The same run reports TFLOPS/TOPS and roofline fractions
+per (mode, M), and, at one GPU, the other workloads of the layer (fused FFN
+pair at M=64, the M=8192 prefill, the 248k-row int8 lm_head), each with a
+parity spot check against the CPU oracle.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "W4A8/W4A16 GEMM TOPS & weight-read GB/s vs M (1–8192), % of GB300 roofline"
+N = K = 5120
+MS = (1, 4, 16, 64)
+LAYERS = 32
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def w4_bytes(n, k):
+    return n * k // 2 + 2 * n * (k // 128)
+
+
+def w8_bytes(n, k):
+    return n * k + 2 * n * (k // 128)
+
+
+# ------------------------------------------------------------ clocks sampler --
+class Clocks:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            self.path = f"/tmp/qgemm_clocks_{os.getpid()}.csv"
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- distributed --
+def dist_setup(backend):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, ws, device):
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle leg --
+def oracle_sample(seconds=12.0):
+    """Time the oracle, as it stands, on a bounded sample of the workload: the
+    projection at each M and mode over a subset of output rows; returns
+    (weight bytes covered, seconds, description)."""
+    import oracle
+    p = synth.projection(64)
+    x = p.x
+    qa, sx = oracle.quant_act_int8(x)
+    # size the column sample from a short calibration run
+    t0 = time.perf_counter()
+    oracle.w4a16(x[:16], p.codes[:64], p.scales[:64])
+    cal = (time.perf_counter() - t0) / (16 * 64 * K)
+    per_col = sum(MS) * K * 2 * cal
+    cols = int(max(64, min(N, seconds / max(per_col, 1e-12))))
+    cols = (cols // 64) * 64
+    c, s = p.codes[:cols], p.scales[:cols]
+    t0 = time.perf_counter()
+    for M in MS:
+        oracle.w4a16(x[:M], c, s)
+        oracle.w4a8(qa[:M], sx[:M], c, s)
+    dt = time.perf_counter() - t0
+    wb = 2 * len(MS) * w4_bytes(cols, K)
+    desc = (f"oracle W4A16 + W4A8 at M={list(MS)} on {cols} of 5120 output rows of one "
+            f"K=N=5120 layer ({wb / 1e6:.1f} MB of packed-weight equivalent)")
+    return wb, dt, desc
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle on the host cores (rank 0 only)."""
+    ws, rank, _ = dist_setup("gloo")
+    if rank != 0:
+        return
+    cores = len(os.sched_getaffinity(0))
+    budget = 3.0
+    times, wbs, desc = [], [], ""
+    for i in range(args.warmup + args.steps):
+        wb, dt, desc = oracle_sample(budget)
+        if i >= args.warmup:
+            times.append(dt)
+            wbs.append(wb)
+    value = sum(wbs) / sum(times) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "projection K=N=5120, M in {1,4,16,64}, W4A16 + W4A8; "
+                                   "bounded CPU sample per step"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm --
+def time_graph(g, stream, reps=1):
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e.record(stream)
+    return s, e
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()                                    # eager warm-up: sets attributes, caches
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def parity_err(y, ref):
+    y = y.float().cpu().numpy().astype(np.float64)
+    ref = np.asarray(ref).astype(np.float64)
+    if not np.isfinite(y).all():
+        return float("inf")
+    return float(np.abs(y - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+def run_ours(args):
+    import __graft_entry__
+    __graft_entry__.build()
+    import int8_weight_quantized_int4_gb300 as q
+
+    ws_n, rank, local = dist_setup("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    pk, pk_src = peaks()
+    hbm = float(pk["hbm_gbs"])
+
+    # ---- inputs (seeded, synthetic), weights resident in HBM
+    p = synth.projection(64)
+    packed0 = q.qpack_w4(p.codes.to(dev), p.scales.to(dev))
+    packed = [packed0] + [packed0.clone() for _ in range(LAYERS - 1)]
+    gen = synth.generator(1000 + rank)
+    X = {M: synth.activations(LAYERS * M, K, gen, outlier_frac=0.01).view(LAYERS, M, K).to(dev)
+         for M in MS}
+    Y16 = {M: torch.empty((LAYERS, M, N), dtype=torch.float16, device=dev) for M in MS}
+    Y8 = {M: torch.empty((LAYERS, M, N), dtype=torch.float16, device=dev) for M in MS}
+    XQ = {M: torch.empty((LAYERS, M, K), dtype=torch.int8, device=dev) for M in MS}
+    XS = {M: torch.empty((LAYERS, M), dtype=torch.float32, device=dev) for M in MS}
+    wsp = q.Workspace(dev)
+    for M in MS:
+        for mode in (q.MODE_W4A16, q.MODE_W4A8):
+            wsp.get(mode, M, N, K)
+    torch.cuda.synchronize()
+
+    def block16(M):
+        def f():
+            for r in range(LAYERS):
+                q.qgemm_w4a16(X[M][r], packed[r], N, K, y=Y16[M][r], ws=wsp)
+        return f
+
+    def block8(M):
+        def f():
+            for r in range(LAYERS):
+                q.quant_act_int8(X[M][r], XQ[M][r], XS[M][r])
+                q.qgemm_w4a8(XQ[M][r], XS[M][r], packed[r], N, K, y=Y8[M][r], ws=wsp)
+        return f
+
+    n0 = q.num_kernel_launches()
+    graphs = []
+    for M in MS:
+        graphs.append(("w4a16", M, capture(block16(M), stream)))
+    for M in MS:
+        graphs.append(("w4a8", M, capture(block8(M), stream)))
+    launches_per_step = (q.num_kernel_launches() - n0) // 2   # eager warm-up + capture
+    step_wbytes = len(graphs) * LAYERS * w4_bytes(N, K)
+
+    def step(events=None):
+        for mode, M, g in graphs:
+            if events is not None:
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                g.replay()
+                e.record(stream)
+                events.append((mode, M, s, e))
+            else:
+                g.replay()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    barrier(ws_n)
+
+    clocks = Clocks(local)
+    clocks.start()
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    blocks = []
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step(blocks)
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(elapsed_ms, ws_n, dev)
+    ms_per_step = elapsed_ms / args.steps
+    value = ws_n * step_wbytes * args.steps / (elapsed_ms / 1e3) / 1e9
+
+    # ---- per (mode, M) figures from the block events
+    per = {}
+    for mode, M, s, e in blocks:
+        per.setdefault((mode, M), []).append(s.elapsed_time(e))
+    per_m = {}
+    roof_bytes = roof_ms = 0.0
+    for (mode, M), v in per.items():
+        ms = statistics.median(v)
+        us = 1e3 * ms / LAYERS
+        flops = 2.0 * M * N * K
+        act_b = M * K * (2 if mode == "w4a16" else 1) + (4 * M if mode == "w4a8" else 0)
+        alg = w4_bytes(N, K) + act_b + 2 * M * N
+        per_m[f"{mode}_M{M}"] = {
+            "us_per_layer": round(us, 3), "weight_GBps": round(w4_bytes(N, K) / us / 1e3, 1),
+            "TFLOPS": round(flops / us / 1e6, 2), "alg_GBps": round(alg / us / 1e3, 1),
+            "frac_hbm": round(alg / us / 1e3 / hbm, 4),
+            "kernels_per_layer": 1 if mode == "w4a16" else 3}
+        if mode == "w4a16":
+            roof_bytes += alg * LAYERS * len(v)
+            roof_ms += sum(v)
+    achieved = roof_bytes / (roof_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "qgemm_tc_kernel (W4A16, M=1..64, K=N=5120)",
+                "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "peak_source": pk_src,
+                "traffic": None,
+                "per_launch_alg_bytes": "13,516,800 B packed weights + 2MK activation + 2MN output"}
+
+    # ---- parity spot check of the timed outputs (the pages' lesson: a kernel can
+    #      benchmark beautifully while producing garbage)
+    import oracle
+    cols = np.arange(0, N, 37)
+    parity = {}
+    for M in MS:
+        xc = X[M][LAYERS - 1].cpu()
+        ref16 = oracle.w4a16(xc, p.codes[cols], p.scales[cols])
+        parity[f"w4a16_M{M}"] = parity_err(Y16[M][LAYERS - 1].cpu()[:, cols], ref16)
+        oq, os_ = oracle.quant_act_int8(xc)
+        ref8 = oracle.w4a8(oq, os_, p.codes[cols], p.scales[cols])
+        parity[f"w4a8_M{M}"] = parity_err(Y8[M][LAYERS - 1].cpu()[:, cols], ref8)
+
+    # ---- end to end: host (pinned) inputs in, results out, every step
+    hx = {M: X[M].cpu().pin_memory() for M in MS}
+    hy16 = {M: torch.empty_like(Y16[M], device="cpu").pin_memory() for M in MS}
+    hy8 = {M: torch.empty_like(Y8[M], device="cpu").pin_memory() for M in MS}
+    h2d = sum(hx[M].numel() * 2 for M in MS)
+    d2h = sum((hy16[M].numel() + hy8[M].numel()) * 2 for M in MS)
+
+    def e2e_step():
+        for M in MS:
+            X[M].copy_(hx[M], non_blocking=True)
+        step()
+        for M in MS:
+            hy16[M].copy_(Y16[M], non_blocking=True)
+            hy8[M].copy_(Y8[M], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(ws_n)
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        es.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        ee.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(es.elapsed_time(ee), ws_n, dev)
+    e2e = {"value": round(ws_n * step_wbytes * args.steps / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "note": "pinned host activations in and fp16 outputs out every step, graphs of the "
+                   "public calls in between"}
+
+    derr = q.device_error()
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws_n,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic",
+            "config": {"workload": "decode/verify projection K=N=5120, M in {1,4,16,64}, "
+                                   "W4A16 and W4A8 (per-token int8 act quant), 32 layers",
+                       "l2": "inputs larger than L2: 32 distinct 13.5 MB packed weights (432 MB) "
+                             "rotate, each GEMM streams its weights from HBM",
+                       "weight_bytes_per_step": step_wbytes, "graphs": True,
+                       "parallelism": f"replicas x{ws_n}"},
+            "roofline": roofline, "per_M": per_m, "parity": parity,
+            "gpu_launches": int(launches_per_step * args.steps), "clocks": clk, "e2e": e2e,
+            "device_error": derr}
+
+    if ws_n == 1 and not args.no_extras:
+        line["configs"] = extras(q, dev, stream, pk, pk_src)
+    if rank == 0 and ws_n == 1:
+        cores = len(os.sched_getaffinity(0))
+        wb, dt, desc = oracle_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(wb / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+                                "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------- the other workloads --
+def extras(q, dev, stream, pk, pk_src):
+    """FFN pair (M=64, W4A8), prefill (M=8192, both modes), lm_head (W8A16).
+    Each timed with CUDA events on graph replays, with a parity spot check."""
+    import oracle
+    hbm = float(pk["hbm_gbs"])
+    peak16 = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+    out = {}
+
+    def timeit(fn, reps):
+        g = capture(fn, stream)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                g.replay()
+            s, e = time_graph(g, stream, reps)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / reps
+
+    # FFN pair at M=64, W4A8: up 5120 -> 34816 and down 17408 -> 5120, 4 rotating copies
+    for name, prob in (("ffn_up_m64_w4a8", synth.ffn_up(64)), ("ffn_down_m64_w4a8", synth.ffn_down(64))):
+        pkd = q.qpack_w4(prob.codes.to(dev), prob.scales.to(dev))
+        copies = [pkd] + [pkd.clone() for _ in range(3)]
+        x = prob.x.to(dev)
+        xq, xs = q.quant_act_int8(x)
+        y = torch.empty((64, prob.N), dtype=torch.float16, device=dev)
+        wsp = q.Workspace(dev)
+        wsp.get(q.MODE_W4A8, 64, prob.N, prob.K)
+
+        def f():
+            for c in copies:
+                q.quant_act_int8(x, xq, xs)
+                q.qgemm_w4a8(xq, xs, c, prob.N, prob.K, y=y, ws=wsp)
+        ms = timeit(f, 20) / len(copies)
+        wb = w4_bytes(prob.N, prob.K)
+        cols = np.arange(0, prob.N, max(1, prob.N // 512))
+        oq, os_ = oracle.quant_act_int8(prob.x)
+        ref = oracle.w4a8(oq, os_, prob.codes[cols], prob.scales[cols])
+        out[name] = {"us": round(ms * 1e3, 2), "weight_GBps": round(wb / ms / 1e6, 1),
+                     "TOPS": round(2 * 64 * prob.N * prob.K / ms / 1e9, 2),
+                     "frac_hbm": round((wb + 64 * prob.K + 256 + 128 * prob.N) / ms / 1e6 / hbm, 4),
+                     "kernels": 3, "parity": parity_err(y.cpu()[:, cols], ref)}
+        del copies, pkd
+
+    # prefill M=8192, W4A16 and W4A8 on identical weights
+    pp = synth.prefill(8192)
+    pkd = q.qpack_w4(pp.codes.to(dev), pp.scales.to(dev))
+    x = pp.x.to(dev)
+    y = torch.empty((8192, pp.N), dtype=torch.float16, device=dev)
+    xq, xs = q.quant_act_int8(x)
+    wsp = q.Workspace(dev)
+    wsp.get(q.MODE_W4A8, 8192, pp.N, pp.K)
+    flops = 2.0 * 8192 * pp.N * pp.K
+    rows = np.arange(0, 8192, 61)
+    cols = np.arange(0, pp.N, 211)
+    for mode in ("w4a16", "w4a8"):
+        if mode == "w4a16":
+            f = lambda: q.qgemm_w4a16(x, pkd, pp.N, pp.K, y=y, ws=wsp)  # noqa: E731
+        else:
+            def f():
+                q.quant_act_int8(x, xq, xs)
+                q.qgemm_w4a8(xq, xs, pkd, pp.N, pp.K, y=y, ws=wsp)
+        ms = timeit(f, 5)
+        xr = pp.x.numpy()[rows]
+        if mode == "w4a16":
+            ref = oracle.w4a16(xr, pp.codes[cols], pp.scales[cols])
+        else:
+            oq, os_ = oracle.quant_act_int8(xr)
+            ref = oracle.w4a8(oq, os_, pp.codes[cols], pp.scales[cols])
+        tf = flops / ms / 1e9
+        out[f"prefill_m8192_{mode}"] = {
+            "ms": round(ms, 3), "TFLOPS": round(tf, 1), "frac_f16_peak": round(tf / peak16, 4),
+            "f16_peak_TFLOPS": peak16, "peak_source": pk_src + " (bf16 sustained; fp16 dense rate is the same)",
+            "int8_peak": None, "parity": parity_err(y.cpu().numpy()[rows][:, cols], ref)}
+    del pkd, x, y, xq, xs, wsp
+    torch.cuda.empty_cache()
+
+    # lm_head W8A16: 248,320 x 5120 int8 (1.29 GB > L2)
+    lh = synth.lm_head(64)
+    pk8 = q.qpack_w8(lh.codes.to(dev), lh.scales.to(dev))
+    wb = w8_bytes(lh.N, lh.K)
+    cols = np.concatenate([np.arange(0, lh.N, 997), [lh.N - 1]])
+    wsp = q.Workspace(dev)
+    for M in (1, 8, 16, 64):
+        x = lh.x[:M].contiguous().to(dev)
+        y = torch.empty((M, lh.N), dtype=torch.float16, device=dev)
+        wsp.get(q.MODE_W8A16, M, lh.N, lh.K)
+        ms = timeit(lambda: q.qgemm_w8a16(x, pk8, lh.N, lh.K, y=y, ws=wsp), 10)
+        ref = oracle.w8a16(lh.x[:M], lh.codes[cols], lh.scales[cols])
+        alg = wb + 2 * M * lh.K + 2 * M * lh.N
+        out[f"lm_head_w8a16_M{M}"] = {"us": round(ms * 1e3, 1), "weight_GBps": round(wb / ms / 1e6, 1),
+                                      "frac_hbm": round(alg / ms / 1e6 / hbm, 4),
+                                      "TFLOPS": round(2 * M * lh.N * lh.K / ms / 1e9, 2),
+                                      "parity": parity_err(y.cpu()[:, cols], ref)}
+    del pk8
+    torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/*
+ * qgemm.h -- C ABI of the GB300 (sm_103a) weight-quantized linear layer.
+ *
+ * The method: "What this repo does that stock vLLM doesn't"
+ * (qwen38-27b-rtx3090 docs/optimizations.md), section "In full":
+ *   item 4  int4 weights with symmetric group-128 fp16 scales (about half of them
+ *           negative), activations either fp16 (W4A16) or quantized to int8 per
+ *           token (W4A8); the bug the page reports came from reading the group
+ *           scales as unsigned, and its fix keeps each scale's sign;
+ *   item 1  lm_head / embed_tokens requantized to int8 group-128 (~0.6 % error);
+ *   item 5  the 248k-row int8 lm_head run for every draft token (W8A16).
+ *
+ * The linear layer is  y[M,N] = x[M,K] . W^T  with the logical weight
+ * W[n,k] = code[n,k] * scale[n, k/128]  (groups of 128 along K).
+ *
+ * Conventions for every function below:
+ *   - All tensors are dense, row-major, and live in device memory owned by the
+ *     caller.  The library never allocates device memory and never synchronizes
+ *     on the calls marked "async"; they are enqueued on `stream`.
+ *   - fp16 means IEEE binary16, passed as its bit pattern (uint16_t).
+ *   - Return value: QW_OK (0) or a negative QW_ERR_* code.  Argument checks
+ *     happen on the host before anything is enqueued; on an error nothing is
+ *     enqueued and qw_last_error_string() describes it.  No C++ exception
+ *     crosses this boundary.
+ *   - Errors found on the device (a pipeline wait that exceeded its time limit,
+ *     int4 codes out of range in qpack_w4) are recorded in a per-device error
+ *     word; qw_device_error() reads and clears it.
+ *   - Shapes: K and N must be positive multiples of 128.  M = 0 or N = 0 is
+ *     an empty problem and returns QW_OK without enqueuing work.
+ *   - Every pointer must be 16-byte aligned.
+ *   - The device must be compute capability 10.3 (GB300); otherwise QW_ERR_ARCH.
+ *   - There is no CPU fallback: every computing call runs hand-written CUDA
+ *     kernels on the current device.
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st *qw_stream_t;
+
+enum {
+    QW_OK = 0,
+    QW_ERR_INVALID_ARG = -1,        /* null pointer, negative size */
+    QW_ERR_UNSUPPORTED_SHAPE = -2,  /* K or N not a multiple of 128, or too large */
+    QW_ERR_ALIGNMENT = -3,          /* a pointer is not 16-byte aligned */
+    QW_ERR_WORKSPACE = -4,          /* workspace missing or smaller than required */
+    QW_ERR_ARCH = -5,               /* no device, or the device is not sm_103 */
+    QW_ERR_CUDA = -6,               /* a CUDA runtime call failed */
+    QW_ERR_TIMEOUT = -7,            /* (device) a pipeline wait exceeded its limit */
+    QW_ERR_BAD_CODES = -8           /* (device) qpack_w4 saw a code outside [-8, 7] */
+};
+
+enum { QW_MODE_W4A16 = 0, QW_MODE_W4A8 = 1, QW_MODE_W8A16 = 2 };
+
+/* ------------------------------------------------------------------------
+ * Weight packing (load time, not on the hot path).
+ *
+ * Repacks logical weights into the tile-major layout the GEMM kernels stream
+ * with one bulk copy per (128 rows x 128 K) chunk.  The sign of every group
+ * scale is kept as it is: no folding into the codes, no unsigned
+ * reinterpretation ("In full" item 4 describes the failure that unsigned
+ * scales caused).
+ *
+ *   codes   [N, K] int8, device.  qpack_w4: each code in [-8, 7]; a code out of
+ *           that range is packed as (code & 15) and sets QW_ERR_BAD_CODES in
+ *           the device error word.  qpack_w8: any int8.
+ *   scales  [N, K/128] fp16, device, signed.
+ *   packed  device buffer of qpack_w4_bytes(N, K) / qpack_w8_bytes(N, K) bytes,
+ *           written completely.  Its layout, chunk (t, g) for row tile
+ *           t = n/128 and group g = k/128 at byte offset (t*(K/128)+g)*CHUNK:
+ *             W4: CHUNK = 8448.  Bytes [0, 8192): for slice j in 0..3 and row
+ *                 r in 0..127, 16 bytes at j*2048 + r*16 hold the 32 codes
+ *                 k = 128g + 32j + 8i + e (word i = 0..3, e = 0..7) of row
+ *                 128t + r, as nibbles (code + 8) at bit 4*p of word i where
+ *                 p = 4*(e % 2) + e/2.  Bytes [8192, 8448): the 128 scales of
+ *                 the rows, fp16, in row order.
+ *             W8: CHUNK = 16640.  Bytes [0, 16384): for slice j in 0..7 and row
+ *                 r, 16 bytes at j*2048 + r*16 hold codes k = 128g + 16j + b
+ *                 (b = 0..15, byte b) stored as (code XOR 0x80).  Bytes
+ *                 [16384, 16640): the 128 scales, fp16.
+ *   Async.  Returns QW_OK, QW_ERR_INVALID_ARG, QW_ERR_UNSUPPORTED_SHAPE,
+ *   QW_ERR_ALIGNMENT, QW_ERR_ARCH or QW_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+size_t qpack_w4_bytes(int N, int K);   /* N*K/2 + 2*N*(K/128); 0 if the shape is invalid */
+size_t qpack_w8_bytes(int N, int K);   /* N*K   + 2*N*(K/128); 0 if the shape is invalid */
+int qpack_w4(const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
+             qw_stream_t stream);
+int qpack_w8(const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
+             qw_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Per-token int8 activation quantization ("In full" item 4: activations are
+ * quantized to int8 per token).  For each row m:
+ *   amax = max_k |x[m,k]|  (binary32),  xs[m] = amax / 127  (IEEE binary32
+ *   divide, round to nearest even),  xq[m,k] = clamp(rne(x[m,k] / xs[m]),
+ *   -127, 127)  (IEEE divide, then round half to even);  a row of zeros gives
+ *   xs[m] = 0 and xq[m,:] = 0.  Codes and scales are bit-exact against that
+ *   definition.
+ *   x  [M, K] fp16, device.   xq [M, K] int8, device.   xs [M] binary32, device.
+ *   K must be a positive multiple of 8.  Async.
+ * ------------------------------------------------------------------------ */
+int quant_act_int8(const uint16_t *x, int M, int K, int8_t *xq, float *xs, qw_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Workspace.  qgemm_workspace_bytes() returns the bytes of scratch device
+ * memory a qgemm_* call of this mode and shape needs on the current device
+ * (0 when it needs none).  The caller allocates it and zero-fills it ONCE
+ * before its first use; every call that returns QW_OK leaves its first
+ * qgemm_workspace_zero_bytes() bytes zero again, so it can be reused by later
+ * calls of any shape whose requirement fits.  A workspace must not be shared by
+ * calls that may run concurrently (different streams).  After QW_ERR_TIMEOUT
+ * zero-fill it again.
+ * ------------------------------------------------------------------------ */
+size_t qgemm_workspace_bytes(int mode, int M, int N, int K);
+size_t qgemm_workspace_zero_bytes(int mode, int M, int N, int K);
+
+/* ------------------------------------------------------------------------
+ * The quantized GEMMs.  y[m,n] = fp16( sum_g scale[n,g] * sum_{k in g}
+ * a[m,k] * code[n,k] ), accumulated in binary32 on tensor cores:
+ *   qgemm_w4a16  a = x (fp16 [M,K]), int4 weights packed by qpack_w4
+ *                ("In full" item 4; the W4A16 body of the model).
+ *   qgemm_w4a8   a = xq (int8 [M,K]) and the result is multiplied by xs[m]
+ *                (binary32 [M]) -- the output of quant_act_int8 ("In full"
+ *                item 4, W4A8).  The int8 products are exact on the fp16
+ *                tensor path used here (sm_103a has no int8 tcgen05 MMA).
+ *   qgemm_w8a16  a = x (fp16), int8 weights packed by qpack_w8 (the int8
+ *                group-128 lm_head, "In full" items 1 and 5).
+ *   y [M, N] fp16, device, fully written.  ws / ws_bytes: the workspace above
+ *   (may be NULL when qgemm_workspace_bytes() is 0).
+ *   Accuracy: max|y - y_ref| / max|y_ref| <= 5e-3 against the binary64
+ *   definition; results are bit-identical between repeated calls.
+ *   Async.  Returns QW_OK, QW_ERR_INVALID_ARG, QW_ERR_UNSUPPORTED_SHAPE,
+ *   QW_ERR_ALIGNMENT, QW_ERR_WORKSPACE, QW_ERR_ARCH or QW_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+int qgemm_w4a16(const uint16_t *x, const void *packed_w4, int M, int N, int K, uint16_t *y,
+                void *ws, size_t ws_bytes, qw_stream_t stream);
+int qgemm_w4a8(const int8_t *xq, const float *xs, const void *packed_w4, int M, int N, int K,
+               uint16_t *y, void *ws, size_t ws_bytes, qw_stream_t stream);
+int qgemm_w8a16(const uint16_t *x, const void *packed_w8, int M, int N, int K, uint16_t *y,
+                void *ws, size_t ws_bytes, qw_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics.
+ *   qw_last_error_string  text of the last host-side error of the calling
+ *                         thread ("" if none).  Never NULL.
+ *   qw_device_error       synchronizes the current device, returns the device
+ *                         error word (QW_OK, QW_ERR_TIMEOUT or
+ *                         QW_ERR_BAD_CODES) and clears it.  QW_ERR_CUDA if the
+ *                         read itself fails.
+ *   qw_num_kernel_launches  number of kernels this library has enqueued in
+ *                         this process (all devices, all threads).
+ * ------------------------------------------------------------------------ */
+const char *qw_last_error_string(void);
+int qw_device_error(void);
+long long qw_num_kernel_launches(void);
+
+/* ------------------------------------------------------------------------
+ * Schedule query (host only, no device access): how a qgemm call of this shape
+ * is split over `num_sms` persistent CTAs.  For tests and tooling.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int bn;                 /* tokens per tile (the MMA N): 16, 32, 64, 128 or 256 */
+    int token_tiles;        /* ceil(M / bn) */
+    int row_tiles;          /* N / 128 */
+    int groups;             /* K / 128 */
+    long long tiles;        /* token_tiles * row_tiles */
+    long long chunks;       /* tiles * groups: one chunk = 128 rows x 128 K */
+    int grid;               /* persistent CTAs launched */
+    int stream_k;           /* 1: contiguous chunk ranges with a reduction; 0: whole tiles */
+    int stages;             /* shared-memory pipeline depth */
+    int smem_bytes;         /* dynamic shared memory per CTA */
+    size_t ws_bytes;        /* workspace bytes (see qgemm_workspace_bytes) */
+    size_t ws_zero_bytes;   /* leading workspace bytes that must be zero */
+} qw_plan_t;
+
+int qw_plan(int mode, int M, int N, int K, int num_sms, qw_plan_t *out);
+
+/* The segments (tile, first group, end group, partial slot or -1) CTA `cta`
+ * processes under `plan`, in order; returns how many, writing at most `cap`. */
+int qw_plan_segments(const qw_plan_t *plan, int cta, int cap, long long *tile, int *g0,
+                     int *g1, int *slot);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QGEMM_H */

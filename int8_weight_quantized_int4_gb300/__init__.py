@@ -1,0 +1,269 @@
+"""Python binding of libqgemm (include/qgemm.h): the GB300 weight-quantized
+linear layer.  Argument marshalling only -- every computing step runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback.  PyTorch supplies
+device memory and the current CUDA stream.
+
+Entry points (same names as the C ABI):
+    qpack_w4(codes, scales) -> packed        qpack_w8(codes, scales) -> packed
+    quant_act_int8(x) -> (xq, xs)
+    qgemm_w4a16(x, packed, N, K) -> y        qgemm_w4a8(xq, xs, packed, N, K) -> y
+    qgemm_w8a16(x, packed, N, K) -> y
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqgemm.so")
+
+QW_OK = 0
+QW_ERR_INVALID_ARG = -1
+QW_ERR_UNSUPPORTED_SHAPE = -2
+QW_ERR_ALIGNMENT = -3
+QW_ERR_WORKSPACE = -4
+QW_ERR_ARCH = -5
+QW_ERR_CUDA = -6
+QW_ERR_TIMEOUT = -7
+QW_ERR_BAD_CODES = -8
+MODE_W4A16, MODE_W4A8, MODE_W8A16 = 0, 1, 2
+
+# every function the header declares: name -> (restype, argtypes)
+_p, _i, _sz, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("bn", _i), ("token_tiles", _i), ("row_tiles", _i), ("groups", _i),
+                ("tiles", _ll), ("chunks", _ll), ("grid", _i), ("stream_k", _i), ("stages", _i),
+                ("smem_bytes", _i), ("ws_bytes", _sz), ("ws_zero_bytes", _sz)]
+
+
+SIGNATURES = {
+    "qpack_w4_bytes": (_sz, [_i, _i]),
+    "qpack_w8_bytes": (_sz, [_i, _i]),
+    "qpack_w4": (_i, [_p, _p, _i, _i, _p, _p]),
+    "qpack_w8": (_i, [_p, _p, _i, _i, _p, _p]),
+    "quant_act_int8": (_i, [_p, _i, _i, _p, _p, _p]),
+    "qgemm_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "qgemm_workspace_zero_bytes": (_sz, [_i, _i, _i, _i]),
+    "qgemm_w4a16": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
+    "qgemm_w4a8": (_i, [_p, _p, _p, _i, _i, _i, _p, _p, _sz, _p]),
+    "qgemm_w8a16": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
+    "qw_last_error_string": (ctypes.c_char_p, []),
+    "qw_device_error": (_i, []),
+    "qw_num_kernel_launches": (_ll, []),
+    "qw_plan": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(Plan)]),
+    "qw_plan_segments": (_i, [ctypes.POINTER(Plan), _i, _i, _p, _p, _p, _p]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class QgemmError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"qgemm error {code}: {msg}")
+        self.code = code
+
+
+def lib():
+    """Load libqgemm.so (built by build.py / __graft_entry__.build()); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with "
+                                  "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != QW_OK:
+        raise QgemmError(rc, lib().qw_last_error_string().decode())
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _need(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+
+
+# ------------------------------------------------------------------ packing --
+def qpack_w4_bytes(N: int, K: int) -> int:
+    return int(lib().qpack_w4_bytes(N, K))
+
+
+def qpack_w8_bytes(N: int, K: int) -> int:
+    return int(lib().qpack_w8_bytes(N, K))
+
+
+def _pack(bits, codes, scales, out=None):
+    _need(codes, torch.int8, "codes", 2)
+    _need(scales, torch.float16, "scales", 2)
+    N, K = codes.shape
+    nbytes = (qpack_w4_bytes if bits == 4 else qpack_w8_bytes)(N, K)
+    if out is None:
+        out = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=codes.device)
+    fn = lib().qpack_w4 if bits == 4 else lib().qpack_w8
+    with torch.cuda.device(codes.device):
+        _check(fn(_ptr(codes), _ptr(scales), N, K, _ptr(out), _stream(codes)))
+    return out
+
+
+def qpack_w4(codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor | None = None):
+    """int4 codes int8 [N,K] in [-8,7] + signed fp16 scales [N,K/128] -> packed uint8 buffer."""
+    return _pack(4, codes, scales, out)
+
+
+def qpack_w8(codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor | None = None):
+    """int8 codes [N,K] + signed fp16 scales [N,K/128] -> packed uint8 buffer."""
+    return _pack(8, codes, scales, out)
+
+
+# ------------------------------------------------------- activation quant --
+def quant_act_int8(x: torch.Tensor, xq: torch.Tensor | None = None, xs: torch.Tensor | None = None):
+    """fp16 [M,K] -> (int8 codes [M,K], binary32 per-token scales [M])."""
+    _need(x, torch.float16, "x", 2)
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if xs is None:
+        xs = torch.empty((M,), dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        _check(lib().quant_act_int8(_ptr(x), M, K, _ptr(xq), _ptr(xs), _stream(x)))
+    return xq, xs
+
+
+# -------------------------------------------------------------- workspace --
+def workspace_bytes(mode: int, M: int, N: int, K: int) -> int:
+    return int(lib().qgemm_workspace_bytes(mode, M, N, K))
+
+
+class Workspace:
+    """A zero-initialised device workspace that grows on demand (one per stream)."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+
+    def get(self, mode: int, M: int, N: int, K: int):
+        with torch.cuda.device(self.device):
+            need = workspace_bytes(mode, M, N, K)
+        if need == 0:
+            return None, 0
+        if self.buf is None or self.buf.numel() < need:
+            self.buf = torch.zeros(need, dtype=torch.uint8, device=self.device)
+        return self.buf, self.buf.numel()
+
+
+_default_ws = {}
+
+
+def _ws_for(t, mode, M, N, K, ws):
+    if ws is None:
+        key = (t.device, torch.cuda.current_stream(t.device).cuda_stream)
+        ws = _default_ws.setdefault(key, Workspace(t.device))
+    return ws.get(mode, M, N, K)
+
+
+# ------------------------------------------------------------------ GEMMs --
+def _out(y, M, N, dev):
+    if y is None:
+        return torch.empty((M, N), dtype=torch.float16, device=dev)
+    _need(y, torch.float16, "y", 2)
+    if tuple(y.shape) != (M, N):
+        raise ValueError("y has the wrong shape")
+    return y
+
+
+def qgemm_w4a16(x, packed, N: int, K: int, y=None, ws: Workspace | None = None):
+    """y[M,N] = x[M,K] . W^T with W int4 group-128 (packed by qpack_w4), fp16 out."""
+    _need(x, torch.float16, "x", 2)
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("x.shape[1] != K")
+    y = _out(y, M, N, x.device)
+    wbuf, wbytes = _ws_for(x, MODE_W4A16, M, N, K, ws)
+    with torch.cuda.device(x.device):
+        _check(lib().qgemm_w4a16(_ptr(x), _ptr(packed), M, N, K, _ptr(y), _ptr(wbuf), wbytes,
+                                 _stream(x)))
+    return y
+
+
+def qgemm_w4a8(xq, xs, packed, N: int, K: int, y=None, ws: Workspace | None = None):
+    """y[M,N] = xs[m] * (xq[M,K] . W^T) with int8 per-token activations, int4 weights."""
+    _need(xq, torch.int8, "xq", 2)
+    _need(xs, torch.float32, "xs", 1)
+    M = xq.shape[0]
+    if xq.shape[1] != K or xs.shape[0] != M:
+        raise ValueError("shape mismatch")
+    y = _out(y, M, N, xq.device)
+    wbuf, wbytes = _ws_for(xq, MODE_W4A8, M, N, K, ws)
+    with torch.cuda.device(xq.device):
+        _check(lib().qgemm_w4a8(_ptr(xq), _ptr(xs), _ptr(packed), M, N, K, _ptr(y), _ptr(wbuf),
+                                wbytes, _stream(xq)))
+    return y
+
+
+def qgemm_w8a16(x, packed, N: int, K: int, y=None, ws: Workspace | None = None):
+    """y[M,N] = x[M,K] . W^T with W int8 group-128 (packed by qpack_w8), fp16 out."""
+    _need(x, torch.float16, "x", 2)
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("x.shape[1] != K")
+    y = _out(y, M, N, x.device)
+    wbuf, wbytes = _ws_for(x, MODE_W8A16, M, N, K, ws)
+    with torch.cuda.device(x.device):
+        _check(lib().qgemm_w8a16(_ptr(x), _ptr(packed), M, N, K, _ptr(y), _ptr(wbuf), wbytes,
+                                 _stream(x)))
+    return y
+
+
+# -------------------------------------------------------------- diagnostics --
+def device_error() -> int:
+    """Synchronize and return (and clear) the device error word of the current device."""
+    return int(lib().qw_device_error())
+
+
+def num_kernel_launches() -> int:
+    return int(lib().qw_num_kernel_launches())
+
+
+def plan(mode: int, M: int, N: int, K: int, num_sms: int) -> Plan:
+    p = Plan()
+    _check(lib().qw_plan(mode, M, N, K, num_sms, ctypes.byref(p)))
+    return p
+
+
+def plan_segments(p: Plan, cta: int):
+    n = lib().qw_plan_segments(ctypes.byref(p), cta, 0, None, None, None, None)
+    if n < 0:
+        _check(n)
+    tile = (ctypes.c_longlong * max(n, 1))()
+    g0 = (ctypes.c_int * max(n, 1))()
+    g1 = (ctypes.c_int * max(n, 1))()
+    slot = (ctypes.c_int * max(n, 1))()
+    lib().qw_plan_segments(ctypes.byref(p), cta, n, tile, g0, g1, slot)
+    return [(tile[i], g0[i], g1[i], slot[i]) for i in range(n)]

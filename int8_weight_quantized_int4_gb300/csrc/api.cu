@@ -1,0 +1,315 @@
+// api.cu -- the C ABI declared in include/qgemm.h: argument checks, device
+// checks, planning and launches.  No allocation, no synchronization on the
+// compute calls, no CPU fallback.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+#include <atomic>
+#include <mutex>
+#include <cuda_runtime.h>
+#include "qgemm.h"
+#include "launch.h"
+#include "schedule.h"
+
+// Per-device error word written by the kernels (pipeline timeouts, bad codes).
+__device__ int g_qw_err;
+
+namespace {
+
+thread_local char tl_err[512];
+std::atomic<long long> g_launches{0};
+
+int fail(int code, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(tl_err, sizeof tl_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int fail_cuda(cudaError_t e, const char *what) {
+  return fail(QW_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+  bool ready = false;
+  int status = QW_OK;
+  int sms = 0;
+  int smem_optin = 0;
+  int *err = nullptr;
+};
+
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+
+// Current device, checked to be an sm_103 part; caches SM count and the address
+// of the error word.
+int current_device(DevInfo *&out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return fail(QW_ERR_ARCH, "no usable CUDA device (%s)", cudaGetErrorString(e));
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo &d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (major != 10 || minor != 3) {
+      d.status = fail(QW_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                      major, minor);
+    } else {
+      void *p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_qw_err);
+      if (e != cudaSuccess) d.status = fail_cuda(e, "cudaGetSymbolAddress(error word)");
+      d.err = static_cast<int *>(p);
+    }
+    d.ready = true;
+  }
+  if (d.status != QW_OK) return fail(d.status, "device %d is not usable by this library", dev);
+  out = &d;
+  return QW_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int kMaxN = 1 << 26;
+constexpr int kMaxK = 1 << 20;
+
+int check_shape(int M, int N, int K) {
+  if (M < 0 || N < 0 || K < 0) return fail(QW_ERR_INVALID_ARG, "negative size (M=%d N=%d K=%d)", M, N, K);
+  if (K == 0 || K % 128 || N % 128 || N > kMaxN || K > kMaxK)
+    return fail(QW_ERR_UNSUPPORTED_SHAPE,
+                "K and N must be positive multiples of 128 (K<=%d, N<=%d); got N=%d K=%d", kMaxK,
+                kMaxN, N, K);
+  return QW_OK;
+}
+
+int gemm_common(int mode, const void *act, const float *xs, const void *packed, int M, int N, int K,
+                uint16_t *y, void *ws, size_t ws_bytes, qw_stream_t stream) {
+  int rc = check_shape(M, N, K);
+  if (rc) return rc;
+  if (M == 0 || N == 0) return QW_OK;
+  if (!act || !packed || !y || (mode == QW_MODE_W4A8 && !xs))
+    return fail(QW_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned(act, 16) || !aligned(packed, 16) || !aligned(y, 2) || (xs && !aligned(xs, 4)) ||
+      (ws && !aligned(ws, 256)))
+    return fail(QW_ERR_ALIGNMENT, "activations and packed weights must be 16-byte aligned, "
+                                  "the workspace 256-byte aligned");
+  DevInfo *d = nullptr;
+  if ((rc = current_device(d))) return rc;
+  qw::Plan P;
+  if (qw::make_plan(mode, M, N, K, d->sms, P)) return fail(QW_ERR_UNSUPPORTED_SHAPE, "no plan");
+  if (P.stages < 2 || P.smem_bytes > d->smem_optin)
+    return fail(QW_ERR_UNSUPPORTED_SHAPE, "pipeline needs %d B of shared memory, device has %d",
+                P.smem_bytes, d->smem_optin);
+  if (P.ws_bytes > 0 && (!ws || ws_bytes < P.ws_bytes))
+    return fail(QW_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", P.ws_bytes,
+                ws ? ws_bytes : (size_t)0);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  qw::GemmArgs a;
+  a.P = P;
+  a.xs = xs;
+  a.wpack = static_cast<const uint8_t *>(packed);
+  a.y = y;
+  a.counters = P.ws_counters ? reinterpret_cast<int *>(w) : nullptr;
+  a.partials = P.ws_partials ? reinterpret_cast<float *>(w + P.ws_counters) : nullptr;
+  a.err = d->err;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (mode == QW_MODE_W4A8) {
+    uint16_t *wide = reinterpret_cast<uint16_t *>(w + P.ws_counters + P.ws_partials);
+    e = qw::launch_widen_i8(static_cast<const int8_t *>(act), wide, (size_t)M * K, d->sms, st);
+    if (e != cudaSuccess) return fail_cuda(e, "widen kernel launch");
+    a.act = wide;
+    e = qw::launch_gemm_w4a8(a, st);
+  } else {
+    a.act = static_cast<const uint16_t *>(act);
+    e = mode == QW_MODE_W8A16 ? qw::launch_gemm_w8a16(a, st) : qw::launch_gemm_w4a16(a, st);
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "GEMM kernel launch");
+  return QW_OK;
+}
+
+size_t pack_bytes(int N, int K, int bytes_per_code_x2) {
+  if (N < 0 || K <= 0 || N % 128 || K % 128 || N > kMaxN || K > kMaxK) return 0;
+  return (size_t)N * K * bytes_per_code_x2 / 2 + (size_t)2 * N * (K / 128);
+}
+
+int pack_common(int bits, const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
+                qw_stream_t stream) {
+  int rc = check_shape(0, N, K);
+  if (rc) return rc;
+  if (N == 0) return QW_OK;
+  if (!codes || !scales || !packed) return fail(QW_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned(codes, 16) || !aligned(packed, 16) || !aligned(scales, 2))
+    return fail(QW_ERR_ALIGNMENT, "codes and packed buffer must be 16-byte aligned");
+  DevInfo *d = nullptr;
+  if ((rc = current_device(d))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = bits == 4 ? qw::launch_pack_w4(codes, scales, N, K, packed, d->err, d->sms, st)
+                            : qw::launch_pack_w8(codes, scales, N, K, packed, d->sms, st);
+  if (e != cudaSuccess) return fail_cuda(e, "pack kernel launch");
+  return QW_OK;
+}
+
+}  // namespace
+
+namespace qw {
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+cudaError_t ensure_smem_attr(const void *func, int bytes) {
+  struct Entry { const void *f; int dev; int bytes; };
+  static Entry done[256];
+  static int ndone = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < ndone; ++i)
+    if (done[i].f == func && done[i].dev == dev && done[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < ndone; ++i)
+    if (done[i].f == func && done[i].dev == dev) { done[i].bytes = bytes; return cudaSuccess; }
+  if (ndone < 256) done[ndone++] = Entry{func, dev, bytes};
+  return cudaSuccess;
+}
+
+}  // namespace qw
+
+extern "C" {
+
+size_t qpack_w4_bytes(int N, int K) { return pack_bytes(N, K, 1); }
+size_t qpack_w8_bytes(int N, int K) { return pack_bytes(N, K, 2); }
+
+int qpack_w4(const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
+             qw_stream_t stream) {
+  return pack_common(4, codes, scales, N, K, packed, stream);
+}
+
+int qpack_w8(const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
+             qw_stream_t stream) {
+  return pack_common(8, codes, scales, N, K, packed, stream);
+}
+
+int quant_act_int8(const uint16_t *x, int M, int K, int8_t *xq, float *xs, qw_stream_t stream) {
+  if (M < 0 || K < 0) return fail(QW_ERR_INVALID_ARG, "negative size (M=%d K=%d)", M, K);
+  if (K == 0 || K % 8 || K > (1 << 28))
+    return fail(QW_ERR_UNSUPPORTED_SHAPE, "K must be a positive multiple of 8; got %d", K);
+  if (M == 0) return QW_OK;
+  if (!x || !xq || !xs) return fail(QW_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned(x, 16) || !aligned(xq, 8) || !aligned(xs, 4))
+    return fail(QW_ERR_ALIGNMENT, "x must be 16-byte aligned, xq 8-byte aligned");
+  DevInfo *d = nullptr;
+  int rc = current_device(d);
+  if (rc) return rc;
+  cudaError_t e = qw::launch_quant_act(x, M, K, xq, xs, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "quant kernel launch");
+  return QW_OK;
+}
+
+size_t qgemm_workspace_bytes(int mode, int M, int N, int K) {
+  DevInfo *d = nullptr;
+  if (current_device(d)) return 0;
+  qw::Plan P;
+  if (qw::make_plan(mode, M, N, K, d->sms, P)) return 0;
+  return P.ws_bytes;
+}
+
+size_t qgemm_workspace_zero_bytes(int mode, int M, int N, int K) {
+  DevInfo *d = nullptr;
+  if (current_device(d)) return 0;
+  qw::Plan P;
+  if (qw::make_plan(mode, M, N, K, d->sms, P)) return 0;
+  return P.ws_zero;
+}
+
+int qgemm_w4a16(const uint16_t *x, const void *packed_w4, int M, int N, int K, uint16_t *y, void *ws,
+                size_t ws_bytes, qw_stream_t stream) {
+  return gemm_common(QW_MODE_W4A16, x, nullptr, packed_w4, M, N, K, y, ws, ws_bytes, stream);
+}
+
+int qgemm_w4a8(const int8_t *xq, const float *xs, const void *packed_w4, int M, int N, int K,
+               uint16_t *y, void *ws, size_t ws_bytes, qw_stream_t stream) {
+  return gemm_common(QW_MODE_W4A8, xq, xs, packed_w4, M, N, K, y, ws, ws_bytes, stream);
+}
+
+int qgemm_w8a16(const uint16_t *x, const void *packed_w8, int M, int N, int K, uint16_t *y, void *ws,
+                size_t ws_bytes, qw_stream_t stream) {
+  return gemm_common(QW_MODE_W8A16, x, nullptr, packed_w8, M, N, K, y, ws, ws_bytes, stream);
+}
+
+const char *qw_last_error_string(void) { return tl_err; }
+
+int qw_device_error(void) {
+  DevInfo *d = nullptr;
+  int rc = current_device(d);
+  if (rc) return rc;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_qw_err, sizeof v);
+  if (e != cudaSuccess) return fail_cuda(e, "read error word");
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_qw_err, &zero, sizeof zero);
+  if (e != cudaSuccess) return fail_cuda(e, "clear error word");
+  return v;
+}
+
+long long qw_num_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int qw_plan(int mode, int M, int N, int K, int num_sms, qw_plan_t *out) {
+  if (!out) return fail(QW_ERR_INVALID_ARG, "null output");
+  qw::Plan P;
+  const int rc = qw::make_plan(mode, M, N, K, num_sms, P);
+  if (rc == -1) return fail(QW_ERR_INVALID_ARG, "bad mode or size");
+  if (rc) return fail(QW_ERR_UNSUPPORTED_SHAPE, "K and N must be multiples of 128");
+  out->bn = P.bn;
+  out->token_tiles = P.U;
+  out->row_tiles = P.T;
+  out->groups = P.G;
+  out->tiles = P.tiles;
+  out->chunks = P.chunks;
+  out->grid = P.grid;
+  out->stream_k = P.stream_k;
+  out->stages = P.stages;
+  out->smem_bytes = P.smem_bytes;
+  out->ws_bytes = P.ws_bytes;
+  out->ws_zero_bytes = P.ws_zero;
+  return QW_OK;
+}
+
+int qw_plan_segments(const qw_plan_t *plan, int cta, int cap, long long *tile, int *g0, int *g1,
+                     int *slot) {
+  if (!plan || cta < 0 || cta >= plan->grid || cap < 0) return fail(QW_ERR_INVALID_ARG, "bad query");
+  qw::Plan P{};
+  P.bn = plan->bn;
+  P.U = plan->token_tiles;
+  P.T = plan->row_tiles;
+  P.G = plan->groups;
+  P.tiles = plan->tiles;
+  P.chunks = plan->chunks;
+  P.grid = plan->grid;
+  P.stream_k = plan->stream_k;
+  int n = 0;
+  qw::Seg s;
+  for (int i = 0; qw::segment(P, cta, i, s); ++i, ++n) {
+    if (n < cap) {
+      if (tile) tile[n] = s.tile;
+      if (g0) g0[n] = s.g0;
+      if (g1) g1[n] = s.g1;
+      if (slot) slot[n] = s.slot;
+    }
+  }
+  return n;
+}
+
+}  // extern "C"

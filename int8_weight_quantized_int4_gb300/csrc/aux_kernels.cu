@@ -1,0 +1,215 @@
+// aux_kernels.cu -- the memory-bound kernels around the GEMM: per-token int8
+// activation quantizer, weight packers, and the int8 -> fp16 code widening
+// used by the W4A8 GEMM.
+#include <stdint.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include "launch.h"
+#include "ptx.cuh"
+#include "schedule.h"
+
+namespace qw {
+
+// --------------------------------------------------------------------------
+// Per-token int8 quantization ("In full" item 4 of "What this repo does that
+// stock vLLM doesn't": activations quantized to int8 per token).
+// One CTA per row.  amax over the row (warp shuffles, then shared memory),
+// s = amax / 127 with the IEEE divide, q = rne(x / s) clamped to [-127, 127].
+// The row is kept in registers (up to kQuantRegs 16-byte vectors per thread);
+// longer rows are re-read for the second pass.
+constexpr int kQuantThreads = 256;
+constexpr int kQuantRegs = 12;
+
+__global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const uint16_t *__restrict__ x, int K,
+                                                                  int8_t *__restrict__ q,
+                                                                  float *__restrict__ s) {
+  __shared__ float red[kQuantThreads / 32];
+  const size_t row = blockIdx.x;
+  const uint4 *xr = reinterpret_cast<const uint4 *>(x + row * (size_t)K);
+  const int nv = K / 8;
+  uint4 keep[kQuantRegs];
+  float amax = 0.0f;
+#pragma unroll
+  for (int r = 0; r < kQuantRegs; ++r) {
+    const int i = threadIdx.x + r * kQuantThreads;
+    if (i < nv) {
+      keep[r] = __ldg(xr + i);
+      const __half2 *h = reinterpret_cast<const __half2 *>(&keep[r]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(h[e]);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+  }
+  for (int i = threadIdx.x + kQuantRegs * kQuantThreads; i < nv; i += kQuantThreads) {
+    uint4 v = __ldg(xr + i);
+    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(h[e]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+
+  const float sc = __fdiv_rn(amax, 127.0f);
+  if (threadIdx.x == 0) s[row] = (amax == 0.0f) ? 0.0f : sc;
+  uint2 *qr = reinterpret_cast<uint2 *>(q + row * (size_t)K);
+
+  auto quant8 = [&](const uint4 &v) -> uint2 {
+    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
+    uint32_t out[2] = {0u, 0u};
+    if (amax != 0.0f) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(h[e]);
+        int q0 = __float2int_rn(__fdiv_rn(f.x, sc));
+        int q1 = __float2int_rn(__fdiv_rn(f.y, sc));
+        q0 = max(-127, min(127, q0));
+        q1 = max(-127, min(127, q1));
+        const uint32_t pair = ((uint32_t)(q0 & 0xff)) | ((uint32_t)(q1 & 0xff) << 8);
+        out[e >> 1] |= pair << (16 * (e & 1));
+      }
+    }
+    return make_uint2(out[0], out[1]);
+  };
+#pragma unroll
+  for (int r = 0; r < kQuantRegs; ++r) {
+    const int i = threadIdx.x + r * kQuantThreads;
+    if (i < nv) qr[i] = quant8(keep[r]);
+  }
+  for (int i = threadIdx.x + kQuantRegs * kQuantThreads; i < nv; i += kQuantThreads)
+    qr[i] = quant8(__ldg(xr + i));
+}
+
+// --------------------------------------------------------------------------
+// int8 codes -> fp16 values (exact), for the fp16 tensor-core W4A8 path.
+__global__ void widen_i8_kernel(const int8_t *__restrict__ src, uint16_t *__restrict__ dst, size_t n16) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint4 o[2];
+    uint32_t *op = reinterpret_cast<uint32_t *>(o);
+    const __half2 k1152 = __float2half2_rn(1152.0f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t u = w[j] ^ 0x80808080u;       // two's complement -> offset binary (q + 128)
+      // (1024 + u) - 1152 = q, exact in fp16
+      op[2 * j] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(u, 0x64646464u, 0x4140)), k1152));
+      op[2 * j + 1] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(u, 0x64646464u, 0x4342)), k1152));
+    }
+    uint4 *d = reinterpret_cast<uint4 *>(dst) + 2 * i;
+    d[0] = o[0];
+    d[1] = o[1];
+  }
+}
+
+// --------------------------------------------------------------------------
+// Packers.  One thread per 16-byte slice of a chunk; see qgemm.h for the layout.
+__global__ void pack_w4_kernel(const int8_t *__restrict__ codes, const uint16_t *__restrict__ scales,
+                               int N, int K, uint8_t *__restrict__ packed, int *err) {
+  const int G = K / kGroup;
+  const size_t total = (size_t)N * K / 32;   // 16-byte slices
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const size_t chunk = idx / 512;
+    const int j = (int)((idx / 128) % 4);
+    const int r = (int)(idx % 128);
+    const size_t t = chunk / G;
+    const int g = (int)(chunk % G);
+    const size_t n = t * kRows + r;
+    const int8_t *src = codes + n * K + (size_t)g * kGroup + 32 * j;
+    const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src));
+    const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src + 16));
+    const int8_t *c8a = reinterpret_cast<const int8_t *>(&a);
+    const int8_t *c8b = reinterpret_cast<const int8_t *>(&b);
+    uint32_t wds[4];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t wd = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int kk = 8 * i + e;
+        const int c = kk < 16 ? c8a[kk] : c8b[kk - 16];
+        bad |= (c < -8 || c > 7);
+        const uint32_t u = (uint32_t)(c + 8) & 15u;
+        const int p = 4 * (e & 1) + (e >> 1);
+        wd |= u << (4 * p);
+      }
+      wds[i] = wd;
+    }
+    if (bad) atomicCAS(err, 0, -8);
+    uint8_t *dst = packed + chunk * kChunkW4;
+    *reinterpret_cast<uint4 *>(dst + j * 2048 + r * 16) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+    if (j == 0) *reinterpret_cast<uint16_t *>(dst + 8192 + r * 2) = scales[n * G + g];
+  }
+}
+
+__global__ void pack_w8_kernel(const int8_t *__restrict__ codes, const uint16_t *__restrict__ scales,
+                               int N, int K, uint8_t *__restrict__ packed) {
+  const int G = K / kGroup;
+  const size_t total = (size_t)N * K / 16;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const size_t chunk = idx / 1024;
+    const int j = (int)((idx / 128) % 8);
+    const int r = (int)(idx % 128);
+    const size_t t = chunk / G;
+    const int g = (int)(chunk % G);
+    const size_t n = t * kRows + r;
+    uint4 v = __ldg(reinterpret_cast<const uint4 *>(codes + n * K + (size_t)g * kGroup + 16 * j));
+    v.x ^= 0x80808080u; v.y ^= 0x80808080u; v.z ^= 0x80808080u; v.w ^= 0x80808080u;
+    uint8_t *dst = packed + chunk * kChunkW8;
+    *reinterpret_cast<uint4 *>(dst + j * 2048 + r * 16) = v;
+    if (j == 0) *reinterpret_cast<uint16_t *>(dst + 16384 + r * 2) = scales[n * G + g];
+  }
+}
+
+// ------------------------------------------------------------- launchers --
+static int grid_for(size_t items, int threads, int sms) {
+  size_t b = (items + threads - 1) / threads;
+  const size_t cap = (size_t)sms * 8;
+  if (b > cap) b = cap;
+  return (int)(b < 1 ? 1 : b);
+}
+
+cudaError_t launch_quant_act(const uint16_t *x, int M, int K, int8_t *q, float *s, cudaStream_t st) {
+  quant_act_kernel<<<M, kQuantThreads, 0, st>>>(x, K, q, s);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_widen_i8(const int8_t *src, uint16_t *dst, size_t n, int sms, cudaStream_t st) {
+  const size_t n16 = n / 16;
+  widen_i8_kernel<<<grid_for(n16, 256, sms), 256, 0, st>>>(src, dst, n16);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_w4(const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
+                           int *err, int sms, cudaStream_t st) {
+  const size_t total = (size_t)N * K / 32;
+  pack_w4_kernel<<<grid_for(total, 256, sms), 256, 0, st>>>(codes, scales, N, K,
+                                                            static_cast<uint8_t *>(packed), err);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_w8(const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
+                           int sms, cudaStream_t st) {
+  const size_t total = (size_t)N * K / 16;
+  pack_w8_kernel<<<grid_for(total, 256, sms), 256, 0, st>>>(codes, scales, N, K,
+                                                            static_cast<uint8_t *>(packed));
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace qw

@@ -1,0 +1,368 @@
+// gemm_kernel.cuh -- the quantized linear layer on 5th-generation tensor cores.
+//
+// y[m,n] = sum_g s[n,g] * sum_{k in g} a[m,k] * q[n,k]   ("In full" item 4 of
+// "What this repo does that stock vLLM doesn't": int4 weights, signed group-128
+// scales; W8 variant for the int8 group-128 lm_head, items 1 and 5).
+//
+// Orientation: the weights are the MMA's A operand (M = 128 weight rows, one per
+// TMEM lane) and the tokens are its N (16..256), so a decode batch of 1..64
+// tokens still fills the 128-row MMA.  Per 128 x 128 weight chunk:
+//   bulk-copy warp   : one 1-D bulk copy of the packed chunk (codes + signed
+//                      scales) HBM -> shared memory
+//   producer warps   : cp.async of the bn x 128 fp16 activation tile into the
+//                      128-byte-swizzled K-major layout (zero-fill past M)
+//   dequant warps    : int4/int8 codes -> fp16 (q * s) in registers, with the
+//                      scale's sign, stored into TMEM as the A operand
+//   MMA warp         : 8 x tcgen05.mma kind::f16 (K = 16 each), fp32 accumulator
+//                      in TMEM; tcgen05.commit frees the stage
+//   epilogue warps   : tcgen05.ld the accumulator, scale by the token scale (W4A8),
+//                      write fp16 y, or a binary32 partial for a tile cut by the
+//                      stream-K split; the last CTA of a cut tile sums its
+//                      partials in CTA order (deterministic, no waiting).
+#pragma once
+#include <stdint.h>
+#include <cuda_fp16.h>
+#include "ptx.cuh"
+#include "schedule.h"
+#include "launch.h"
+
+namespace qw {
+
+
+constexpr int kDeqWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kProdWarps = 4;
+constexpr int kWarpEpi0 = kDeqWarps;                 // 8
+constexpr int kWarpProd0 = kWarpEpi0 + kEpiWarps;    // 12
+constexpr int kWarpTma = kWarpProd0 + kProdWarps;    // 16
+constexpr int kWarpMma = kWarpTma + 1;               // 17
+constexpr int kThreads = (kWarpMma + 1) * 32;        // 576
+constexpr int kAStages = 4;                          // TMEM A-operand ring (64 columns each)
+constexpr int kTmemCols = 512;
+constexpr int kAccCol0 = kAStages * 64;              // 256
+
+// offsets inside the barrier block that follows the stages
+constexpr int kBarFull = 0;
+constexpr int kBarEmpty = kBarFull + 8 * kMaxStages;
+constexpr int kBarAFull = kBarEmpty + 8 * kMaxStages;
+constexpr int kBarAEmpty = kBarAFull + 8 * kAStages;
+constexpr int kBarAccFull = kBarAEmpty + 8 * kAStages;
+constexpr int kBarAccEmpty = kBarAccFull + 8 * 2;
+constexpr int kTmemSlot = kBarAccEmpty + 8 * 2;
+constexpr int kAbortSlot = kTmemSlot + 4;
+constexpr int kBcastSlot = kAbortSlot + 4;
+
+// ---- dequantization: packed codes -> 32 half2 (64 fp16 values q*s) per thread ----
+
+// W4: two 16-byte slices (64 codes) of one row; nibble (q + 8) at bit 4p of each
+// word holds element e = 2*(p % 4) + p / 4, so the masks below yield (k, k+1) pairs.
+__device__ __forceinline__ void dequant_w4(const uint4 (&v)[2], __half2 s2, uint32_t (&o)[32]) {
+  const __half2 k1032 = __float2half2_rn(1032.0f);
+  const __half2 k16th = __float2half2_rn(0.0625f);
+  const __half2 km72 = __float2half2_rn(-72.0f);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = w[i], hi = w[i] >> 8;
+      // (1024 + u) - 1032 = q  and  (1024 + 16u)/16 - 72 = q, both exact in fp16
+      const __half2 q0 = __hsub2(u32_as_h2(lop3_and_or(lo, 0x000f000fu, 0x64006400u)), k1032);
+      const __half2 q1 = __hfma2(u32_as_h2(lop3_and_or(lo, 0x00f000f0u, 0x64006400u)), k16th, km72);
+      const __half2 q2 = __hsub2(u32_as_h2(lop3_and_or(hi, 0x000f000fu, 0x64006400u)), k1032);
+      const __half2 q3 = __hfma2(u32_as_h2(lop3_and_or(hi, 0x00f000f0u, 0x64006400u)), k16th, km72);
+      o[16 * j + 4 * i + 0] = h2_as_u32(__hmul2_rn(q0, s2));
+      o[16 * j + 4 * i + 1] = h2_as_u32(__hmul2_rn(q1, s2));
+      o[16 * j + 4 * i + 2] = h2_as_u32(__hmul2_rn(q2, s2));
+      o[16 * j + 4 * i + 3] = h2_as_u32(__hmul2_rn(q3, s2));
+    }
+  }
+}
+
+// W8: four 16-byte slices (64 codes) of one row, bytes (q XOR 0x80) in K order.
+__device__ __forceinline__ void dequant_w8(const uint4 (&v)[4], __half2 s2, uint32_t (&o)[32]) {
+  const __half2 k1152 = __float2half2_rn(1152.0f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 q0 = __hsub2(u32_as_h2(__byte_perm(w[i], 0x64646464u, 0x4140)), k1152);
+      const __half2 q1 = __hsub2(u32_as_h2(__byte_perm(w[i], 0x64646464u, 0x4342)), k1152);
+      o[8 * j + 2 * i + 0] = h2_as_u32(__hmul2_rn(q0, s2));
+      o[8 * j + 2 * i + 1] = h2_as_u32(__hmul2_rn(q1, s2));
+    }
+  }
+}
+
+template <int BN, int WBITS, bool TOKSCALE>
+__global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_constant__ GemmArgs a) {
+  constexpr int kMode = WBITS == 8 ? 2 : (TOKSCALE ? 1 : 0);
+  constexpr uint32_t kChunk = WBITS == 8 ? kChunkW8 : kChunkW4;
+  constexpr uint32_t kWAligned = (kChunk + 1023) / 1024 * 1024;
+  constexpr uint32_t kStage = kWAligned + BN * kGroup * 2;
+  constexpr int kNAcc = BN <= 128 ? 2 : 1;
+  constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
+  (void)kMode;
+
+  extern __shared__ uint8_t smem_raw[];
+  const Plan &P = a.P;
+  const int S = P.stages;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *gbase = smem_raw + (sbase - raw);
+  const uint32_t bars = sbase + (uint32_t)S * kStage;
+  uint8_t *gbars = gbase + (size_t)S * kStage;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(gbars + kAbortSlot);
+  volatile int *bcast = reinterpret_cast<volatile int *>(gbars + kBcastSlot);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int cta = blockIdx.x;
+
+  auto full_bar = [&](int s) { return bars + kBarFull + 8 * s; };
+  auto empty_bar = [&](int s) { return bars + kBarEmpty + 8 * s; };
+  auto afull_bar = [&](int i) { return bars + kBarAFull + 8 * i; };
+  auto aempty_bar = [&](int i) { return bars + kBarAEmpty + 8 * i; };
+  auto accfull_bar = [&](int i) { return bars + kBarAccFull + 8 * i; };
+  auto accempty_bar = [&](int i) { return bars + kBarAccEmpty + 8 * i; };
+  auto w_smem = [&](int s) { return sbase + (uint32_t)s * kStage; };
+  auto b_smem = [&](int s) { return sbase + (uint32_t)s * kStage + kWAligned; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1 + kProdWarps);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(afull_bar(i), kDeqWarps);
+      mbar_init(aempty_bar(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(accfull_bar(i), 1);
+      mbar_init(accempty_bar(i), kEpiWarps);
+    }
+    *abort_flag = 0;
+    *bcast = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(bars + kTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbars + kTmemSlot);
+
+  Seg sg;
+  if (warp == kWarpTma) {
+    // ------------------------------------------------ weight bulk copies --
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
+        int u, t;
+        tile_coords(P, sg.tile, u, t);
+        for (int g = sg.g0; g < sg.g1; ++g, ++it) {
+          const int s = (int)(it % (uint32_t)S);
+          const uint32_t ph = (it / (uint32_t)S) & 1u;
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(full_bar(s), kChunk);
+          const uint8_t *src = a.wpack + ((size_t)t * P.G + g) * kChunk;
+          bulk_g2s(w_smem(s), src, kChunk, full_bar(s), pol);
+        }
+      }
+    }
+  } else if (warp >= kWarpProd0 && warp < kWarpProd0 + kProdWarps) {
+    // ------------------------------------------- activation tile producer --
+    const int pt = threadIdx.x - kWarpProd0 * 32;   // 0..127
+    const int D = S >= 3 ? 2 : 1;                   // chunks of copies kept in flight
+    uint32_t it = 0;
+    bool ok = true;
+    for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
+      int u, t;
+      tile_coords(P, sg.tile, u, t);
+      for (int g = sg.g0; g < sg.g1; ++g, ++it) {
+        const int s = (int)(it % (uint32_t)S);
+        const uint32_t ph = (it / (uint32_t)S) & 1u;
+        if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
+        const uint32_t bs = b_smem(s);
+#pragma unroll 4
+        for (int pc = pt; pc < BN * 16; pc += kProdWarps * 32) {
+          const int r = pc >> 4, c = pc & 15;
+          const int kc = c >> 3, cc = c & 7;
+          const int tok = u * BN + r;
+          const bool in = tok < P.M;
+          const uint16_t *src = in ? a.act + (size_t)tok * P.K + (size_t)g * kGroup + c * 8 : a.act;
+          const uint32_t dst = bs + (uint32_t)(kc * BN * 128 + r * 128 + ((cc ^ (r & 7)) << 4));
+          cp_async16(dst, src, in ? 16u : 0u);
+        }
+        cp_async_commit();
+        if (it >= (uint32_t)D) {
+          if (D == 2) cp_async_wait<2>(); else cp_async_wait<1>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full_bar((int)((it - D) % (uint32_t)S)));
+        }
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (ok && lane == 0) {
+      const uint32_t first = it >= (uint32_t)D ? it - D : 0;
+      for (uint32_t j = first; j < it; ++j) mbar_arrive(full_bar((int)(j % (uint32_t)S)));
+    }
+  } else if (warp < kDeqWarps) {
+    // ------------------------------------------------------- dequantize --
+    const int quad = warp & 3, half_k = warp >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
+      for (int g = sg.g0; g < sg.g1; ++g, ++it) {
+        const int s = (int)(it % (uint32_t)S);
+        const int ai = (int)(it % kAStages);
+        if (!mbar_wait(full_bar(s), (it / (uint32_t)S) & 1u, abort_flag, a.err)) { ok = false; break; }
+        if (!mbar_wait(aempty_bar(ai), ((it / kAStages) & 1u) ^ 1u, abort_flag, a.err)) { ok = false; break; }
+        const uint8_t *wc = gbase + (size_t)s * kStage;
+        uint32_t o[32];
+        if constexpr (WBITS == 4) {
+          uint4 v[2];
+          v[0] = *reinterpret_cast<const uint4 *>(wc + (2 * half_k) * 2048 + row * 16);
+          v[1] = *reinterpret_cast<const uint4 *>(wc + (2 * half_k + 1) * 2048 + row * 16);
+          const __half sc = *reinterpret_cast<const __half *>(wc + 8192 + row * 2);
+          dequant_w4(v, __half2half2(sc), o);
+        } else {
+          uint4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            v[j] = *reinterpret_cast<const uint4 *>(wc + (4 * half_k + j) * 2048 + row * 16);
+          const __half sc = *reinterpret_cast<const __half *>(wc + 16384 + row * 2);
+          dequant_w8(v, __half2half2(sc), o);
+        }
+        tmem_st32(tmem + lane_base + (uint32_t)(ai * 64 + half_k * 32), o);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(afull_bar(ai));
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------- MMA --
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
+        const int b = i % kNAcc;
+        if (!mbar_wait(accempty_bar(b), ((i / kNAcc) & 1) ^ 1, abort_flag, a.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(kAccCol0 + b * BN);
+        for (int g = sg.g0; g < sg.g1; ++g, ++it) {
+          const int s = (int)(it % (uint32_t)S);
+          const int ai = (int)(it % kAStages);
+          if (!mbar_wait(afull_bar(ai), (it / kAStages) & 1u, abort_flag, a.err)) { ok = false; break; }
+          if (!mbar_wait(full_bar(s), (it / (uint32_t)S) & 1u, abort_flag, a.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t bs = b_smem(s);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t bdesc = smem_desc_sw128(bs + (uint32_t)((k >> 2) * BN * 128 + (k & 3) * 32));
+            mma_f16_ts(d, tmem + (uint32_t)(ai * 64 + k * 8), bdesc, kIdesc,
+                       (g > sg.g0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(empty_bar(s));
+          mma_commit(aempty_bar(ai));
+        }
+        if (ok) mma_commit(accfull_bar(b));
+      }
+    }
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
+    // -------------------------------------------------------- epilogue --
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int ept = threadIdx.x - kWarpEpi0 * 32;   // 0..127
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    for (int i = 0; segment(P, cta, i, sg); ++i) {
+      const int b = i % kNAcc;
+      mbar_wait(accfull_bar(b), (i / kNAcc) & 1, abort_flag, a.err);
+      named_bar_sync(1, kEpiWarps * 32);           // all four warps decide together
+      if (*abort_flag) break;
+      tc_fence_after();
+      int u, t;
+      tile_coords(P, sg.tile, u, t);
+      const int n = t * kRows + row;
+      const int m0 = u * BN;
+      const uint32_t tacc = tmem + lane_base + (uint32_t)(kAccCol0 + b * BN);
+      float *part = sg.slot >= 0 ? a.partials + (size_t)sg.slot * (BN * kRows) : nullptr;
+#pragma unroll 1
+      for (int cc = 0; cc < BN; cc += 32) {
+        uint32_t v[32];
+        if constexpr (BN == 16) tmem_ld16(tacc, v); else tmem_ld32(tacc + (uint32_t)cc, v);
+        tmem_wait_ld();
+        constexpr int W = BN < 32 ? BN : 32;
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+          const float acc = __uint_as_float(v[j]);
+          const int m = m0 + cc + j;
+          if (part) {
+            part[(cc + j) * kRows + row] = acc;
+          } else if (m < P.M) {
+            const float val = TOKSCALE ? acc * a.xs[m] : acc;
+            a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(accempty_bar(b));
+      if (part) {
+        // publish this partial; the last contributor of the tile reduces it
+        __threadfence();
+        named_bar_sync(1, kEpiWarps * 32);
+        int pf, pl;
+        tile_contributors(P, sg.tile, pf, pl);
+        if (ept == 0) {
+          const int old = atomicAdd(a.counters + sg.tile, 1);
+          const int last = (old == pl - pf) ? 1 : 0;
+          if (last) {
+            a.counters[sg.tile] = 0;    // leave the workspace zeroed for the next call
+            __threadfence();
+          }
+          *bcast = last;
+        }
+        named_bar_sync(1, kEpiWarps * 32);
+        if (*bcast) {
+          for (int j = 0; j < BN; ++j) {
+            const int m = m0 + j;
+            if (m >= P.M) break;
+            float acc = 0.0f;
+            for (int p = pf; p <= pl; ++p)
+              acc += __ldcg(a.partials + (size_t)partial_slot(P, p, sg.tile) * (BN * kRows) +
+                            j * kRows + row);
+            const float val = TOKSCALE ? acc * a.xs[m] : acc;
+            a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
+          }
+        }
+      }
+    }
+  }
+
+  // --------------------------------------------------------------- teardown --
+  __syncthreads();
+  if (*abort_flag) {
+    // let bulk copies and MMAs already issued land before the memory goes away
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace qw

@@ -1,0 +1,27 @@
+// gemm_w8a16.cu -- instantiations of the tensor-core GEMM for W8A16 (one per token tile size).
+#include "gemm_kernel.cuh"
+
+namespace qw {
+
+template <int BN>
+static cudaError_t run_w8a16(const GemmArgs &a, cudaStream_t st) {
+  auto *k = qgemm_tc_kernel<BN, 8, false>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(k), a.P.smem_bytes);
+  if (e != cudaSuccess) return e;
+  k<<<a.P.grid, kThreads, a.P.smem_bytes, st>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_w8a16(const GemmArgs &a, cudaStream_t st) {
+  switch (a.P.bn) {
+    case 16: return run_w8a16<16>(a, st);
+    case 32: return run_w8a16<32>(a, st);
+    case 64: return run_w8a16<64>(a, st);
+    case 128: return run_w8a16<128>(a, st);
+    case 256: return run_w8a16<256>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace qw

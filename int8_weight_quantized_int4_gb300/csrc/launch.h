@@ -1,0 +1,37 @@
+// launch.h -- internal interface between the C ABI (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+#include <stdint.h>
+#include <stddef.h>
+#include <cuda_runtime.h>
+#include "schedule.h"
+
+namespace qw {
+
+struct GemmArgs {
+  Plan P;
+  const uint16_t *act;      // fp16 [M,K] activations (W4A8: the widened int8 codes)
+  const float *xs;          // token scales [M] (W4A8) or nullptr
+  const uint8_t *wpack;     // packed weights
+  uint16_t *y;              // fp16 [M,N]
+  int *counters;            // [tiles] arrival counters (stream-K)
+  float *partials;          // [2*grid][bn][128] binary32 partial sums (stream-K)
+  int *err;                 // device error word
+};
+
+void count_launch();
+// Raise the dynamic shared-memory limit of `func` on the current device (once).
+cudaError_t ensure_smem_attr(const void *func, int bytes);
+
+cudaError_t launch_quant_act(const uint16_t *x, int M, int K, int8_t *q, float *s, cudaStream_t st);
+cudaError_t launch_widen_i8(const int8_t *src, uint16_t *dst, size_t n, int sms, cudaStream_t st);
+cudaError_t launch_pack_w4(const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
+                           int *err, int sms, cudaStream_t st);
+cudaError_t launch_pack_w8(const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
+                           int sms, cudaStream_t st);
+
+cudaError_t launch_gemm_w4a16(const GemmArgs &a, cudaStream_t st);
+cudaError_t launch_gemm_w4a8(const GemmArgs &a, cudaStream_t st);
+cudaError_t launch_gemm_w8a16(const GemmArgs &a, cudaStream_t st);
+
+}  // namespace qw

@@ -1,0 +1,145 @@
+"""CPU tests of the C-ABI library: it loads, exports every declared symbol, checks
+its arguments before touching a device, and its schedule (shared host/device
+code) covers every chunk exactly once.  No compute call reaches a GPU here."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+import torch
+
+import int8_weight_quantized_int4_gb300 as q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemm.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from int8_weight_quantized_int4_gb300 import build
+    build.build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while", "sizeof")))
+
+
+def test_exports_every_declared_symbol():
+    names = declared_functions()
+    assert len(names) >= 15, names
+    L = ctypes.CDLL(q.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(q.SIGNATURES), set(names) ^ set(q.SIGNATURES)
+
+
+def test_packed_sizes():
+    assert q.qpack_w4_bytes(5120, 5120) == 13_516_800
+    assert q.qpack_w4_bytes(34816, 5120) == 91_914_240
+    assert q.qpack_w4_bytes(5120, 17408) == 45_957_120
+    assert q.qpack_w8_bytes(248320, 5120) == 1_291_264_000
+    assert q.qpack_w4_bytes(100, 128) == 0 and q.qpack_w8_bytes(128, 100) == 0
+    assert q.qpack_w4_bytes(-128, 128) == 0
+
+
+def test_lm_head_size_matches_pages():
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "lm_head_bytes.json")))
+    gb = q.qpack_w8_bytes(g["rows"], g["K"]) / 1e9
+    lo, hi = g["accept_GB"]
+    assert lo <= gb <= hi
+
+
+FAKE = ctypes.c_void_p(1 << 20)          # aligned, never dereferenced on this path
+MIS = ctypes.c_void_p((1 << 20) + 2)     # misaligned
+
+
+def test_argument_errors_before_device():
+    L = q.lib()
+    n = ctypes.c_void_p(0)
+    assert L.qgemm_w4a16(FAKE, FAKE, 4, 512, 100, FAKE, n, 0, n) == q.QW_ERR_UNSUPPORTED_SHAPE
+    assert L.qgemm_w4a16(FAKE, FAKE, 4, 500, 256, FAKE, n, 0, n) == q.QW_ERR_UNSUPPORTED_SHAPE
+    assert L.qgemm_w4a16(FAKE, FAKE, -1, 512, 256, FAKE, n, 0, n) == q.QW_ERR_INVALID_ARG
+    assert L.qgemm_w4a16(n, FAKE, 4, 512, 256, FAKE, n, 0, n) == q.QW_ERR_INVALID_ARG
+    assert L.qgemm_w4a8(FAKE, n, FAKE, 4, 512, 256, FAKE, n, 0, n) == q.QW_ERR_INVALID_ARG
+    assert L.qgemm_w8a16(MIS, FAKE, 4, 512, 256, FAKE, n, 0, n) == q.QW_ERR_ALIGNMENT
+    assert L.qgemm_w4a16(FAKE, FAKE, 4, 512, 256, FAKE, MIS, 1 << 20, n) == q.QW_ERR_ALIGNMENT
+    assert b"multiple of 128" in L.qw_last_error_string() or L.qw_last_error_string()
+    # empty problems succeed without touching anything
+    assert L.qgemm_w4a16(n, n, 0, 512, 256, n, n, 0, n) == q.QW_OK
+    assert L.qgemm_w4a16(n, n, 4, 0, 256, n, n, 0, n) == q.QW_OK
+    assert L.quant_act_int8(n, 0, 256, n, n, n) == q.QW_OK
+    assert L.quant_act_int8(FAKE, 2, 12, FAKE, FAKE, n) == q.QW_ERR_UNSUPPORTED_SHAPE
+    assert L.quant_act_int8(n, 2, 16, FAKE, FAKE, n) == q.QW_ERR_INVALID_ARG
+    assert L.qpack_w4(n, FAKE, 128, 128, FAKE, n) == q.QW_ERR_INVALID_ARG
+    assert L.qpack_w8(FAKE, FAKE, 128, 130, FAKE, n) == q.QW_ERR_UNSUPPORTED_SHAPE
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_no_device_reports_arch():
+    L = q.lib()
+    n = ctypes.c_void_p(0)
+    assert L.qgemm_w4a16(FAKE, FAKE, 4, 512, 256, FAKE, n, 0, n) == q.QW_ERR_ARCH
+    assert L.quant_act_int8(FAKE, 2, 16, FAKE, FAKE, n) == q.QW_ERR_ARCH
+    assert L.qgemm_workspace_bytes(0, 4, 512, 256) == 0
+
+
+SHAPES = [
+    (0, 4, 512, 256, 152), (1, 1, 5120, 5120, 152), (0, 64, 5120, 5120, 152),
+    (1, 64, 34816, 5120, 152), (1, 64, 5120, 17408, 152), (0, 8192, 34816, 5120, 152),
+    (2, 64, 248320, 5120, 152), (2, 1, 248320, 5120, 148), (0, 130, 384, 640, 152),
+    (0, 512, 5120, 5120, 152), (0, 3, 128, 128, 152), (1, 300, 1280, 1152, 7),
+]
+
+
+@pytest.mark.parametrize("mode,M,N,K,sms", SHAPES)
+def test_schedule_covers_every_chunk_once(mode, M, N, K, sms):
+    p = q.plan(mode, M, N, K, sms)
+    assert p.bn in (16, 32, 64, 128, 256) and p.bn >= min(M, 256)
+    assert p.token_tiles == -(-M // p.bn) and p.row_tiles == N // 128 and p.groups == K // 128
+    assert 1 <= p.grid <= sms and p.stages >= 2 and p.smem_bytes <= 232448
+    seen = {}
+    slots = set()
+    pieces = {}
+    for cta in range(p.grid):
+        segs = q.plan_segments(p, cta)
+        assert segs, "every CTA gets work"
+        for tile, g0, g1, slot in segs:
+            assert 0 <= tile < p.tiles and 0 <= g0 < g1 <= p.groups
+            for g in range(g0, g1):
+                assert (tile, g) not in seen
+                seen[(tile, g)] = cta
+            whole = (g0 == 0 and g1 == p.groups)
+            assert (slot < 0) == whole
+            if slot >= 0:
+                assert p.stream_k and slot not in slots and slot // 2 == cta
+                slots.add(slot)
+                pieces.setdefault(tile, []).append((g0, cta, slot))
+    assert len(seen) == p.chunks
+    # a cut tile's pieces come from consecutive CTAs, in K order
+    for tile, ps in pieces.items():
+        ps.sort()
+        ctas = [c for _, c, _ in ps]
+        assert ctas == list(range(ctas[0], ctas[0] + len(ctas)))
+        assert len(ps) >= 2
+    if p.stream_k:
+        assert p.ws_bytes >= p.ws_zero_bytes >= p.tiles * 4
+    load = {}
+    for (tile, g), cta in seen.items():
+        load[cta] = load.get(cta, 0) + 1
+    if p.stream_k:
+        assert max(load.values()) - min(load.values()) <= 1
+
+
+def test_schedule_whole_tiles_for_prefill():
+    p = q.plan(0, 8192, 34816, 5120, 152)
+    assert p.stream_k == 0 and p.bn == 256 and p.tiles == 32 * 272
+    assert p.ws_bytes == 0
+
+
+def test_w4a8_workspace_holds_widened_codes():
+    p = q.plan(1, 8192, 34816, 5120, 152)
+    assert p.ws_bytes >= 8192 * 5120 * 2

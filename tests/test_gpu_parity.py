@@ -1,0 +1,320 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, on the
+same seeded inputs.
+
+Bars: activation codes and scales bit-exact; packed bytes bit-exact against the
+layout the header documents; GEMM outputs within
+max|y - y_ref| / max|y_ref| <= 5e-3 (fp16 outputs); repeated calls bit-identical.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 5e-3
+
+
+@pytest.fixture(scope="module")
+def q():
+    import __graft_entry__
+    __graft_entry__.build()
+    import int8_weight_quantized_int4_gb300 as q
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    return q
+
+
+DEV = torch.device("cuda:0")
+
+
+def nerr(y, ref):
+    y = (y.float().cpu().numpy() if isinstance(y, torch.Tensor) else y).astype(np.float64)
+    ref = np.asarray(ref).astype(np.float64)
+    assert np.isfinite(y).all()
+    return float(np.abs(y - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+def bits(t):
+    return t.cpu().contiguous().view(torch.int16).numpy() if isinstance(t, torch.Tensor) else t.view(np.int16)
+
+
+# --------------------------------------------------------------- quantizer --
+
+def _special_rows(x):
+    x = x.clone()
+    K = x.shape[1]
+    if x.shape[0] >= 4:
+        x[0] = 0
+        x[1] = 0
+        x[1, K // 3] = -7.25
+        x[2] = ((torch.arange(K) % 17) - 8).to(torch.float16) * 2 ** -20     # subnormals
+        x[3, :8] = torch.tensor([127, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 3.5], dtype=torch.float16)
+        x[3, 8:] = 0
+    return x
+
+
+@pytest.mark.parametrize("M,K", [(1, 5120), (4, 5120), (16, 5120), (64, 5120), (64, 17408),
+                                 (7, 136), (5, 8), (33, 24576 + 64)])
+def test_quant_act_bitexact(q, M, K):
+    x = synth.activations(M, K, synth.generator(100 + M + K), outlier_frac=0.01)
+    x = _special_rows(x)
+    xq, xs = q.quant_act_int8(x.to(DEV))
+    oq, os_ = oracle.quant_act_int8(x)
+    assert np.array_equal(xs.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(xq.cpu().numpy(), oq)
+
+
+def test_quant_act_prefill_size(q):
+    x = synth.activations(8192, 5120, synth.generator(4))
+    xq, xs = q.quant_act_int8(x.to(DEV))
+    oq, os_ = oracle.quant_act_int8(x)
+    assert np.array_equal(xs.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(xq.cpu().numpy(), oq)
+
+
+# ----------------------------------------------------------------- packing --
+
+def np_pack_w4(codes, scales):
+    """The documented W4 layout, written independently in numpy."""
+    c = codes.numpy().astype(np.int64)
+    N, K = c.shape
+    T, G = N // 128, K // 128
+    u = ((c + 8) & 15).astype(np.uint32).reshape(T, 128, G, 4, 4, 8)   # t r g j i e
+    e = np.arange(8)
+    shift = (4 * (4 * (e % 2) + e // 2)).astype(np.uint32)
+    words = (u << shift).sum(axis=-1).astype(np.uint32)               # t r g j i
+    words = words.transpose(0, 2, 3, 1, 4)                            # t g j r i
+    out = np.zeros((T, G, 8448), np.uint8)
+    out[:, :, :8192] = words.reshape(T, G, -1).view(np.uint8).reshape(T, G, 8192)
+    s = scales.numpy().view(np.uint16).reshape(T, 128, G).transpose(0, 2, 1)
+    out[:, :, 8192:] = np.ascontiguousarray(s).view(np.uint8).reshape(T, G, 256)
+    return out.reshape(-1)
+
+
+def np_pack_w8(codes, scales):
+    c = codes.numpy().view(np.uint8) ^ 0x80
+    N, K = c.shape
+    T, G = N // 128, K // 128
+    b = c.reshape(T, 128, G, 8, 16).transpose(0, 2, 3, 1, 4)          # t g j r b
+    out = np.zeros((T, G, 16640), np.uint8)
+    out[:, :, :16384] = b.reshape(T, G, 16384)
+    s = scales.numpy().view(np.uint16).reshape(T, 128, G).transpose(0, 2, 1)
+    out[:, :, 16384:] = np.ascontiguousarray(s).view(np.uint8).reshape(T, G, 256)
+    return out.reshape(-1)
+
+
+def test_pack_w4_layout_bitexact(q):
+    p = synth.make_problem(1, 384, 640, seed=201)
+    pk = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
+    assert pk.numel() == q.qpack_w4_bytes(384, 640)
+    assert np.array_equal(pk.cpu().numpy(), np_pack_w4(p.codes, p.scales))
+    assert q.device_error() == 0
+
+
+def test_pack_w8_layout_bitexact(q):
+    p = synth.make_problem(1, 256, 384, seed=202, bits=8, code_range=(-128, 127))
+    pk = q.qpack_w8(p.codes.to(DEV), p.scales.to(DEV))
+    assert np.array_equal(pk.cpu().numpy(), np_pack_w8(p.codes, p.scales))
+
+
+def test_pack_w4_flags_out_of_range_codes(q):
+    p = synth.make_problem(1, 128, 128, seed=203)
+    bad = p.codes.clone()
+    bad[5, 7] = 9
+    q.qpack_w4(bad.to(DEV), p.scales.to(DEV))
+    assert q.device_error() == q.QW_ERR_BAD_CODES
+    assert q.device_error() == 0
+
+
+# ------------------------------------------------------------------- GEMMs --
+
+def run_modes(q, p, modes=("w4a16", "w4a8"), cols=None, rows=None):
+    """Run the GPU path for each mode and compare with the oracle (optionally on a
+    sample of output columns / token rows).  Returns {mode: normalized error}."""
+    out = {}
+    xd = p.x.to(DEV)
+    cd, sd = p.codes.to(DEV), p.scales.to(DEV)
+    cs = p.codes if cols is None else p.codes[cols]
+    ss = p.scales if cols is None else p.scales[cols]
+    rsel = slice(None) if rows is None else rows.numpy()
+    if p.bits == 4:
+        packed = q.qpack_w4(cd, sd)
+    else:
+        packed = q.qpack_w8(cd, sd)
+    for mode in modes:
+        if mode == "w4a16":
+            y = q.qgemm_w4a16(xd, packed, p.N, p.K)
+            ref = oracle.w4a16(p.x.numpy()[rsel], cs, ss)
+        elif mode == "w8a16":
+            y = q.qgemm_w8a16(xd, packed, p.N, p.K)
+            ref = oracle.w8a16(p.x.numpy()[rsel], cs, ss)
+        else:
+            xq, xs = q.quant_act_int8(xd)
+            oq, os_ = oracle.quant_act_int8(p.x.numpy()[rsel])
+            assert np.array_equal(xq.cpu().numpy()[rsel], oq)
+            y = q.qgemm_w4a8(xq, xs, packed, p.N, p.K)
+            ref = oracle.w4a8(oq, os_, cs, ss)
+        yc = y.cpu().numpy()[rsel]
+        if cols is not None:
+            yc = yc[:, cols.numpy()]
+        out[mode] = nerr(yc, ref)
+    torch.cuda.synchronize()
+    assert q.device_error() == 0
+    return out
+
+
+def test_tiny_config_all_modes(q):
+    p = synth.tiny_w4a16()
+    e = run_modes(q, p, ("w4a16", "w4a8"))
+    p8 = synth.make_problem(4, 512, 256, seed=0, bits=8, scale_lo=0.001, scale_hi=0.01)
+    e.update(run_modes(q, p8, ("w8a16",)))
+    assert max(e.values()) <= TOL, e
+
+
+def test_residue_sweep_all_M(q):
+    """Every M from 1 to 130 (all residues of the 16/32/64/128 token tiles)."""
+    base = synth.make_problem(130, 256, 384, seed=301, outlier_frac=0.02)
+    packed = q.qpack_w4(base.codes.to(DEV), base.scales.to(DEV))
+    ref_all = oracle.w4a16(base.x, base.codes, base.scales)
+    xd = base.x.to(DEV)
+    worst = 0.0
+    for M in range(1, 131):
+        y = q.qgemm_w4a16(xd[:M].contiguous(), packed, 256, 384)
+        worst = max(worst, nerr(y, ref_all[:M]))
+    assert worst <= TOL, worst
+    assert q.device_error() == 0
+
+
+@pytest.mark.parametrize("M", [1, 3, 17, 64, 100, 129, 300])
+def test_w4a8_and_w8a16_ragged(q, M):
+    p = synth.make_problem(M, 384, 512, seed=400 + M, outlier_frac=0.01)
+    e = run_modes(q, p, ("w4a16", "w4a8"))
+    p8 = synth.make_problem(M, 256, 384, seed=500 + M, bits=8, scale_lo=0.001, scale_hi=0.01)
+    e.update(run_modes(q, p8, ("w8a16",)))
+    assert max(e.values()) <= TOL, e
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 64])
+def test_projection_5120(q, M):
+    """Decode/verify projection K=N=5120 with 1% outlier channels, both modes, all outputs."""
+    e = run_modes(q, synth.projection(M))
+    assert max(e.values()) <= TOL, e
+
+
+def test_projection_512_tokens(q):
+    p = synth.projection(512)
+    cols = torch.randperm(5120, generator=synth.generator(9))[:512].sort().values
+    e = run_modes(q, p, cols=cols)
+    assert max(e.values()) <= TOL, e
+
+
+def test_ffn_pair_m64_w4a8(q):
+    cols = torch.randperm(34816, generator=synth.generator(10))[:768].sort().values
+    e_up = run_modes(q, synth.ffn_up(64), ("w4a8", "w4a16"), cols=cols)
+    e_dn = run_modes(q, synth.ffn_down(64), ("w4a8", "w4a16"))
+    assert max(e_up.values()) <= TOL and max(e_dn.values()) <= TOL, (e_up, e_dn)
+
+
+@pytest.mark.slow
+def test_prefill_8192_sampled(q):
+    p = synth.prefill(8192)
+    cols = torch.randperm(34816, generator=synth.generator(11))[:384].sort().values
+    rows = torch.randperm(8192, generator=synth.generator(12))[:192].sort().values
+    e = run_modes(q, p, ("w4a16", "w4a8"), cols=cols, rows=rows)
+    assert max(e.values()) <= TOL, e
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M", [1, 8, 16, 64])
+def test_lm_head_w8a16(q, M):
+    p = _lm_head(M)
+    cols = torch.randperm(248320, generator=synth.generator(13))[:1024].sort().values
+    # include the first and last row tiles
+    cols = torch.cat([torch.arange(0, 64), cols, torch.arange(248320 - 64, 248320)]).unique()
+    e = run_modes(q, p, ("w8a16",), cols=cols)
+    assert e["w8a16"] <= TOL, e
+
+
+_LM = {}
+
+
+def _lm_head(M):
+    if "p" not in _LM:
+        _LM["p"] = synth.lm_head(64)
+    p = _LM["p"]
+    return synth.Problem(M, p.N, p.K, p.codes, p.scales, p.x[:M].contiguous(), 8)
+
+
+# ----------------------------------------------------- determinism, invariants --
+
+def test_repeated_calls_bit_identical(q):
+    p = synth.projection(16)                   # a stream-K shape
+    packed = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
+    xd = p.x.to(DEV)
+    ys = [q.qgemm_w4a16(xd, packed, p.N, p.K).cpu() for _ in range(10)]
+    for y in ys[1:]:
+        assert torch.equal(y.view(torch.int16), ys[0].view(torch.int16))
+
+
+def test_invariant_b_w4a8_matches_w4a16_on_int8_exact_activations(q):
+    gen = synth.generator(601)
+    M, N, K = 24, 1024, 1280
+    x = synth.int8_exact_activations(M, K, gen)
+    codes = synth.codes_int4(N, K, gen)
+    scales = synth.signed_scales(N, K // 128, gen, 0.002, 0.02)
+    packed = q.qpack_w4(codes.to(DEV), scales.to(DEV))
+    xd = x.to(DEV)
+    y16 = q.qgemm_w4a16(xd, packed, N, K)
+    xq, xs = q.quant_act_int8(xd)
+    y8 = q.qgemm_w4a8(xq, xs, packed, N, K)
+    ref = oracle.w4a16(x, codes, scales)
+    assert nerr(y16, ref) <= TOL and nerr(y8, ref) <= TOL
+    # power-of-two token scales commute with every rounding: identical bits
+    assert torch.equal(y16.cpu().view(torch.int16), y8.cpu().view(torch.int16))
+
+
+def test_signed_scales_sign_fold_equivalence(q):
+    """(q, s) and (-q, -s) give bit-identical results (codes in [-7, 7]); all-negative
+    scales match the oracle -- the unsigned-scale failure mode would break both."""
+    p = synth.make_problem(16, 512, 768, seed=701, code_range=(-7, 7))
+    neg = synth.make_problem(16, 512, 768, seed=701, code_range=(-7, 7))
+    neg.scales = -neg.scales.abs()
+    e = run_modes(q, neg, ("w4a16", "w4a8"))
+    assert max(e.values()) <= TOL, e
+    pa = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
+    pb = q.qpack_w4((-p.codes).to(DEV), (-p.scales).to(DEV))
+    xd = p.x.to(DEV)
+    ya = q.qgemm_w4a16(xd, pa, p.N, p.K)
+    yb = q.qgemm_w4a16(xd, pb, p.N, p.K)
+    assert torch.equal(ya.cpu().view(torch.int16), yb.cpu().view(torch.int16))
+
+
+def test_workspace_contract(q):
+    p = synth.projection(4)
+    packed = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
+    need = q.workspace_bytes(q.MODE_W4A16, 4, 5120, 5120)
+    zero = int(q.lib().qgemm_workspace_zero_bytes(q.MODE_W4A16, 4, 5120, 5120))
+    assert need > 0 and 0 < zero <= need
+    ws = q.Workspace(DEV)
+    y = q.qgemm_w4a16(p.x.to(DEV), packed, p.N, p.K, ws=ws)
+    torch.cuda.synchronize()
+    assert int(ws.buf[:zero].count_nonzero()) == 0
+    small = torch.zeros(need // 2 // 256 * 256, dtype=torch.uint8, device=DEV)
+    import ctypes
+    rc = q.lib().qgemm_w4a16(ctypes.c_void_p(p.x.to(DEV).data_ptr()), ctypes.c_void_p(packed.data_ptr()),
+                             4, 5120, 5120, ctypes.c_void_p(y.data_ptr()),
+                             ctypes.c_void_p(small.data_ptr()), small.numel(), None)
+    assert rc == q.QW_ERR_WORKSPACE
+
+
+def test_empty_and_single_tile(q):
+    p = synth.make_problem(1, 128, 128, seed=801)
+    e = run_modes(q, p, ("w4a16", "w4a8"))
+    assert max(e.values()) <= TOL
+    packed = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
+    y = q.qgemm_w4a16(torch.empty((0, 128), dtype=torch.float16, device=DEV), packed, 128, 128)
+    assert y.shape == (0, 128)
+    assert q.device_error() == 0
