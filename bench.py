@@ -172,7 +172,7 @@ def run_reference(args):
     if rank != 0:
         return
     cores = len(os.sched_getaffinity(0))
-    budget = 3.0
+    budget = args.cpu_seconds / 4.0
     times, wbs, desc = [], [], ""
     for i in range(args.warmup + args.steps):
         wb, dt, desc = oracle_sample(budget)

@@ -123,7 +123,12 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
   a.err = d->err;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (mode == QW_MODE_W4A8) {
+  a.act8 = nullptr;
+  if (mode == QW_MODE_W4A8 && qw::act8_in_kernel(mode, P.bn)) {
+    a.act = nullptr;
+    a.act8 = static_cast<const int8_t *>(act);
+    e = qw::launch_gemm_w4a8(a, st);
+  } else if (mode == QW_MODE_W4A8) {
     uint16_t *wide = reinterpret_cast<uint16_t *>(w + P.ws_counters + P.ws_partials);
     e = qw::launch_widen_i8(static_cast<const int8_t *>(act), wide, (size_t)M * K, d->sms, st);
     if (e != cudaSuccess) return fail_cuda(e, "widen kernel launch");

@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const uint16_t
                                                                   int8_t *__restrict__ q,
                                                                   float *__restrict__ s) {
   __shared__ float red[kQuantThreads / 32];
+  griddep_wait();
+  griddep_launch_dependents();
   const size_t row = blockIdx.x;
   const uint4 *xr = reinterpret_cast<const uint4 *>(x + row * (size_t)K);
   const int nv = K / 8;
@@ -92,6 +94,8 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const uint16_t
 // --------------------------------------------------------------------------
 // int8 codes -> fp16 values (exact), for the fp16 tensor-core W4A8 path.
 __global__ void widen_i8_kernel(const int8_t *__restrict__ src, uint16_t *__restrict__ dst, size_t n16) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x) {
     const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -115,6 +119,8 @@ __global__ void widen_i8_kernel(const int8_t *__restrict__ src, uint16_t *__rest
 // Packers.  One thread per 16-byte slice of a chunk; see qgemm.h for the layout.
 __global__ void pack_w4_kernel(const int8_t *__restrict__ codes, const uint16_t *__restrict__ scales,
                                int N, int K, uint8_t *__restrict__ packed, int *err) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int G = K / kGroup;
   const size_t total = (size_t)N * K / 32;   // 16-byte slices
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
@@ -155,6 +161,8 @@ __global__ void pack_w4_kernel(const int8_t *__restrict__ codes, const uint16_t 
 
 __global__ void pack_w8_kernel(const int8_t *__restrict__ codes, const uint16_t *__restrict__ scales,
                                int N, int K, uint8_t *__restrict__ packed) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int G = K / kGroup;
   const size_t total = (size_t)N * K / 16;
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
@@ -182,34 +190,40 @@ static int grid_for(size_t items, int threads, int sms) {
 }
 
 cudaError_t launch_quant_act(const uint16_t *x, int M, int K, int8_t *q, float *s, cudaStream_t st) {
-  quant_act_kernel<<<M, kQuantThreads, 0, st>>>(x, K, q, s);
+  cudaError_t e = launch_pdl(reinterpret_cast<const void *>(quant_act_kernel), dim3(M),
+                             dim3(kQuantThreads), 0, st, x, K, q, s);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_widen_i8(const int8_t *src, uint16_t *dst, size_t n, int sms, cudaStream_t st) {
   const size_t n16 = n / 16;
-  widen_i8_kernel<<<grid_for(n16, 256, sms), 256, 0, st>>>(src, dst, n16);
+  cudaError_t e = launch_pdl(reinterpret_cast<const void *>(widen_i8_kernel),
+                             dim3(grid_for(n16, 256, sms)), dim3(256), 0, st, src, dst, n16);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_pack_w4(const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
                            int *err, int sms, cudaStream_t st) {
   const size_t total = (size_t)N * K / 32;
-  pack_w4_kernel<<<grid_for(total, 256, sms), 256, 0, st>>>(codes, scales, N, K,
-                                                            static_cast<uint8_t *>(packed), err);
+  uint8_t *out = static_cast<uint8_t *>(packed);
+  cudaError_t e = launch_pdl(reinterpret_cast<const void *>(pack_w4_kernel),
+                             dim3(grid_for(total, 256, sms)), dim3(256), 0, st, codes, scales, N, K,
+                             out, err);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_pack_w8(const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
                            int sms, cudaStream_t st) {
   const size_t total = (size_t)N * K / 16;
-  pack_w8_kernel<<<grid_for(total, 256, sms), 256, 0, st>>>(codes, scales, N, K,
-                                                            static_cast<uint8_t *>(packed));
+  uint8_t *out = static_cast<uint8_t *>(packed);
+  cudaError_t e = launch_pdl(reinterpret_cast<const void *>(pack_w8_kernel),
+                             dim3(grid_for(total, 256, sms)), dim3(256), 0, st, codes, scales, N, K,
+                             out);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace qw

@@ -95,12 +95,41 @@ __device__ __forceinline__ void dequant_w8(const uint4 (&v)[4], __half2 s2, uint
   }
 }
 
+// W4A8: widen this thread's int8 pieces of one stage (staging slot right after the
+// bn x 128 fp16 tile) into the swizzled fp16 tile.  Each thread converts exactly
+// the 16-byte pieces it copied itself, so no cross-thread synchronization is needed.
+template <int BN>
+__device__ __forceinline__ void widen_stage(uint8_t *btile, int pt) {
+  const uint8_t *stg = btile + BN * kGroup * 2;
+  const __half2 k1152 = __float2half2_rn(1152.0f);
+#pragma unroll 2
+  for (int pc = pt; pc < BN * 8; pc += kProdWarps * 32) {
+    const int r = pc >> 3, c8 = pc & 7;
+    const uint4 v = *reinterpret_cast<const uint4 *>(stg + pc * 16);
+    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
+                           v.w ^ 0x80808080u};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w[i], 0x64646464u, 0x4140)), k1152));
+      o[2 * i + 1] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w[i], 0x64646464u, 0x4342)), k1152));
+    }
+    // 16 codes = fp16 pieces 2*c8 and 2*c8+1 (8 values each) of row r
+    const int kc = c8 >> 2;
+    const int cc0 = (2 * c8) & 7;
+    uint8_t *row = btile + kc * BN * 128 + r * 128;
+    *reinterpret_cast<uint4 *>(row + ((cc0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(row + (((cc0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 template <int BN, int WBITS, bool TOKSCALE>
 __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_constant__ GemmArgs a) {
   constexpr int kMode = WBITS == 8 ? 2 : (TOKSCALE ? 1 : 0);
   constexpr uint32_t kChunk = WBITS == 8 ? kChunkW8 : kChunkW4;
   constexpr uint32_t kWAligned = (kChunk + 1023) / 1024 * 1024;
-  constexpr uint32_t kStage = kWAligned + BN * kGroup * 2;
+  constexpr bool kAct8 = TOKSCALE && BN <= kAct8InKernelMaxBn;
+  constexpr uint32_t kStage = kWAligned + BN * kGroup * 2 + (kAct8 ? BN * kGroup : 0);
   constexpr int kNAcc = BN <= 128 ? 2 : 1;
   constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
   (void)kMode;
@@ -156,6 +185,20 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbars + kTmemSlot);
 
   Seg sg;
+  // Everything above overlaps the tail of the preceding kernel (programmatic
+  // dependent launch).  Before waiting for it, only warm L2 with this CTA's
+  // first weight chunks: L2 is coherent, so this is safe even if the preceding
+  // kernel wrote the weights.  No global memory is read or written before the wait.
+  if (warp == kWarpTma && lane == 0 && segment(P, cta, 0, sg)) {
+    int u, t;
+    tile_coords(P, sg.tile, u, t);
+    const int n = (sg.g1 - sg.g0) < S ? (sg.g1 - sg.g0) : S;
+    for (int g = sg.g0; g < sg.g0 + n; ++g)
+      prefetch_l2(a.wpack + ((size_t)t * P.G + g) * kChunk, kChunk);
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+
   if (warp == kWarpTma) {
     // ------------------------------------------------ weight bulk copies --
     if (lane == 0) {
@@ -189,31 +232,50 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         const uint32_t ph = (it / (uint32_t)S) & 1u;
         if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
         const uint32_t bs = b_smem(s);
+        if constexpr (kAct8) {
+          // int8 codes: 16 per copy into the staging slot; widened after they land
+          const uint32_t stg = bs + BN * kGroup * 2;
+#pragma unroll 2
+          for (int pc = pt; pc < BN * 8; pc += kProdWarps * 32) {
+            const int r = pc >> 3, c8 = pc & 7;
+            const int tok = u * BN + r;
+            const bool in = tok < P.M;
+            const int8_t *src = in ? a.act8 + (size_t)tok * P.K + (size_t)g * kGroup + c8 * 16 : a.act8;
+            cp_async16(stg + (uint32_t)(pc * 16), src, in ? 16u : 0u);
+          }
+        } else {
 #pragma unroll 4
-        for (int pc = pt; pc < BN * 16; pc += kProdWarps * 32) {
-          const int r = pc >> 4, c = pc & 15;
-          const int kc = c >> 3, cc = c & 7;
-          const int tok = u * BN + r;
-          const bool in = tok < P.M;
-          const uint16_t *src = in ? a.act + (size_t)tok * P.K + (size_t)g * kGroup + c * 8 : a.act;
-          const uint32_t dst = bs + (uint32_t)(kc * BN * 128 + r * 128 + ((cc ^ (r & 7)) << 4));
-          cp_async16(dst, src, in ? 16u : 0u);
+          for (int pc = pt; pc < BN * 16; pc += kProdWarps * 32) {
+            const int r = pc >> 4, c = pc & 15;
+            const int kc = c >> 3, cc = c & 7;
+            const int tok = u * BN + r;
+            const bool in = tok < P.M;
+            const uint16_t *src = in ? a.act + (size_t)tok * P.K + (size_t)g * kGroup + c * 8 : a.act;
+            const uint32_t dst = bs + (uint32_t)(kc * BN * 128 + r * 128 + ((cc ^ (r & 7)) << 4));
+            cp_async16(dst, src, in ? 16u : 0u);
+          }
         }
         cp_async_commit();
         if (it >= (uint32_t)D) {
           if (D == 2) cp_async_wait<2>(); else cp_async_wait<1>();
+          const int sd = (int)((it - D) % (uint32_t)S);
+          if constexpr (kAct8) widen_stage<BN>(gbase + (size_t)sd * kStage + kWAligned, pt);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(full_bar((int)((it - D) % (uint32_t)S)));
+          if (lane == 0) mbar_arrive(full_bar(sd));
         }
       }
     }
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (ok && lane == 0) {
+    if (ok) {
       const uint32_t first = it >= (uint32_t)D ? it - D : 0;
-      for (uint32_t j = first; j < it; ++j) mbar_arrive(full_bar((int)(j % (uint32_t)S)));
+      for (uint32_t j = first; j < it; ++j) {
+        const int sd = (int)(j % (uint32_t)S);
+        if constexpr (kAct8) widen_stage<BN>(gbase + (size_t)sd * kStage + kWAligned, pt);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full_bar(sd));
+      }
     }
   } else if (warp < kDeqWarps) {
     // ------------------------------------------------------- dequantize --
@@ -336,15 +398,28 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         }
         named_bar_sync(1, kEpiWarps * 32);
         if (*bcast) {
-          for (int j = 0; j < BN; ++j) {
-            const int m = m0 + j;
-            if (m >= P.M) break;
-            float acc = 0.0f;
-            for (int p = pf; p <= pl; ++p)
-              acc += __ldcg(a.partials + (size_t)partial_slot(P, p, sg.tile) * (BN * kRows) +
-                            j * kRows + row);
-            const float val = TOKSCALE ? acc * a.xs[m] : acc;
-            a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
+          // sum the partials in CTA (= K) order, 32 tokens at a time so that the
+          // loads of one contributor are independent and in flight together
+          const int mv = P.M - m0 < BN ? P.M - m0 : BN;
+          for (int jc = 0; jc < mv; jc += 32) {
+            float acc[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+            for (int p = pf; p <= pl; ++p) {
+              const float *src = a.partials + (size_t)partial_slot(P, p, sg.tile) * (BN * kRows) +
+                                 (size_t)jc * kRows + row;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (jc + j < mv) acc[j] += __ldcg(src + j * kRows);
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int m = m0 + jc + j;
+              if (jc + j < mv) {
+                const float val = TOKSCALE ? acc[j] * a.xs[m] : acc[j];
+                a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
+              }
+            }
           }
         }
       }

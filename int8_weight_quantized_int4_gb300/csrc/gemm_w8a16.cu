@@ -8,9 +8,10 @@ static cudaError_t run_w8a16(const GemmArgs &a, cudaStream_t st) {
   auto *k = qgemm_tc_kernel<BN, 8, false>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(k), a.P.smem_bytes);
   if (e != cudaSuccess) return e;
-  k<<<a.P.grid, kThreads, a.P.smem_bytes, st>>>(a);
+  e = launch_pdl(reinterpret_cast<const void *>(k), dim3(a.P.grid), dim3(kThreads),
+                 (size_t)a.P.smem_bytes, st, a);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_gemm_w8a16(const GemmArgs &a, cudaStream_t st) {

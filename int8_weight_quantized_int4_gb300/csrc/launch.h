@@ -10,7 +10,8 @@ namespace qw {
 
 struct GemmArgs {
   Plan P;
-  const uint16_t *act;      // fp16 [M,K] activations (W4A8: the widened int8 codes)
+  const uint16_t *act;      // fp16 [M,K] activations (W4A8 with bn > 64: the widened codes)
+  const int8_t *act8;       // W4A8 int8 codes [M,K], widened inside the kernel (bn <= 64)
   const float *xs;          // token scales [M] (W4A8) or nullptr
   const uint8_t *wpack;     // packed weights
   uint16_t *y;              // fp16 [M,N]
@@ -20,6 +21,27 @@ struct GemmArgs {
 };
 
 void count_launch();
+
+// Launch `func` with programmatic stream serialization: it may start while the
+// preceding kernel on the stream finishes; every kernel of this library executes
+// griddepcontrol.wait before its first global-memory access (the GEMM only
+// prefetches weights into L2 before it).
+template <typename... Args>
+cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       const Args &...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void *argv[] = {const_cast<void *>(static_cast<const void *>(&args))...};
+  return cudaLaunchKernelExC(&cfg, func, argv);
+}
 // Raise the dynamic shared-memory limit of `func` on the current device (once).
 cudaError_t ensure_smem_attr(const void *func, int bytes);
 

@@ -88,6 +88,19 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// Warm L2 with `bytes` (multiple of 16) starting at `src`; no shared memory, no completion.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch: wait until the preceding kernel of the stream has
+// completed and its memory is visible (no-op when launched without the attribute),
+// and allow the following kernel to begin its own prologue.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 16-byte asynchronous copy global -> shared; bytes beyond src_bytes are zero-filled.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)

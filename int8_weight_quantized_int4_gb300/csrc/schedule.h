@@ -119,12 +119,20 @@ QW_HD size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 constexpr int kSmemLimit = 232448;        // 227 KB opt-in dynamic shared memory per CTA
 constexpr int kSmemReserve = 2048;        // barriers and bookkeeping
 constexpr int kMaxStages = 12;
+constexpr int kStreamKMaxTilesPerSm = 32;  // stream-K only below this many tiles per SM
 
 QW_HD int chunk_bytes(int mode) { return mode == 2 ? kChunkW8 : kChunkW4; }
 
-// Stage = one weight chunk (aligned to 1024 B) + the bn x 128 fp16 activation tile.
+// W4A8 widens int8 activation codes to fp16 inside the GEMM (through a staging
+// slot) for token tiles up to this size; larger tiles use a separate widening pass.
+constexpr int kAct8InKernelMaxBn = 64;
+QW_HD bool act8_in_kernel(int mode, int bn) { return mode == 1 && bn <= kAct8InKernelMaxBn; }
+
+// Stage = one weight chunk (aligned to 1024 B) + the bn x 128 fp16 activation tile
+// (+ a bn x 128 int8 staging slot when W4A8 widens in the kernel).
 QW_HD int stage_bytes(int mode, int bn) {
-  return (int)align_up((size_t)chunk_bytes(mode), 1024) + bn * kGroup * 2;
+  return (int)align_up((size_t)chunk_bytes(mode), 1024) + bn * kGroup * 2 +
+         (act8_in_kernel(mode, bn) ? bn * kGroup : 0);
 }
 
 // Fill in a plan; returns 0 or -2 (unsupported shape) / -1 (bad argument).
@@ -138,7 +146,7 @@ QW_HD int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   P.G = K / kGroup;
   P.tiles = (long long)P.U * P.T;
   P.chunks = P.tiles * P.G;
-  const bool many = P.tiles >= 32LL * num_sms || (P.tiles % num_sms) == 0;
+  const bool many = P.tiles >= (long long)kStreamKMaxTilesPerSm * num_sms || (P.tiles % num_sms) == 0;
   P.stream_k = (P.chunks > 0 && !many) ? 1 : 0;
   if (P.chunks == 0) P.grid = 0;
   else if (P.stream_k) P.grid = (int)(P.chunks < num_sms ? P.chunks : num_sms);
@@ -148,9 +156,13 @@ QW_HD int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   if (st > kMaxStages) st = kMaxStages;
   P.stages = st;
   P.smem_bytes = st * sb + kSmemReserve;
-  P.ws_counters = P.stream_k ? align_up((size_t)P.tiles * 4, 256) : 0;
+  // Tile counters live in a fixed region at the start of every workspace, sized for
+  // the largest stream-K plan (fewer than kStreamKMaxTilesPerSm tiles per SM), so
+  // that no plan's partials or widened activations ever overlap another plan's
+  // counters: a workspace zeroed once stays valid for calls of any shape.
+  P.ws_counters = align_up((size_t)kStreamKMaxTilesPerSm * num_sms * 4, 256);
   P.ws_partials = P.stream_k ? (size_t)2 * P.grid * P.bn * kRows * 4 : 0;
-  P.ws_act = (mode == 1) ? align_up((size_t)M * K * 2, 256) : 0;   // fp16 copy of int8 codes
+  P.ws_act = (mode == 1 && !act8_in_kernel(mode, P.bn)) ? align_up((size_t)M * K * 2, 256) : 0;
   P.ws_zero = P.ws_counters;
   P.ws_bytes = P.ws_counters + P.ws_partials + P.ws_act;
   return 0;

@@ -137,7 +137,19 @@ def test_schedule_covers_every_chunk_once(mode, M, N, K, sms):
 def test_schedule_whole_tiles_for_prefill():
     p = q.plan(0, 8192, 34816, 5120, 152)
     assert p.stream_k == 0 and p.bn == 256 and p.tiles == 32 * 272
-    assert p.ws_bytes == 0
+    assert p.ws_bytes == p.ws_zero_bytes          # only the counter region
+
+
+def test_counter_region_is_shared_by_every_plan():
+    """Every plan puts its tile counters in the same leading region and nothing else
+    there, so one workspace zeroed once serves calls of any shape."""
+    zs = set()
+    for mode, M, N, K, sms in SHAPES:
+        p = q.plan(mode, M, N, K, sms if sms == 152 else 152)
+        zs.add(p.ws_zero_bytes)
+        if p.stream_k:
+            assert p.tiles * 4 <= p.ws_zero_bytes
+    assert len(zs) == 1
 
 
 def test_w4a8_workspace_holds_widened_codes():

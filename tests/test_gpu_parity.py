@@ -310,6 +310,28 @@ def test_workspace_contract(q):
     assert rc == q.QW_ERR_WORKSPACE
 
 
+def test_one_workspace_across_shapes(q):
+    """A workspace zeroed once serves a sequence of calls of different shapes and modes
+    (partials of one call must never land where another call keeps its counters)."""
+    ws = q.Workspace(DEV)
+    shapes = [(300, 1280, 1152), (64, 8192, 1024), (16, 256, 4096), (300, 1280, 1152), (64, 8192, 1024)]
+    for i, (M, N, K) in enumerate(shapes):
+        p = synth.make_problem(M, N, K, seed=900 + i, outlier_frac=0.01)
+        packed = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
+        xd = p.x.to(DEV)
+        cols = np.arange(0, N, 7)
+        y = q.qgemm_w4a16(xd, packed, N, K, ws=ws)
+        assert nerr(y.cpu().numpy()[:, cols], oracle.w4a16(p.x, p.codes[cols], p.scales[cols])) <= TOL
+        xq, xs = q.quant_act_int8(xd)
+        y8 = q.qgemm_w4a8(xq, xs, packed, N, K, ws=ws)
+        oq, os_ = oracle.quant_act_int8(p.x)
+        assert nerr(y8.cpu().numpy()[:, cols], oracle.w4a8(oq, os_, p.codes[cols], p.scales[cols])) <= TOL
+    zero = int(q.lib().qgemm_workspace_zero_bytes(q.MODE_W4A16, 4, 5120, 5120))
+    torch.cuda.synchronize()
+    assert int(ws.buf[:zero].count_nonzero()) == 0
+    assert q.device_error() == 0
+
+
 def test_empty_and_single_tile(q):
     p = synth.make_problem(1, 128, 128, seed=801)
     e = run_modes(q, p, ("w4a16", "w4a8"))
