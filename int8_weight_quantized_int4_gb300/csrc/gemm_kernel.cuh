@@ -99,11 +99,11 @@ __device__ __forceinline__ void dequant_w8(const uint4 (&v)[4], __half2 s2, uint
 // bn x 128 fp16 tile) into the swizzled fp16 tile.  Each thread converts exactly
 // the 16-byte pieces it copied itself, so no cross-thread synchronization is needed.
 template <int BN>
-__device__ __forceinline__ void widen_stage(uint8_t *btile, int pt) {
+__device__ __forceinline__ void widen_stage(uint8_t *btile, int pt, int rows_valid) {
   const uint8_t *stg = btile + BN * kGroup * 2;
   const __half2 k1152 = __float2half2_rn(1152.0f);
 #pragma unroll 2
-  for (int pc = pt; pc < BN * 8; pc += kProdWarps * 32) {
+  for (int pc = pt; pc < rows_valid * 8; pc += kProdWarps * 32) {
     const int r = pc >> 3, c8 = pc & 7;
     const uint4 v = *reinterpret_cast<const uint4 *>(stg + pc * 16);
     const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
@@ -222,6 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     // ------------------------------------------- activation tile producer --
     const int pt = threadIdx.x - kWarpProd0 * 32;   // 0..127
     const int D = S >= 3 ? 2 : 1;                   // chunks of copies kept in flight
+    // in-kernel widening is only used when M <= BN (a single token tile)
+    const int rows_act8 = P.M < BN ? P.M : BN;
     uint32_t it = 0;
     bool ok = true;
     for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
@@ -232,34 +234,34 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         const uint32_t ph = (it / (uint32_t)S) & 1u;
         if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
         const uint32_t bs = b_smem(s);
+        // Token rows past M are neither copied nor cleared: row j of the tile only
+        // feeds accumulator column j, and columns of tokens >= M are never stored.
+        const int rows_valid = P.M - u * BN < BN ? P.M - u * BN : BN;
         if constexpr (kAct8) {
           // int8 codes: 16 per copy into the staging slot; widened after they land
           const uint32_t stg = bs + BN * kGroup * 2;
 #pragma unroll 2
-          for (int pc = pt; pc < BN * 8; pc += kProdWarps * 32) {
+          for (int pc = pt; pc < rows_valid * 8; pc += kProdWarps * 32) {
             const int r = pc >> 3, c8 = pc & 7;
             const int tok = u * BN + r;
-            const bool in = tok < P.M;
-            const int8_t *src = in ? a.act8 + (size_t)tok * P.K + (size_t)g * kGroup + c8 * 16 : a.act8;
-            cp_async16(stg + (uint32_t)(pc * 16), src, in ? 16u : 0u);
+            cp_async16(stg + (uint32_t)(pc * 16), a.act8 + (size_t)tok * P.K + (size_t)g * kGroup + c8 * 16, 16u);
           }
         } else {
 #pragma unroll 4
-          for (int pc = pt; pc < BN * 16; pc += kProdWarps * 32) {
+          for (int pc = pt; pc < rows_valid * 16; pc += kProdWarps * 32) {
             const int r = pc >> 4, c = pc & 15;
             const int kc = c >> 3, cc = c & 7;
             const int tok = u * BN + r;
-            const bool in = tok < P.M;
-            const uint16_t *src = in ? a.act + (size_t)tok * P.K + (size_t)g * kGroup + c * 8 : a.act;
+            const uint16_t *src = a.act + (size_t)tok * P.K + (size_t)g * kGroup + c * 8;
             const uint32_t dst = bs + (uint32_t)(kc * BN * 128 + r * 128 + ((cc ^ (r & 7)) << 4));
-            cp_async16(dst, src, in ? 16u : 0u);
+            cp_async16(dst, src, 16u);
           }
         }
         cp_async_commit();
         if (it >= (uint32_t)D) {
           if (D == 2) cp_async_wait<2>(); else cp_async_wait<1>();
           const int sd = (int)((it - D) % (uint32_t)S);
-          if constexpr (kAct8) widen_stage<BN>(gbase + (size_t)sd * kStage + kWAligned, pt);
+          if constexpr (kAct8) widen_stage<BN>(gbase + (size_t)sd * kStage + kWAligned, pt, rows_act8);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(full_bar(sd));
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       const uint32_t first = it >= (uint32_t)D ? it - D : 0;
       for (uint32_t j = first; j < it; ++j) {
         const int sd = (int)(j % (uint32_t)S);
-        if constexpr (kAct8) widen_stage<BN>(gbase + (size_t)sd * kStage + kWAligned, pt);
+        if constexpr (kAct8) widen_stage<BN>(gbase + (size_t)sd * kStage + kWAligned, pt, rows_act8);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(full_bar(sd));
@@ -371,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
           const float acc = __uint_as_float(v[j]);
           const int m = m0 + cc + j;
           if (part) {
-            part[(cc + j) * kRows + row] = acc;
+            if (m < P.M) part[(cc + j) * kRows + row] = acc;
           } else if (m < P.M) {
             const float val = TOKSCALE ? acc * a.xs[m] : acc;
             a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
