@@ -215,7 +215,9 @@ def capture(fn, stream):
 
 
 def parity_err(y, ref):
-    y = y.float().cpu().numpy().astype(np.float64)
+    if isinstance(y, torch.Tensor):
+        y = y.float().cpu().numpy()
+    y = np.asarray(y).astype(np.float64)
     ref = np.asarray(ref).astype(np.float64)
     if not np.isfinite(y).all():
         return float("inf")
@@ -396,8 +398,15 @@ def run_ours(args):
             "gpu_launches": int(launches_per_step * args.steps), "clocks": clk, "e2e": e2e,
             "device_error": derr}
 
+    print(json.dumps({k: line[k] for k in ("value", "ms_per_step", "roofline", "per_M", "parity")}),
+          file=sys.stderr, flush=True)
     if ws_n == 1 and not args.no_extras:
-        line["configs"] = extras(q, dev, stream, pk, pk_src)
+        try:
+            line["configs"] = extras(q, dev, stream, pk, pk_src)
+        except Exception as ex:          # report, keep the headline line
+            import traceback
+            traceback.print_exc()
+            line["configs"] = {"error": repr(ex)}
     if rank == 0 and ws_n == 1:
         cores = len(os.sched_getaffinity(0))
         wb, dt, desc = oracle_sample(args.cpu_seconds)
@@ -447,6 +456,7 @@ def extras(q, dev, stream, pk, pk_src):
         cols = np.arange(0, prob.N, max(1, prob.N // 512))
         oq, os_ = oracle.quant_act_int8(prob.x)
         ref = oracle.w4a8(oq, os_, prob.codes[cols], prob.scales[cols])
+        print(name, round(ms * 1e3, 2), "us", file=sys.stderr, flush=True)
         out[name] = {"us": round(ms * 1e3, 2), "weight_GBps": round(wb / ms / 1e6, 1),
                      "TOPS": round(2 * 64 * prob.N * prob.K / ms / 1e9, 2),
                      "frac_hbm": round((wb + 64 * prob.K + 256 + 128 * prob.N) / ms / 1e6 / hbm, 4),

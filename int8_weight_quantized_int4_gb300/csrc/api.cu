@@ -6,6 +6,8 @@
 #include <string.h>
 #include <atomic>
 #include <mutex>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include "qgemm.h"
 #include "launch.h"
@@ -77,6 +79,34 @@ int current_device(DevInfo *&out) {
   return QW_OK;
 }
 
+// cuTensorMapEncodeTiled, fetched once through the runtime's driver entry point
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int encode_act_map(CUtensorMap *map, const void *ptr, int M, int K, int bn, bool int8) {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    cudaGetLastError();
+  });
+  if (!g_encode) return fail(QW_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t gstride[1] = {(cuuint64_t)K * (int8 ? 1 : 2)};
+  const cuuint32_t box[2] = {int8 ? 128u : 64u, (cuuint32_t)bn};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r = g_encode(map, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                              2, const_cast<void *>(ptr), gdim, gstride, box, estride,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(QW_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return QW_OK;
+}
+
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 constexpr int kMaxN = 1 << 26;
@@ -123,19 +153,17 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
   a.err = d->err;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  a.act8 = nullptr;
   if (mode == QW_MODE_W4A8 && qw::act8_in_kernel(mode, P.bn)) {
-    a.act = nullptr;
-    a.act8 = static_cast<const int8_t *>(act);
+    if ((rc = encode_act_map(&a.tmap, act, M, K, P.bn, true))) return rc;
     e = qw::launch_gemm_w4a8(a, st);
   } else if (mode == QW_MODE_W4A8) {
     uint16_t *wide = reinterpret_cast<uint16_t *>(w + P.ws_counters + P.ws_partials);
+    if ((rc = encode_act_map(&a.tmap, wide, M, K, P.bn, false))) return rc;
     e = qw::launch_widen_i8(static_cast<const int8_t *>(act), wide, (size_t)M * K, d->sms, st);
     if (e != cudaSuccess) return fail_cuda(e, "widen kernel launch");
-    a.act = wide;
     e = qw::launch_gemm_w4a8(a, st);
   } else {
-    a.act = static_cast<const uint16_t *>(act);
+    if ((rc = encode_act_map(&a.tmap, act, M, K, P.bn, false))) return rc;
     e = mode == QW_MODE_W8A16 ? qw::launch_gemm_w8a16(a, st) : qw::launch_gemm_w4a16(a, st);
   }
   if (e != cudaSuccess) return fail_cuda(e, "GEMM kernel launch");

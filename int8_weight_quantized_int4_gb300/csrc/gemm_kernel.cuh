@@ -7,18 +7,19 @@
 // Orientation: the weights are the MMA's A operand (M = 128 weight rows, one per
 // TMEM lane) and the tokens are its N (16..256), so a decode batch of 1..64
 // tokens still fills the 128-row MMA.  Per 128 x 128 weight chunk:
-//   bulk-copy warp   : one 1-D bulk copy of the packed chunk (codes + signed
-//                      scales) HBM -> shared memory
-//   producer warps   : cp.async of the bn x 128 fp16 activation tile into the
-//                      128-byte-swizzled K-major layout (zero-fill past M)
-//   dequant warps    : int4/int8 codes -> fp16 (q * s) in registers, with the
-//                      scale's sign, stored into TMEM as the A operand
-//   MMA warp         : 8 x tcgen05.mma kind::f16 (K = 16 each), fp32 accumulator
-//                      in TMEM; tcgen05.commit frees the stage
-//   epilogue warps   : tcgen05.ld the accumulator, scale by the token scale (W4A8),
-//                      write fp16 y, or a binary32 partial for a tile cut by the
-//                      stream-K split; the last CTA of a cut tile sums its
-//                      partials in CTA order (deterministic, no waiting).
+//   copy warp      : one 1-D bulk copy of the packed chunk (codes + signed scales)
+//                    and TMA tensor copies of the activation tile (128-byte
+//                    swizzle, zero fill past M), all completing on one mbarrier
+//   widen warps    : W4A8 at decode sizes only -- int8 codes -> fp16 (exact) into
+//                    the swizzled tile
+//   dequant warps  : int4/int8 codes -> fp16 (q * s) in registers, with the
+//                    scale's sign, stored into TMEM as the A operand
+//   MMA warp       : 8 x tcgen05.mma kind::f16 (K = 16 each), fp32 accumulator in
+//                    TMEM; tcgen05.commit frees the stage
+//   epilogue warps : tcgen05.ld the accumulator, scale by the token scale (W4A8),
+//                    write fp16 y, or a binary32 partial for a tile cut by the
+//                    stream-K split; the last CTA of a cut tile sums the partials
+//                    in CTA order (deterministic, no waiting).
 #pragma once
 #include <stdint.h>
 #include <cuda_fp16.h>
@@ -28,13 +29,12 @@
 
 namespace qw {
 
-
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
-constexpr int kProdWarps = 4;
+constexpr int kWidenWarps = 4;
 constexpr int kWarpEpi0 = kDeqWarps;                 // 8
-constexpr int kWarpProd0 = kWarpEpi0 + kEpiWarps;    // 12
-constexpr int kWarpTma = kWarpProd0 + kProdWarps;    // 16
+constexpr int kWarpWiden0 = kWarpEpi0 + kEpiWarps;   // 12
+constexpr int kWarpTma = kWarpWiden0 + kWidenWarps;  // 16
 constexpr int kWarpMma = kWarpTma + 1;               // 17
 constexpr int kThreads = (kWarpMma + 1) * 32;        // 576
 constexpr int kAStages = 4;                          // TMEM A-operand ring (64 columns each)
@@ -44,13 +44,15 @@ constexpr int kAccCol0 = kAStages * 64;              // 256
 // offsets inside the barrier block that follows the stages
 constexpr int kBarFull = 0;
 constexpr int kBarEmpty = kBarFull + 8 * kMaxStages;
-constexpr int kBarAFull = kBarEmpty + 8 * kMaxStages;
+constexpr int kBarBFull = kBarEmpty + 8 * kMaxStages;
+constexpr int kBarAFull = kBarBFull + 8 * kMaxStages;
 constexpr int kBarAEmpty = kBarAFull + 8 * kAStages;
 constexpr int kBarAccFull = kBarAEmpty + 8 * kAStages;
 constexpr int kBarAccEmpty = kBarAccFull + 8 * 2;
 constexpr int kTmemSlot = kBarAccEmpty + 8 * 2;
 constexpr int kAbortSlot = kTmemSlot + 4;
 constexpr int kBcastSlot = kAbortSlot + 4;
+static_assert(kBcastSlot + 4 <= kSmemReserve - 1024, "barrier block too large");
 
 // ---- dequantization: packed codes -> 32 half2 (64 fp16 values q*s) per thread ----
 
@@ -95,15 +97,15 @@ __device__ __forceinline__ void dequant_w8(const uint4 (&v)[4], __half2 s2, uint
   }
 }
 
-// W4A8: widen this thread's int8 pieces of one stage (staging slot right after the
-// bn x 128 fp16 tile) into the swizzled fp16 tile.  Each thread converts exactly
-// the 16-byte pieces it copied itself, so no cross-thread synchronization is needed.
+// W4A8 at decode sizes: widen the int8 staging tile (rows of 128 codes, unswizzled,
+// right after the bn x 128 fp16 tile) into the 128-byte-swizzled fp16 tile.
+// (1024 + (q XOR 0x80)) - 1152 = q, exact in fp16.
 template <int BN>
-__device__ __forceinline__ void widen_stage(uint8_t *btile, int pt, int rows_valid) {
+__device__ __forceinline__ void widen_stage(uint8_t *btile, int t, int rows) {
   const uint8_t *stg = btile + BN * kGroup * 2;
   const __half2 k1152 = __float2half2_rn(1152.0f);
 #pragma unroll 2
-  for (int pc = pt; pc < rows_valid * 8; pc += kProdWarps * 32) {
+  for (int pc = t; pc < rows * 8; pc += kWidenWarps * 32) {
     const int r = pc >> 3, c8 = pc & 7;
     const uint4 v = *reinterpret_cast<const uint4 *>(stg + pc * 16);
     const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
@@ -125,14 +127,13 @@ __device__ __forceinline__ void widen_stage(uint8_t *btile, int pt, int rows_val
 
 template <int BN, int WBITS, bool TOKSCALE>
 __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_constant__ GemmArgs a) {
-  constexpr int kMode = WBITS == 8 ? 2 : (TOKSCALE ? 1 : 0);
   constexpr uint32_t kChunk = WBITS == 8 ? kChunkW8 : kChunkW4;
   constexpr uint32_t kWAligned = (kChunk + 1023) / 1024 * 1024;
   constexpr bool kAct8 = TOKSCALE && BN <= kAct8InKernelMaxBn;
   constexpr uint32_t kStage = kWAligned + BN * kGroup * 2 + (kAct8 ? BN * kGroup : 0);
+  constexpr uint32_t kActBytes = kAct8 ? BN * kGroup : BN * kGroup * 2;
   constexpr int kNAcc = BN <= 128 ? 2 : 1;
   constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
-  (void)kMode;
 
   extern __shared__ uint8_t smem_raw[];
   const Plan &P = a.P;
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 
   auto full_bar = [&](int s) { return bars + kBarFull + 8 * s; };
   auto empty_bar = [&](int s) { return bars + kBarEmpty + 8 * s; };
+  auto bfull_bar = [&](int s) { return bars + kBarBFull + 8 * s; };
   auto afull_bar = [&](int i) { return bars + kBarAFull + 8 * i; };
   auto aempty_bar = [&](int i) { return bars + kBarAEmpty + 8 * i; };
   auto accfull_bar = [&](int i) { return bars + kBarAccFull + 8 * i; };
@@ -160,8 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1 + kProdWarps);
+      mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(bfull_bar(s), kWidenWarps);
     }
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(afull_bar(i), kDeqWarps);
@@ -175,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     *bcast = 0;
     fence_mbar_init();
   }
+  if (warp == kWarpTma && lane == 0) prefetch_tensormap(&a.tmap);
   if (warp == 0) {
     tmem_alloc(bars + kTmemSlot, kTmemCols);
     tmem_relinquish();
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   griddep_launch_dependents();
 
   if (warp == kWarpTma) {
-    // ------------------------------------------------ weight bulk copies --
+    // ------------------------------------------- weight + activation copies --
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       uint32_t it = 0;
@@ -212,71 +216,35 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
           const int s = (int)(it % (uint32_t)S);
           const uint32_t ph = (it / (uint32_t)S) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(full_bar(s), kChunk);
-          const uint8_t *src = a.wpack + ((size_t)t * P.G + g) * kChunk;
-          bulk_g2s(w_smem(s), src, kChunk, full_bar(s), pol);
+          mbar_arrive_expect_tx(full_bar(s), kChunk + kActBytes);
+          bulk_g2s(w_smem(s), a.wpack + ((size_t)t * P.G + g) * kChunk, kChunk, full_bar(s), pol);
+          if constexpr (kAct8) {
+            // int8 codes: one 128 x BN box into the staging slot (unswizzled)
+            tma_load_2d(b_smem(s) + BN * kGroup * 2, &a.tmap, g * kGroup, u * BN, full_bar(s));
+          } else {
+            // fp16: two 64 x BN boxes, 128-byte swizzle, one per 64-wide half of the group
+            tma_load_2d(b_smem(s), &a.tmap, g * kGroup, u * BN, full_bar(s));
+            tma_load_2d(b_smem(s) + BN * 128, &a.tmap, g * kGroup + 64, u * BN, full_bar(s));
+          }
         }
       }
     }
-  } else if (warp >= kWarpProd0 && warp < kWarpProd0 + kProdWarps) {
-    // ------------------------------------------- activation tile producer --
-    const int pt = threadIdx.x - kWarpProd0 * 32;   // 0..127
-    const int D = S >= 3 ? 2 : 1;                   // chunks of copies kept in flight
-    // in-kernel widening is only used when M <= BN (a single token tile)
-    const int rows_act8 = P.M < BN ? P.M : BN;
-    uint32_t it = 0;
-    bool ok = true;
-    for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
-      int u, t;
-      tile_coords(P, sg.tile, u, t);
-      for (int g = sg.g0; g < sg.g1; ++g, ++it) {
-        const int s = (int)(it % (uint32_t)S);
-        const uint32_t ph = (it / (uint32_t)S) & 1u;
-        if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-        const uint32_t bs = b_smem(s);
-        // Token rows past M are neither copied nor cleared: row j of the tile only
-        // feeds accumulator column j, and columns of tokens >= M are never stored.
-        const int rows_valid = P.M - u * BN < BN ? P.M - u * BN : BN;
-        if constexpr (kAct8) {
-          // int8 codes: 16 per copy into the staging slot; widened after they land
-          const uint32_t stg = bs + BN * kGroup * 2;
-#pragma unroll 2
-          for (int pc = pt; pc < rows_valid * 8; pc += kProdWarps * 32) {
-            const int r = pc >> 3, c8 = pc & 7;
-            const int tok = u * BN + r;
-            cp_async16(stg + (uint32_t)(pc * 16), a.act8 + (size_t)tok * P.K + (size_t)g * kGroup + c8 * 16, 16u);
-          }
-        } else {
-#pragma unroll 4
-          for (int pc = pt; pc < rows_valid * 16; pc += kProdWarps * 32) {
-            const int r = pc >> 4, c = pc & 15;
-            const int kc = c >> 3, cc = c & 7;
-            const int tok = u * BN + r;
-            const uint16_t *src = a.act + (size_t)tok * P.K + (size_t)g * kGroup + c * 8;
-            const uint32_t dst = bs + (uint32_t)(kc * BN * 128 + r * 128 + ((cc ^ (r & 7)) << 4));
-            cp_async16(dst, src, 16u);
-          }
-        }
-        cp_async_commit();
-        if (it >= (uint32_t)D) {
-          if (D == 2) cp_async_wait<2>(); else cp_async_wait<1>();
-          const int sd = (int)((it - D) % (uint32_t)S);
-          if constexpr (kAct8) widen_stage<BN>(gbase + (size_t)sd * kStage + kWAligned, pt, rows_act8);
+  } else if (warp >= kWarpWiden0 && warp < kWarpWiden0 + kWidenWarps) {
+    // ------------------------------------------ W4A8 int8 -> fp16 widening --
+    if constexpr (kAct8) {
+      const int wt = threadIdx.x - kWarpWiden0 * 32;   // 0..127
+      const int rows = P.M < BN ? P.M : BN;            // a single token tile when widening here
+      uint32_t it = 0;
+      bool ok = true;
+      for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
+        for (int g = sg.g0; g < sg.g1; ++g, ++it) {
+          const int s = (int)(it % (uint32_t)S);
+          if (!mbar_wait(full_bar(s), (it / (uint32_t)S) & 1u, abort_flag, a.err)) { ok = false; break; }
+          widen_stage<BN>(gbase + (size_t)s * kStage + kWAligned, wt, rows);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(full_bar(sd));
+          if (lane == 0) mbar_arrive(bfull_bar(s));
         }
-      }
-    }
-    cp_async_wait<0>();
-    if (ok) {
-      const uint32_t first = it >= (uint32_t)D ? it - D : 0;
-      for (uint32_t j = first; j < it; ++j) {
-        const int sd = (int)(j % (uint32_t)S);
-        if constexpr (kAct8) widen_stage<BN>(gbase + (size_t)sd * kStage + kWAligned, pt, rows_act8);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full_bar(sd));
       }
     }
   } else if (warp < kDeqWarps) {
@@ -328,8 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         for (int g = sg.g0; g < sg.g1; ++g, ++it) {
           const int s = (int)(it % (uint32_t)S);
           const int ai = (int)(it % kAStages);
+          const uint32_t ph = (it / (uint32_t)S) & 1u;
           if (!mbar_wait(afull_bar(ai), (it / kAStages) & 1u, abort_flag, a.err)) { ok = false; break; }
-          if (!mbar_wait(full_bar(s), (it / (uint32_t)S) & 1u, abort_flag, a.err)) { ok = false; break; }
+          if (!mbar_wait(kAct8 ? bfull_bar(s) : full_bar(s), ph, abort_flag, a.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t bs = b_smem(s);
 #pragma unroll
@@ -360,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       tile_coords(P, sg.tile, u, t);
       const int n = t * kRows + row;
       const int m0 = u * BN;
+      const int mv = P.M - m0 < BN ? P.M - m0 : BN;   // valid tokens of this tile
       const uint32_t tacc = tmem + lane_base + (uint32_t)(kAccCol0 + b * BN);
       float *part = sg.slot >= 0 ? a.partials + (size_t)sg.slot * (BN * kRows) : nullptr;
 #pragma unroll 1
@@ -371,12 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 #pragma unroll
         for (int j = 0; j < W; ++j) {
           const float acc = __uint_as_float(v[j]);
-          const int m = m0 + cc + j;
-          if (part) {
-            if (m < P.M) part[(cc + j) * kRows + row] = acc;
-          } else if (m < P.M) {
-            const float val = TOKSCALE ? acc * a.xs[m] : acc;
-            a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
+          if (cc + j < mv) {
+            if (part) {
+              part[(cc + j) * kRows + row] = acc;
+            } else {
+              const int m = m0 + cc + j;
+              const float val = TOKSCALE ? acc * a.xs[m] : acc;
+              a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
+            }
           }
         }
       }
@@ -400,24 +372,33 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         }
         named_bar_sync(1, kEpiWarps * 32);
         if (*bcast) {
-          // sum the partials in CTA (= K) order, 32 tokens at a time so that the
-          // loads of one contributor are independent and in flight together
-          const int mv = P.M - m0 < BN ? P.M - m0 : BN;
-          for (int jc = 0; jc < mv; jc += 32) {
-            float acc[32];
+          // sum the partials in CTA (= K) order; 8 tokens x up to 4 contributors
+          // of independent loads in flight at a time
+          for (int jc = 0; jc < mv; jc += 8) {
+            float acc[8];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
-            for (int p = pf; p <= pl; ++p) {
-              const float *src = a.partials + (size_t)partial_slot(P, p, sg.tile) * (BN * kRows) +
-                                 (size_t)jc * kRows + row;
+            for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+            for (int p = pf; p <= pl; p += 4) {
+              float vv[4][8];
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (jc + j < mv) acc[j] += __ldcg(src + j * kRows);
+              for (int q = 0; q < 4; ++q) {
+                const float *src = a.partials +
+                                   (size_t)partial_slot(P, p + q <= pl ? p + q : pl, sg.tile) * (BN * kRows) +
+                                   (size_t)jc * kRows + row;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  vv[q][j] = (p + q <= pl && jc + j < mv) ? __ldcg(src + j * kRows) : 0.0f;
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  if (p + q <= pl) acc[j] += vv[q][j];
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int m = m0 + jc + j;
+            for (int j = 0; j < 8; ++j) {
               if (jc + j < mv) {
+                const int m = m0 + jc + j;
                 const float val = TOKSCALE ? acc[j] * a.xs[m] : acc[j];
                 a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
               }

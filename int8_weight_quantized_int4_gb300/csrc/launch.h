@@ -3,15 +3,16 @@
 #pragma once
 #include <stdint.h>
 #include <stddef.h>
+#include <cuda.h>            // CUtensorMap (type only; the driver is reached through the runtime)
 #include <cuda_runtime.h>
 #include "schedule.h"
 
 namespace qw {
 
 struct GemmArgs {
+  CUtensorMap tmap;         // activations: fp16 [M,K] (64 x bn boxes, 128-byte swizzle) or
+                            // int8 [M,K] (128 x bn boxes) for W4A8 at decode sizes
   Plan P;
-  const uint16_t *act;      // fp16 [M,K] activations (W4A8 with bn > 64: the widened codes)
-  const int8_t *act8;       // W4A8 int8 codes [M,K], widened inside the kernel (bn <= 64)
   const float *xs;          // token scales [M] (W4A8) or nullptr
   const uint8_t *wpack;     // packed weights
   uint16_t *y;              // fp16 [M,N]
