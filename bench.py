@@ -518,8 +518,50 @@ def extras(q, dev, stream, pk, pk_src):
     return out
 
 
+NCU_CASES = {
+    # name: (mode, M, N, K, bits)
+    "proj_w4a16_m1": ("w4a16", 1, 5120, 5120, 4),
+    "proj_w4a16_m16": ("w4a16", 16, 5120, 5120, 4),
+    "proj_w4a16_m64": ("w4a16", 64, 5120, 5120, 4),
+    "proj_w4a8_m16": ("w4a8", 16, 5120, 5120, 4),
+    "ffn_up_w4a8_m64": ("w4a8", 64, 34816, 5120, 4),
+    "lm_head_w8a16_m16": ("w8a16", 16, 248320, 5120, 8),
+    "prefill_w4a16_m2048": ("w4a16", 2048, 34816, 5120, 4),
+}
+
+
+def run_ncu_case(name):
+    """A small case for profiler captures: 3 eager warm-up launches of one GEMM,
+    then the launch to capture (the 4th GEMM launch of the process)."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import int8_weight_quantized_int4_gb300 as q
+    mode, M, N, K, bits = NCU_CASES[name]
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    p = synth.make_problem(M, N, K, seed=1, bits=bits, outlier_frac=0.01)
+    packed = (q.qpack_w4 if bits == 4 else q.qpack_w8)(p.codes.to(dev), p.scales.to(dev))
+    x = p.x.to(dev)
+    ws = q.Workspace(dev)
+    if mode == "w4a8":
+        xq, xs = q.quant_act_int8(x)
+        fn = lambda: q.qgemm_w4a8(xq, xs, packed, N, K, ws=ws)  # noqa: E731
+    elif mode == "w8a16":
+        fn = lambda: q.qgemm_w8a16(x, packed, N, K, ws=ws)  # noqa: E731
+    else:
+        fn = lambda: q.qgemm_w4a16(x, packed, N, K, ws=ws)  # noqa: E731
+    for _ in range(4):
+        y = fn()
+    torch.cuda.synchronize()
+    assert q.device_error() == 0
+    print(json.dumps({"ncu_case": name, "M": M, "N": N, "K": K, "mode": mode,
+                      "y_absmax": float(y.float().abs().max())}))
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--ncu-case", choices=sorted(NCU_CASES), default=None,
+                    help="run one small GEMM case for a profiler capture and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
@@ -529,7 +571,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
