@@ -94,15 +94,26 @@ int encode_act_map(CUtensorMap *map, const void *ptr, int M, int K, int bn, bool
     cudaGetLastError();
   });
   if (!g_encode) return fail(QW_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
-  const cuuint64_t gstride[1] = {(cuuint64_t)K * (int8 ? 1 : 2)};
-  const cuuint32_t box[2] = {int8 ? 128u : 64u, (cuuint32_t)bn};
-  const cuuint32_t estride[2] = {1, 1};
-  const CUresult r = g_encode(map, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                              2, const_cast<void *>(ptr), gdim, gstride, box, estride,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r;
+  if (int8) {
+    // int8 codes [M,K]: 128 x bn boxes, unswizzled (widened in the kernel)
+    const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t gstride[1] = {(cuuint64_t)K};
+    const cuuint32_t box[2] = {128u, (cuuint32_t)bn};
+    r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), gdim, gstride, box,
+                 estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    // fp16 [M,K] seen as [K/64][M][64]: one 64 x bn x 2 box per 128-wide group lands as
+    // two K-major 64-column halves with the 128-byte swizzle the MMA descriptor expects
+    const cuuint64_t gdim[3] = {64, (cuuint64_t)M, (cuuint64_t)K / 64};
+    const cuuint64_t gstride[2] = {(cuuint64_t)K * 2, 128};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)bn, 2u};
+    r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), gdim, gstride, box,
+                 estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) return fail(QW_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return QW_OK;
 }
@@ -328,10 +339,11 @@ int qw_plan_segments(const qw_plan_t *plan, int cta, int cap, long long *tile, i
   P.U = plan->token_tiles;
   P.T = plan->row_tiles;
   P.G = plan->groups;
-  P.tiles = plan->tiles;
-  P.chunks = plan->chunks;
+  P.tiles = (int)plan->tiles;
+  P.chunks = (int)plan->chunks;
   P.grid = plan->grid;
   P.stream_k = plan->stream_k;
+  qw::fill_begin(P);
   int n = 0;
   qw::Seg s;
   for (int i = 0; qw::segment(P, cta, i, s); ++i, ++n) {

@@ -7,9 +7,10 @@
 // Orientation: the weights are the MMA's A operand (M = 128 weight rows, one per
 // TMEM lane) and the tokens are its N (16..256), so a decode batch of 1..64
 // tokens still fills the 128-row MMA.  Per 128 x 128 weight chunk:
-//   copy warp      : one 1-D bulk copy of the packed chunk (codes + signed scales)
-//                    and TMA tensor copies of the activation tile (128-byte
-//                    swizzle, zero fill past M), all completing on one mbarrier
+//   copy warps     : one issues the 1-D bulk copy of each packed chunk (codes +
+//                    signed scales), another the TMA tensor copy of the matching
+//                    activation tile (128-byte swizzle, zero fill past M); both
+//                    complete on the stage's mbarrier
 //   widen warps    : W4A8 at decode sizes only -- int8 codes -> fp16 (exact) into
 //                    the swizzled tile
 //   dequant warps  : int4/int8 codes -> fp16 (q * s) in registers, with the
@@ -36,7 +37,8 @@ constexpr int kWarpEpi0 = kDeqWarps;                 // 8
 constexpr int kWarpWiden0 = kWarpEpi0 + kEpiWarps;   // 12
 constexpr int kWarpTma = kWarpWiden0 + kWidenWarps;  // 16
 constexpr int kWarpMma = kWarpTma + 1;               // 17
-constexpr int kThreads = (kWarpMma + 1) * 32;        // 576
+constexpr int kWarpAct = kWarpMma + 1;               // 18: activation tile copies
+constexpr int kThreads = (kWarpAct + 1) * 32;        // 608
 constexpr int kAStages = 4;                          // TMEM A-operand ring (64 columns each)
 constexpr int kTmemCols = 512;
 constexpr int kAccCol0 = kAStages * 64;              // 256
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 2);
       mbar_init(empty_bar(s), 1);
       mbar_init(bfull_bar(s), kWidenWarps);
     }
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     *bcast = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpTma && lane == 0) prefetch_tensormap(&a.tmap);
+  if (warp == kWarpAct && lane == 0) prefetch_tensormap(&a.tmap);
   if (warp == 0) {
     tmem_alloc(bars + kTmemSlot, kTmemCols);
     tmem_relinquish();
@@ -190,42 +192,49 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 
   Seg sg;
   // Everything above overlaps the tail of the preceding kernel (programmatic
-  // dependent launch).  Before waiting for it, only warm L2 with this CTA's
-  // first weight chunks: L2 is coherent, so this is safe even if the preceding
-  // kernel wrote the weights.  No global memory is read or written before the wait.
-  if (warp == kWarpTma && lane == 0 && segment(P, cta, 0, sg)) {
-    int u, t;
-    tile_coords(P, sg.tile, u, t);
-    const int n = (sg.g1 - sg.g0) < S ? (sg.g1 - sg.g0) : S;
-    for (int g = sg.g0; g < sg.g0 + n; ++g)
-      prefetch_l2(a.wpack + ((size_t)t * P.G + g) * kChunk, kChunk);
-  }
+  // dependent launch); no global memory is touched before this wait.
   griddep_wait();
   griddep_launch_dependents();
 
   if (warp == kWarpTma) {
-    // ------------------------------------------- weight + activation copies --
+    // ------------------------------------------------------ weight copies --
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      uint32_t it = 0;
+      int s = 0;
+      uint32_t ph = 0;
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         int u, t;
         tile_coords(P, sg.tile, u, t);
-        for (int g = sg.g0; g < sg.g1; ++g, ++it) {
-          const int s = (int)(it % (uint32_t)S);
-          const uint32_t ph = (it / (uint32_t)S) & 1u;
+        const uint8_t *src = a.wpack + ((size_t)t * P.G + sg.g0) * kChunk;
+        for (int g = sg.g0; g < sg.g1; ++g, src += kChunk) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(full_bar(s), kChunk + kActBytes);
-          bulk_g2s(w_smem(s), a.wpack + ((size_t)t * P.G + g) * kChunk, kChunk, full_bar(s), pol);
+          mbar_arrive_expect_tx(full_bar(s), kChunk);
+          bulk_g2s(w_smem(s), src, kChunk, full_bar(s), pol);
+          if (++s == S) { s = 0; ph ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == kWarpAct) {
+    // -------------------------------------------------- activation copies --
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
+        int u, t;
+        tile_coords(P, sg.tile, u, t);
+        for (int g = sg.g0; g < sg.g1; ++g) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(full_bar(s), kActBytes);
           if constexpr (kAct8) {
             // int8 codes: one 128 x BN box into the staging slot (unswizzled)
             tma_load_2d(b_smem(s) + BN * kGroup * 2, &a.tmap, g * kGroup, u * BN, full_bar(s));
           } else {
-            // fp16: two 64 x BN boxes, 128-byte swizzle, one per 64-wide half of the group
-            tma_load_2d(b_smem(s), &a.tmap, g * kGroup, u * BN, full_bar(s));
-            tma_load_2d(b_smem(s) + BN * 128, &a.tmap, g * kGroup + 64, u * BN, full_bar(s));
+            // fp16: one 64 x BN x 2 box (both 64-wide halves of the group), 128-byte swizzle
+            tma_load_3d(b_smem(s), &a.tmap, 0, u * BN, 2 * g, full_bar(s));
           }
+          if (++s == S) { s = 0; ph ^= 1u; }
         }
       }
     }
@@ -234,16 +243,17 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     if constexpr (kAct8) {
       const int wt = threadIdx.x - kWarpWiden0 * 32;   // 0..127
       const int rows = P.M < BN ? P.M : BN;            // a single token tile when widening here
-      uint32_t it = 0;
+      int s = 0;
+      uint32_t ph = 0;
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
-        for (int g = sg.g0; g < sg.g1; ++g, ++it) {
-          const int s = (int)(it % (uint32_t)S);
-          if (!mbar_wait(full_bar(s), (it / (uint32_t)S) & 1u, abort_flag, a.err)) { ok = false; break; }
+        for (int g = sg.g0; g < sg.g1; ++g) {
+          if (!mbar_wait(full_bar(s), ph, abort_flag, a.err)) { ok = false; break; }
           widen_stage<BN>(gbase + (size_t)s * kStage + kWAligned, wt, rows);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(bfull_bar(s));
+          if (++s == S) { s = 0; ph ^= 1u; }
         }
       }
     }
@@ -252,14 +262,13 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     const int quad = warp & 3, half_k = warp >> 2;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    uint32_t it = 0;
+    int s = 0, ai = 0;
+    uint32_t ph = 0, aph = 0;
     bool ok = true;
     for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
-      for (int g = sg.g0; g < sg.g1; ++g, ++it) {
-        const int s = (int)(it % (uint32_t)S);
-        const int ai = (int)(it % kAStages);
-        if (!mbar_wait(full_bar(s), (it / (uint32_t)S) & 1u, abort_flag, a.err)) { ok = false; break; }
-        if (!mbar_wait(aempty_bar(ai), ((it / kAStages) & 1u) ^ 1u, abort_flag, a.err)) { ok = false; break; }
+      for (int g = sg.g0; g < sg.g1; ++g) {
+        if (!mbar_wait(full_bar(s), ph, abort_flag, a.err)) { ok = false; break; }
+        if (!mbar_wait(aempty_bar(ai), aph ^ 1u, abort_flag, a.err)) { ok = false; break; }
         const uint8_t *wc = gbase + (size_t)s * kStage;
         uint32_t o[32];
         if constexpr (WBITS == 4) {
@@ -281,34 +290,38 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(afull_bar(ai));
+        if (++s == S) { s = 0; ph ^= 1u; }
+        if (++ai == kAStages) { ai = 0; aph ^= 1u; }
       }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------- MMA --
     if (lane == 0) {
-      uint32_t it = 0;
+      int s = 0, ai = 0;
+      uint32_t ph = 0, aph = 0;
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         const int b = i % kNAcc;
         if (!mbar_wait(accempty_bar(b), ((i / kNAcc) & 1) ^ 1, abort_flag, a.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(kAccCol0 + b * BN);
-        for (int g = sg.g0; g < sg.g1; ++g, ++it) {
-          const int s = (int)(it % (uint32_t)S);
-          const int ai = (int)(it % kAStages);
-          const uint32_t ph = (it / (uint32_t)S) & 1u;
-          if (!mbar_wait(afull_bar(ai), (it / kAStages) & 1u, abort_flag, a.err)) { ok = false; break; }
+        for (int g = sg.g0; g < sg.g1; ++g) {
+          if (!mbar_wait(afull_bar(ai), aph, abort_flag, a.err)) { ok = false; break; }
           if (!mbar_wait(kAct8 ? bfull_bar(s) : full_bar(s), ph, abort_flag, a.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t bs = b_smem(s);
+          // descriptor start addresses advance by (offset >> 4); no carry out of the
+          // 14-bit field since shared-memory addresses stay below 256 KB
+          const uint64_t bdesc0 = smem_desc_sw128(b_smem(s));
+          const uint32_t a0 = tmem + (uint32_t)(ai * 64);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t bdesc = smem_desc_sw128(bs + (uint32_t)((k >> 2) * BN * 128 + (k & 3) * 32));
-            mma_f16_ts(d, tmem + (uint32_t)(ai * 64 + k * 8), bdesc, kIdesc,
+          for (int k = 0; k < 8; ++k)
+            mma_f16_ts(d, a0 + (uint32_t)(k * 8),
+                       bdesc0 + (uint64_t)(((k >> 2) * BN * 128 + (k & 3) * 32) >> 4), kIdesc,
                        (g > sg.g0 || k > 0) ? 1u : 0u);
-          }
           mma_commit(empty_bar(s));
           mma_commit(aempty_bar(ai));
+          if (++s == S) { s = 0; ph ^= 1u; }
+          if (++ai == kAStages) { ai = 0; aph ^= 1u; }
         }
         if (ok) mma_commit(accfull_bar(b));
       }

@@ -46,22 +46,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Time limit of every pipeline wait.  A wait that exceeds it raises the CTA's
 // abort flag and records QW_ERR_TIMEOUT (-7) in the device error word; every
-// other wait of the CTA then gives up within a few polls, so a broken pipeline
-// ends the kernel instead of hanging the GPU.
+// other wait of the CTA then gives up at its next wake-up (within the suspend
+// hint below), so a broken pipeline ends the kernel instead of hanging the GPU.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
+// try_wait with a suspend-time hint: a waiting thread is parked by the hardware
+// until the phase completes (or the hint expires) instead of spinning, so waiting
+// warps do not take issue slots from the warps doing the work.
+constexpr uint32_t kSuspendHintNs = 1000000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                            int *err) {
+                                                   int *err) {
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        atomicCAS(err, 0, -7);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicCAS(err, 0, -7);
+      return false;
     }
   }
 }
@@ -95,6 +108,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// 3-D tiled TMA load of the box at (x, y, z).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {

@@ -1,6 +1,8 @@
 // schedule.h -- work decomposition of the quantized GEMM over persistent CTAs.
 // Host and device share this code, so the host-side tests check exactly what
-// the kernels execute.
+// the kernels execute.  All device-side arithmetic is 32-bit, and the per-CTA
+// chunk ranges are a table computed once on the host (no integer division by
+// runtime values inside the pipeline loops).
 //
 // Work unit ("chunk"): 128 weight rows x one 128-wide K group of one token tile.
 // A tile is (token tile u, row tile t); tile index tau orders tiles so that CTAs
@@ -9,10 +11,10 @@
 // Two assignments:
 //  * whole tiles, round-robin (tile p, p+grid, ...): used when there are many
 //    more tiles than CTAs; no partial sums, no workspace traffic.
-//  * stream-K: CTA p takes the contiguous chunk range
-//    [floor(p*C/grid), floor((p+1)*C/grid)); a tile cut between CTAs is summed
-//    from binary32 partials by the last CTA to finish it, in CTA order, so the
-//    result does not depend on which CTA finishes last (deterministic).
+//  * stream-K: CTA p takes the contiguous chunk range [begin[p], begin[p+1]) with
+//    begin[p] = floor(p*C/grid); a tile cut between CTAs is summed from binary32
+//    partials by the last CTA to finish it, in CTA order, so the result does not
+//    depend on which CTA finishes last (deterministic).
 #pragma once
 #include <stdint.h>
 #include <stddef.h>
@@ -30,17 +32,20 @@ constexpr int kGroup = 128;        // K per group / per chunk
 constexpr int kChunkW4 = 8192 + 256;
 constexpr int kChunkW8 = 16384 + 256;
 constexpr int kTokenSuperTiles = 16;   // token tiles kept hot in L2 together
+constexpr int kMaxGrid = 256;          // persistent CTAs at most (one per SM)
 
 struct Plan {
   int mode, M, N, K;
   int bn, U, T, G;
-  long long tiles, chunks;
+  int tiles, chunks;
   int grid, stream_k, stages, smem_bytes;
+  float grid_per_chunk;          // grid / chunks, to estimate a chunk's owner
   size_t ws_counters, ws_partials, ws_act, ws_bytes, ws_zero;
+  int begin[kMaxGrid + 1];       // stream-K: first chunk of each CTA (begin[grid] = chunks)
 };
 
 struct Seg {
-  long long tile;
+  int tile;
   int g0, g1;       // groups [g0, g1) of the tile
   int slot;         // partial-sum slot, or -1 when the segment covers the whole tile
 };
@@ -51,67 +56,66 @@ QW_HD int pick_bn(int M) {
 
 // tile index -> (token tile u, row tile t).  Token tiles are taken in supergroups
 // of kTokenSuperTiles; inside one, the token tile varies fastest.
-QW_HD void tile_coords(const Plan &P, long long tau, int &u, int &t) {
-  const long long Z = P.U < kTokenSuperTiles ? P.U : kTokenSuperTiles;
-  const long long full = P.U / Z;                  // full supergroups
-  const long long per = (long long)P.T * Z;
-  const long long zg = tau / per;
+QW_HD void tile_coords(const Plan &P, int tau, int &u, int &t) {
+  if (P.U == 1) { u = 0; t = tau; return; }
+  const int Z = P.U < kTokenSuperTiles ? P.U : kTokenSuperTiles;
+  const int full = P.U / Z;                  // full supergroups
+  const int per = P.T * Z;
+  const int zg = tau / per;
   if (zg < full) {
-    const long long r = tau - zg * per;
-    t = (int)(r / Z);
-    u = (int)(zg * Z + r % Z);
+    const int r = tau - zg * per;
+    t = r / Z;
+    u = zg * Z + r % Z;
   } else {
-    const long long Zl = P.U - full * Z;           // last, partial supergroup
-    const long long r = tau - full * per;
-    t = (int)(r / Zl);
-    u = (int)(full * Z + r % Zl);
+    const int Zl = P.U - full * Z;           // last, partial supergroup
+    const int r = tau - full * per;
+    t = r / Zl;
+    u = full * Z + r % Zl;
   }
 }
 
-// first chunk of CTA p (stream-K)
-QW_HD long long sk_begin(const Plan &P, int p) {
-  return (long long)p * P.chunks / P.grid;
-}
-
-// CTA owning chunk c (stream-K): the largest p with sk_begin(p) <= c
-QW_HD int sk_owner(const Plan &P, long long c) {
-  return (int)(((c + 1) * (long long)P.grid - 1) / P.chunks);
+// CTA owning chunk c (stream-K): the largest p with begin[p] <= c.
+QW_HD int sk_owner(const Plan &P, int c) {
+  int p = (int)((float)c * P.grid_per_chunk);
+  if (p > P.grid - 1) p = P.grid - 1;
+  if (p < 0) p = 0;
+  while (p + 1 < P.grid && P.begin[p + 1] <= c) ++p;
+  while (p > 0 && P.begin[p] > c) --p;
+  return p;
 }
 
 // i-th segment of CTA p; false when there is none.
 QW_HD bool segment(const Plan &P, int p, int i, Seg &s) {
   if (!P.stream_k) {
-    const long long tau = (long long)p + (long long)i * P.grid;
+    const int tau = p + i * P.grid;
     if (tau >= P.tiles) return false;
     s.tile = tau; s.g0 = 0; s.g1 = P.G; s.slot = -1;
     return true;
   }
-  const long long c0 = sk_begin(P, p), c1 = sk_begin(P, p + 1);
-  // walk segment boundaries: segment 0 starts at c0, later ones at tile starts
-  long long c = c0;
-  if (i > 0) {
-    const long long first_tile = c0 / P.G;
-    c = (first_tile + i) * (long long)P.G;
-  }
+  const int c0 = P.begin[p], c1 = P.begin[p + 1];
+  // segment 0 starts at c0, later ones at tile starts
+  const int first_tile = c0 / P.G;
+  const int c = i == 0 ? c0 : (first_tile + i) * P.G;
   if (c >= c1) return false;
-  s.tile = c / P.G;
-  s.g0 = (int)(c - s.tile * P.G);
-  const long long end = (s.tile + 1) * (long long)P.G < c1 ? (s.tile + 1) * (long long)P.G : c1;
-  s.g1 = (int)(end - s.tile * P.G);
+  s.tile = first_tile + i;
+  s.g0 = c - s.tile * P.G;
+  const int tile_end = (s.tile + 1) * P.G;
+  s.g1 = (tile_end < c1 ? tile_end : c1) - s.tile * P.G;
   const bool whole = (s.g0 == 0 && s.g1 == P.G);
   s.slot = whole ? -1 : (i == 0 ? 2 * p : 2 * p + 1);
   return true;
 }
 
 // For a tile cut between CTAs: the CTAs that hold its partials, in K order.
-QW_HD void tile_contributors(const Plan &P, long long tile, int &p_first, int &p_last) {
+QW_HD void tile_contributors(const Plan &P, int tile, int &p_first, int &p_last) {
   p_first = sk_owner(P, tile * P.G);
   p_last = sk_owner(P, tile * P.G + P.G - 1);
 }
 
-// Slot in which CTA p stored its partial of `tile`.
-QW_HD int partial_slot(const Plan &P, int p, long long tile) {
-  return (sk_begin(P, p) / P.G == tile) ? 2 * p : 2 * p + 1;
+// Slot in which CTA p stored its partial of `tile` (its first or its last segment).
+QW_HD int partial_slot(const Plan &P, int p, int tile) {
+  const int b = P.begin[p];
+  return (b >= tile * P.G && b < (tile + 1) * P.G) ? 2 * p : 2 * p + 1;
 }
 
 QW_HD size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -135,22 +139,34 @@ QW_HD int stage_bytes(int mode, int bn) {
          (act8_in_kernel(mode, bn) ? bn * kGroup : 0);
 }
 
-// Fill in a plan; returns 0 or -2 (unsupported shape) / -1 (bad argument).
-QW_HD int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
+// Fill the stream-K chunk table from grid and chunks (host).
+inline void fill_begin(Plan &P) {
+  for (int p = 0; p <= kMaxGrid; ++p)
+    P.begin[p] = (P.grid && p <= P.grid) ? (int)((long long)p * P.chunks / P.grid) : P.chunks;
+  P.grid_per_chunk = P.chunks ? (float)P.grid / (float)P.chunks : 0.0f;
+}
+
+// Fill in a plan (host); returns 0, -2 (unsupported shape) or -1 (bad argument).
+inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   if (mode < 0 || mode > 2 || M < 0 || N < 0 || K < 0 || num_sms < 1) return -1;
   if (N % kRows || K % kGroup) return -2;
+  if (num_sms > kMaxGrid) num_sms = kMaxGrid;
   P.mode = mode; P.M = M; P.N = N; P.K = K;
   P.bn = pick_bn(M);
   P.U = (M + P.bn - 1) / P.bn;
   P.T = N / kRows;
   P.G = K / kGroup;
-  P.tiles = (long long)P.U * P.T;
-  P.chunks = P.tiles * P.G;
-  const bool many = P.tiles >= (long long)kStreamKMaxTilesPerSm * num_sms || (P.tiles % num_sms) == 0;
+  const long long tiles = (long long)P.U * P.T;
+  const long long chunks = tiles * P.G;
+  if (chunks >= (1LL << 30)) return -2;      // 32-bit chunk indices with headroom
+  P.tiles = (int)tiles;
+  P.chunks = (int)chunks;
+  const bool many = P.tiles >= kStreamKMaxTilesPerSm * num_sms || (P.tiles % num_sms) == 0;
   P.stream_k = (P.chunks > 0 && !many) ? 1 : 0;
   if (P.chunks == 0) P.grid = 0;
-  else if (P.stream_k) P.grid = (int)(P.chunks < num_sms ? P.chunks : num_sms);
-  else P.grid = (int)(P.tiles < num_sms ? P.tiles : num_sms);
+  else if (P.stream_k) P.grid = P.chunks < num_sms ? P.chunks : num_sms;
+  else P.grid = P.tiles < num_sms ? P.tiles : num_sms;
+  fill_begin(P);
   const int sb = stage_bytes(mode, P.bn);
   int st = (kSmemLimit - kSmemReserve) / sb;
   if (st > kMaxStages) st = kMaxStages;
