@@ -147,6 +147,28 @@ int qgemm_w8a16(const uint16_t *x, const void *packed_w8, int M, int N, int K, u
                 void *ws, size_t ws_bytes, qw_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * qgemm_w4a16_noalloc -- qgemm_w4a16 for callers that cannot allocate device
+ * memory (for instance a plugin inside a host runtime that owns every device
+ * allocation and gives its kernels only input and output buffers, or a decode
+ * loop in which a cudaMalloc, which may synchronize the device, is not
+ * allowed).  The source pages have no counterpart to this entry point.
+ *
+ * Same arguments and result as qgemm_w4a16 minus the workspace: the scratch
+ * memory is a fixed 4 MiB array inside the library on every GPU that loads it
+ * (held until the process exits).  That covers M <= 16 at any N and K, and
+ * shapes with at least 32 x (number of SMs) output tiles; a shape that needs
+ * more returns QW_ERR_WORKSPACE with the sizes in qw_last_error_string().
+ * The call allocates nothing.  Its first call on a device sets up that device's
+ * scratch (looks up its address and clears it, synchronously), so make that
+ * first call outside any stream capture.  Every call on a device shares the
+ * same scratch: calls that may overlap on the GPU race and must be serialized
+ * by the caller.  After QW_ERR_TIMEOUT the scratch may hold stale counters and
+ * the process should stop using this entry point.
+ * ------------------------------------------------------------------------ */
+int qgemm_w4a16_noalloc(const uint16_t *x, const void *packed_w4, int M, int N, int K, uint16_t *y,
+                        qw_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics.
  *   qw_last_error_string  text of the last host-side error of the calling
  *                         thread ("" if none).  Never NULL.

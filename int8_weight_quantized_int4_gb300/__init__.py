@@ -52,6 +52,7 @@ SIGNATURES = {
     "qgemm_w4a16": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "qgemm_w4a8": (_i, [_p, _p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "qgemm_w8a16": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
+    "qgemm_w4a16_noalloc": (_i, [_p, _p, _i, _i, _i, _p, _p]),
     "qw_last_error_string": (ctypes.c_char_p, []),
     "qw_device_error": (_i, []),
     "qw_num_kernel_launches": (_ll, []),
@@ -238,6 +239,19 @@ def qgemm_w8a16(x, packed, N: int, K: int, y=None, ws: Workspace | None = None):
     with torch.cuda.device(x.device):
         _check(lib().qgemm_w8a16(_ptr(x), _ptr(packed), M, N, K, _ptr(y), _ptr(wbuf), wbytes,
                                  _stream(x)))
+    return y
+
+
+def qgemm_w4a16_noalloc(x, packed, N: int, K: int, y=None):
+    """qgemm_w4a16 with the library's built-in scratch instead of a workspace (for
+    callers that cannot allocate device memory; see include/qgemm.h)."""
+    _need(x, torch.float16, "x", 2)
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("x.shape[1] != K")
+    y = _out(y, M, N, x.device)
+    with torch.cuda.device(x.device):
+        _check(lib().qgemm_w4a16_noalloc(_ptr(x), _ptr(packed), M, N, K, _ptr(y), _stream(x)))
     return y
 
 

@@ -209,6 +209,8 @@ namespace qw {
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+int set_last_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
 cudaError_t ensure_smem_attr(const void *func, int bytes) {
   struct Entry { const void *f; int dev; int bytes; };
   static Entry done[256];

@@ -22,6 +22,8 @@ struct GemmArgs {
 };
 
 void count_launch();
+// Record a host-side error for qw_last_error_string(); returns `code`.
+int set_last_error(int code, const char *msg);
 
 // Launch `func` with programmatic stream serialization: it may start while the
 // preceding kernel on the stream finishes; every kernel of this library executes
