@@ -15,8 +15,12 @@
 //                    the swizzled tile
 //   dequant warps  : int4/int8 codes -> fp16 (q * s) in registers, with the
 //                    scale's sign, stored into TMEM as the A operand
-//   MMA warp       : 8 x tcgen05.mma kind::f16 (K = 16 each), fp32 accumulator in
-//                    TMEM; tcgen05.commit frees the stage
+//   MMA warps      : 8 x tcgen05.mma kind::f16 (K = 16 each) per chunk, fp32
+//                    accumulator in TMEM; tcgen05.commit frees the stage.  For
+//                    token tiles of up to 64 two warps issue alternate chunks into
+//                    two accumulators (an MMA with N <= 64 costs about as much issue
+//                    time as a full one, so one issuing thread cannot keep up with
+//                    HBM); the epilogue adds the two in a fixed order
 //   epilogue warps : tcgen05.ld the accumulator, scale by the token scale (W4A8),
 //                    write fp16 y, or a binary32 partial for a tile cut by the
 //                    stream-K split; the last CTA of a cut tile sums the partials
@@ -38,7 +42,8 @@ constexpr int kWarpWiden0 = kWarpEpi0 + kEpiWarps;   // 12
 constexpr int kWarpTma = kWarpWiden0 + kWidenWarps;  // 16
 constexpr int kWarpMma = kWarpTma + 1;               // 17
 constexpr int kWarpAct = kWarpMma + 1;               // 18: activation tile copies
-constexpr int kThreads = (kWarpAct + 1) * 32;        // 608
+constexpr int kWarpMma2 = kWarpAct + 1;              // 19: second MMA issuer (token tiles <= 64)
+constexpr int kThreads = (kWarpMma2 + 1) * 32;       // 640
 constexpr int kAStages = 4;                          // TMEM A-operand ring (64 columns each)
 constexpr int kTmemCols = 512;
 constexpr int kAccCol0 = kAStages * 64;              // 256
@@ -135,6 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   constexpr uint32_t kStage = kWAligned + BN * kGroup * 2 + (kAct8 ? BN * kGroup : 0);
   constexpr uint32_t kActBytes = kAct8 ? BN * kGroup : BN * kGroup * 2;
   constexpr int kNAcc = BN <= 128 ? 2 : 1;
+  constexpr bool kDual = BN <= 64;                     // two MMA issuers, two accumulators
+  constexpr int kIssuers = kDual ? 2 : 1;
   constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -173,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       mbar_init(aempty_bar(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(accfull_bar(i), 1);
+      mbar_init(accfull_bar(i), kIssuers);
       mbar_init(accempty_bar(i), kEpiWarps);
     }
     *abort_flag = 0;
@@ -294,18 +301,25 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         if (++ai == kAStages) { ai = 0; aph ^= 1u; }
       }
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp == kWarpMma || (kDual && warp == kWarpMma2)) {
     // ------------------------------------------------------------- MMA --
     if (lane == 0) {
-      int s = 0, ai = 0;
+      const int q = warp == kWarpMma ? 0 : 1;          // issuer: chunks of CTA-wide parity q
+      int s = 0, ai = 0, cidx = 0;
       uint32_t ph = 0, aph = 0;
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         const int b = i % kNAcc;
         if (!mbar_wait(accempty_bar(b), ((i / kNAcc) & 1) ^ 1, abort_flag, a.err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(kAccCol0 + b * BN);
-        for (int g = sg.g0; g < sg.g1; ++g) {
+        const uint32_t d = tmem + (uint32_t)(kAccCol0 + (kDual ? 2 * b + q : b) * BN);
+        bool first = true;
+        for (int g = sg.g0; g < sg.g1; ++g, ++cidx) {
+          if (kDual && (cidx & 1) != q) {
+            if (++s == S) { s = 0; ph ^= 1u; }
+            if (++ai == kAStages) { ai = 0; aph ^= 1u; }
+            continue;
+          }
           if (!mbar_wait(afull_bar(ai), aph, abort_flag, a.err)) { ok = false; break; }
           if (!mbar_wait(kAct8 ? bfull_bar(s) : full_bar(s), ph, abort_flag, a.err)) { ok = false; break; }
           tc_fence_after();
@@ -317,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
           for (int k = 0; k < 8; ++k)
             mma_f16_ts(d, a0 + (uint32_t)(k * 8),
                        bdesc0 + (uint64_t)(((k >> 2) * BN * 128 + (k & 3) * 32) >> 4), kIdesc,
-                       (g > sg.g0 || k > 0) ? 1u : 0u);
+                       (!first || k > 0) ? 1u : 0u);
+          first = false;
           mma_commit(empty_bar(s));
           mma_commit(aempty_bar(ai));
           if (++s == S) { s = 0; ph ^= 1u; }
@@ -332,8 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     const int row = quad * 32 + lane;
     const int ept = threadIdx.x - kWarpEpi0 * 32;   // 0..127
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    int cidx = 0;                                   // CTA-wide index of the segment's first chunk
     for (int i = 0; segment(P, cta, i, sg); ++i) {
       const int b = i % kNAcc;
+      const int nch = sg.g1 - sg.g0;
+      // with two issuers, accumulator q holds the segment's chunks of parity q (if any)
+      const bool valid0 = !kDual || nch >= 2 || (cidx & 1) == 0;
+      const bool valid1 = kDual && (nch >= 2 || (cidx & 1) == 1);
+      cidx += nch;
       mbar_wait(accfull_bar(b), (i / kNAcc) & 1, abort_flag, a.err);
       named_bar_sync(1, kEpiWarps * 32);           // all four warps decide together
       if (*abort_flag) break;
@@ -343,17 +364,23 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       const int n = t * kRows + row;
       const int m0 = u * BN;
       const int mv = P.M - m0 < BN ? P.M - m0 : BN;   // valid tokens of this tile
-      const uint32_t tacc = tmem + lane_base + (uint32_t)(kAccCol0 + b * BN);
+      const uint32_t tacc = tmem + lane_base + (uint32_t)(kAccCol0 + (kDual ? 2 * b : b) * BN);
       float *part = sg.slot >= 0 ? a.partials + (size_t)sg.slot * (BN * kRows) : nullptr;
+      constexpr int W = kDual ? 16 : 32;              // columns per TMEM load
 #pragma unroll 1
-      for (int cc = 0; cc < BN; cc += 32) {
-        uint32_t v[32];
-        if constexpr (BN == 16) tmem_ld16(tacc, v); else tmem_ld32(tacc + (uint32_t)cc, v);
+      for (int cc = 0; cc < BN; cc += W) {
+        uint32_t v[32], v1[32];
+        if constexpr (kDual) {
+          tmem_ld16(tacc + (uint32_t)cc, v);
+          tmem_ld16(tacc + (uint32_t)(BN + cc), v1);
+        } else {
+          tmem_ld32(tacc + (uint32_t)cc, v);
+        }
         tmem_wait_ld();
-        constexpr int W = BN < 32 ? BN : 32;
 #pragma unroll
         for (int j = 0; j < W; ++j) {
-          const float acc = __uint_as_float(v[j]);
+          float acc = valid0 ? __uint_as_float(v[j]) : 0.0f;
+          if (kDual && valid1) acc += __uint_as_float(v1[j]);
           if (cc + j < mv) {
             if (part) {
               part[(cc + j) * kRows + row] = acc;
@@ -369,18 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       __syncwarp();
       if (lane == 0) mbar_arrive(accempty_bar(b));
       if (part) {
-        // publish this partial; the last contributor of the tile reduces it
-        __threadfence();
+        // publish this partial: the barrier orders every thread's partial stores
+        // before one thread's device-scope acquire-release add, which also makes the
+        // other contributors' partials visible to the last one, who reduces the tile
         named_bar_sync(1, kEpiWarps * 32);
         int pf, pl;
         tile_contributors(P, sg.tile, pf, pl);
         if (ept == 0) {
-          const int old = atomicAdd(a.counters + sg.tile, 1);
+          const int old = atom_add_acq_rel_gpu(a.counters + sg.tile, 1);
           const int last = (old == pl - pf) ? 1 : 0;
-          if (last) {
-            a.counters[sg.tile] = 0;    // leave the workspace zeroed for the next call
-            __threadfence();
-          }
+          if (last) a.counters[sg.tile] = 0;    // leave the workspace zeroed for the next call
           *bcast = last;
         }
         named_bar_sync(1, kEpiWarps * 32);
