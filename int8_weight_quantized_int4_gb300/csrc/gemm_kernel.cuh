@@ -44,17 +44,18 @@ constexpr int kWarpMma = kWarpTma + 1;               // 17
 constexpr int kWarpAct = kWarpMma + 1;               // 18: activation tile copies
 constexpr int kWarpMma2 = kWarpAct + 1;              // 19: second MMA issuer (token tiles <= 64)
 constexpr int kThreads = (kWarpMma2 + 1) * 32;       // 640
-constexpr int kAStages = 4;                          // TMEM A-operand ring (64 columns each)
+constexpr int kMaxAStages = 8;                       // TMEM A-operand ring (64 columns per stage)
+constexpr int kDeqGroups = 2;                        // dequant warp groups, alternate chunks
+constexpr int kDeqGroupWarps = kDeqWarps / kDeqGroups;
 constexpr int kTmemCols = 512;
-constexpr int kAccCol0 = kAStages * 64;              // 256
 
 // offsets inside the barrier block that follows the stages
 constexpr int kBarFull = 0;
 constexpr int kBarEmpty = kBarFull + 8 * kMaxStages;
 constexpr int kBarBFull = kBarEmpty + 8 * kMaxStages;
 constexpr int kBarAFull = kBarBFull + 8 * kMaxStages;
-constexpr int kBarAEmpty = kBarAFull + 8 * kAStages;
-constexpr int kBarAccFull = kBarAEmpty + 8 * kAStages;
+constexpr int kBarAEmpty = kBarAFull + 8 * kMaxAStages;
+constexpr int kBarAccFull = kBarAEmpty + 8 * kMaxAStages;
 constexpr int kBarAccEmpty = kBarAccFull + 8 * 2;
 constexpr int kTmemSlot = kBarAccEmpty + 8 * 2;
 constexpr int kAbortSlot = kTmemSlot + 4;
@@ -142,6 +143,12 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   constexpr int kNAcc = BN <= 128 ? 2 : 1;
   constexpr bool kDual = BN <= 64;                     // two MMA issuers, two accumulators
   constexpr int kIssuers = kDual ? 2 : 1;
+  // A-operand ring depth: whatever TMEM the accumulators leave free (6 stages for
+  // token tiles up to 32, 4 otherwise); accumulators start after the ring
+  constexpr int kAStages = BN <= 32 ? 6 : 4;
+  constexpr int kAccCol0 = kAStages * 64;
+  static_assert(kAccCol0 + (kDual ? 4 : kNAcc) * BN <= kTmemCols, "TMEM budget");
+  static_assert(kAStages <= kMaxAStages, "A ring");
   constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -176,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       mbar_init(bfull_bar(s), kWidenWarps);
     }
     for (int i = 0; i < kAStages; ++i) {
-      mbar_init(afull_bar(i), kDeqWarps);
+      mbar_init(afull_bar(i), kDeqGroupWarps);
       mbar_init(aempty_bar(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -266,37 +273,46 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     }
   } else if (warp < kDeqWarps) {
     // ------------------------------------------------------- dequantize --
-    const int quad = warp & 3, half_k = warp >> 2;
+    // Two groups of four warps take alternate chunks (CTA-wide chunk parity), so
+    // two chunks are being dequantized at once; within a group each warp covers 32
+    // rows (its TMEM lane quarter) over the whole 128-wide group, in two halves.
+    const int quad = warp & 3, grp = warp / kDeqGroupWarps;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    int s = 0, ai = 0;
+    int s = 0, ai = 0, cidx = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
     for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
-      for (int g = sg.g0; g < sg.g1; ++g) {
-        if (!mbar_wait(full_bar(s), ph, abort_flag, a.err)) { ok = false; break; }
-        if (!mbar_wait(aempty_bar(ai), aph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-        const uint8_t *wc = gbase + (size_t)s * kStage;
-        uint32_t o[32];
-        if constexpr (WBITS == 4) {
-          uint4 v[2];
-          v[0] = *reinterpret_cast<const uint4 *>(wc + (2 * half_k) * 2048 + row * 16);
-          v[1] = *reinterpret_cast<const uint4 *>(wc + (2 * half_k + 1) * 2048 + row * 16);
-          const __half sc = *reinterpret_cast<const __half *>(wc + 8192 + row * 2);
-          dequant_w4(v, __half2half2(sc), o);
-        } else {
-          uint4 v[4];
+      for (int g = sg.g0; g < sg.g1; ++g, ++cidx) {
+        if ((cidx & 1) == grp) {
+          if (!mbar_wait(full_bar(s), ph, abort_flag, a.err)) { ok = false; break; }
+          if (!mbar_wait(aempty_bar(ai), aph ^ 1u, abort_flag, a.err)) { ok = false; break; }
+          const uint8_t *wc = gbase + (size_t)s * kStage;
+          const uint32_t tcol = tmem + lane_base + (uint32_t)(ai * 64);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            v[j] = *reinterpret_cast<const uint4 *>(wc + (4 * half_k + j) * 2048 + row * 16);
-          const __half sc = *reinterpret_cast<const __half *>(wc + 16384 + row * 2);
-          dequant_w8(v, __half2half2(sc), o);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t o[32];
+            if constexpr (WBITS == 4) {
+              uint4 v[2];
+              v[0] = *reinterpret_cast<const uint4 *>(wc + (2 * h) * 2048 + row * 16);
+              v[1] = *reinterpret_cast<const uint4 *>(wc + (2 * h + 1) * 2048 + row * 16);
+              const __half sc = *reinterpret_cast<const __half *>(wc + 8192 + row * 2);
+              dequant_w4(v, __half2half2(sc), o);
+            } else {
+              uint4 v[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                v[j] = *reinterpret_cast<const uint4 *>(wc + (4 * h + j) * 2048 + row * 16);
+              const __half sc = *reinterpret_cast<const __half *>(wc + 16384 + row * 2);
+              dequant_w8(v, __half2half2(sc), o);
+            }
+            tmem_st32(tcol + (uint32_t)(h * 32), o);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(afull_bar(ai));
         }
-        tmem_st32(tmem + lane_base + (uint32_t)(ai * 64 + half_k * 32), o);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(afull_bar(ai));
         if (++s == S) { s = 0; ph ^= 1u; }
         if (++ai == kAStages) { ai = 0; aph ^= 1u; }
       }
