@@ -24,7 +24,9 @@
 //   epilogue warps : tcgen05.ld the accumulator, scale by the token scale (W4A8),
 //                    write fp16 y, or a binary32 partial for a tile cut by the
 //                    stream-K split; the last CTA of a cut tile sums the partials
-//                    in CTA order (deterministic, no waiting).
+//                    in CTA order (deterministic, no waiting) once its own work
+//                    is done, pulling all of them into the idle stage buffers
+//                    with bulk copies in a single round trip.
 #pragma once
 #include <stdint.h>
 #include <cuda_fp16.h>
@@ -57,7 +59,8 @@ constexpr int kBarAFull = kBarBFull + 8 * kMaxStages;
 constexpr int kBarAEmpty = kBarAFull + 8 * kMaxAStages;
 constexpr int kBarAccFull = kBarAEmpty + 8 * kMaxAStages;
 constexpr int kBarAccEmpty = kBarAccFull + 8 * 2;
-constexpr int kTmemSlot = kBarAccEmpty + 8 * 2;
+constexpr int kBarRed = kBarAccEmpty + 8 * 2;        // stream-K reduction loads
+constexpr int kTmemSlot = kBarRed + 8;
 constexpr int kAbortSlot = kTmemSlot + 4;
 constexpr int kBcastSlot = kAbortSlot + 4;
 static_assert(kBcastSlot + 4 <= kSmemReserve - 1024, "barrier block too large");
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       mbar_init(accfull_bar(i), kIssuers);
       mbar_init(accempty_bar(i), kEpiWarps);
     }
+    mbar_init(bars + kBarRed, 1);
     *abort_flag = 0;
     *bcast = 0;
     fence_mbar_init();
@@ -364,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     const int ept = threadIdx.x - kWarpEpi0 * 32;   // 0..127
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     int cidx = 0;                                   // CTA-wide index of the segment's first chunk
+    int npend = 0, pend_tile[2] = {0, 0};           // cut tiles this CTA must reduce (<= 2)
+    bool aborted = false;
     for (int i = 0; segment(P, cta, i, sg); ++i) {
       const int b = i % kNAcc;
       const int nch = sg.g1 - sg.g0;
@@ -373,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       cidx += nch;
       mbar_wait(accfull_bar(b), (i / kNAcc) & 1, abort_flag, a.err);
       named_bar_sync(1, kEpiWarps * 32);           // all four warps decide together
-      if (*abort_flag) break;
+      if (*abort_flag) { aborted = true; break; }
       tc_fence_after();
       int u, t;
       tile_coords(P, sg.tile, u, t);
@@ -425,40 +431,48 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
           *bcast = last;
         }
         named_bar_sync(1, kEpiWarps * 32);
-        if (*bcast) {
-          // sum the partials in CTA (= K) order; 8 tokens x up to 4 contributors
-          // of independent loads in flight at a time
-          for (int jc = 0; jc < mv; jc += 8) {
-            float acc[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-            for (int p = pf; p <= pl; p += 4) {
-              float vv[4][8];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float *src = a.partials +
-                                   (size_t)partial_slot(P, p + q <= pl ? p + q : pl, sg.tile) * (BN * kRows) +
-                                   (size_t)jc * kRows + row;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  vv[q][j] = (p + q <= pl && jc + j < mv) ? __ldcg(src + j * kRows) : 0.0f;
-              }
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  if (p + q <= pl) acc[j] += vv[q][j];
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (jc + j < mv) {
-                const int m = m0 + jc + j;
-                const float val = TOKSCALE ? acc[j] * a.xs[m] : acc[j];
-                a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
-              }
-            }
-          }
+        if (*bcast) pend_tile[npend++] = sg.tile;    // reduced once this CTA's own work is done
+      }
+    }
+    // ---- stream-K reductions: all MMAs of this CTA have completed (its last
+    // accumulator was read), so every stage buffer is idle.  Pull the contributors'
+    // partials of each cut tile this CTA finished last into shared memory with
+    // bulk copies (all in flight at once), then sum them in CTA order.
+    uint32_t red_phase = 0;
+    const uint32_t avail = (uint32_t)S * kStage;
+    for (int r = 0; r < npend && !aborted; ++r) {
+      const int tile = pend_tile[r];
+      int pf, pl, u, t;
+      tile_contributors(P, tile, pf, pl);
+      tile_coords(P, tile, u, t);
+      const int n = t * kRows + row;
+      const int m0 = u * BN;
+      const int mv = P.M - m0 < BN ? P.M - m0 : BN;
+      const int nseg = pl - pf + 1;
+      int jt = (int)(avail / ((uint32_t)nseg * kRows * 4));   // tokens per pass
+      if (jt > mv) jt = mv;
+      for (int j0 = 0; j0 < mv; j0 += jt) {
+        const int jn = mv - j0 < jt ? mv - j0 : jt;
+        const uint32_t bytes = (uint32_t)jn * kRows * 4;
+        if (ept == 0) {
+          fence_proxy_async_all();
+          mbar_arrive_expect_tx(bars + kBarRed, bytes * nseg);
+          for (int p = pf; p <= pl; ++p)
+            bulk_g2s_nohint(sbase + (uint32_t)(p - pf) * bytes,
+                            a.partials + (size_t)partial_slot(P, p, tile) * (BN * kRows) + (size_t)j0 * kRows,
+                            bytes, bars + kBarRed);
         }
+        if (!mbar_wait(bars + kBarRed, red_phase, abort_flag, a.err)) { aborted = true; break; }
+        red_phase ^= 1u;
+        const float *buf = reinterpret_cast<const float *>(gbase);
+        for (int j = 0; j < jn; ++j) {
+          float acc = 0.0f;
+          for (int p = 0; p < nseg; ++p) acc += buf[(size_t)p * jn * kRows + (size_t)j * kRows + row];
+          const int m = m0 + j0 + j;
+          const float val = TOKSCALE ? acc * a.xs[m] : acc;
+          a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
+        }
+        named_bar_sync(1, kEpiWarps * 32);          // buffer free before the next pass
       }
     }
   }

@@ -146,6 +146,20 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Order this thread's view of generic-proxy memory (shared and global) before its
+// subsequent async-proxy operations (bulk copies), and vice versa.
+__device__ __forceinline__ void fence_proxy_async_all() {
+  asm volatile("fence.proxy.async;" ::: "memory");
+}
+
+// 1-D bulk copy global -> shared without a cache hint.
+__device__ __forceinline__ void bulk_g2s_nohint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
