@@ -169,6 +169,27 @@ int qgemm_w4a16_noalloc(const uint16_t *x, const void *packed_w4, int M, int N, 
                         qw_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Options (process-wide, read when a qgemm_* call is made; a CUDA graph keeps
+ * the value in force when the call was captured).
+ *
+ *   QW_OPT_WEIGHTS_IMMUTABLE (default 0).  Every kernel of this library may
+ *   start while the preceding kernel on its stream is still finishing
+ *   (programmatic dependent launch); by default it touches no global memory
+ *   until that kernel has completed.  Setting this option to 1 declares that the
+ *   packed weights passed to qgemm_* are never written by the kernel that
+ *   immediately precedes the call on its stream (true when the weights were
+ *   packed once at load time and the stream was synchronized since).  The GEMM
+ *   then streams and dequantizes its weights before that kernel completes, so
+ *   consecutive layers overlap.  Leave it 0 when a weight-writing kernel (e.g.
+ *   qpack_*) may directly precede a GEMM on the same stream.
+ *   qw_set_option returns QW_OK or QW_ERR_INVALID_ARG; qw_get_option returns the
+ *   value or QW_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------ */
+enum { QW_OPT_WEIGHTS_IMMUTABLE = 1 };
+int qw_set_option(int option, int value);
+int qw_get_option(int option);
+
+/* ------------------------------------------------------------------------
  * Diagnostics.
  *   qw_last_error_string  text of the last host-side error of the calling
  *                         thread ("" if none).  Never NULL.

@@ -56,6 +56,8 @@ SIGNATURES = {
     "qw_last_error_string": (ctypes.c_char_p, []),
     "qw_device_error": (_i, []),
     "qw_num_kernel_launches": (_ll, []),
+    "qw_set_option": (_i, [_i, _i]),
+    "qw_get_option": (_i, [_i]),
     "qw_plan": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(Plan)]),
     "qw_plan_segments": (_i, [ctypes.POINTER(Plan), _i, _i, _p, _p, _p, _p]),
 }
@@ -259,6 +261,16 @@ def qgemm_w4a16_noalloc(x, packed, N: int, K: int, y=None):
 def device_error() -> int:
     """Synchronize and return (and clear) the device error word of the current device."""
     return int(lib().qw_device_error())
+
+
+QW_OPT_WEIGHTS_IMMUTABLE = 1
+
+
+def set_weights_immutable(flag: bool = True):
+    """Declare that packed weights are never written by the kernel that directly
+    precedes a GEMM on its stream, letting each GEMM stream its weights while the
+    preceding kernel finishes (see include/qgemm.h)."""
+    _check(lib().qw_set_option(QW_OPT_WEIGHTS_IMMUTABLE, 1 if flag else 0))
 
 
 def num_kernel_launches() -> int:

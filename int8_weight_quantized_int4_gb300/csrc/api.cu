@@ -20,6 +20,7 @@ namespace {
 
 thread_local char tl_err[512];
 std::atomic<long long> g_launches{0};
+std::atomic<int> g_opt_weights_immutable{0};
 
 int fail(int code, const char *fmt, ...) {
   va_list ap;
@@ -162,6 +163,7 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
   a.counters = P.ws_counters ? reinterpret_cast<int *>(w) : nullptr;
   a.partials = P.ws_partials ? reinterpret_cast<float *>(w + P.ws_counters) : nullptr;
   a.err = d->err;
+  a.early_weights = g_opt_weights_immutable.load(std::memory_order_relaxed);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (mode == QW_MODE_W4A8 && qw::act8_in_kernel(mode, P.bn)) {
@@ -311,6 +313,18 @@ int qw_device_error(void) {
 }
 
 long long qw_num_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int qw_set_option(int option, int value) {
+  if (option != QW_OPT_WEIGHTS_IMMUTABLE || (value != 0 && value != 1))
+    return fail(QW_ERR_INVALID_ARG, "unknown option %d or value %d", option, value);
+  g_opt_weights_immutable.store(value, std::memory_order_relaxed);
+  return QW_OK;
+}
+
+int qw_get_option(int option) {
+  if (option != QW_OPT_WEIGHTS_IMMUTABLE) return fail(QW_ERR_INVALID_ARG, "unknown option %d", option);
+  return g_opt_weights_immutable.load(std::memory_order_relaxed);
+}
 
 int qw_plan(int mode, int M, int N, int K, int num_sms, qw_plan_t *out) {
   if (!out) return fail(QW_ERR_INVALID_ARG, "null output");

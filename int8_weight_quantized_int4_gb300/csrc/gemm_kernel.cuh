@@ -210,8 +210,15 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 
   Seg sg;
   // Everything above overlaps the tail of the preceding kernel (programmatic
-  // dependent launch); no global memory is touched before this wait.
-  griddep_wait();
+  // dependent launch).  By default every thread waits for that kernel here, before
+  // touching global memory.  When the caller has declared the packed weights
+  // immutable (QW_OPT_WEIGHTS_IMMUTABLE), the weight-copy and dequant warps go
+  // ahead: they read only the weights and write only shared memory and TMEM, so the
+  // next layer's weights stream in while the previous kernel finishes.  The roles
+  // that read activations or write global memory (activation copies, epilogue)
+  // still wait first; the MMA and widen warps only consume what those produce.
+  const bool early = a.early_weights != 0;
+  if (!early) griddep_wait();
   griddep_launch_dependents();
 
   if (warp == kWarpTma) {
@@ -236,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   } else if (warp == kWarpAct) {
     // -------------------------------------------------- activation copies --
     if (lane == 0) {
+      if (early) griddep_wait();
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -363,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     }
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
     // -------------------------------------------------------- epilogue --
+    if (early) griddep_wait();
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const int ept = threadIdx.x - kWarpEpi0 * 32;   // 0..127

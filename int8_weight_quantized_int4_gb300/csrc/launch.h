@@ -19,6 +19,7 @@ struct GemmArgs {
   int *counters;            // [tiles] arrival counters (stream-K)
   float *partials;          // [2*grid][bn][128] binary32 partial sums (stream-K)
   int *err;                 // device error word
+  int early_weights;        // weights may be streamed before the preceding kernel ends
 };
 
 void count_launch();

@@ -78,6 +78,17 @@ def test_argument_errors_before_device():
     assert L.qpack_w8(FAKE, FAKE, 128, 130, FAKE, n) == q.QW_ERR_UNSUPPORTED_SHAPE
 
 
+def test_options_host_only():
+    L = q.lib()
+    assert L.qw_get_option(q.QW_OPT_WEIGHTS_IMMUTABLE) == 0
+    assert L.qw_set_option(q.QW_OPT_WEIGHTS_IMMUTABLE, 1) == q.QW_OK
+    assert L.qw_get_option(q.QW_OPT_WEIGHTS_IMMUTABLE) == 1
+    assert L.qw_set_option(q.QW_OPT_WEIGHTS_IMMUTABLE, 0) == q.QW_OK
+    assert L.qw_set_option(7, 1) == q.QW_ERR_INVALID_ARG
+    assert L.qw_set_option(q.QW_OPT_WEIGHTS_IMMUTABLE, 2) == q.QW_ERR_INVALID_ARG
+    assert L.qw_get_option(7) == q.QW_ERR_INVALID_ARG
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_no_device_reports_arch():
     L = q.lib()

@@ -340,3 +340,28 @@ def test_empty_and_single_tile(q):
     y = q.qgemm_w4a16(torch.empty((0, 128), dtype=torch.float16, device=DEV), packed, 128, 128)
     assert y.shape == (0, 128)
     assert q.device_error() == 0
+
+
+def test_weights_immutable_option_back_to_back(q):
+    """With QW_OPT_WEIGHTS_IMMUTABLE each GEMM streams its weights before the previous
+    kernel on the stream has finished; results of a chain of back-to-back layers
+    (with the int8 quantizer in between) must still match the oracle."""
+    q.set_weights_immutable(True)
+    try:
+        layers = [synth.make_problem(16, 1024, 1280, seed=950 + i, outlier_frac=0.01) for i in range(4)]
+        packed = [q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV)) for p in layers]
+        torch.cuda.synchronize()                     # packing done before the option matters
+        ys, ys8 = [], []
+        for p, pk in zip(layers, packed):
+            xd = p.x.to(DEV)
+            ys.append(q.qgemm_w4a16(xd, pk, p.N, p.K))
+            xq, xs = q.quant_act_int8(xd)
+            ys8.append(q.qgemm_w4a8(xq, xs, pk, p.N, p.K))
+        torch.cuda.synchronize()
+        for p, y, y8 in zip(layers, ys, ys8):
+            assert nerr(y, oracle.w4a16(p.x, p.codes, p.scales)) <= TOL
+            oq, os_ = oracle.quant_act_int8(p.x)
+            assert nerr(y8, oracle.w4a8(oq, os_, p.codes, p.scales)) <= TOL
+        assert q.device_error() == 0
+    finally:
+        q.set_weights_immutable(False)
