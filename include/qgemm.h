@@ -217,10 +217,12 @@ typedef struct {
     long long chunks;       /* tiles * groups: one chunk = 128 rows x 128 K */
     int grid;               /* persistent CTAs launched */
     int stream_k;           /* 1: contiguous chunk ranges with a reduction; 0: whole tiles */
-    int stages;             /* shared-memory pipeline depth */
+    int stages;             /* weight ring depth in shared memory (packed chunks) */
     int smem_bytes;         /* dynamic shared memory per CTA */
     size_t ws_bytes;        /* workspace bytes (see qgemm_workspace_bytes) */
     size_t ws_zero_bytes;   /* leading workspace bytes that must be zero */
+    int act_stages;         /* activation ring depth in shared memory (blocks) */
+    int act_block;          /* K groups per activation block (one tensor copy) */
 } qw_plan_t;
 
 int qw_plan(int mode, int M, int N, int K, int num_sms, qw_plan_t *out);

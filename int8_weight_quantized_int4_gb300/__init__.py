@@ -38,7 +38,8 @@ _p, _i, _sz, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_long
 class Plan(ctypes.Structure):
     _fields_ = [("bn", _i), ("token_tiles", _i), ("row_tiles", _i), ("groups", _i),
                 ("tiles", _ll), ("chunks", _ll), ("grid", _i), ("stream_k", _i), ("stages", _i),
-                ("smem_bytes", _i), ("ws_bytes", _sz), ("ws_zero_bytes", _sz)]
+                ("smem_bytes", _i), ("ws_bytes", _sz), ("ws_zero_bytes", _sz),
+                ("act_stages", _i), ("act_block", _i)]
 
 
 SIGNATURES = {

@@ -84,7 +84,7 @@ int current_device(DevInfo *&out) {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-int encode_act_map(CUtensorMap *map, const void *ptr, int M, int K, int bn, bool int8) {
+int encode_act_map(CUtensorMap *map, const void *ptr, int M, int K, int bn, int block, bool int8) {
   std::call_once(g_encode_once, [] {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -98,19 +98,21 @@ int encode_act_map(CUtensorMap *map, const void *ptr, int M, int K, int bn, bool
   const cuuint32_t estride[3] = {1, 1, 1};
   CUresult r;
   if (int8) {
-    // int8 codes [M,K]: 128 x bn boxes, unswizzled (widened in the kernel)
-    const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    const cuuint64_t gstride[1] = {(cuuint64_t)K};
-    const cuuint32_t box[2] = {128u, (cuuint32_t)bn};
-    r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), gdim, gstride, box,
+    // int8 codes [M,K] seen as [K/128][M][128]: one 128 x bn x block box brings the
+    // codes of `block` consecutive groups, unswizzled (widened in the kernel)
+    const cuuint64_t gdim[3] = {128, (cuuint64_t)M, (cuuint64_t)K / 128};
+    const cuuint64_t gstride[2] = {(cuuint64_t)K, 128};
+    const cuuint32_t box[3] = {128u, (cuuint32_t)bn, (cuuint32_t)block};
+    r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), gdim, gstride, box,
                  estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
-    // fp16 [M,K] seen as [K/64][M][64]: one 64 x bn x 2 box per 128-wide group lands as
-    // two K-major 64-column halves with the 128-byte swizzle the MMA descriptor expects
+    // fp16 [M,K] seen as [K/64][M][64]: one 64 x bn x (2 block) box lands as the two
+    // K-major 64-column halves of `block` consecutive groups, with the 128-byte
+    // swizzle the MMA descriptor expects
     const cuuint64_t gdim[3] = {64, (cuuint64_t)M, (cuuint64_t)K / 64};
     const cuuint64_t gstride[2] = {(cuuint64_t)K * 2, 128};
-    const cuuint32_t box[3] = {64u, (cuuint32_t)bn, 2u};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)bn, (cuuint32_t)(2 * block)};
     r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), gdim, gstride, box,
                  estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -167,16 +169,16 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (mode == QW_MODE_W4A8 && qw::act8_in_kernel(mode, P.bn)) {
-    if ((rc = encode_act_map(&a.tmap, act, M, K, P.bn, true))) return rc;
+    if ((rc = encode_act_map(&a.tmap, act, M, K, P.bn, P.xblock, true))) return rc;
     e = qw::launch_gemm_w4a8(a, st);
   } else if (mode == QW_MODE_W4A8) {
     uint16_t *wide = reinterpret_cast<uint16_t *>(w + P.ws_counters + P.ws_partials);
-    if ((rc = encode_act_map(&a.tmap, wide, M, K, P.bn, false))) return rc;
+    if ((rc = encode_act_map(&a.tmap, wide, M, K, P.bn, P.xblock, false))) return rc;
     e = qw::launch_widen_i8(static_cast<const int8_t *>(act), wide, (size_t)M * K, d->sms, st);
     if (e != cudaSuccess) return fail_cuda(e, "widen kernel launch");
     e = qw::launch_gemm_w4a8(a, st);
   } else {
-    if ((rc = encode_act_map(&a.tmap, act, M, K, P.bn, false))) return rc;
+    if ((rc = encode_act_map(&a.tmap, act, M, K, P.bn, P.xblock, false))) return rc;
     e = mode == QW_MODE_W8A16 ? qw::launch_gemm_w8a16(a, st) : qw::launch_gemm_w4a16(a, st);
   }
   if (e != cudaSuccess) return fail_cuda(e, "GEMM kernel launch");
@@ -344,6 +346,8 @@ int qw_plan(int mode, int M, int N, int K, int num_sms, qw_plan_t *out) {
   out->smem_bytes = P.smem_bytes;
   out->ws_bytes = P.ws_bytes;
   out->ws_zero_bytes = P.ws_zero;
+  out->act_stages = P.xstages;
+  out->act_block = P.xblock;
   return QW_OK;
 }
 

@@ -8,19 +8,20 @@
 // TMEM lane) and the tokens are its N (16..256), so a decode batch of 1..64
 // tokens still fills the 128-row MMA.  Per 128 x 128 weight chunk:
 //   copy warps     : one issues the 1-D bulk copy of each packed chunk (codes +
-//                    signed scales), another the TMA tensor copy of the matching
-//                    activation tile (128-byte swizzle, zero fill past M); both
-//                    complete on the stage's mbarrier
+//                    signed scales) into the weight ring, another one TMA tensor
+//                    copy per block of up to four groups of activations (128-byte
+//                    swizzle, zero fill past M) into the activation ring
 //   widen warps    : W4A8 at decode sizes only -- int8 codes -> fp16 (exact) into
 //                    the swizzled tile
 //   dequant warps  : int4/int8 codes -> fp16 (q * s) in registers, with the
 //                    scale's sign, stored into TMEM as the A operand
 //   MMA warps      : 8 x tcgen05.mma kind::f16 (K = 16 each) per chunk, fp32
-//                    accumulator in TMEM; tcgen05.commit frees the stage.  For
-//                    token tiles of up to 64 two warps issue alternate chunks into
-//                    two accumulators (an MMA with N <= 64 costs about as much issue
-//                    time as a full one, so one issuing thread cannot keep up with
-//                    HBM); the epilogue adds the two in a fixed order
+//                    accumulator in TMEM; tcgen05.commit frees the operands.  An
+//                    MMA holds its issuing thread for about 50 ns whatever its N, so
+//                    one thread cannot keep up with HBM on small token tiles: up to
+//                    four warps issue chunks round-robin into their own accumulators
+//                    (4 for token tiles <= 32, 2 for 64, as TMEM allows), and the
+//                    epilogue adds them in a fixed order
 //   epilogue warps : tcgen05.ld the accumulator, scale by the token scale (W4A8),
 //                    write fp16 y, or a binary32 partial for a tile cut by the
 //                    stream-K split; the last CTA of a cut tile sums the partials
@@ -38,24 +39,26 @@ namespace qw {
 
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
-constexpr int kWidenWarps = 4;
+constexpr int kWidenWarps = 2;
+constexpr int kMaxIssuers = 4;
 constexpr int kWarpEpi0 = kDeqWarps;                 // 8
 constexpr int kWarpWiden0 = kWarpEpi0 + kEpiWarps;   // 12
-constexpr int kWarpTma = kWarpWiden0 + kWidenWarps;  // 16
-constexpr int kWarpMma = kWarpTma + 1;               // 17
-constexpr int kWarpAct = kWarpMma + 1;               // 18: activation tile copies
-constexpr int kWarpMma2 = kWarpAct + 1;              // 19: second MMA issuer (token tiles <= 64)
-constexpr int kThreads = (kWarpMma2 + 1) * 32;       // 640
+constexpr int kWarpTma = kWarpWiden0 + kWidenWarps;  // 14: weight chunk copies
+constexpr int kWarpAct = kWarpTma + 1;               // 15: activation block copies
+constexpr int kWarpMma0 = kWarpAct + 1;              // 16..19: MMA issuers
+constexpr int kThreads = (kWarpMma0 + kMaxIssuers) * 32;   // 640
 constexpr int kMaxAStages = 8;                       // TMEM A-operand ring (64 columns per stage)
 constexpr int kDeqGroups = 2;                        // dequant warp groups, alternate chunks
 constexpr int kDeqGroupWarps = kDeqWarps / kDeqGroups;
 constexpr int kTmemCols = 512;
 
-// offsets inside the barrier block that follows the stages
-constexpr int kBarFull = 0;
-constexpr int kBarEmpty = kBarFull + 8 * kMaxStages;
-constexpr int kBarBFull = kBarEmpty + 8 * kMaxStages;
-constexpr int kBarAFull = kBarBFull + 8 * kMaxStages;
+// offsets inside the barrier block that follows the rings
+constexpr int kBarWFull = 0;                                  // weight ring
+constexpr int kBarWEmpty = kBarWFull + 8 * kMaxWStages;
+constexpr int kBarXFull = kBarWEmpty + 8 * kMaxWStages;       // activation ring
+constexpr int kBarXEmpty = kBarXFull + 8 * kMaxXStages;
+constexpr int kBarBFull = kBarXEmpty + 8 * kMaxXStages;       // W4A8: block widened
+constexpr int kBarAFull = kBarBFull + 8 * kMaxXStages;        // TMEM A ring
 constexpr int kBarAEmpty = kBarAFull + 8 * kMaxAStages;
 constexpr int kBarAccFull = kBarAEmpty + 8 * kMaxAStages;
 constexpr int kBarAccEmpty = kBarAccFull + 8 * 2;
@@ -108,15 +111,14 @@ __device__ __forceinline__ void dequant_w8(const uint4 (&v)[4], __half2 s2, uint
   }
 }
 
-// W4A8 at decode sizes: widen the int8 staging tile (rows of 128 codes, unswizzled,
-// right after the bn x 128 fp16 tile) into the 128-byte-swizzled fp16 tile.
+// W4A8 at decode sizes: widen one int8 staging tile (rows of 128 codes, unswizzled)
+// into the 128-byte-swizzled fp16 tile of the same chunk.
 // (1024 + (q XOR 0x80)) - 1152 = q, exact in fp16.
-template <int BN>
-__device__ __forceinline__ void widen_stage(uint8_t *btile, int t, int rows) {
-  const uint8_t *stg = btile + BN * kGroup * 2;
+template <int BN, int NT>
+__device__ __forceinline__ void widen_chunk(uint8_t *btile, const uint8_t *stg, int t, int rows) {
   const __half2 k1152 = __float2half2_rn(1152.0f);
 #pragma unroll 2
-  for (int pc = t; pc < rows * 8; pc += kWidenWarps * 32) {
+  for (int pc = t; pc < rows * 8; pc += NT) {
     const int r = pc >> 3, c8 = pc & 7;
     const uint4 v = *reinterpret_cast<const uint4 *>(stg + pc * 16);
     const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
@@ -139,29 +141,50 @@ __device__ __forceinline__ void widen_stage(uint8_t *btile, int t, int rows) {
 template <int BN, int WBITS, bool TOKSCALE>
 __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_constant__ GemmArgs a) {
   constexpr uint32_t kChunk = WBITS == 8 ? kChunkW8 : kChunkW4;
-  constexpr uint32_t kWAligned = (kChunk + 1023) / 1024 * 1024;
+  constexpr uint32_t kWStage = (kChunk + 127) / 128 * 128;
+  static_assert(kChunk % 128 == 0, "weight slots stay 128-byte aligned");
   constexpr bool kAct8 = TOKSCALE && BN <= kAct8InKernelMaxBn;
-  constexpr uint32_t kStage = kWAligned + BN * kGroup * 2 + (kAct8 ? BN * kGroup : 0);
-  constexpr uint32_t kActBytes = kAct8 ? BN * kGroup : BN * kGroup * 2;
-  constexpr int kNAcc = BN <= 128 ? 2 : 1;
-  constexpr bool kDual = BN <= 64;                     // two MMA issuers, two accumulators
-  constexpr int kIssuers = kDual ? 2 : 1;
-  // A-operand ring depth: whatever TMEM the accumulators leave free (6 stages for
-  // token tiles up to 32, 4 otherwise); accumulators start after the ring
-  constexpr int kAStages = BN <= 32 ? 6 : 4;
+  constexpr int kXBlock = act_block(BN);                 // chunks per activation copy
+  constexpr uint32_t kXChunk = BN * kGroup * 2;          // one fp16 tile (two swizzled halves)
+  constexpr uint32_t kXStage = kXBlock * (kXChunk + (kAct8 ? BN * kGroup : 0));
+  constexpr uint32_t kXBytes = kXBlock * (kAct8 ? BN * kGroup : kXChunk);   // per copy
+  constexpr int kNAcc = BN <= 128 ? 2 : 1;             // accumulator sets (double buffer)
+  constexpr int kIssuers = BN <= 32 ? 4 : BN <= 64 ? 2 : 1;   // one accumulator each
+  static_assert(kIssuers <= kMaxIssuers && (kIssuers & (kIssuers - 1)) == 0, "issuers");
+  // W4A8 widening: the two widen warps, plus the two issuer warps left idle when a
+  // token tile needs at most two issuers
+  constexpr int kWidenW = kIssuers <= 2 ? kWidenWarps + 2 : kWidenWarps;
+  // A-operand ring: whatever TMEM the accumulators leave free (64 columns a stage),
+  // in two halves, one per chunk parity (see the ring note below)
+  constexpr int kAccCols = kNAcc * kIssuers * BN;
+  constexpr int kAStagesFit = (kTmemCols - kAccCols) / 64;
+  constexpr int kAStages = (kAStagesFit < kMaxAStages ? kAStagesFit : kMaxAStages) & ~1;
+  constexpr int kAHalf = kAStages / 2;
   constexpr int kAccCol0 = kAStages * 64;
-  static_assert(kAccCol0 + (kDual ? 4 : kNAcc) * BN <= kTmemCols, "TMEM budget");
-  static_assert(kAStages <= kMaxAStages, "A ring");
+  static_assert(kAHalf >= 1 && kAccCol0 + kAccCols <= kTmemCols, "TMEM budget");
   constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
 
   extern __shared__ uint8_t smem_raw[];
   const Plan &P = a.P;
-  const int S = P.stages;
+  const int SW = P.stages, SX = P.xstages;
+  // Ring note.  A waiter on a slot's barrier by phase parity must not be able to
+  // wait for fill n+1 while fill n is still pending.  Chunks alternate between the
+  // two dequant groups by parity, so the weight ring and the TMEM A ring are split
+  // into one half per parity: every slot has one producer that fills it in order.
+  // The weight half has one consumer (its group).  An A slot is read by the issuers
+  // of chunks c, c + 2 kAHalf, ... in turn; an issuer reaching chunk c has already
+  // seen chunk c - 2 of the same half complete, which the group filled after chunk
+  // c - 2 kAHalf, so the previous fill of the slot is complete too.  Every issuer
+  // and the widen warps wait on every activation block, whether or not they use it.
+  const int SWH = SW >> 1;                                   // weight slots per parity
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (sbase - raw);
-  const uint32_t bars = sbase + (uint32_t)S * kStage;
-  uint8_t *gbars = gbase + (size_t)S * kStage;
+  // activation ring first (1024-byte aligned slots for the swizzle), then weights
+  const uint32_t wbase = sbase + (uint32_t)SX * kXStage;
+  const uint32_t ring_bytes = (uint32_t)SX * kXStage + (uint32_t)SW * kWStage;
+  const uint32_t bars = sbase + ring_bytes;
+  uint8_t *gbars = gbase + ring_bytes;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gbars + kAbortSlot);
   volatile int *bcast = reinterpret_cast<volatile int *>(gbars + kBcastSlot);
 
@@ -169,21 +192,27 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   const int lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
 
-  auto full_bar = [&](int s) { return bars + kBarFull + 8 * s; };
-  auto empty_bar = [&](int s) { return bars + kBarEmpty + 8 * s; };
+  auto wfull_bar = [&](int s) { return bars + kBarWFull + 8 * s; };
+  auto wempty_bar = [&](int s) { return bars + kBarWEmpty + 8 * s; };
+  auto xfull_bar = [&](int s) { return bars + kBarXFull + 8 * s; };
+  auto xempty_bar = [&](int s) { return bars + kBarXEmpty + 8 * s; };
   auto bfull_bar = [&](int s) { return bars + kBarBFull + 8 * s; };
   auto afull_bar = [&](int i) { return bars + kBarAFull + 8 * i; };
   auto aempty_bar = [&](int i) { return bars + kBarAEmpty + 8 * i; };
   auto accfull_bar = [&](int i) { return bars + kBarAccFull + 8 * i; };
   auto accempty_bar = [&](int i) { return bars + kBarAccEmpty + 8 * i; };
-  auto w_smem = [&](int s) { return sbase + (uint32_t)s * kStage; };
-  auto b_smem = [&](int s) { return sbase + (uint32_t)s * kStage + kWAligned; };
+  auto w_smem = [&](int s) { return wbase + (uint32_t)s * kWStage; };
+  auto x_smem = [&](int s) { return sbase + (uint32_t)s * kXStage; };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 2);
-      mbar_init(empty_bar(s), 1);
-      mbar_init(bfull_bar(s), kWidenWarps);
+    for (int s = 0; s < SW; ++s) {
+      mbar_init(wfull_bar(s), 1);
+      mbar_init(wempty_bar(s), kDeqGroupWarps);
+    }
+    for (int s = 0; s < SX; ++s) {
+      mbar_init(xfull_bar(s), 1);
+      mbar_init(xempty_bar(s), kIssuers);
+      mbar_init(bfull_bar(s), kWidenW);
     }
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(afull_bar(i), kDeqGroupWarps);
@@ -214,9 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   // touching global memory.  When the caller has declared the packed weights
   // immutable (QW_OPT_WEIGHTS_IMMUTABLE), the weight-copy and dequant warps go
   // ahead: they read only the weights and write only shared memory and TMEM, so the
-  // next layer's weights stream in while the previous kernel finishes.  The roles
-  // that read activations or write global memory (activation copies, epilogue)
-  // still wait first; the MMA and widen warps only consume what those produce.
+  // next layer's weights stream in and are dequantized while the previous kernel
+  // finishes.  The roles that read activations or write global memory (activation
+  // copies, epilogue) still wait first; the MMA and widen warps only consume what
+  // those produce.
   const bool early = a.early_weights != 0;
   if (!early) griddep_wait();
   griddep_launch_dependents();
@@ -225,23 +255,26 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     // ------------------------------------------------------ weight copies --
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int s = 0;
-      uint32_t ph = 0;
+      int s[2] = {0, 0}, cidx = 0;
+      uint32_t ph[2] = {0, 0};
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         int u, t;
         tile_coords(P, sg.tile, u, t);
         const uint8_t *src = a.wpack + ((size_t)t * P.G + sg.g0) * kChunk;
-        for (int g = sg.g0; g < sg.g1; ++g, src += kChunk) {
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(full_bar(s), kChunk);
-          bulk_g2s(w_smem(s), src, kChunk, full_bar(s), pol);
-          if (++s == S) { s = 0; ph ^= 1u; }
+        for (int g = sg.g0; g < sg.g1; ++g, ++cidx, src += kChunk) {
+          const int p = cidx & 1, slot = p * SWH + s[p];
+          if (!mbar_wait(wempty_bar(slot), ph[p] ^ 1u, abort_flag, a.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(wfull_bar(slot), kChunk);
+          bulk_g2s(w_smem(slot), src, kChunk, wfull_bar(slot), pol);
+          if (++s[p] == SWH) { s[p] = 0; ph[p] ^= 1u; }
         }
       }
     }
   } else if (warp == kWarpAct) {
     // -------------------------------------------------- activation copies --
+    // one tensor copy per block of up to kXBlock consecutive groups of a segment;
+    // a block that runs past the segment (or past K) brings data nobody reads
     if (lane == 0) {
       if (early) griddep_wait();
       int s = 0;
@@ -250,36 +283,42 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         int u, t;
         tile_coords(P, sg.tile, u, t);
-        for (int g = sg.g0; g < sg.g1; ++g) {
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(full_bar(s), kActBytes);
+        for (int g = sg.g0; g < sg.g1; g += kXBlock) {
+          if (!mbar_wait(xempty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(xfull_bar(s), kXBytes);
           if constexpr (kAct8) {
-            // int8 codes: one 128 x BN box into the staging slot (unswizzled)
-            tma_load_2d(b_smem(s) + BN * kGroup * 2, &a.tmap, g * kGroup, u * BN, full_bar(s));
+            // int8 codes: a 128 x BN x kXBlock box into the staging tiles (unswizzled)
+            tma_load_3d(x_smem(s) + kXBlock * kXChunk, &a.tmap, 0, u * BN, g, xfull_bar(s));
           } else {
-            // fp16: one 64 x BN x 2 box (both 64-wide halves of the group), 128-byte swizzle
-            tma_load_3d(b_smem(s), &a.tmap, 0, u * BN, 2 * g, full_bar(s));
+            // fp16: a 64 x BN x (2 kXBlock) box, both 64-wide halves of every group,
+            // 128-byte swizzle
+            tma_load_3d(x_smem(s), &a.tmap, 0, u * BN, 2 * g, xfull_bar(s));
           }
-          if (++s == S) { s = 0; ph ^= 1u; }
+          if (++s == SX) { s = 0; ph ^= 1u; }
         }
       }
     }
-  } else if (warp >= kWarpWiden0 && warp < kWarpWiden0 + kWidenWarps) {
+  } else if ((warp >= kWarpWiden0 && warp < kWarpWiden0 + kWidenWarps) ||
+             (kWidenW > kWidenWarps && warp >= kWarpMma0 + 2)) {
     // ------------------------------------------ W4A8 int8 -> fp16 widening --
     if constexpr (kAct8) {
-      const int wt = threadIdx.x - kWarpWiden0 * 32;   // 0..127
+      const int wt = warp < kWarpTma ? threadIdx.x - kWarpWiden0 * 32                 // 0..63
+                                     : kWidenWarps * 32 + threadIdx.x - (kWarpMma0 + 2) * 32;
       const int rows = P.M < BN ? P.M : BN;            // a single token tile when widening here
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
-        for (int g = sg.g0; g < sg.g1; ++g) {
-          if (!mbar_wait(full_bar(s), ph, abort_flag, a.err)) { ok = false; break; }
-          widen_stage<BN>(gbase + (size_t)s * kStage + kWAligned, wt, rows);
+        for (int g = sg.g0; g < sg.g1; g += kXBlock) {
+          if (!mbar_wait(xfull_bar(s), ph, abort_flag, a.err)) { ok = false; break; }
+          const int nb = sg.g1 - g < kXBlock ? sg.g1 - g : kXBlock;
+          uint8_t *xs = gbase + (size_t)s * kXStage;
+          for (int j = 0; j < nb; ++j)
+            widen_chunk<BN, kWidenW * 32>(xs + j * kXChunk, xs + kXBlock * kXChunk + j * (BN * kGroup), wt, rows);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(bfull_bar(s));
-          if (++s == S) { s = 0; ph ^= 1u; }
+          if (++s == SX) { s = 0; ph ^= 1u; }
         }
       }
     }
@@ -288,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     // Two groups of four warps take alternate chunks (CTA-wide chunk parity), so
     // two chunks are being dequantized at once; within a group each warp covers 32
     // rows (its TMEM lane quarter) over the whole 128-wide group, in two halves.
+    // The weight slot is handed back as soon as it has been read.
     const int quad = warp & 3, grp = warp / kDeqGroupWarps;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -297,74 +337,92 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
       for (int g = sg.g0; g < sg.g1; ++g, ++cidx) {
         if ((cidx & 1) == grp) {
-          if (!mbar_wait(full_bar(s), ph, abort_flag, a.err)) { ok = false; break; }
-          if (!mbar_wait(aempty_bar(ai), aph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-          const uint8_t *wc = gbase + (size_t)s * kStage;
-          const uint32_t tcol = tmem + lane_base + (uint32_t)(ai * 64);
+          const int slot = grp * SWH + s, aslot = grp * kAHalf + ai;
+          if (!mbar_wait(aempty_bar(aslot), aph ^ 1u, abort_flag, a.err)) { ok = false; break; }
+          if (!mbar_wait(wfull_bar(slot), ph, abort_flag, a.err)) { ok = false; break; }
+          const uint8_t *wc = gbase + (size_t)SX * kXStage + (size_t)slot * kWStage;
+          const uint32_t tcol = tmem + lane_base + (uint32_t)(aslot * 64);
+          uint32_t o[2][32];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            uint32_t o[32];
             if constexpr (WBITS == 4) {
               uint4 v[2];
               v[0] = *reinterpret_cast<const uint4 *>(wc + (2 * h) * 2048 + row * 16);
               v[1] = *reinterpret_cast<const uint4 *>(wc + (2 * h + 1) * 2048 + row * 16);
               const __half sc = *reinterpret_cast<const __half *>(wc + 8192 + row * 2);
-              dequant_w4(v, __half2half2(sc), o);
+              dequant_w4(v, __half2half2(sc), o[h]);
             } else {
               uint4 v[4];
 #pragma unroll
               for (int j = 0; j < 4; ++j)
                 v[j] = *reinterpret_cast<const uint4 *>(wc + (4 * h + j) * 2048 + row * 16);
               const __half sc = *reinterpret_cast<const __half *>(wc + 16384 + row * 2);
-              dequant_w8(v, __half2half2(sc), o);
+              dequant_w8(v, __half2half2(sc), o[h]);
             }
-            tmem_st32(tcol + (uint32_t)(h * 32), o);
+            if (h == 1) {
+              // every lane's reads of the slot are done (their results are in registers)
+              __syncwarp();
+              if (lane == 0) mbar_arrive(wempty_bar(slot));
+            }
+            tmem_st32(tcol + (uint32_t)(h * 32), o[h]);
           }
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(afull_bar(ai));
+          if (lane == 0) mbar_arrive(afull_bar(aslot));
+          if (++s == SWH) { s = 0; ph ^= 1u; }
+          if (++ai == kAHalf) { ai = 0; aph ^= 1u; }
         }
-        if (++s == S) { s = 0; ph ^= 1u; }
-        if (++ai == kAStages) { ai = 0; aph ^= 1u; }
       }
     }
-  } else if (warp == kWarpMma || (kDual && warp == kWarpMma2)) {
+  } else if (warp >= kWarpMma0 && warp < kWarpMma0 + kIssuers) {
     // ------------------------------------------------------------- MMA --
+    // Issuer q takes the chunks with CTA-wide index = q (mod kIssuers).  Each issuer
+    // waits for every activation block and hands it back exactly once: by a commit
+    // (completes when its MMAs on the block are done) if it used the block, else by
+    // a plain arrive.
     if (lane == 0) {
-      const int q = warp == kWarpMma ? 0 : 1;          // issuer: chunks of CTA-wide parity q
-      int s = 0, ai = 0, cidx = 0;
-      uint32_t ph = 0, aph = 0;
+      const int q = warp - kWarpMma0;
+      int xs = 0, cidx = 0;
+      uint32_t xph = 0;
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         const int b = i % kNAcc;
         if (!mbar_wait(accempty_bar(b), ((i / kNAcc) & 1) ^ 1, abort_flag, a.err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(kAccCol0 + (kDual ? 2 * b + q : b) * BN);
-        bool first = true;
+        const uint32_t d = tmem + (uint32_t)(kAccCol0 + (b * kIssuers + q) * BN);
+        bool first = true, xready = false, used = false;
+        int j = 0;                                     // chunk within the activation block
         for (int g = sg.g0; g < sg.g1; ++g, ++cidx) {
-          if (kDual && (cidx & 1) != q) {
-            if (++s == S) { s = 0; ph ^= 1u; }
-            if (++ai == kAStages) { ai = 0; aph ^= 1u; }
-            continue;
+          if (!xready) {
+            if (!mbar_wait(kAct8 ? bfull_bar(xs) : xfull_bar(xs), xph, abort_flag, a.err)) { ok = false; break; }
+            xready = true;
           }
-          if (!mbar_wait(afull_bar(ai), aph, abort_flag, a.err)) { ok = false; break; }
-          if (!mbar_wait(kAct8 ? bfull_bar(s) : full_bar(s), ph, abort_flag, a.err)) { ok = false; break; }
-          tc_fence_after();
-          // descriptor start addresses advance by (offset >> 4); no carry out of the
-          // 14-bit field since shared-memory addresses stay below 256 KB
-          const uint64_t bdesc0 = smem_desc_sw128(b_smem(s));
-          const uint32_t a0 = tmem + (uint32_t)(ai * 64);
+          if ((cidx & (kIssuers - 1)) == q) {
+            const int h = cidx >> 1;                   // position in the parity's half
+            const int aslot = (cidx & 1) * kAHalf + h % kAHalf;
+            if (!mbar_wait(afull_bar(aslot), (uint32_t)(h / kAHalf) & 1u, abort_flag, a.err)) { ok = false; break; }
+            tc_fence_after();
+            // descriptor start addresses advance by (offset >> 4); no carry out of the
+            // 14-bit field since shared-memory addresses stay below 256 KB
+            const uint64_t bdesc0 = smem_desc_sw128(x_smem(xs) + (uint32_t)j * kXChunk);
+            const uint32_t a0 = tmem + (uint32_t)(aslot * 64);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_f16_ts(d, a0 + (uint32_t)(k * 8),
-                       bdesc0 + (uint64_t)(((k >> 2) * BN * 128 + (k & 3) * 32) >> 4), kIdesc,
-                       (!first || k > 0) ? 1u : 0u);
-          first = false;
-          mma_commit(empty_bar(s));
-          mma_commit(aempty_bar(ai));
-          if (++s == S) { s = 0; ph ^= 1u; }
-          if (++ai == kAStages) { ai = 0; aph ^= 1u; }
+            for (int k = 0; k < 8; ++k)
+              mma_f16_ts(d, a0 + (uint32_t)(k * 8),
+                         bdesc0 + (uint64_t)(((k >> 2) * BN * 128 + (k & 3) * 32) >> 4), kIdesc,
+                         (!first || k > 0) ? 1u : 0u);
+            first = false;
+            used = true;
+            mma_commit(aempty_bar(aslot));
+          }
+          if (++j == kXBlock || g + 1 == sg.g1) {
+            if (used) mma_commit(xempty_bar(xs));
+            else mbar_arrive(xempty_bar(xs));
+            if (++xs == SX) { xs = 0; xph ^= 1u; }
+            j = 0;
+            xready = used = false;
+          }
         }
         if (ok) mma_commit(accfull_bar(b));
       }
@@ -378,13 +436,18 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     int cidx = 0;                                   // CTA-wide index of the segment's first chunk
     int npend = 0, pend_tile[2] = {0, 0};           // cut tiles this CTA must reduce (<= 2)
+    int pend_cut[2] = {0, 0};
+    // contributors of this CTA's first and last segment (read now, while the
+    // preceding kernel may still run, so the lookup is off the critical path)
+    const int cut_first = P.cut[cta][0], cut_last = P.cut[cta][1];
     bool aborted = false;
     for (int i = 0; segment(P, cta, i, sg); ++i) {
       const int b = i % kNAcc;
       const int nch = sg.g1 - sg.g0;
-      // with two issuers, accumulator q holds the segment's chunks of parity q (if any)
-      const bool valid0 = !kDual || nch >= 2 || (cidx & 1) == 0;
-      const bool valid1 = kDual && (nch >= 2 || (cidx & 1) == 1);
+      // accumulator q holds the segment's chunks with index = q (mod kIssuers), if any
+      bool valid[kIssuers];
+#pragma unroll
+      for (int q = 0; q < kIssuers; ++q) valid[q] = nch >= kIssuers || ((q - cidx) & (kIssuers - 1)) < nch;
       cidx += nch;
       mbar_wait(accfull_bar(b), (i / kNAcc) & 1, abort_flag, a.err);
       named_bar_sync(1, kEpiWarps * 32);           // all four warps decide together
@@ -395,23 +458,25 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       const int n = t * kRows + row;
       const int m0 = u * BN;
       const int mv = P.M - m0 < BN ? P.M - m0 : BN;   // valid tokens of this tile
-      const uint32_t tacc = tmem + lane_base + (uint32_t)(kAccCol0 + (kDual ? 2 * b : b) * BN);
+      const uint32_t tacc = tmem + lane_base + (uint32_t)(kAccCol0 + b * kIssuers * BN);
       float *part = sg.slot >= 0 ? a.partials + (size_t)sg.slot * (BN * kRows) : nullptr;
-      constexpr int W = kDual ? 16 : 32;              // columns per TMEM load
+      constexpr int W = 32 / kIssuers;                // columns per TMEM load
 #pragma unroll 1
       for (int cc = 0; cc < BN; cc += W) {
-        uint32_t v[32], v1[32];
-        if constexpr (kDual) {
-          tmem_ld16(tacc + (uint32_t)cc, v);
-          tmem_ld16(tacc + (uint32_t)(BN + cc), v1);
-        } else {
-          tmem_ld32(tacc + (uint32_t)cc, v);
+        uint32_t v[kIssuers][W];
+#pragma unroll
+        for (int q = 0; q < kIssuers; ++q) {
+          if constexpr (W == 32) tmem_ld32(tacc + (uint32_t)(q * BN + cc), v[q]);
+          else if constexpr (W == 16) tmem_ld16(tacc + (uint32_t)(q * BN + cc), v[q]);
+          else tmem_ld8(tacc + (uint32_t)(q * BN + cc), v[q]);
         }
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < W; ++j) {
-          float acc = valid0 ? __uint_as_float(v[j]) : 0.0f;
-          if (kDual && valid1) acc += __uint_as_float(v1[j]);
+          float acc = 0.0f;                            // fixed order: issuer 0, 1, ...
+#pragma unroll
+          for (int q = 0; q < kIssuers; ++q)
+            if (valid[q]) acc += __uint_as_float(v[q][j]);
           if (cc + j < mv) {
             if (part) {
               part[(cc + j) * kRows + row] = acc;
@@ -431,8 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         // before one thread's device-scope acquire-release add, which also makes the
         // other contributors' partials visible to the last one, who reduces the tile
         named_bar_sync(1, kEpiWarps * 32);
-        int pf, pl;
-        tile_contributors(P, sg.tile, pf, pl);
+        // a cut segment is this CTA's first or its last
+        const int cut = i == 0 ? cut_first : cut_last;
+        const int pf = cut & 0xff, pl = (cut >> 8) & 0xff;
         if (ept == 0) {
           const int old = atom_add_acq_rel_gpu(a.counters + sg.tile, 1);
           const int last = (old == pl - pf) ? 1 : 0;
@@ -440,24 +506,57 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
           *bcast = last;
         }
         named_bar_sync(1, kEpiWarps * 32);
-        if (*bcast) pend_tile[npend++] = sg.tile;    // reduced once this CTA's own work is done
+        if (*bcast) {                                // reduced once this CTA's own work is done
+          pend_tile[npend] = sg.tile;
+          pend_cut[npend++] = cut;
+        }
       }
     }
     // ---- stream-K reductions: all MMAs of this CTA have completed (its last
-    // accumulator was read), so every stage buffer is idle.  Pull the contributors'
-    // partials of each cut tile this CTA finished last into shared memory with
-    // bulk copies (all in flight at once), then sum them in CTA order.
+    // accumulator was read), so every ring buffer is idle.  Sum the contributors'
+    // partials of each cut tile this CTA finished last, in CTA order.  Up to 4
+    // tokens each thread reads its row straight from L2; larger tiles pull all
+    // partials into shared memory with bulk copies (all in flight at once).
     uint32_t red_phase = 0;
-    const uint32_t avail = (uint32_t)S * kStage;
+    const uint32_t avail = ring_bytes;
     for (int r = 0; r < npend && !aborted; ++r) {
       const int tile = pend_tile[r];
-      int pf, pl, u, t;
-      tile_contributors(P, tile, pf, pl);
+      const int pf = pend_cut[r] & 0xff, pl = (pend_cut[r] >> 8) & 0xff, pf_slot = pend_cut[r] >> 16;
+      int u, t;
       tile_coords(P, tile, u, t);
       const int n = t * kRows + row;
       const int m0 = u * BN;
       const int mv = P.M - m0 < BN ? P.M - m0 : BN;
       const int nseg = pl - pf + 1;
+      auto put = [&](int m, float acc) {
+        const float val = TOKSCALE ? acc * a.xs[m] : acc;
+        a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
+      };
+      if (mv <= 4) {
+        // the atomic's acquire (thread 0) and the named barrier order these reads
+        // after every contributor's release; .cg reads bypass L1.  Eight
+        // contributors' loads are in flight at once, then summed in CTA order.
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int p0 = pf; p0 <= pl; p0 += 8) {
+          float v[8][4];
+#pragma unroll
+          for (int pp = 0; pp < 8; ++pp) {
+            const int p = p0 + pp;
+            const float *src = a.partials + (size_t)(p == pf ? pf_slot : 2 * p) * (BN * kRows) + row;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[pp][j] = (p <= pl && j < mv) ? __ldcg(src + j * kRows) : 0.0f;
+          }
+#pragma unroll
+          for (int pp = 0; pp < 8; ++pp)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (p0 + pp <= pl) acc[j] += v[pp][j];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < mv) put(m0 + j, acc[j]);
+        continue;
+      }
       int jt = (int)(avail / ((uint32_t)nseg * kRows * 4));   // tokens per pass
       if (jt > mv) jt = mv;
       for (int j0 = 0; j0 < mv; j0 += jt) {
@@ -468,18 +567,32 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
           mbar_arrive_expect_tx(bars + kBarRed, bytes * nseg);
           for (int p = pf; p <= pl; ++p)
             bulk_g2s_nohint(sbase + (uint32_t)(p - pf) * bytes,
-                            a.partials + (size_t)partial_slot(P, p, tile) * (BN * kRows) + (size_t)j0 * kRows,
+                            a.partials + (size_t)(p == pf ? pf_slot : 2 * p) * (BN * kRows) + (size_t)j0 * kRows,
                             bytes, bars + kBarRed);
         }
         if (!mbar_wait(bars + kBarRed, red_phase, abort_flag, a.err)) { aborted = true; break; }
         red_phase ^= 1u;
-        const float *buf = reinterpret_cast<const float *>(gbase);
-        for (int j = 0; j < jn; ++j) {
+        // eight tokens at a time so that the shared-memory loads overlap; each
+        // token's sum still runs over the contributors in CTA order
+        const float *buf = reinterpret_cast<const float *>(gbase) + row;
+        const int pstride = jn * kRows;
+        int j = 0;
+        for (; j + 8 <= jn; j += 8) {
+          float acc[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) acc[jj] = 0.0f;
+          for (int p = 0; p < nseg; ++p) {
+            const float *bp = buf + p * pstride + j * kRows;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) acc[jj] += bp[jj * kRows];
+          }
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) put(m0 + j0 + j + jj, acc[jj]);
+        }
+        for (; j < jn; ++j) {
           float acc = 0.0f;
-          for (int p = 0; p < nseg; ++p) acc += buf[(size_t)p * jn * kRows + (size_t)j * kRows + row];
-          const int m = m0 + j0 + j;
-          const float val = TOKSCALE ? acc * a.xs[m] : acc;
-          a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
+          for (int p = 0; p < nseg; ++p) acc += buf[p * pstride + j * kRows];
+          put(m0 + j0 + j, acc);
         }
         named_bar_sync(1, kEpiWarps * 32);          // buffer free before the next pass
       }

@@ -38,10 +38,19 @@ struct Plan {
   int mode, M, N, K;
   int bn, U, T, G;
   int tiles, chunks;
-  int grid, stream_k, stages, smem_bytes;
+  int grid, stream_k;
+  int stages;                    // weight ring depth (packed chunks)
+  int xstages;                   // activation ring depth (blocks of xblock chunks)
+  int xblock;                    // chunks per activation block (one tensor copy)
+  int smem_bytes;
   float grid_per_chunk;          // grid / chunks, to estimate a chunk's owner
   size_t ws_counters, ws_partials, ws_act, ws_bytes, ws_zero;
   int begin[kMaxGrid + 1];       // stream-K: first chunk of each CTA (begin[grid] = chunks)
+  // stream-K: for CTA p's first ([p][0]) and last ([p][1]) segment, when that segment
+  // is a cut tile, its contributors packed as  p_first | p_last << 8 | slot << 16
+  // (slot = partial slot of p_first; the others use 2 p'), else 0.  Lets a kernel
+  // find the partials of a cut tile without searching the begin table.
+  int cut[kMaxGrid][2];
 };
 
 struct Seg {
@@ -122,7 +131,8 @@ QW_HD size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr int kSmemLimit = 232448;        // 227 KB opt-in dynamic shared memory per CTA
 constexpr int kSmemReserve = 2048;        // barriers and bookkeeping
-constexpr int kMaxStages = 12;
+constexpr int kMaxWStages = 16;           // weight ring
+constexpr int kMaxXStages = 4;            // activation ring
 constexpr int kStreamKMaxTilesPerSm = 32;  // stream-K only below this many tiles per SM
 
 QW_HD int chunk_bytes(int mode) { return mode == 2 ? kChunkW8 : kChunkW4; }
@@ -132,18 +142,55 @@ QW_HD int chunk_bytes(int mode) { return mode == 2 ? kChunkW8 : kChunkW4; }
 constexpr int kAct8InKernelMaxBn = 64;
 QW_HD bool act8_in_kernel(int mode, int bn) { return mode == 1 && bn <= kAct8InKernelMaxBn; }
 
-// Stage = one weight chunk (aligned to 1024 B) + the bn x 128 fp16 activation tile
-// (+ a bn x 128 int8 staging slot when W4A8 widens in the kernel).
-QW_HD int stage_bytes(int mode, int bn) {
-  return (int)align_up((size_t)chunk_bytes(mode), 1024) + bn * kGroup * 2 +
-         (act8_in_kernel(mode, bn) ? bn * kGroup : 0);
+// Chunks per activation block: one tensor copy brings the activations of this many
+// consecutive K groups of a token tile, so that small token tiles (4 KB per group
+// at 16 tokens) do not pay one copy instruction per group.
+QW_HD constexpr int act_block(int bn) { return bn <= 32 ? 4 : bn <= 64 ? 2 : 1; }
+
+// Weight slot: one packed chunk (a multiple of 128 B; bulk copies need 16).
+QW_HD int wstage_bytes(int mode) { return (int)align_up((size_t)chunk_bytes(mode), 128); }
+
+// Activation slot: act_block(bn) fp16 tiles of bn x 128 (+ as many bn x 128 int8
+// staging tiles when W4A8 widens in the kernel).
+QW_HD int xstage_bytes(int mode, int bn) {
+  return act_block(bn) * (bn * kGroup * 2 + (act8_in_kernel(mode, bn) ? bn * kGroup : 0));
 }
 
-// Fill the stream-K chunk table from grid and chunks (host).
+// Ring depths: the deepest activation ring (at most kMaxXStages, or 3 for token
+// tiles up to 64 whose blocks already span several groups, at least 2) that still
+// leaves four weight slots; the weight ring takes the rest (at most kMaxWStages),
+// rounded down to an even count (half per dequant group).  Returns false when
+// even 2 + 4 slots do not fit.
+QW_HD bool ring_depths(int mode, int bn, int &xst, int &wst) {
+  const int xb = xstage_bytes(mode, bn), wb = wstage_bytes(mode);
+  for (int x = bn <= 64 ? 3 : kMaxXStages; x >= 2; --x) {
+    int w = (kSmemLimit - kSmemReserve - x * xb) / wb;
+    if (w > kMaxWStages) w = kMaxWStages;
+    w &= ~1;
+    if (w >= 4) { xst = x; wst = w; return true; }
+  }
+  return false;
+}
+
+// Fill the stream-K chunk table and the cut-tile contributors from grid and chunks (host).
 inline void fill_begin(Plan &P) {
   for (int p = 0; p <= kMaxGrid; ++p)
     P.begin[p] = (P.grid && p <= P.grid) ? (int)((long long)p * P.chunks / P.grid) : P.chunks;
   P.grid_per_chunk = P.chunks ? (float)P.grid / (float)P.chunks : 0.0f;
+  for (int p = 0; p < kMaxGrid; ++p) P.cut[p][0] = P.cut[p][1] = 0;
+  if (!P.stream_k) return;
+  for (int p = 0; p < P.grid; ++p) {
+    Seg s;
+    int last = -1;
+    for (int i = 0; segment(P, p, i, s); ++i) last = i;
+    for (int e = 0; e < 2 && last >= 0; ++e) {
+      segment(P, p, e == 0 ? 0 : last, s);
+      if (s.slot < 0) continue;
+      int pf, pl;
+      tile_contributors(P, s.tile, pf, pl);
+      P.cut[p][e] = pf | (pl << 8) | (partial_slot(P, pf, s.tile) << 16);
+    }
+  }
 }
 
 // Fill in a plan (host); returns 0, -2 (unsupported shape) or -1 (bad argument).
@@ -167,11 +214,9 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   else if (P.stream_k) P.grid = P.chunks < num_sms ? P.chunks : num_sms;
   else P.grid = P.tiles < num_sms ? P.tiles : num_sms;
   fill_begin(P);
-  const int sb = stage_bytes(mode, P.bn);
-  int st = (kSmemLimit - kSmemReserve) / sb;
-  if (st > kMaxStages) st = kMaxStages;
-  P.stages = st;
-  P.smem_bytes = st * sb + kSmemReserve;
+  P.xblock = act_block(P.bn);
+  if (!ring_depths(mode, P.bn, P.xstages, P.stages)) return -2;
+  P.smem_bytes = P.xstages * xstage_bytes(mode, P.bn) + P.stages * wstage_bytes(mode) + kSmemReserve;
   // Tile counters live in a fixed region at the start of every workspace, sized for
   // the largest stream-K plan (fewer than kStreamKMaxTilesPerSm tiles per SM), so
   // that no plan's partials or widened activations ever overlap another plan's
