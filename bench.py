@@ -21,8 +21,10 @@ parity spot check against the CPU oracle.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -51,6 +53,28 @@ def peaks():
         return d, "measured"
     except Exception:
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "qgemm_tc_kernel_proj_w4a16_m16.md")
+KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "schedule.h")
+
+
+def profiled_traffic():
+    """DRAM bytes (read + write) of one headline GEMM launch, from the committed ncu
+    summary, provided the kernel sources still hash to what was profiled; else None."""
+    try:
+        text = open(TRAFFIC_PROFILE).read()
+    except OSError:
+        return None
+    sha = re.search(r"^kernel_sources_sha256: ([0-9a-f]{64})", text, re.M)
+    nbytes = re.search(r"^dram_bytes_per_launch: (\d+)", text, re.M)
+    if not (sha and nbytes):
+        return None
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "int8_weight_quantized_int4_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return int(nbytes.group(1)) if h.hexdigest() == sha.group(1) else None
 
 
 def w4_bytes(n, k):
@@ -350,10 +374,14 @@ def run_ours(args):
             roof_bytes += alg * LAYERS * len(v)
             roof_ms += sum(v)
     achieved = roof_bytes / (roof_ms / 1e3) / 1e9
+    traffic = profiled_traffic()
     roofline = {"bound": "hbm", "kernel": "qgemm_tc_kernel (W4A16, M=1..64, K=N=5120)",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "peak_source": pk_src,
-                "traffic": None,
+                "traffic": traffic,
+                "traffic_source": ("ncu capture of one M=16 launch, DRAM read + write bytes "
+                                   "(profiles/qgemm_tc_kernel_proj_w4a16_m16.md)" if traffic is not None
+                                   else "null: kernel sources changed since the last ncu capture"),
                 "per_launch_alg_bytes": "13,516,800 B packed weights + 2MK activation + 2MN output"}
 
     # ---- parity spot check of the timed outputs (the pages' lesson: a kernel can
