@@ -172,10 +172,37 @@ QW_HD bool ring_depths(int mode, int bn, int &xst, int &wst) {
   return false;
 }
 
+// Tile-aligned split for short stream-K launches: at least 3 CTAs per tile and at
+// most this many chunks per CTA.
+constexpr int kAlignedMaxChunksPerCta = 16;
+
+QW_HD bool aligned_split(const Plan &P) {
+  return P.stream_k && P.tiles > 0 && 3LL * P.tiles <= P.grid &&
+         (long long)P.chunks <= (long long)kAlignedMaxChunksPerCta * P.grid;
+}
+
 // Fill the stream-K chunk table and the cut-tile contributors from grid and chunks (host).
+//
+// Two splits.  Long launches: CTA p takes chunks [floor(p C / grid), floor((p+1) C / grid)),
+// balanced to one chunk.  Short launches (aligned_split): every tile is cut into b or
+// b + 1 equal pieces (b = grid / tiles, the pieces summing to grid) and each CTA takes
+// exactly one piece, tiles with the larger pieces first.  A CTA then holds a single
+// segment, all contributors of a tile finish together, and the CTAs with the highest
+// index -- the last to become resident when a launch follows another (they wait for the
+// preceding kernel's slowest CTAs to leave their SM) -- get the smaller pieces.
 inline void fill_begin(Plan &P) {
-  for (int p = 0; p <= kMaxGrid; ++p)
-    P.begin[p] = (P.grid && p <= P.grid) ? (int)((long long)p * P.chunks / P.grid) : P.chunks;
+  if (aligned_split(P)) {
+    const int b = P.grid / P.tiles, big = P.tiles - P.grid % P.tiles;   // tiles cut into b pieces
+    int p = 0;
+    for (int t = 0; t < P.tiles; ++t) {
+      const int k = t < big ? b : b + 1;
+      for (int j = 0; j < k; ++j) P.begin[p++] = t * P.G + (j * P.G) / k;
+    }
+    for (; p <= kMaxGrid; ++p) P.begin[p] = P.chunks;
+  } else {
+    for (int p = 0; p <= kMaxGrid; ++p)
+      P.begin[p] = (P.grid && p <= P.grid) ? (int)((long long)p * P.chunks / P.grid) : P.chunks;
+  }
   P.grid_per_chunk = P.chunks ? (float)P.grid / (float)P.chunks : 0.0f;
   for (int p = 0; p < kMaxGrid; ++p) P.cut[p][0] = P.cut[p][1] = 0;
   if (!P.stream_k) return;

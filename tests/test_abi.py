@@ -141,8 +141,41 @@ def test_schedule_covers_every_chunk_once(mode, M, N, K, sms):
     load = {}
     for (tile, g), cta in seen.items():
         load[cta] = load.get(cta, 0) + 1
-    if p.stream_k:
+    aligned = p.stream_k and 3 * p.tiles <= p.grid and p.chunks <= 16 * p.grid
+    if p.stream_k and not aligned:
         assert max(load.values()) - min(load.values()) <= 1
+    if aligned:                                   # one piece per CTA: G/b or G/(b+1) groups
+        b = p.grid // p.tiles
+        assert max(load.values()) <= -(-p.groups // b) and min(load.values()) >= p.groups // (b + 1)
+
+
+def test_schedule_tile_aligned_split_for_short_launches():
+    """Projection-sized stream-K launches (>= 3 CTAs per tile, <= 16 chunks per CTA) cut
+    every tile into b or b+1 equal pieces, one piece per CTA, larger pieces first."""
+    for mode, M in ((0, 1), (1, 16), (0, 64)):
+        p = q.plan(mode, M, 5120, 5120, 152)
+        assert p.stream_k == 1 and p.tiles == 40 and p.grid == 152
+        pieces = {}
+        for cta in range(p.grid):
+            segs = q.plan_segments(p, cta)
+            assert len(segs) == 1, "one segment per CTA"
+            tile, g0, g1, slot = segs[0]
+            pieces.setdefault(tile, []).append((cta, g1 - g0))
+        counts = [len(pieces[t]) for t in range(p.tiles)]
+        assert sorted(set(counts)) == [3, 4] and sum(counts) == p.grid
+        assert counts == sorted(counts), "tiles with larger pieces come first"
+        for t, ps in pieces.items():
+            sizes = [n for _, n in ps]
+            assert sum(sizes) == p.groups and max(sizes) - min(sizes) <= 1
+            ctas = [c for c, _ in ps]
+            assert ctas == list(range(ctas[0], ctas[0] + len(ctas))), "contributors are consecutive"
+
+
+def test_schedule_long_launches_stay_balanced():
+    """Longer stream-K launches keep the chunk-balanced split (within one chunk)."""
+    p = q.plan(1, 64, 5120, 17408, 152)          # FFN down: 35.8 chunks per CTA
+    sizes = [sum(g1 - g0 for _, g0, g1, _ in q.plan_segments(p, c)) for c in range(p.grid)]
+    assert max(sizes) - min(sizes) <= 1
 
 
 def test_schedule_whole_tiles_for_prefill():
