@@ -449,6 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 #pragma unroll
       for (int q = 0; q < kIssuers; ++q) valid[q] = nch >= kIssuers || ((q - cidx) & (kIssuers - 1)) < nch;
       cidx += nch;
+      if constexpr (TOKSCALE) {
+        // token scales of this tile into L1 while the accumulator is being produced
+        int u_, t_;
+        tile_coords(P, sg.tile, u_, t_);
+        for (int m = u_ * BN + row; m < P.M && m < (u_ + 1) * BN; m += kRows) prefetch_l1(a.xs + m);
+      }
       mbar_wait(accfull_bar(b), (i / kNAcc) & 1, abort_flag, a.err);
       named_bar_sync(1, kEpiWarps * 32);           // all four warps decide together
       if (*abort_flag) { aborted = true; break; }
@@ -482,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
               part[(cc + j) * kRows + row] = acc;
             } else {
               const int m = m0 + cc + j;
-              const float val = TOKSCALE ? acc * a.xs[m] : acc;
+              const float val = TOKSCALE ? acc * __ldg(a.xs + m) : acc;
               a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
             }
           }
@@ -529,9 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       const int mv = P.M - m0 < BN ? P.M - m0 : BN;
       const int nseg = pl - pf + 1;
       auto put = [&](int m, float acc) {
-        const float val = TOKSCALE ? acc * a.xs[m] : acc;
+        const float val = TOKSCALE ? acc * __ldg(a.xs + m) : acc;
         a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
       };
+      if constexpr (TOKSCALE)          // warm L1 with this tile's token scales
+        for (int m = m0 + row; m < m0 + mv; m += kRows) prefetch_l1(a.xs + m);
       if (mv <= 4) {
         // the atomic's acquire (thread 0) and the named barrier order these reads
         // after every contributor's release; .cg reads bypass L1.  Eight

@@ -123,6 +123,12 @@ __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
 }
 
 // Warm L2 with `bytes` (multiple of 16) starting at `src`; no shared memory, no completion.
+// Bring the line holding `p` into L1 (no result; used to warm small tables ahead of
+// a dependent chain of reads).
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
