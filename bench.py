@@ -77,6 +77,14 @@ def profiled_traffic():
     return int(nbytes.group(1)) if h.hexdigest() == sha.group(1) else None
 
 
+def w4a8_kernels(M, N, K):
+    """Kernels one qgemm_w4a8_fused call launches: 1 when the quantizer runs inside
+    the GEMM, else quantizer + GEMM (+ the int8 -> fp16 widening pass above 64 tokens)."""
+    import int8_weight_quantized_int4_gb300 as q
+    p = q.plan(q.MODE_W4A8_FUSED, M, N, K, torch.cuda.get_device_properties(0).multi_processor_count)
+    return 1 if p.fused else (2 if p.bn <= 64 else 3)
+
+
 def w4_bytes(n, k):
     return n * k // 2 + 2 * n * (k // 128)
 
@@ -269,11 +277,9 @@ def run_ours(args):
          for M in MS}
     Y16 = {M: torch.empty((LAYERS, M, N), dtype=torch.float16, device=dev) for M in MS}
     Y8 = {M: torch.empty((LAYERS, M, N), dtype=torch.float16, device=dev) for M in MS}
-    XQ = {M: torch.empty((LAYERS, M, K), dtype=torch.int8, device=dev) for M in MS}
-    XS = {M: torch.empty((LAYERS, M), dtype=torch.float32, device=dev) for M in MS}
     wsp = q.Workspace(dev)
     for M in MS:
-        for mode in (q.MODE_W4A16, q.MODE_W4A8):
+        for mode in (q.MODE_W4A16, q.MODE_W4A8_FUSED):
             wsp.get(mode, M, N, K)
     torch.cuda.synchronize()
 
@@ -284,10 +290,11 @@ def run_ours(args):
         return f
 
     def block8(M):
+        # the W4A8 layer from fp16 activations: per-token int8 quantization + GEMM
+        # (one kernel for small batches, the quantizer then the GEMM otherwise)
         def f():
             for r in range(LAYERS):
-                q.quant_act_int8(X[M][r], XQ[M][r], XS[M][r])
-                q.qgemm_w4a8(XQ[M][r], XS[M][r], packed[r], N, K, y=Y8[M][r], ws=wsp)
+                q.qgemm_w4a8_fused(X[M][r], packed[r], N, K, y=Y8[M][r], ws=wsp)
         return f
 
     # The same step with the library default (every kernel waits for its predecessor
@@ -369,7 +376,7 @@ def run_ours(args):
             "us_per_layer": round(us, 3), "weight_GBps": round(w4_bytes(N, K) / us / 1e3, 1),
             "TFLOPS": round(flops / us / 1e6, 2), "alg_GBps": round(alg / us / 1e3, 1),
             "frac_hbm": round(alg / us / 1e3 / hbm, 4),
-            "kernels_per_layer": 1 if mode == "w4a16" else 3}
+            "kernels_per_layer": 1 if mode == "w4a16" else w4a8_kernels(M, N, K)}
         if mode == "w4a16":
             roof_bytes += alg * LAYERS * len(v)
             roof_ms += sum(v)
@@ -490,15 +497,13 @@ def extras(q, dev, stream, pk, pk_src):
         pkd = q.qpack_w4(prob.codes.to(dev), prob.scales.to(dev))
         copies = [pkd] + [pkd.clone() for _ in range(3)]
         x = prob.x.to(dev)
-        xq, xs = q.quant_act_int8(x)
         y = torch.empty((64, prob.N), dtype=torch.float16, device=dev)
         wsp = q.Workspace(dev)
-        wsp.get(q.MODE_W4A8, 64, prob.N, prob.K)
+        wsp.get(q.MODE_W4A8_FUSED, 64, prob.N, prob.K)
 
         def f():
             for c in copies:
-                q.quant_act_int8(x, xq, xs)
-                q.qgemm_w4a8(xq, xs, c, prob.N, prob.K, y=y, ws=wsp)
+                q.qgemm_w4a8_fused(x, c, prob.N, prob.K, y=y, ws=wsp)
         ms = timeit(f, 20) / len(copies)
         wb = w4_bytes(prob.N, prob.K)
         cols = np.arange(0, prob.N, max(1, prob.N // 512))
@@ -508,7 +513,7 @@ def extras(q, dev, stream, pk, pk_src):
         out[name] = {"us": round(ms * 1e3, 2), "weight_GBps": round(wb / ms / 1e6, 1),
                      "TOPS": round(2 * 64 * prob.N * prob.K / ms / 1e9, 2),
                      "frac_hbm": round((wb + 64 * prob.K + 256 + 128 * prob.N) / ms / 1e6 / hbm, 4),
-                     "kernels": 3, "parity": parity_err(y.cpu()[:, cols], ref)}
+                     "kernels": w4a8_kernels(64, prob.N, prob.K), "parity": parity_err(y.cpu()[:, cols], ref)}
         del copies, pkd
 
     # prefill M=8192, W4A16 and W4A8 on identical weights
@@ -516,9 +521,8 @@ def extras(q, dev, stream, pk, pk_src):
     pkd = q.qpack_w4(pp.codes.to(dev), pp.scales.to(dev))
     x = pp.x.to(dev)
     y = torch.empty((8192, pp.N), dtype=torch.float16, device=dev)
-    xq, xs = q.quant_act_int8(x)
     wsp = q.Workspace(dev)
-    wsp.get(q.MODE_W4A8, 8192, pp.N, pp.K)
+    wsp.get(q.MODE_W4A8_FUSED, 8192, pp.N, pp.K)
     flops = 2.0 * 8192 * pp.N * pp.K
     rows = np.arange(0, 8192, 61)
     cols = np.arange(0, pp.N, 211)
@@ -526,9 +530,7 @@ def extras(q, dev, stream, pk, pk_src):
         if mode == "w4a16":
             f = lambda: q.qgemm_w4a16(x, pkd, pp.N, pp.K, y=y, ws=wsp)  # noqa: E731
         else:
-            def f():
-                q.quant_act_int8(x, xq, xs)
-                q.qgemm_w4a8(xq, xs, pkd, pp.N, pp.K, y=y, ws=wsp)
+            f = lambda: q.qgemm_w4a8_fused(x, pkd, pp.N, pp.K, y=y, ws=wsp)  # noqa: E731
         ms = timeit(f, 5)
         xr = pp.x.numpy()[rows]
         if mode == "w4a16":
@@ -541,7 +543,7 @@ def extras(q, dev, stream, pk, pk_src):
             "ms": round(ms, 3), "TFLOPS": round(tf, 1), "frac_f16_peak": round(tf / peak16, 4),
             "f16_peak_TFLOPS": peak16, "peak_source": pk_src + " (bf16 sustained; fp16 dense rate is the same)",
             "int8_peak": None, "parity": parity_err(y.cpu().numpy()[rows][:, cols], ref)}
-    del pkd, x, y, xq, xs, wsp
+    del pkd, x, y, wsp
     torch.cuda.empty_cache()
 
     # lm_head W8A16: 248,320 x 5120 int8 (1.29 GB > L2)
@@ -572,6 +574,7 @@ NCU_CASES = {
     "proj_w4a16_m16": ("w4a16", 16, 5120, 5120, 4),
     "proj_w4a16_m64": ("w4a16", 64, 5120, 5120, 4),
     "proj_w4a8_m16": ("w4a8", 16, 5120, 5120, 4),
+    "proj_w4a8_fused_m4": ("w4a8f", 4, 5120, 5120, 4),
     "ffn_up_w4a8_m64": ("w4a8", 64, 34816, 5120, 4),
     "lm_head_w8a16_m16": ("w8a16", 16, 248320, 5120, 8),
     "prefill_w4a16_m2048": ("w4a16", 2048, 34816, 5120, 4),
@@ -594,6 +597,8 @@ def run_ncu_case(name):
     if mode == "w4a8":
         xq, xs = q.quant_act_int8(x)
         fn = lambda: q.qgemm_w4a8(xq, xs, packed, N, K, ws=ws)  # noqa: E731
+    elif mode == "w4a8f":
+        fn = lambda: q.qgemm_w4a8_fused(x, packed, N, K, ws=ws)  # noqa: E731
     elif mode == "w8a16":
         fn = lambda: q.qgemm_w8a16(x, packed, N, K, ws=ws)  # noqa: E731
     else:

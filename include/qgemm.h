@@ -57,7 +57,7 @@ enum {
     QW_ERR_BAD_CODES = -8           /* (device) qpack_w4 saw a code outside [-8, 7] */
 };
 
-enum { QW_MODE_W4A16 = 0, QW_MODE_W4A8 = 1, QW_MODE_W8A16 = 2 };
+enum { QW_MODE_W4A16 = 0, QW_MODE_W4A8 = 1, QW_MODE_W8A16 = 2, QW_MODE_W4A8_FUSED = 3 };
 
 /* ------------------------------------------------------------------------
  * Weight packing (load time, not on the hot path).
@@ -147,6 +147,21 @@ int qgemm_w8a16(const uint16_t *x, const void *packed_w8, int M, int N, int K, u
                 void *ws, size_t ws_bytes, qw_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * qgemm_w4a8_fused -- the W4A8 layer from fp16 activations: y is bit-identical
+ * to quant_act_int8(x) followed by qgemm_w4a8 on the same weights ("In full"
+ * item 4: activations quantized to int8 per token, int4 weights).
+ *   x [M, K] fp16, device, 16-byte aligned.  Other arguments as qgemm_w4a16;
+ *   the workspace is qgemm_workspace_bytes(QW_MODE_W4A8_FUSED, M, N, K).
+ * When M <= 16 and the M fp16 rows take at most 48 KB (M*K*2 bytes), one kernel
+ * copies the rows into shared memory, computes the token scales and quantizes
+ * there, so no int8 activations are written; otherwise the quantizer writes its
+ * codes and scales into the workspace and the W4A8 GEMM follows.  Async.
+ * Returns as qgemm_w4a8.
+ * ------------------------------------------------------------------------ */
+int qgemm_w4a8_fused(const uint16_t *x, const void *packed_w4, int M, int N, int K, uint16_t *y,
+                     void *ws, size_t ws_bytes, qw_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * qgemm_w4a16_noalloc -- qgemm_w4a16 for callers that cannot allocate device
  * memory (for instance a plugin inside a host runtime that owns every device
  * allocation and gives its kernels only input and output buffers, or a decode
@@ -223,6 +238,7 @@ typedef struct {
     size_t ws_zero_bytes;   /* leading workspace bytes that must be zero */
     int act_stages;         /* activation ring depth in shared memory (blocks) */
     int act_block;          /* K groups per activation block (one tensor copy) */
+    int fused;              /* QW_MODE_W4A8_FUSED: 1 when the quantizer runs inside the GEMM */
 } qw_plan_t;
 
 int qw_plan(int mode, int M, int N, int K, int num_sms, qw_plan_t *out);

@@ -7,6 +7,7 @@ Entry points (same names as the C ABI):
     qpack_w4(codes, scales) -> packed        qpack_w8(codes, scales) -> packed
     quant_act_int8(x) -> (xq, xs)
     qgemm_w4a16(x, packed, N, K) -> y        qgemm_w4a8(xq, xs, packed, N, K) -> y
+    qgemm_w4a8_fused(x, packed, N, K) -> y
     qgemm_w8a16(x, packed, N, K) -> y
 """
 from __future__ import annotations
@@ -29,7 +30,7 @@ QW_ERR_ARCH = -5
 QW_ERR_CUDA = -6
 QW_ERR_TIMEOUT = -7
 QW_ERR_BAD_CODES = -8
-MODE_W4A16, MODE_W4A8, MODE_W8A16 = 0, 1, 2
+MODE_W4A16, MODE_W4A8, MODE_W8A16, MODE_W4A8_FUSED = 0, 1, 2, 3
 
 # every function the header declares: name -> (restype, argtypes)
 _p, _i, _sz, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
@@ -39,7 +40,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("bn", _i), ("token_tiles", _i), ("row_tiles", _i), ("groups", _i),
                 ("tiles", _ll), ("chunks", _ll), ("grid", _i), ("stream_k", _i), ("stages", _i),
                 ("smem_bytes", _i), ("ws_bytes", _sz), ("ws_zero_bytes", _sz),
-                ("act_stages", _i), ("act_block", _i)]
+                ("act_stages", _i), ("act_block", _i), ("fused", _i)]
 
 
 SIGNATURES = {
@@ -52,6 +53,7 @@ SIGNATURES = {
     "qgemm_workspace_zero_bytes": (_sz, [_i, _i, _i, _i]),
     "qgemm_w4a16": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "qgemm_w4a8": (_i, [_p, _p, _p, _i, _i, _i, _p, _p, _sz, _p]),
+    "qgemm_w4a8_fused": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "qgemm_w8a16": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "qgemm_w4a16_noalloc": (_i, [_p, _p, _i, _i, _i, _p, _p]),
     "qw_last_error_string": (ctypes.c_char_p, []),
@@ -228,6 +230,21 @@ def qgemm_w4a8(xq, xs, packed, N: int, K: int, y=None, ws: Workspace | None = No
     with torch.cuda.device(xq.device):
         _check(lib().qgemm_w4a8(_ptr(xq), _ptr(xs), _ptr(packed), M, N, K, _ptr(y), _ptr(wbuf),
                                 wbytes, _stream(xq)))
+    return y
+
+
+def qgemm_w4a8_fused(x, packed, N: int, K: int, y=None, ws: Workspace | None = None):
+    """The W4A8 layer from fp16 activations: bit-identical to qgemm_w4a8 applied to
+    quant_act_int8(x).  Small batches quantize inside the GEMM kernel."""
+    _need(x, torch.float16, "x", 2)
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("x.shape[1] != K")
+    y = _out(y, M, N, x.device)
+    wbuf, wbytes = _ws_for(x, MODE_W4A8_FUSED, M, N, K, ws)
+    with torch.cuda.device(x.device):
+        _check(lib().qgemm_w4a8_fused(_ptr(x), _ptr(packed), M, N, K, _ptr(y), _ptr(wbuf), wbytes,
+                                      _stream(x)))
     return y
 
 

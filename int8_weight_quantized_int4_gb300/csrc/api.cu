@@ -157,7 +157,7 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
     return fail(QW_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", P.ws_bytes,
                 ws ? ws_bytes : (size_t)0);
   uint8_t *w = static_cast<uint8_t *>(ws);
-  qw::GemmArgs a;
+  qw::GemmArgs a{};
   a.P = P;
   a.xs = xs;
   a.wpack = static_cast<const uint8_t *>(packed);
@@ -168,6 +168,22 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
   a.early_weights = g_opt_weights_immutable.load(std::memory_order_relaxed);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (mode == QW_MODE_W4A8_FUSED && P.fused) {
+    a.xf16 = static_cast<const uint16_t *>(act);
+    e = qw::launch_gemm_w4a8_fused(a, st);
+    if (e != cudaSuccess) return fail_cuda(e, "GEMM kernel launch");
+    return QW_OK;
+  }
+  if (mode == QW_MODE_W4A8_FUSED) {
+    // the standalone quantizer into the workspace, then the W4A8 GEMM (plan mode 1)
+    int8_t *q = reinterpret_cast<int8_t *>(w + P.ws_counters + P.ws_partials + P.ws_act);
+    float *s = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(q) + qw::align_up((size_t)M * K, 256));
+    e = qw::launch_quant_act(static_cast<const uint16_t *>(act), M, K, q, s, st);
+    if (e != cudaSuccess) return fail_cuda(e, "quant kernel launch");
+    act = q;
+    a.xs = s;
+    mode = QW_MODE_W4A8;
+  }
   if (mode == QW_MODE_W4A8 && qw::act8_in_kernel(mode, P.bn)) {
     if ((rc = encode_act_map(&a.tmap, act, M, K, P.bn, P.xblock, true))) return rc;
     e = qw::launch_gemm_w4a8(a, st);
@@ -292,6 +308,11 @@ int qgemm_w4a8(const int8_t *xq, const float *xs, const void *packed_w4, int M, 
   return gemm_common(QW_MODE_W4A8, xq, xs, packed_w4, M, N, K, y, ws, ws_bytes, stream);
 }
 
+int qgemm_w4a8_fused(const uint16_t *x, const void *packed_w4, int M, int N, int K, uint16_t *y,
+                     void *ws, size_t ws_bytes, qw_stream_t stream) {
+  return gemm_common(QW_MODE_W4A8_FUSED, x, nullptr, packed_w4, M, N, K, y, ws, ws_bytes, stream);
+}
+
 int qgemm_w8a16(const uint16_t *x, const void *packed_w8, int M, int N, int K, uint16_t *y, void *ws,
                 size_t ws_bytes, qw_stream_t stream) {
   return gemm_common(QW_MODE_W8A16, x, nullptr, packed_w8, M, N, K, y, ws, ws_bytes, stream);
@@ -348,6 +369,7 @@ int qw_plan(int mode, int M, int N, int K, int num_sms, qw_plan_t *out) {
   out->ws_zero_bytes = P.ws_zero;
   out->act_stages = P.xstages;
   out->act_block = P.xblock;
+  out->fused = P.fused;
   return QW_OK;
 }
 

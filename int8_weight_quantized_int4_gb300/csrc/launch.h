@@ -14,6 +14,7 @@ struct GemmArgs {
                             // int8 [M,K] (128 x bn boxes) for W4A8 at decode sizes
   Plan P;
   const float *xs;          // token scales [M] (W4A8) or nullptr
+  const uint16_t *xf16;     // fused W4A8: fp16 activations [M,K], quantized in the kernel
   const uint8_t *wpack;     // packed weights
   uint16_t *y;              // fp16 [M,N]
   int *counters;            // [tiles] arrival counters (stream-K)
@@ -58,6 +59,7 @@ cudaError_t launch_pack_w8(const int8_t *codes, const uint16_t *scales, int N, i
 
 cudaError_t launch_gemm_w4a16(const GemmArgs &a, cudaStream_t st);
 cudaError_t launch_gemm_w4a8(const GemmArgs &a, cudaStream_t st);
+cudaError_t launch_gemm_w4a8_fused(const GemmArgs &a, cudaStream_t st);
 cudaError_t launch_gemm_w8a16(const GemmArgs &a, cudaStream_t st);
 
 }  // namespace qw

@@ -43,8 +43,10 @@ struct Plan {
   int xstages;                   // activation ring depth (blocks of xblock chunks)
   int xblock;                    // chunks per activation block (one tensor copy)
   int smem_bytes;
+  int fused;                     // W4A8 with the per-token quantizer inside the GEMM
+  int rows_bytes;                // fused: shared-memory copy of the M fp16 rows
   float grid_per_chunk;          // grid / chunks, to estimate a chunk's owner
-  size_t ws_counters, ws_partials, ws_act, ws_bytes, ws_zero;
+  size_t ws_counters, ws_partials, ws_act, ws_quant, ws_bytes, ws_zero;
   int begin[kMaxGrid + 1];       // stream-K: first chunk of each CTA (begin[grid] = chunks)
   // stream-K: for CTA p's first ([p][0]) and last ([p][1]) segment, when that segment
   // is a cut tile, its contributors packed as  p_first | p_last << 8 | slot << 16
@@ -137,6 +139,16 @@ constexpr int kStreamKMaxTilesPerSm = 32;  // stream-K only below this many tile
 
 QW_HD int chunk_bytes(int mode) { return mode == 2 ? kChunkW8 : kChunkW4; }
 
+// Modes (as in the C ABI): 0 W4A16, 1 W4A8, 2 W8A16, 3 W4A8 from fp16 activations
+// (quantized per token by the library).  Mode 3 quantizes inside the GEMM when the
+// fp16 rows fit in shared memory next to the pipeline (at most kFusedRowsMax bytes,
+// token tiles of 16); otherwise it runs the standalone quantizer into the workspace
+// and then the mode-1 GEMM.
+constexpr int kFusedRowsMax = 48 * 1024;
+QW_HD bool quant_in_kernel(int mode, int M, int K) {
+  return mode == 3 && M >= 1 && M <= 16 && (long long)M * K * 2 <= kFusedRowsMax;
+}
+
 // W4A8 widens int8 activation codes to fp16 inside the GEMM (through a staging
 // slot) for token tiles up to this size; larger tiles use a separate widening pass.
 constexpr int kAct8InKernelMaxBn = 64;
@@ -161,10 +173,10 @@ QW_HD int xstage_bytes(int mode, int bn) {
 // leaves four weight slots; the weight ring takes the rest (at most kMaxWStages),
 // rounded down to an even count (half per dequant group).  Returns false when
 // even 2 + 4 slots do not fit.
-QW_HD bool ring_depths(int mode, int bn, int &xst, int &wst) {
+QW_HD bool ring_depths(int mode, int bn, int &xst, int &wst, int extra = 0) {
   const int xb = xstage_bytes(mode, bn), wb = wstage_bytes(mode);
   for (int x = bn <= 64 ? 3 : kMaxXStages; x >= 2; --x) {
-    int w = (kSmemLimit - kSmemReserve - x * xb) / wb;
+    int w = (kSmemLimit - kSmemReserve - extra - x * xb) / wb;
     if (w > kMaxWStages) w = kMaxWStages;
     w &= ~1;
     if (w >= 4) { xst = x; wst = w; return true; }
@@ -222,9 +234,14 @@ inline void fill_begin(Plan &P) {
 
 // Fill in a plan (host); returns 0, -2 (unsupported shape) or -1 (bad argument).
 inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
-  if (mode < 0 || mode > 2 || M < 0 || N < 0 || K < 0 || num_sms < 1) return -1;
+  if (mode < 0 || mode > 3 || M < 0 || N < 0 || K < 0 || num_sms < 1) return -1;
   if (N % kRows || K % kGroup) return -2;
   if (num_sms > kMaxGrid) num_sms = kMaxGrid;
+  P.fused = quant_in_kernel(mode, M, K) ? 1 : 0;
+  P.rows_bytes = P.fused ? (int)align_up((size_t)M * K * 2, 1024) : 0;
+  // mode 3 outside the fused range is the quantizer followed by a mode-1 plan
+  const bool quant_first = mode == 3 && !P.fused;
+  if (quant_first) mode = 1;
   P.mode = mode; P.M = M; P.N = N; P.K = K;
   P.bn = pick_bn(M);
   P.U = (M + P.bn - 1) / P.bn;
@@ -242,8 +259,9 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   else P.grid = P.tiles < num_sms ? P.tiles : num_sms;
   fill_begin(P);
   P.xblock = act_block(P.bn);
-  if (!ring_depths(mode, P.bn, P.xstages, P.stages)) return -2;
-  P.smem_bytes = P.xstages * xstage_bytes(mode, P.bn) + P.stages * wstage_bytes(mode) + kSmemReserve;
+  if (!ring_depths(mode, P.bn, P.xstages, P.stages, P.rows_bytes)) return -2;
+  P.smem_bytes = P.xstages * xstage_bytes(mode, P.bn) + P.stages * wstage_bytes(mode) + P.rows_bytes +
+                 kSmemReserve;
   // Tile counters live in a fixed region at the start of every workspace, sized for
   // the largest stream-K plan (fewer than kStreamKMaxTilesPerSm tiles per SM), so
   // that no plan's partials or widened activations ever overlap another plan's
@@ -251,8 +269,10 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   P.ws_counters = align_up((size_t)kStreamKMaxTilesPerSm * num_sms * 4, 256);
   P.ws_partials = P.stream_k ? (size_t)2 * P.grid * P.bn * kRows * 4 : 0;
   P.ws_act = (mode == 1 && !act8_in_kernel(mode, P.bn)) ? align_up((size_t)M * K * 2, 256) : 0;
+  // quantizer output (int8 codes, then binary32 token scales) when it runs first
+  P.ws_quant = quant_first ? align_up((size_t)M * K, 256) + align_up((size_t)M * 4, 256) : 0;
   P.ws_zero = P.ws_counters;
-  P.ws_bytes = P.ws_counters + P.ws_partials + P.ws_act;
+  P.ws_bytes = P.ws_counters + P.ws_partials + P.ws_act + P.ws_quant;
   return 0;
 }
 

@@ -292,6 +292,76 @@ def test_signed_scales_sign_fold_equivalence(q):
     assert torch.equal(ya.cpu().view(torch.int16), yb.cpu().view(torch.int16))
 
 
+# ------------------------------------------------ W4A8 with the fused quantizer --
+
+@pytest.mark.parametrize("M,N,K", [(1, 5120, 5120), (2, 640, 5120), (3, 384, 1280), (4, 5120, 5120),
+                                   (7, 256, 3072), (16, 640, 640), (5, 640, 5120), (16, 5120, 5120),
+                                   (17, 640, 640), (64, 640, 1024)])
+def test_w4a8_fused_bit_identical_to_two_step(q, M, N, K):
+    """qgemm_w4a8_fused(x) equals qgemm_w4a8(quant_act_int8(x)) bit for bit -- inside
+    one kernel (M <= 16 and M*K*2 <= 48 KB) and through the quantizer-then-GEMM
+    path -- and meets the tolerance against the oracle."""
+    p = synth.make_problem(M, N, K, seed=11 + M, outlier_frac=0.01)
+    x = _special_rows(p.x) if M >= 4 else p.x
+    xd = x.to(DEV)
+    packed = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
+    xq, xs = q.quant_act_int8(xd)
+    y2 = q.qgemm_w4a8(xq, xs, packed, N, K)
+    y1 = q.qgemm_w4a8_fused(xd, packed, N, K)
+    torch.cuda.synchronize()
+    assert q.device_error() == 0
+    pl = q.plan(q.MODE_W4A8_FUSED, M, N, K, torch.cuda.get_device_properties(DEV).multi_processor_count)
+    assert pl.fused == (1 if (M <= 16 and M * K * 2 <= 48 * 1024) else 0)
+    assert np.array_equal(bits(y1), bits(y2))
+    oq, os_ = oracle.quant_act_int8(x.numpy())
+    assert nerr(y1, oracle.w4a8(oq, os_, p.codes, p.scales)) <= TOL
+
+
+def test_w4a8_fused_quantizer_near_ties(q):
+    """Quotients x / s a few 2^-12 from half-integers, with scales that are not powers of
+    two: through identity weights (y[m,n] = s_m * q[m,n]) every code the fused kernel
+    produces shows in y, which must equal the two-step path bit for bit."""
+    M, N, K = 4, 1280, 1280
+    rng = np.random.default_rng(5)
+    x = np.zeros((M, K), np.float16)
+    for m, amax in enumerate((100.0, 3.3, 0.0173, 55.5)):
+        s = np.float64(np.float16(amax)) / 127.0
+        n = rng.integers(-127, 127, K)
+        delta = rng.integers(-3, 4, K) * 2.0 ** -12
+        x[m] = ((n + 0.5 + delta) * s).astype(np.float16)
+        x[m, 0] = np.float16(amax)
+    codes = torch.zeros((N, K), dtype=torch.int8)
+    codes[torch.arange(N), torch.arange(N)] = 1
+    scales = torch.ones((N, K // 128), dtype=torch.float16)
+    packed = q.qpack_w4(codes.to(DEV), scales.to(DEV))
+    xd = torch.from_numpy(x).to(DEV)
+    xq, xs = q.quant_act_int8(xd)
+    y2 = q.qgemm_w4a8(xq, xs, packed, N, K)
+    y1 = q.qgemm_w4a8_fused(xd, packed, N, K)
+    torch.cuda.synchronize()
+    assert q.device_error() == 0
+    assert np.array_equal(bits(y1), bits(y2))
+    oq, os_ = oracle.quant_act_int8(x)
+    assert np.array_equal(xq.cpu().numpy(), oq)
+    expect = (oq.astype(np.float64) * os_.astype(np.float64)[:, None]).astype(np.float16)
+    assert nerr(y1, expect) <= 1e-3
+
+
+def test_w4a8_fused_workspace_and_empty(q):
+    """The fused entry leaves the workspace's zero region zero and accepts M = 0."""
+    p = synth.projection(4)
+    packed = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
+    zero = int(q.lib().qgemm_workspace_zero_bytes(q.MODE_W4A8_FUSED, 4, 5120, 5120))
+    ws = q.Workspace(DEV)
+    for _ in range(3):
+        q.qgemm_w4a8_fused(p.x.to(DEV), packed, p.N, p.K, ws=ws)
+    torch.cuda.synchronize()
+    assert q.device_error() == 0
+    assert int(ws.buf[:zero].count_nonzero()) == 0
+    y = q.qgemm_w4a8_fused(torch.empty((0, 5120), dtype=torch.float16, device=DEV), packed, p.N, p.K)
+    assert tuple(y.shape) == (0, 5120)
+
+
 def test_workspace_contract(q):
     p = synth.projection(4)
     packed = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
