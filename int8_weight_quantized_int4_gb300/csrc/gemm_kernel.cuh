@@ -260,29 +260,43 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   auto w_smem = [&](int s) { return wbase + (uint32_t)s * kWStage; };
   auto x_smem = [&](int s) { return sbase + (uint32_t)s * kXStage; };
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < SW; ++s) {
-      mbar_init(wfull_bar(s), 1);
-      mbar_init(wempty_bar(s), kDeqGroupWarps);
+  // Warm the constant cache with this CTA's schedule entries (read by every role's
+  // first segment() call), so that the miss overlaps the set-up below.
+  if (threadIdx.x == 64) {
+    const int warm = P.begin[cta] + P.begin[cta + 1] + P.cut[cta][0] + P.cut[cta][1];
+    asm volatile("" ::"r"(warm));
+  }
+  // Barrier set-up spread over two warps (lane l initializes the l-th barrier of
+  // each ring), each initializing thread fencing its own inits.
+  if (threadIdx.x >= 32 && threadIdx.x < 64) {
+    const int l = threadIdx.x - 32;
+    if (l < SW) {
+      mbar_init(wfull_bar(l), 1);
+      mbar_init(wempty_bar(l), kDeqGroupWarps);
     }
-    for (int s = 0; s < SX; ++s) {
-      mbar_init(xfull_bar(s), 1);
-      mbar_init(xempty_bar(s), kIssuers);
-      mbar_init(bfull_bar(s), QIN ? 1 : kWidenW);
+    if (l < SX) {
+      mbar_init(xfull_bar(l), 1);
+      mbar_init(xempty_bar(l), kIssuers);
+      mbar_init(bfull_bar(l), QIN ? 1 : kWidenW);
     }
-    for (int i = 0; i < kAStages; ++i) {
-      mbar_init(afull_bar(i), kDeqGroupWarps);
-      mbar_init(aempty_bar(i), 1);
+    fence_mbar_init();
+  } else if (threadIdx.x >= 96 && threadIdx.x < 128) {
+    const int l = threadIdx.x - 96;
+    if (l < kAStages) {
+      mbar_init(afull_bar(l), kDeqGroupWarps);
+      mbar_init(aempty_bar(l), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(accfull_bar(i), kIssuers);
-      mbar_init(accempty_bar(i), kEpiWarps);
+    if (l < 2) {
+      mbar_init(accfull_bar(l), kIssuers);
+      mbar_init(accempty_bar(l), kEpiWarps);
     }
-    mbar_init(bars + kBarRed, 1);
-    mbar_init(bars + kBarRows, 1);
-    mbar_init(bars + kBarScales, 1);
-    *abort_flag = 0;
-    *bcast = 0;
+    if (l == 2) mbar_init(bars + kBarRed, 1);
+    if (l == 3) mbar_init(bars + kBarRows, 1);
+    if (l == 4) mbar_init(bars + kBarScales, 1);
+    if (l == 5) {
+      *abort_flag = 0;
+      *bcast = 0;
+    }
     fence_mbar_init();
   }
   if (!QIN && warp == kWarpAct && lane == 0) prefetch_tensormap(&a.tmap);
