@@ -169,13 +169,14 @@ QW_HD int xstage_bytes(int mode, int bn) {
 }
 
 // Ring depths: the deepest activation ring (at most kMaxXStages, or 3 for token
-// tiles up to 64 whose blocks already span several groups, at least 2) that still
+// tiles up to 64 whose blocks already span several groups -- except the fused W4A8
+// mode, whose quantized blocks are all written up front -- at least 2) that still
 // leaves four weight slots; the weight ring takes the rest (at most kMaxWStages),
 // rounded down to an even count (half per dequant group).  Returns false when
 // even 2 + 4 slots do not fit.
 QW_HD bool ring_depths(int mode, int bn, int &xst, int &wst, int extra = 0) {
   const int xb = xstage_bytes(mode, bn), wb = wstage_bytes(mode);
-  for (int x = bn <= 64 ? 3 : kMaxXStages; x >= 2; --x) {
+  for (int x = (bn <= 64 && mode != 3) ? 3 : kMaxXStages; x >= 2; --x) {
     int w = (kSmemLimit - kSmemReserve - extra - x * xb) / wb;
     if (w > kMaxWStages) w = kMaxWStages;
     w &= ~1;
