@@ -484,7 +484,8 @@ def run_ours(args):
 
 # ----------------------------------------------------- the other workloads --
 def extras(q, dev, stream, pk, pk_src):
-    """FFN pair (M=64, W4A8), prefill (M=8192, both modes), lm_head (W8A16).
+    """FFN pair (M=64, W4A8), prefill (M=8192, both modes), 2048-token prefill chunks on
+    the three layer shapes (both modes), lm_head (W8A16).
     Each timed with CUDA events on graph replays, with a parity spot check."""
     import oracle
     hbm = float(pk["hbm_gbs"])
@@ -552,6 +553,35 @@ def extras(q, dev, stream, pk, pk_src):
             "f16_peak_TFLOPS": peak16, "peak_source": pk_src + " (bf16 sustained; fp16 dense rate is the same)",
             "int8_peak": None, "parity": parity_err(y.cpu().numpy()[rows][:, cols], ref)}
     del pkd, x, y, wsp
+    torch.cuda.empty_cache()
+
+    # 2048-token prefill chunks (the serving stack's chunk size) on the three layer shapes
+    for name, prob in (("proj", synth.projection(2048)), ("ffn_up", synth.ffn_up(2048)),
+                       ("ffn_down", synth.ffn_down(2048))):
+        pkd = q.qpack_w4(prob.codes.to(dev), prob.scales.to(dev))
+        x = prob.x.to(dev)
+        y = torch.empty((2048, prob.N), dtype=torch.float16, device=dev)
+        wsp = q.Workspace(dev)
+        for mode in (q.MODE_W4A16, q.MODE_W4A8_FUSED):
+            wsp.get(mode, 2048, prob.N, prob.K)
+        flops = 2.0 * 2048 * prob.N * prob.K
+        rows = np.arange(0, 2048, 97)
+        cols = np.arange(0, prob.N, max(1, prob.N // 256))
+        xr = prob.x.numpy()[rows]
+        for mode in ("w4a16", "w4a8"):
+            if mode == "w4a16":
+                f = lambda: q.qgemm_w4a16(x, pkd, prob.N, prob.K, y=y, ws=wsp)  # noqa: E731
+                ref = oracle.w4a16(xr, prob.codes[cols], prob.scales[cols])
+            else:
+                f = lambda: q.qgemm_w4a8_fused(x, pkd, prob.N, prob.K, y=y, ws=wsp)  # noqa: E731
+                oq, os_ = oracle.quant_act_int8(xr)
+                ref = oracle.w4a8(oq, os_, prob.codes[cols], prob.scales[cols])
+            ms = timeit(f, 10)
+            tf = flops / ms / 1e9
+            out[f"prefill_chunk_m2048_{name}_{mode}"] = {
+                "us": round(ms * 1e3, 1), "TFLOPS": round(tf, 1), "frac_f16_peak": round(tf / peak16, 4),
+                "N": prob.N, "K": prob.K, "parity": parity_err(y.cpu().numpy()[rows][:, cols], ref)}
+        del pkd, x, y, wsp
     torch.cuda.empty_cache()
 
     # lm_head W8A16: 248,320 x 5120 int8 (1.29 GB > L2)

@@ -62,8 +62,10 @@ def _load():
             getattr(lib, name).argtypes = [p, p, p, i64, i64, i64, p]
         lib.oracle_w4a8.argtypes = [p, p, p, p, i64, i64, i64, p]
         lib.oracle_roundtrip_int8_g128.argtypes = [p, i64, i64, p, p, ctypes.POINTER(ctypes.c_double)]
+        lib.oracle_embed_w8.argtypes = [p, i64, p, p, i64, i64, p]
+        lib.oracle_topk.argtypes = [p, i64, i64, i64, p, p]
         for name in ("oracle_quant_act_int8", "oracle_w4a16", "oracle_w8a16", "oracle_w4a8",
-                     "oracle_roundtrip_int8_g128"):
+                     "oracle_roundtrip_int8_g128", "oracle_embed_w8", "oracle_topk"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -163,3 +165,27 @@ def roundtrip_int8_g128(w):
     _check(_load().oracle_roundtrip_int8_g128(_ptr(ww), N, K, _ptr(codes), _ptr(scales),
                                               ctypes.byref(err)), "roundtrip_int8_g128")
     return codes, scales.view(np.float16), float(err.value)
+
+
+def embed_w8(ids, codes, scales):
+    """Dequant-on-gather: out[t,k] = fp16(codes[ids[t],k] * scales[ids[t],k/128]).
+    ids [T] integers in [0, V), codes [V,D] int8, scales [V,D/128] f16 -> out [T,D] f16."""
+    i = _as(ids, np.int64)
+    c = _as(codes, np.int8)
+    sb = _half_bits(scales)
+    V, D = c.shape
+    assert sb.shape == (V, D // 128)
+    out = np.zeros((i.shape[0], D), np.uint16)
+    _check(_load().oracle_embed_w8(_ptr(i), i.shape[0], _ptr(c), _ptr(sb), V, D, _ptr(out)), "embed_w8")
+    return out.view(np.float16)
+
+
+def topk(logits, k: int):
+    """Per row the k largest logits, largest first, ties to the smaller index.
+    logits [M,N] f16 -> (values [M,k] f16, indices [M,k] int64)."""
+    lb = _half_bits(logits)
+    M, N = lb.shape
+    vals = np.zeros((M, k), np.uint16)
+    idx = np.zeros((M, k), np.int64)
+    _check(_load().oracle_topk(_ptr(lb), M, N, k, _ptr(vals), _ptr(idx)), "topk")
+    return vals.view(np.float16), idx

@@ -1,7 +1,8 @@
 /*
  * oracle.c -- plain, slow, obviously-correct CPU definition of the
  * weight-quantized linear layer (W4A16, W4A8, W8A16), the per-token int8
- * activation quantizer and the int8 group-128 weight round trip.
+ * activation quantizer, the int8 group-128 weight round trip, the int8
+ * group-128 embedding gather and the top-k over logits.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, calls or
  * includes this file; only the tests, the smoke check and the CPU-baseline leg
@@ -35,6 +36,7 @@
 #include <stddef.h>
 #include <math.h>
 #include <fenv.h>
+#include <stdlib.h>
 
 #define GROUP 128
 
@@ -233,5 +235,79 @@ int oracle_roundtrip_int8_g128(const float *w, int64_t N, int64_t K,
         }
     }
     *rel_err = den > 0.0 ? sqrt(num / den) : 0.0;
+    return 0;
+}
+
+/* ---------- dequant-on-gather embedding (int8 group-128 table) ---------- */
+
+/*
+ * "What this repo does that stock vLLM doesn't", "In full" items 1 and 2: the
+ * embedding table is requantized to int8 with group-128 fp16 scales and read
+ * through a dequant-on-gather kernel.  For token t and feature k:
+ *   out[t,k] = fp16_rne( codes[ids[t],k] * scales[ids[t], k/128] )
+ * (the product of an 8-bit code and an 11-bit scale is exact in binary64).
+ * ids [T] int64, codes [V,D] int8, scales [V,D/128] binary16, out [T,D] binary16.
+ * Returns -4 (rows set to zero) when an id lies outside [0, V).
+ */
+int oracle_embed_w8(const int64_t *ids, int64_t T, const int8_t *codes, const uint16_t *scales,
+                    int64_t V, int64_t D, uint16_t *out)
+{
+    if (T < 0 || V < 0 || D < 0 || D % GROUP) return -1;
+    if (fegetround() != FE_TONEAREST) return -2;
+    int64_t G = D / GROUP;
+    int bad = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t v = ids[t];
+        if (v < 0 || v >= V) {
+            for (int64_t k = 0; k < D; ++k) out[t * D + k] = 0;
+            bad = 1;
+            continue;
+        }
+        for (int64_t k = 0; k < D; ++k) {
+            double s = oracle_half_to_double(scales[v * G + k / GROUP]);
+            out[t * D + k] = oracle_double_to_half((double)codes[v * D + k] * s);
+        }
+    }
+    return bad ? -4 : 0;
+}
+
+/* ---------- top-k over logits ---------- */
+
+/*
+ * "What this repo does that stock vLLM doesn't", "In full" item 6: with top-k
+ * known on the host the sampler's mask is a small top-k over the logits.  Per
+ * row: the k largest values, largest first, ties broken by the smaller index
+ * (values compared as numbers, so -0 and +0 tie).
+ * logits [M,N] binary16 (no NaN), vals [M,k] binary16, idx [M,k] int64.
+ */
+static const uint16_t *g_topk_row;
+static int topk_cmp(const void *a, const void *b)
+{
+    int64_t i = *(const int64_t *)a, j = *(const int64_t *)b;
+    double vi = oracle_half_to_double(g_topk_row[i]), vj = oracle_half_to_double(g_topk_row[j]);
+    if (vi > vj) return -1;
+    if (vi < vj) return 1;
+    return (i < j) ? -1 : (i > j) ? 1 : 0;
+}
+
+int oracle_topk(const uint16_t *logits, int64_t M, int64_t N, int64_t k, uint16_t *vals, int64_t *idx)
+{
+    if (M < 0 || N < 0 || k < 0 || k > N) return -1;
+    int64_t *order = (int64_t *)malloc((size_t)(N > 0 ? N : 1) * sizeof(int64_t));
+    if (!order) return -5;
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *row = logits + m * N;
+        for (int64_t n = 0; n < N; ++n) {
+            if (oracle_half_to_double(row[n]) != oracle_half_to_double(row[n])) { free(order); return -6; }
+            order[n] = n;
+        }
+        g_topk_row = row;           /* qsort has no context argument; single-threaded */
+        qsort(order, (size_t)N, sizeof(int64_t), topk_cmp);
+        for (int64_t j = 0; j < k; ++j) {
+            idx[m * k + j] = order[j];
+            vals[m * k + j] = row[order[j]];
+        }
+    }
+    free(order);
     return 0;
 }

@@ -143,3 +143,28 @@ def gemm_w4a8(qa: np.ndarray, sx: np.ndarray, codes: np.ndarray, sbits: np.ndarr
                 acc += sf[n][g] * inner
             y[m, n] = fraction_to_half_bits(to_half(sm * acc))
     return y
+
+
+def embed_w8(ids, codes: np.ndarray, sbits: np.ndarray) -> np.ndarray:
+    """Exact out[t,k] = fp16(codes[ids[t],k] * scale[ids[t],k/128]) as binary16 bits."""
+    T = len(ids)
+    D = codes.shape[1]
+    out = np.zeros((T, D), np.uint16)
+    for t, v in enumerate(ids):
+        for k in range(D):
+            sb = int(sbits[v, k // GROUP])
+            c = int(codes[v, k])
+            p = c * half_bits_to_fraction(sb)
+            if p == 0:
+                # IEEE: the sign of a zero product is the XOR of the operands' signs
+                # (an integer code 0 is +0)
+                out[t, k] = 0x8000 if ((c < 0) != bool(sb & 0x8000)) else 0
+            else:
+                out[t, k] = fraction_to_half_bits(to_half(p))
+    return out
+
+
+def topk(vals: np.ndarray, k: int):
+    """Indices of the k largest values, largest first, ties to the smaller index."""
+    order = sorted(range(len(vals)), key=lambda i: (-float(vals[i]), i))
+    return order[:k]

@@ -255,3 +255,67 @@ def test_quant_act_divide_not_reciprocal_bruteforce():
     bq, bs = _brute.quant_act_int8(_bits(x))
     assert np.array_equal(s.astype(np.float64), bs)
     assert np.array_equal(q.astype(np.int64), bq)
+
+
+# ------------------------------------------------ embedding gather and top-k --
+
+def test_embed_w8_matches_exact_brute_force():
+    """Dequant-on-gather ("In full" items 1-2): exact rational product, rounded once."""
+    rng = np.random.default_rng(21)
+    V, D = 7, 256
+    codes = rng.integers(-128, 128, (V, D)).astype(np.int8)
+    scales = rng.uniform(-0.02, 0.02, (V, D // 128)).astype(np.float16)
+    scales[2, 1] = np.float16(2.0 ** -20)                  # subnormal scale
+    scales[4, 0] = np.float16(-0.0)
+    ids = np.array([0, 6, 2, 2, 4, 3])
+    got = oracle.embed_w8(ids, codes, scales).view(np.uint16)
+    want = _brute.embed_w8(ids, codes, scales.view(np.uint16))
+    assert np.array_equal(got, want)
+
+
+def test_embed_w8_equals_w8a16_on_unit_vectors():
+    """Row v of the gather is the int8 layer applied to unit vectors: W8A16 with
+    x = e_k gives y[k, v] = fp16(scale[v, k/128] * code[v, k]) (one nonzero term)."""
+    rng = np.random.default_rng(22)
+    V, D = 9, 384
+    codes = rng.integers(-127, 128, (V, D)).astype(np.int8)
+    scales = rng.uniform(-0.05, 0.05, (V, D // 128)).astype(np.float16)
+    eye = np.eye(D, dtype=np.float16)
+    y = oracle.w8a16(eye, codes, scales)                    # [D, V]
+    ids = np.arange(V)
+    emb = oracle.embed_w8(ids, codes, scales)               # [V, D]
+    # equal as numbers (exactly; the GEMM's sum turns a -0 product into +0)
+    assert np.array_equal(emb.astype(np.float64), y.T.astype(np.float64))
+
+
+def test_embed_w8_group_boundary_and_bad_id():
+    """Feature 127 takes group 0's scale and 128 group 1's; an id outside [0, V) is rejected."""
+    codes = np.ones((2, 256), np.int8)
+    scales = np.array([[0.5, 0.25], [1.0, 2.0]], np.float16)
+    out = oracle.embed_w8(np.array([1, 0]), codes, scales)
+    assert out[0, 127] == 1.0 and out[0, 128] == 2.0 and out[1, 127] == 0.5 and out[1, 128] == 0.25
+    with pytest.raises(ValueError):
+        oracle.embed_w8(np.array([2]), codes, scales)
+
+
+def test_topk_matches_brute_force_with_ties():
+    """The sampler's top-k ("In full" item 6): largest first, ties to the smaller index;
+    values drawn from a small set so ties are everywhere, +0 and -0 compare equal."""
+    rng = np.random.default_rng(23)
+    M, N, k = 5, 400, 37
+    pool = np.array([-3.5, -0.0, 0.0, 0.125, 1.0, 1.0009765625, 7.0, 65504.0, -65504.0], np.float16)
+    logits = pool[rng.integers(0, len(pool), (M, N))]
+    vals, idx = oracle.topk(logits, k)
+    for m in range(M):
+        want = _brute.topk(logits[m], k)
+        assert list(idx[m]) == want
+        assert np.array_equal(vals[m].view(np.uint16), logits[m][want].view(np.uint16))
+
+
+def test_topk_closed_forms():
+    """k = N is a full stable sort; an all-equal row gives indices 0..k-1."""
+    x = np.array([[2.0, -1.0, 2.0, 0.5]], np.float16)
+    _, idx = oracle.topk(x, 4)
+    assert list(idx[0]) == [0, 2, 3, 1]
+    _, idx = oracle.topk(np.full((2, 50), 3.0, np.float16), 8)
+    assert (idx == np.arange(8)).all()
