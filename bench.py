@@ -485,7 +485,8 @@ def run_ours(args):
 # ----------------------------------------------------- the other workloads --
 def extras(q, dev, stream, pk, pk_src):
     """FFN pair (M=64, W4A8), prefill (M=8192, both modes), 2048-token prefill chunks on
-    the three layer shapes (both modes), lm_head (W8A16).
+    the three layer shapes (both modes), lm_head (W8A16), the embedding gather from the
+    same int8 table, top-k over logits of the lm_head's width.
     Each timed with CUDA events on graph replays, with a parity spot check."""
     import oracle
     hbm = float(pk["hbm_gbs"])
@@ -601,8 +602,32 @@ def extras(q, dev, stream, pk, pk_src):
                                       "frac_hbm": round(alg / ms / 1e6 / hbm, 4),
                                       "TFLOPS": round(2 * M * lh.N * lh.K / ms / 1e9, 2),
                                       "parity": parity_err(y.cpu()[:, cols], ref)}
+
+    # dequant-on-gather from the same int8 group-128 table (the embedding's format)
+    for T in (64, 2048):
+        ids = synth.token_ids(T, lh.N, seed=40 + T).to(dev)
+        emb = torch.empty((T, lh.K), dtype=torch.float16, device=dev)
+        ms = timeit(lambda: q.embed_gather_w8(ids, pk8, lh.N, lh.K, out=emb), 20)
+        sel = np.arange(0, T, max(1, T // 16))
+        ref = oracle.embed_w8(ids.cpu().numpy()[sel], lh.codes, lh.scales)
+        moved = T * (lh.K + 2 * lh.K // 128) + 2 * T * lh.K
+        out[f"embed_gather_w8_T{T}"] = {
+            "us": round(ms * 1e3, 2), "GBps": round(moved / ms / 1e6, 1),
+            "bitexact_sampled_rows": bool(np.array_equal(emb.cpu().numpy()[sel].view(np.uint16),
+                                                         ref.view(np.uint16)))}
     del pk8
     torch.cuda.empty_cache()
+
+    # top-k (k = 64) over synthetic logits of the lm_head's width
+    for M in (1, 16, 64):
+        lg = synth.logits(M, lh.N, seed=50 + M).to(dev)
+        ms = timeit(lambda: q.topk_logits(lg, 64), 20)
+        entry = {"us": round(ms * 1e3, 2), "GBps": round(2 * M * lh.N / ms / 1e6, 1), "k": 64}
+        if M == 1:
+            v, i = q.topk_logits(lg, 64)
+            ov, oi = oracle.topk(lg.cpu().numpy(), 64)
+            entry["exact"] = bool(np.array_equal(i.cpu().numpy().astype(np.int64), oi))
+        out[f"topk_logits_M{M}_N{lh.N}"] = entry
     return out
 
 

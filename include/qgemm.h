@@ -54,7 +54,8 @@ enum {
     QW_ERR_ARCH = -5,               /* no device, or the device is not sm_103 */
     QW_ERR_CUDA = -6,               /* a CUDA runtime call failed */
     QW_ERR_TIMEOUT = -7,            /* (device) a pipeline wait exceeded its limit */
-    QW_ERR_BAD_CODES = -8           /* (device) qpack_w4 saw a code outside [-8, 7] */
+    QW_ERR_BAD_CODES = -8,          /* (device) qpack_w4 saw a code outside [-8, 7] */
+    QW_ERR_BAD_INDEX = -9           /* (device) embed_gather_w8 saw a row id outside [0, V) */
 };
 
 enum { QW_MODE_W4A16 = 0, QW_MODE_W4A8 = 1, QW_MODE_W8A16 = 2, QW_MODE_W4A8_FUSED = 3 };
@@ -145,6 +146,41 @@ int qgemm_w4a8(const int8_t *xq, const float *xs, const void *packed_w4, int M, 
                uint16_t *y, void *ws, size_t ws_bytes, qw_stream_t stream);
 int qgemm_w8a16(const uint16_t *x, const void *packed_w8, int M, int N, int K, uint16_t *y,
                 void *ws, size_t ws_bytes, qw_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * embed_gather_w8 -- dequant-on-gather embedding from an int8 group-128 table
+ * ("In full" items 1 and 2: both embedding matrices requantized to int8
+ * group-128 and read through a dequant-on-gather kernel):
+ *   out[t, k] = fp16_rne( code[ids[t], k] * scale[ids[t], k / 128] )
+ *   ids     [T] int32, device.
+ *   packed  the table [V, D] packed by qpack_w8 (the same format as the int8
+ *           lm_head); V and D multiples of 128.
+ *   out     [T, D] fp16, device, 16-byte aligned, fully written.
+ * An id outside [0, V) gives a row of zeros and sets QW_ERR_BAD_INDEX in the
+ * device error word.  Async.  Returns QW_OK, QW_ERR_INVALID_ARG,
+ * QW_ERR_UNSUPPORTED_SHAPE, QW_ERR_ALIGNMENT, QW_ERR_ARCH or QW_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+int embed_gather_w8(const int32_t *ids, int T, const void *packed_w8, int V, int D, uint16_t *out,
+                    qw_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * topk_logits -- per row of an [M, N] fp16 logit matrix (for instance the
+ * lm_head's output) the k largest values, largest first; equal values are
+ * ordered by the smaller column index, and -0 equals +0 ("In full" item 6: the
+ * sampler's mask with top-k known on the host is one small top-k).
+ *   logits [M, N] fp16, device, 16-byte aligned; N a multiple of 8,
+ *          k <= N <= 262144; NaN is out of contract.  1 <= k <= 64.
+ *   vals [M, k] fp16 (the logits' own bit patterns), idx [M, k] int32, device.
+ *   ws: topk_workspace_bytes(M, N, k) bytes, zero-filled once (the first
+ *   topk_workspace_zero_bytes stay zero after every call that returns QW_OK).
+ * One launch: each slice of a row keeps its k best by radix selection, and the
+ * last slice of the row to finish merges.  Async.  Returns as embed_gather_w8,
+ * or QW_ERR_WORKSPACE.
+ * ------------------------------------------------------------------------ */
+size_t topk_workspace_bytes(int M, int N, int k);
+size_t topk_workspace_zero_bytes(int M, int N, int k);
+int topk_logits(const uint16_t *logits, int M, int N, int k, uint16_t *vals, int32_t *idx, void *ws,
+                size_t ws_bytes, qw_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * qgemm_w4a8_fused -- the W4A8 layer from fp16 activations: y is bit-identical

@@ -9,6 +9,7 @@ Entry points (same names as the C ABI):
     qgemm_w4a16(x, packed, N, K) -> y        qgemm_w4a8(xq, xs, packed, N, K) -> y
     qgemm_w4a8_fused(x, packed, N, K) -> y
     qgemm_w8a16(x, packed, N, K) -> y
+    embed_gather_w8(ids, packed, V, D) -> out        topk_logits(logits, k) -> (vals, idx)
 """
 from __future__ import annotations
 
@@ -30,6 +31,7 @@ QW_ERR_ARCH = -5
 QW_ERR_CUDA = -6
 QW_ERR_TIMEOUT = -7
 QW_ERR_BAD_CODES = -8
+QW_ERR_BAD_INDEX = -9
 MODE_W4A16, MODE_W4A8, MODE_W8A16, MODE_W4A8_FUSED = 0, 1, 2, 3
 
 # every function the header declares: name -> (restype, argtypes)
@@ -54,6 +56,10 @@ SIGNATURES = {
     "qgemm_w4a16": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "qgemm_w4a8": (_i, [_p, _p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "qgemm_w4a8_fused": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
+    "embed_gather_w8": (_i, [_p, _i, _p, _i, _i, _p, _p]),
+    "topk_workspace_bytes": (_sz, [_i, _i, _i]),
+    "topk_workspace_zero_bytes": (_sz, [_i, _i, _i]),
+    "topk_logits": (_i, [_p, _i, _i, _i, _p, _p, _p, _sz, _p]),
     "qgemm_w8a16": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "qgemm_w4a16_noalloc": (_i, [_p, _p, _i, _i, _i, _p, _p]),
     "qw_last_error_string": (ctypes.c_char_p, []),
@@ -260,6 +266,41 @@ def qgemm_w8a16(x, packed, N: int, K: int, y=None, ws: Workspace | None = None):
         _check(lib().qgemm_w8a16(_ptr(x), _ptr(packed), M, N, K, _ptr(y), _ptr(wbuf), wbytes,
                                  _stream(x)))
     return y
+
+
+def embed_gather_w8(ids, packed, V: int, D: int, out=None):
+    """out[t] = the dequantized row ids[t] of an int8 group-128 table [V, D] packed by
+    qpack_w8: fp16(code * scale).  ids int32 [T] on the device."""
+    _need(ids, torch.int32, "ids", 1)
+    T = ids.shape[0]
+    if out is None:
+        out = torch.empty((T, D), dtype=torch.float16, device=ids.device)
+    _need(out, torch.float16, "out", 2)
+    with torch.cuda.device(ids.device):
+        _check(lib().embed_gather_w8(_ptr(ids), T, _ptr(packed), V, D, _ptr(out), _stream(ids)))
+    return out
+
+
+_topk_ws = {}
+
+
+def topk_logits(logits, k: int):
+    """Per row the k largest logits (largest first, ties to the smaller index):
+    returns (values fp16 [M,k], indices int32 [M,k])."""
+    _need(logits, torch.float16, "logits", 2)
+    M, N = logits.shape
+    vals = torch.empty((M, k), dtype=torch.float16, device=logits.device)
+    idx = torch.empty((M, k), dtype=torch.int32, device=logits.device)
+    need = int(lib().topk_workspace_bytes(M, N, k))
+    key = (logits.device, torch.cuda.current_stream(logits.device).cuda_stream)
+    buf = _topk_ws.get(key)
+    if buf is None or buf.numel() < need:
+        buf = torch.zeros(max(need, 256), dtype=torch.uint8, device=logits.device)
+        _topk_ws[key] = buf
+    with torch.cuda.device(logits.device):
+        _check(lib().topk_logits(_ptr(logits), M, N, k, _ptr(vals), _ptr(idx), _ptr(buf), buf.numel(),
+                                 _stream(logits)))
+    return vals, idx
 
 
 def qgemm_w4a16_noalloc(x, packed, N: int, K: int, y=None):

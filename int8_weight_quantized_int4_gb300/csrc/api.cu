@@ -308,6 +308,61 @@ int qgemm_w4a8(const int8_t *xq, const float *xs, const void *packed_w4, int M, 
   return gemm_common(QW_MODE_W4A8, xq, xs, packed_w4, M, N, K, y, ws, ws_bytes, stream);
 }
 
+int embed_gather_w8(const int32_t *ids, int T, const void *packed_w8, int V, int D, uint16_t *out,
+                    qw_stream_t stream) {
+  if (T < 0 || V < 0 || D < 0) return fail(QW_ERR_INVALID_ARG, "negative size");
+  if (V % 128 || D % 128 || D == 0 || D > kMaxK || V > kMaxN)
+    return fail(QW_ERR_UNSUPPORTED_SHAPE, "V and D must be multiples of 128 (D > 0)");
+  if (T == 0) return QW_OK;
+  if (!ids || !packed_w8 || !out) return fail(QW_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned(packed_w8, 16) || !aligned(out, 16) || !aligned(ids, 4))
+    return fail(QW_ERR_ALIGNMENT, "packed table and output must be 16-byte aligned");
+  DevInfo *d = nullptr;
+  int rc = current_device(d);
+  if (rc) return rc;
+  cudaError_t e = qw::launch_embed_gather(ids, T, packed_w8, V, D, out, d->err,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "gather kernel launch");
+  return QW_OK;
+}
+
+static int topk_shape(int M, int N, int k) {
+  if (M < 0 || N < 0 || k < 0) return fail(QW_ERR_INVALID_ARG, "negative size");
+  if (k < 1 || k > 64 || k > N || N > qw::kTopkMaxN || N % 8)
+    return fail(QW_ERR_UNSUPPORTED_SHAPE, "need 1 <= k <= 64, k <= N <= %d, N a multiple of 8",
+                qw::kTopkMaxN);
+  return QW_OK;
+}
+
+size_t topk_workspace_bytes(int M, int N, int k) {
+  if (topk_shape(M, N, k)) return 0;
+  return qw::topk_plan(M, N, k).ws_bytes;
+}
+
+size_t topk_workspace_zero_bytes(int M, int N, int k) {
+  if (topk_shape(M, N, k)) return 0;
+  return qw::topk_plan(M, N, k).ws_counters;
+}
+
+int topk_logits(const uint16_t *logits, int M, int N, int k, uint16_t *vals, int32_t *idx, void *ws,
+                size_t ws_bytes, qw_stream_t stream) {
+  int rc = topk_shape(M, N, k);
+  if (rc) return rc;
+  if (M == 0) return QW_OK;
+  if (!logits || !vals || !idx) return fail(QW_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned(logits, 16) || !aligned(vals, 2) || !aligned(idx, 4) || (ws && !aligned(ws, 256)))
+    return fail(QW_ERR_ALIGNMENT, "logits must be 16-byte aligned, the workspace 256-byte aligned");
+  const qw::TopkPlan tp = qw::topk_plan(M, N, k);
+  if (!ws || ws_bytes < tp.ws_bytes)
+    return fail(QW_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", tp.ws_bytes,
+                ws ? ws_bytes : (size_t)0);
+  DevInfo *d = nullptr;
+  if ((rc = current_device(d))) return rc;
+  cudaError_t e = qw::launch_topk(logits, M, N, k, vals, idx, ws, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "top-k kernel launch");
+  return QW_OK;
+}
+
 int qgemm_w4a8_fused(const uint16_t *x, const void *packed_w4, int M, int N, int K, uint16_t *y,
                      void *ws, size_t ws_bytes, qw_stream_t stream) {
   return gemm_common(QW_MODE_W4A8_FUSED, x, nullptr, packed_w4, M, N, K, y, ws, ws_bytes, stream);

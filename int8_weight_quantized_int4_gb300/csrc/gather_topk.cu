@@ -1,0 +1,231 @@
+// gather_topk.cu -- the two ends of the quantized model around the GEMMs:
+//   embed_gather_kernel : dequant-on-gather from an int8 group-128 table packed by
+//                         qpack_w8 ("In full" items 1-2 of "What this repo does that
+//                         stock vLLM doesn't": embeddings requantized to int8 g128 and
+//                         read through a dequant-on-gather kernel)
+//   topk_kernel         : per row the k largest logits, largest first, ties to the
+//                         smaller index ("In full" item 6: with top-k known on the host
+//                         the sampler's mask is one small top-k)
+#include <stdint.h>
+#include <cuda_fp16.h>
+#include "ptx.cuh"
+#include "schedule.h"
+#include "launch.h"
+
+namespace qw {
+
+// ---------------------------------------------------------------- gather --
+// One CTA per token.  Feature k of table row v sits in chunk (v / 128, k / 128) of the
+// packed table, slice (k % 128) / 16, at byte (v % 128) * 16 + k % 16, stored as
+// code XOR 0x80; the row's fp16 scale follows the slices.  out = fp16(code * scale),
+// one rounding (__hmul_rn of two exact fp16 operands).
+__global__ void __launch_bounds__(256) embed_gather_kernel(const int32_t *__restrict__ ids,
+                                                           const uint8_t *__restrict__ packed, int V,
+                                                           int D, uint16_t *__restrict__ out,
+                                                           int *err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int t = blockIdx.x;
+  const int v = ids[t];
+  const int G = D / kGroup;
+  uint4 *orow = reinterpret_cast<uint4 *>(out + (size_t)t * D);
+  if (v < 0 || v >= V) {
+    for (int p = threadIdx.x; p < D / 8; p += blockDim.x) orow[p] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) atomicCAS(err, 0, -9);
+    return;
+  }
+  const int r = v % kRows;
+  const uint8_t *tile = packed + (size_t)(v / kRows) * G * kChunkW8;
+  for (int p = threadIdx.x; p < G * 8; p += blockDim.x) {       // 16 features per piece
+    const int g = p >> 3, j = p & 7;
+    const uint8_t *chunk = tile + (size_t)g * kChunkW8;
+    const uint4 c = __ldg(reinterpret_cast<const uint4 *>(chunk + j * 2048 + r * 16));
+    const __half s = __ushort_as_half(__ldg(reinterpret_cast<const unsigned short *>(chunk + 16384 + r * 2)));
+    const uint32_t w[4] = {c.x ^ 0x80808080u, c.y ^ 0x80808080u, c.z ^ 0x80808080u, c.w ^ 0x80808080u};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int q0 = (int)(int8_t)((w[i] >> (16 * h)) & 0xffu);
+        const int q1 = (int)(int8_t)((w[i] >> (16 * h + 8)) & 0xffu);
+        const __half a = __hmul_rn(__int2half_rn(q0), s), b = __hmul_rn(__int2half_rn(q1), s);
+        o[2 * i + h] = (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+      }
+    }
+    uint4 *dst = orow + (size_t)(g * kGroup + j * 16) / 8;
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+cudaError_t launch_embed_gather(const int32_t *ids, int T, const void *packed, int V, int D,
+                                uint16_t *out, int *err, cudaStream_t st) {
+  cudaError_t e = launch_pdl(reinterpret_cast<const void *>(embed_gather_kernel), dim3(T), dim3(256), 0,
+                             st, ids, static_cast<const uint8_t *>(packed), V, D, out, err);
+  count_launch();
+  return e;
+}
+
+// ------------------------------------------------------------------ top-k --
+// Order: larger value first, equal values by smaller index.  Each element becomes a
+// unique 40-bit composite  key16 << 24 | (2^24 - 1 - index)  whose numeric order is
+// exactly that order: key16 maps fp16 to an order-preserving 16-bit integer (-0 taken
+// as +0, so the two tie); positions past N get key 0, which no finite fp16 value maps
+// to.  The k largest composites are found by radix selection (five 8-bit passes,
+// histograms in shared memory): afterwards exactly k composites are >= the threshold.
+constexpr int kTopkThreads = 256;
+constexpr int kTopkMaxK = 64;
+constexpr int kTopkMaxSlices = 64;
+constexpr int kTopkMaxVec = 2;                 // 16-byte vectors per thread per slice
+constexpr int kTopkMerge = kTopkMaxSlices * kTopkMaxK / kTopkThreads;   // candidates per thread
+
+__device__ __forceinline__ uint32_t order_key(uint16_t h) {
+  if (h == 0x8000u) h = 0;                      // -0 ties with +0
+  return (h & 0x8000u) ? (uint32_t)(~h & 0xffffu) : (uint32_t)(h | 0x8000u);
+}
+
+__device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t index) {
+  return ((uint64_t)key << 24) | (uint64_t)(0xffffffu - index);
+}
+
+// Radix selection over the CTA: every thread holds n composites in c[]; returns the
+// k-th largest.  hist: 256 ints of shared memory; bc: 2 ints of shared memory.
+template <int NMAX>
+__device__ uint64_t select_kth(const uint64_t (&c)[NMAX], int n, int k, int *hist, int *bc) {
+  uint64_t prefix = 0;
+  int remaining = k;
+#pragma unroll 1
+  for (int pass = 0; pass < 5; ++pass) {
+    const int shift = 32 - 8 * pass;
+    for (int b = threadIdx.x; b < 256; b += kTopkThreads) hist[b] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < NMAX; ++i)
+      if (i < n && (c[i] >> (shift + 8)) == (prefix >> (shift + 8)))
+        atomicAdd(&hist[(int)((c[i] >> shift) & 0xffu)], 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int cum = 0, sel = 0;
+      for (int b = 255; b >= 0; --b) {
+        if (cum + hist[b] >= remaining) { sel = b; break; }
+        cum += hist[b];
+      }
+      bc[0] = sel;
+      bc[1] = remaining - cum;
+    }
+    __syncthreads();
+    prefix |= (uint64_t)bc[0] << shift;
+    remaining = bc[1];
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// grid (slices, rows).  ws: [M] int counters (zero between calls), then candidates
+// [M][slices][k] (uint64 composites).
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t *__restrict__ logits, int N,
+                                                             int k, int slice_len, uint16_t *vals,
+                                                             int32_t *idx, int *counters,
+                                                             uint64_t *cand) {
+  __shared__ int hist[256];
+  __shared__ int bc[2];
+  __shared__ int nsel;
+  __shared__ int last;
+  __shared__ uint64_t sel[kTopkMaxK];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int m = blockIdx.y, sl = blockIdx.x, S = gridDim.x;
+  const uint16_t *row = logits + (size_t)m * N;
+  uint64_t *mycand = cand + ((size_t)m * S + sl) * k;
+
+  // ---- this slice: its k best (padding past N included when the slice is short)
+  {
+    uint64_t c[kTopkMaxVec * 8];
+    const int base = sl * slice_len;
+    const int nvec = slice_len / (8 * kTopkThreads);
+#pragma unroll
+    for (int e = 0; e < kTopkMaxVec; ++e) {
+      const int p = base + 8 * (threadIdx.x + kTopkThreads * e);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      const bool in = e < nvec && p < N;            // N % 8 == 0: a vector is all in or all out
+      if (in) v = __ldg(reinterpret_cast<const uint4 *>(row + p));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t key = in ? order_key((uint16_t)(w[j >> 1] >> (16 * (j & 1)))) : 0u;
+        c[8 * e + j] = composite(key, (uint32_t)(p + j));
+      }
+    }
+    const uint64_t th = select_kth(c, 8 * nvec, k, hist, bc);
+    if (threadIdx.x == 0) nsel = 0;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kTopkMaxVec * 8; ++i)
+      if (i < 8 * nvec && c[i] >= th) mycand[atomicAdd(&nsel, 1)] = c[i];
+  }
+
+  // ---- publish; the last slice CTA of the row merges
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(counters + m, 1);
+    last = (old == S - 1);
+    if (last) counters[m] = 0;                      // leave the workspace zeroed
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+
+  uint64_t c[kTopkMerge];
+  const int total = S * k;
+  const uint64_t *rowcand = cand + (size_t)m * S * k;
+#pragma unroll
+  for (int i = 0; i < kTopkMerge; ++i) {
+    const int q = threadIdx.x + kTopkThreads * i;
+    c[i] = q < total ? __ldcg(reinterpret_cast<const unsigned long long *>(rowcand) + q) : 0ull;
+  }
+  const int nmine = total > threadIdx.x ? (total - 1 - (int)threadIdx.x) / kTopkThreads + 1 : 0;
+  const uint64_t th = select_kth(c, nmine, k, hist, bc);
+  if (threadIdx.x == 0) nsel = 0;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kTopkMerge; ++i)
+    if (i < nmine && c[i] >= th) sel[atomicAdd(&nsel, 1)] = c[i];
+  __syncthreads();
+  // rank sort of the k winners (all distinct), largest first
+  for (int a = threadIdx.x; a < k; a += kTopkThreads) {
+    int rank = 0;
+    for (int b = 0; b < k; ++b) rank += sel[b] > sel[a];
+    const int n = 0xffffff - (int)(sel[a] & 0xffffffu);
+    idx[(size_t)m * k + rank] = n;
+    vals[(size_t)m * k + rank] = row[n];
+  }
+}
+
+TopkPlan topk_plan(int M, int N, int k) {
+  TopkPlan tp{};
+  // slices of 2048 or 4096 elements (one or two vectors per thread), at most 64
+  tp.slices = (N + 2047) / 2048;
+  if (tp.slices > kTopkMaxSlices) tp.slices = kTopkMaxSlices;
+  if (tp.slices < 1) tp.slices = 1;
+  const int per = (N + tp.slices - 1) / tp.slices;
+  tp.slice_len = (per + 2047) / 2048 * 2048;
+  tp.slices = (N + tp.slice_len - 1) / tp.slice_len;
+  tp.ws_counters = align_up((size_t)M * 4, 256);
+  tp.ws_bytes = tp.ws_counters + (size_t)M * tp.slices * k * 8;
+  return tp;
+}
+
+cudaError_t launch_topk(const uint16_t *logits, int M, int N, int k, uint16_t *vals, int32_t *idx,
+                        void *ws, cudaStream_t st) {
+  const TopkPlan tp = topk_plan(M, N, k);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  cudaError_t e = launch_pdl(reinterpret_cast<const void *>(topk_kernel), dim3(tp.slices, M),
+                             dim3(kTopkThreads), 0, st, logits, N, k, tp.slice_len, vals, idx,
+                             reinterpret_cast<int *>(w), reinterpret_cast<uint64_t *>(w + tp.ws_counters));
+  count_launch();
+  return e;
+}
+
+}  // namespace qw

@@ -57,6 +57,18 @@ cudaError_t launch_pack_w4(const int8_t *codes, const uint16_t *scales, int N, i
 cudaError_t launch_pack_w8(const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
                            int sms, cudaStream_t st);
 
+// embedding gather and top-k (gather_topk.cu)
+struct TopkPlan {
+  int slices, slice_len;
+  size_t ws_counters, ws_bytes;
+};
+constexpr int kTopkMaxN = 64 * 4096;
+TopkPlan topk_plan(int M, int N, int k);
+cudaError_t launch_embed_gather(const int32_t *ids, int T, const void *packed, int V, int D,
+                                uint16_t *out, int *err, cudaStream_t st);
+cudaError_t launch_topk(const uint16_t *logits, int M, int N, int k, uint16_t *vals, int32_t *idx,
+                        void *ws, cudaStream_t st);
+
 cudaError_t launch_gemm_w4a16(const GemmArgs &a, cudaStream_t st);
 cudaError_t launch_gemm_w4a8(const GemmArgs &a, cudaStream_t st);
 cudaError_t launch_gemm_w4a8_fused(const GemmArgs &a, cudaStream_t st);

@@ -125,3 +125,23 @@ def prefill(M: int = 8192) -> Problem:
 def lm_head(M: int, N: int = 248320) -> Problem:
     """int8 group-128 lm_head N=248320, K=5120, |s| ~ U(0.001, 0.01) signed, seed 5."""
     return make_problem(M, N, 5120, seed=5, bits=8, scale_lo=0.001, scale_hi=0.01)
+
+
+def logits(M: int, N: int, seed: int, step: float = 0.125) -> torch.Tensor:
+    """fp16 [M, N] logits ~ 4 N(0, 1) on a grid of `step` (so equal values are common),
+    with a few exact +0 / -0 entries per row."""
+    gen = generator(seed)
+    z = torch.round(4.0 * torch.randn((M, N), generator=gen) / step) * step
+    pos = torch.randint(0, N, (M, 4), generator=gen)
+    z.scatter_(1, pos[:, :2], 0.0)
+    z.scatter_(1, pos[:, 2:], -0.0)
+    return z.to(torch.float16)
+
+
+def token_ids(T: int, V: int, seed: int) -> torch.Tensor:
+    """int32 [T] row ids in [0, V), with the first and last rows and repeats present."""
+    gen = generator(seed)
+    ids = torch.randint(0, V, (T,), generator=gen, dtype=torch.int32)
+    if T >= 3:
+        ids[0], ids[1], ids[2] = 0, V - 1, ids[T - 1]
+    return ids

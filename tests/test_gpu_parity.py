@@ -362,6 +362,62 @@ def test_w4a8_fused_workspace_and_empty(q):
     assert tuple(y.shape) == (0, 5120)
 
 
+# ------------------------------------------- embedding gather and top-k (next rows) --
+
+@pytest.mark.parametrize("V,D,T", [(1024, 640, 300), (256, 5120, 64), (128, 128, 1)])
+def test_embed_gather_w8_bitexact(q, V, D, T):
+    """Dequant-on-gather from the qpack_w8 table equals the oracle bit for bit."""
+    p = synth.make_problem(1, V, D, seed=31 + T, bits=8, scale_lo=0.001, scale_hi=0.01)
+    packed = q.qpack_w8(p.codes.to(DEV), p.scales.to(DEV))
+    ids = synth.token_ids(T, V, seed=32 + T)
+    out = q.embed_gather_w8(ids.to(DEV), packed, V, D)
+    torch.cuda.synchronize()
+    assert q.device_error() == 0
+    ref = oracle.embed_w8(ids.numpy(), p.codes, p.scales)
+    assert np.array_equal(bits(out), ref.view(np.int16))
+
+
+def test_embed_gather_w8_bad_id(q):
+    """An id outside [0, V) gives a zero row and QW_ERR_BAD_INDEX in the error word; the
+    other rows are unaffected."""
+    p = synth.make_problem(1, 256, 256, seed=33, bits=8)
+    packed = q.qpack_w8(p.codes.to(DEV), p.scales.to(DEV))
+    ids = torch.tensor([5, -1, 256, 7], dtype=torch.int32)
+    out = q.embed_gather_w8(ids.to(DEV), packed, 256, 256)
+    torch.cuda.synchronize()
+    assert q.device_error() == q.QW_ERR_BAD_INDEX
+    assert q.device_error() == 0
+    o = out.cpu()
+    assert int(o[1].abs().sum()) == 0 and int(o[2].abs().sum()) == 0
+    ref = oracle.embed_w8(np.array([5, 7]), p.codes, p.scales)
+    assert np.array_equal(bits(o[[0, 3]]), ref.view(np.int16))
+
+
+@pytest.mark.parametrize("M,N,k", [(1, 248320, 64), (4, 248320, 8), (64, 32768, 64), (3, 4096, 1),
+                                   (2, 2056, 17), (5, 8, 8), (7, 262144, 50)])
+def test_topk_logits_match_oracle(q, M, N, k):
+    """Top-k over logits: indices and values equal the oracle's (largest first, ties to
+    the smaller index, -0 equal to +0) on tie-heavy synthetic logits."""
+    x = synth.logits(M, N, seed=M * 7 + k)
+    vals, idx = q.topk_logits(x.to(DEV), k)
+    torch.cuda.synchronize()
+    assert q.device_error() == 0
+    ov, oi = oracle.topk(x.numpy(), k)
+    assert np.array_equal(idx.cpu().numpy().astype(np.int64), oi)
+    assert np.array_equal(bits(vals), ov.view(np.int16))
+
+
+def test_topk_logits_constant_rows_and_repeat(q):
+    """All-equal rows give indices 0..k-1; a second call on the same workspace agrees."""
+    x = torch.full((3, 1024), 2.5, dtype=torch.float16)
+    x[1] = -0.0
+    for _ in range(2):
+        vals, idx = q.topk_logits(x.to(DEV), 16)
+        torch.cuda.synchronize()
+        assert (idx.cpu() == torch.arange(16, dtype=torch.int32)).all()
+        assert np.array_equal(bits(vals), x[:, :16].numpy().view(np.int16))
+
+
 def test_workspace_contract(q):
     p = synth.projection(4)
     packed = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
