@@ -618,6 +618,25 @@ def extras(q, dev, stream, pk, pk_src):
     del pk8
     torch.cuda.empty_cache()
 
+    # int4 lm_head (W4A16 at the vocabulary width): 248,320 x 5120 int4, 655 MB packed
+    l4 = synth.lm_head_int4(64)
+    pk4 = q.qpack_w4(l4.codes.to(dev), l4.scales.to(dev))
+    wb4 = w4_bytes(l4.N, l4.K)
+    cols4 = np.concatenate([np.arange(0, l4.N, 997), [l4.N - 1]])
+    for M in (1, 16, 64):
+        x = l4.x[:M].contiguous().to(dev)
+        y = torch.empty((M, l4.N), dtype=torch.float16, device=dev)
+        wsp.get(q.MODE_W4A16, M, l4.N, l4.K)
+        ms = timeit(lambda: q.qgemm_w4a16(x, pk4, l4.N, l4.K, y=y, ws=wsp), 10)
+        ref = oracle.w4a16(l4.x[:M], l4.codes[cols4], l4.scales[cols4])
+        alg = wb4 + 2 * M * l4.K + 2 * M * l4.N
+        out[f"lm_head_w4a16_M{M}"] = {"us": round(ms * 1e3, 1), "weight_GBps": round(wb4 / ms / 1e6, 1),
+                                      "frac_hbm": round(alg / ms / 1e6 / hbm, 4),
+                                      "TFLOPS": round(2 * M * l4.N * l4.K / ms / 1e9, 2),
+                                      "parity": parity_err(y.cpu()[:, cols4], ref)}
+    del pk4, l4
+    torch.cuda.empty_cache()
+
     # top-k (k = 64) over synthetic logits of the lm_head's width
     for M in (1, 16, 64):
         lg = synth.logits(M, lh.N, seed=50 + M).to(dev)

@@ -105,14 +105,35 @@ __device__ uint64_t select_kth(const uint64_t (&c)[NMAX], int n, int k, int *his
       if (i < n && (c[i] >> (shift + 8)) == (prefix >> (shift + 8)))
         atomicAdd(&hist[(int)((c[i] >> shift) & 0xffu)], 1);
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int cum = 0, sel = 0;
-      for (int b = 255; b >= 0; --b) {
-        if (cum + hist[b] >= remaining) { sel = b; break; }
-        cum += hist[b];
+    if (threadIdx.x < 32) {
+      // the bin holding the remaining-th largest, scanning from bin 255 down: lane l
+      // owns bins 255 - 8l .. 248 - 8l; a prefix sum over lanes finds the lane
+      const int lane = threadIdx.x;
+      int cnt[8], local = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cnt[i] = hist[255 - 8 * lane - i];
+        local += cnt[i];
       }
-      bc[0] = sel;
-      bc[1] = remaining - cum;
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, incl >= remaining);
+      if (lane == __ffs(hit) - 1) {
+        int cum = incl - local;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (cum + cnt[i] >= remaining) {
+            bc[0] = 255 - 8 * lane - i;
+            bc[1] = remaining - cum;
+            break;
+          }
+          cum += cnt[i];
+        }
+      }
     }
     __syncthreads();
     prefix |= (uint64_t)bc[0] << shift;

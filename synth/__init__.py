@@ -127,6 +127,11 @@ def lm_head(M: int, N: int = 248320) -> Problem:
     return make_problem(M, N, 5120, seed=5, bits=8, scale_lo=0.001, scale_hi=0.01)
 
 
+def lm_head_int4(M: int, N: int = 248320) -> Problem:
+    """int4 group-128 lm_head (a symmetric GPTQ export's codes minus 8) N=248320, K=5120, seed 6."""
+    return make_problem(M, N, 5120, seed=6, bits=4)
+
+
 def logits(M: int, N: int, seed: int, step: float = 0.125) -> torch.Tensor:
     """fp16 [M, N] logits ~ 4 N(0, 1) on a grid of `step` (so equal values are common),
     with a few exact +0 / -0 entries per row."""

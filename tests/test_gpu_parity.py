@@ -362,6 +362,20 @@ def test_w4a8_fused_workspace_and_empty(q):
     assert tuple(y.shape) == (0, 5120)
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("M", [1, 16])
+def test_lm_head_w4a16_sampled(q, M):
+    """The int4 lm_head (W4A16 at N = 248,320) against the oracle on sampled columns."""
+    p = synth.lm_head_int4(M)
+    packed = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
+    y = q.qgemm_w4a16(p.x.to(DEV), packed, p.N, p.K)
+    torch.cuda.synchronize()
+    assert q.device_error() == 0
+    cols = np.concatenate([np.arange(0, p.N, 499), [p.N - 1]])
+    ref = oracle.w4a16(p.x.numpy(), p.codes[cols], p.scales[cols])
+    assert nerr(y.cpu().numpy()[:, cols], ref) <= TOL
+
+
 # ------------------------------------------- embedding gather and top-k (next rows) --
 
 @pytest.mark.parametrize("V,D,T", [(1024, 640, 300), (256, 5120, 64), (128, 128, 1)])
