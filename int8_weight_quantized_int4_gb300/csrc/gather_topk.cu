@@ -68,12 +68,16 @@ cudaError_t launch_embed_gather(const int32_t *ids, int T, const void *packed, i
 }
 
 // ------------------------------------------------------------------ top-k --
-// Order: larger value first, equal values by smaller index.  Each element becomes a
-// unique 40-bit composite  key16 << 24 | (2^24 - 1 - index)  whose numeric order is
-// exactly that order: key16 maps fp16 to an order-preserving 16-bit integer (-0 taken
-// as +0, so the two tie); positions past N get key 0, which no finite fp16 value maps
-// to.  The k largest composites are found by radix selection (five 8-bit passes,
-// histograms in shared memory): afterwards exactly k composites are >= the threshold.
+// Order: larger value first, equal values by smaller index.  key16 maps fp16 to an
+// order-preserving 16-bit integer (-0 taken as +0, so the two tie); positions past N get
+// key 0, which no finite fp16 value maps to.  Within a slice of at most 4096 positions an
+// element is the 32-bit composite  key16 << 16 | (0xffff - local position), unique and in
+// exactly that order.  The slice's k largest are found by radix selection (8-bit passes,
+// histograms in shared memory) and listed in order in the workspace as 40-bit global
+// composites  key16 << 24 | (2^24 - 1 - index).  The last slice CTA of a row selects
+// again over the row's S k candidates as  key16 << 16 | (0xffff - slot): slices cover
+// ascending index ranges and list their candidates in order, so among equal keys the
+// smaller slot is the smaller index.
 constexpr int kTopkThreads = 256;
 constexpr int kTopkMaxK = 64;
 constexpr int kTopkMaxSlices = 64;
@@ -89,101 +93,119 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t index) {
   return ((uint64_t)key << 24) | (uint64_t)(0xffffffu - index);
 }
 
-// Radix selection over the CTA: every thread holds n composites in c[]; returns the
-// k-th largest.  hist: 256 ints of shared memory; bc: 2 ints of shared memory.
+// Warp 0: the bin (of 256, scanning from the top) holding the remaining-th largest
+// counted element -> bc[0] = bin, bc[1] = how many of it are still wanted, bc[2] = its
+// count.  Lane l owns bins 255 - 8l .. 248 - 8l; a prefix sum over lanes finds the lane.
+__device__ __forceinline__ void find_bin(const int *hist, int remaining, int *bc) {
+  const int lane = threadIdx.x;
+  int cnt[8], local = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    cnt[i] = hist[255 - 8 * lane - i];
+    local += cnt[i];
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, incl >= remaining);
+  if (lane == __ffs(hit) - 1) {
+    int cum = incl - local;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (cum + cnt[i] >= remaining) {
+        bc[0] = 255 - 8 * lane - i;
+        bc[1] = remaining - cum;
+        bc[2] = cnt[i];
+        break;
+      }
+      cum += cnt[i];
+    }
+  }
+}
+
+// Radix selection over the CTA: every thread holds n distinct 32-bit composites in c[];
+// returns a threshold th such that exactly k of them are >= th: the k-th largest, or a
+// prefix of it as soon as the bin holding it holds exactly the elements still wanted
+// (without ties at the boundary, after the two key bytes).  hist: 2 x 256 ints (one per
+// pass in turn, the next one cleared while the current one fills), bc: 3 ints of shared
+// memory.
 template <int NMAX>
-__device__ uint64_t select_kth(const uint64_t (&c)[NMAX], int n, int k, int *hist, int *bc) {
-  uint64_t prefix = 0;
+__device__ uint32_t select_kth(const uint32_t (&c)[NMAX], int n, int k, int *hist, int *bc) {
+  for (int b = threadIdx.x; b < 256; b += kTopkThreads) hist[b] = 0;
+  __syncthreads();
+  uint32_t prefix = 0;
   int remaining = k;
 #pragma unroll 1
-  for (int pass = 0; pass < 5; ++pass) {
-    const int shift = 32 - 8 * pass;
-    for (int b = threadIdx.x; b < 256; b += kTopkThreads) hist[b] = 0;
-    __syncthreads();
+  for (int pass = 0; pass < 4; ++pass) {
+    int *h = hist + 256 * (pass & 1);
+    int *hn = hist + 256 * ((pass + 1) & 1);
+    const int shift = 24 - 8 * pass;
+    const uint32_t above = pass == 0 ? 0u : 0xffffffffu << (shift + 8);   // bits already fixed
 #pragma unroll
     for (int i = 0; i < NMAX; ++i)
-      if (i < n && (c[i] >> (shift + 8)) == (prefix >> (shift + 8)))
-        atomicAdd(&hist[(int)((c[i] >> shift) & 0xffu)], 1);
+      if (i < n && ((c[i] ^ prefix) & above) == 0u) atomicAdd(&h[(c[i] >> shift) & 0xffu], 1);
+    for (int b = threadIdx.x; b < 256; b += kTopkThreads) hn[b] = 0;
     __syncthreads();
-    if (threadIdx.x < 32) {
-      // the bin holding the remaining-th largest, scanning from bin 255 down: lane l
-      // owns bins 255 - 8l .. 248 - 8l; a prefix sum over lanes finds the lane
-      const int lane = threadIdx.x;
-      int cnt[8], local = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        cnt[i] = hist[255 - 8 * lane - i];
-        local += cnt[i];
-      }
-      int incl = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const unsigned hit = __ballot_sync(0xffffffffu, incl >= remaining);
-      if (lane == __ffs(hit) - 1) {
-        int cum = incl - local;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (cum + cnt[i] >= remaining) {
-            bc[0] = 255 - 8 * lane - i;
-            bc[1] = remaining - cum;
-            break;
-          }
-          cum += cnt[i];
-        }
-      }
-    }
+    if (threadIdx.x < 32) find_bin(h, remaining, bc);
     __syncthreads();
-    prefix |= (uint64_t)bc[0] << shift;
+    prefix |= (uint32_t)bc[0] << shift;
     remaining = bc[1];
-    __syncthreads();
+    if (bc[2] == remaining) break;                   // the bin is taken whole: done
   }
   return prefix;
 }
 
 // grid (slices, rows).  ws: [M] int counters (zero between calls), then candidates
-// [M][slices][k] (uint64 composites).
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t *__restrict__ logits, int N,
-                                                             int k, int slice_len, uint16_t *vals,
-                                                             int32_t *idx, int *counters,
-                                                             uint64_t *cand) {
-  __shared__ int hist[256];
-  __shared__ int bc[2];
+// [M][slices][k] (40-bit global composites, each slice's in order).
+// At most 48 registers a thread (five CTAs an SM); the kernel runs many CTAs per row.
+__global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const uint16_t *__restrict__ logits, int N,
+                                                                int k, int slice_len, uint16_t *vals,
+                                                                int32_t *idx, int *counters,
+                                                                uint64_t *cand) {
+  __shared__ int hist[2 * 256];
+  __shared__ int bc[3];
   __shared__ int nsel;
   __shared__ int last;
-  __shared__ uint64_t sel[kTopkMaxK];
+  __shared__ uint32_t sel[kTopkMaxK];
   griddep_wait();
   griddep_launch_dependents();
   const int m = blockIdx.y, sl = blockIdx.x, S = gridDim.x;
   const uint16_t *row = logits + (size_t)m * N;
-  uint64_t *mycand = cand + ((size_t)m * S + sl) * k;
+  uint64_t *rowcand = cand + (size_t)m * S * k;
 
   // ---- this slice: its k best (padding past N included when the slice is short)
   {
-    uint64_t c[kTopkMaxVec * 8];
+    uint32_t c[kTopkMaxVec * 8];
     const int base = sl * slice_len;
     const int nvec = slice_len / (8 * kTopkThreads);
 #pragma unroll
     for (int e = 0; e < kTopkMaxVec; ++e) {
-      const int p = base + 8 * (threadIdx.x + kTopkThreads * e);
+      const int lp = 8 * (threadIdx.x + kTopkThreads * e);
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      const bool in = e < nvec && p < N;            // N % 8 == 0: a vector is all in or all out
-      if (in) v = __ldg(reinterpret_cast<const uint4 *>(row + p));
+      const bool in = e < nvec && base + lp < N;    // N % 8 == 0: a vector is all in or all out
+      if (in) v = __ldg(reinterpret_cast<const uint4 *>(row + base + lp));
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const uint32_t key = in ? order_key((uint16_t)(w[j >> 1] >> (16 * (j & 1)))) : 0u;
-        c[8 * e + j] = composite(key, (uint32_t)(p + j));
+        c[8 * e + j] = (key << 16) | (0xffffu - (uint32_t)(lp + j));
       }
     }
-    const uint64_t th = select_kth(c, 8 * nvec, k, hist, bc);
+    const uint32_t th = select_kth(c, 8 * nvec, k, hist, bc);
     if (threadIdx.x == 0) nsel = 0;
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kTopkMaxVec * 8; ++i)
-      if (i < 8 * nvec && c[i] >= th) mycand[atomicAdd(&nsel, 1)] = c[i];
+      if (i < 8 * nvec && c[i] >= th) sel[atomicAdd(&nsel, 1)] = c[i];
+    __syncthreads();
+    for (int a = threadIdx.x; a < k; a += kTopkThreads) {     // listed in order
+      int rank = 0;
+      for (int b = 0; b < k; ++b) rank += sel[b] > sel[a];
+      rowcand[(size_t)sl * k + rank] = composite(sel[a] >> 16, (uint32_t)base + (0xffffu - (sel[a] & 0xffffu)));
+    }
   }
 
   // ---- publish; the last slice CTA of the row merges
@@ -198,16 +220,16 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t *__re
   if (!last) return;
   __threadfence();
 
-  uint64_t c[kTopkMerge];
+  uint32_t c[kTopkMerge];
   const int total = S * k;
-  const uint64_t *rowcand = cand + (size_t)m * S * k;
+  const unsigned long long *rc = reinterpret_cast<const unsigned long long *>(rowcand);
 #pragma unroll
   for (int i = 0; i < kTopkMerge; ++i) {
     const int q = threadIdx.x + kTopkThreads * i;
-    c[i] = q < total ? __ldcg(reinterpret_cast<const unsigned long long *>(rowcand) + q) : 0ull;
+    c[i] = q < total ? ((uint32_t)(__ldcg(rc + q) >> 24) << 16) | (0xffffu - (uint32_t)q) : 0u;
   }
   const int nmine = total > threadIdx.x ? (total - 1 - (int)threadIdx.x) / kTopkThreads + 1 : 0;
-  const uint64_t th = select_kth(c, nmine, k, hist, bc);
+  const uint32_t th = select_kth(c, nmine, k, hist, bc);
   if (threadIdx.x == 0) nsel = 0;
   __syncthreads();
 #pragma unroll
@@ -218,7 +240,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t *__re
   for (int a = threadIdx.x; a < k; a += kTopkThreads) {
     int rank = 0;
     for (int b = 0; b < k; ++b) rank += sel[b] > sel[a];
-    const int n = 0xffffff - (int)(sel[a] & 0xffffffu);
+    const uint64_t g = __ldcg(rc + (0xffffu - (sel[a] & 0xffffu)));
+    const int n = 0xffffff - (int)(g & 0xffffffu);
     idx[(size_t)m * k + rank] = n;
     vals[(size_t)m * k + rank] = row[n];
   }
