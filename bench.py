@@ -660,18 +660,28 @@ NCU_CASES = {
     "ffn_up_w4a8_m64": ("w4a8", 64, 34816, 5120, 4),
     "lm_head_w8a16_m16": ("w8a16", 16, 248320, 5120, 8),
     "prefill_w4a16_m2048": ("w4a16", 2048, 34816, 5120, 4),
+    # top-k (k = 64) over M rows of N logits: ("topk", M, N, k, 0)
+    "topk_m64": ("topk", 64, 248320, 64, 0),
 }
 
 
 def run_ncu_case(name):
-    """A small case for profiler captures: 3 eager warm-up launches of one GEMM,
-    then the launch to capture (the 4th GEMM launch of the process)."""
+    """A small case for profiler captures: 3 eager warm-up launches of one kernel,
+    then the launch to capture (the 4th launch of that kernel in the process)."""
     import __graft_entry__
     __graft_entry__.build()
     import int8_weight_quantized_int4_gb300 as q
     mode, M, N, K, bits = NCU_CASES[name]
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
+    if mode == "topk":
+        lg = synth.logits(M, N, seed=50 + M).to(dev)
+        for _ in range(4):
+            vals, idx = q.topk_logits(lg, K)
+        torch.cuda.synchronize()
+        assert q.device_error() == 0
+        print(json.dumps({"ncu_case": name, "M": M, "N": N, "k": K, "idx0": int(idx[0, 0])}))
+        return
     p = synth.make_problem(M, N, K, seed=1, bits=bits, outlier_frac=0.01)
     packed = (q.qpack_w4 if bits == 4 else q.qpack_w8)(p.codes.to(dev), p.scales.to(dev))
     x = p.x.to(dev)

@@ -83,6 +83,7 @@ constexpr int kTopkMaxK = 64;
 constexpr int kTopkMaxSlices = 64;
 constexpr int kTopkMaxVec = 2;                 // 16-byte vectors per thread per slice
 constexpr int kTopkMerge = kTopkMaxSlices * kTopkMaxK / kTopkThreads;   // candidates per thread
+static_assert(kTopkMaxSlices * kTopkMaxK <= kTopkMaxVec * 8 * kTopkThreads, "one list serves both selections");
 
 __device__ __forceinline__ uint32_t order_key(uint16_t h) {
   if (h == 0x8000u) h = 0;                      // -0 ties with +0
@@ -129,24 +130,42 @@ __device__ __forceinline__ void find_bin(const int *hist, int remaining, int *bc
 // Radix selection over the CTA: every thread holds n distinct 32-bit composites in c[];
 // returns a threshold th such that exactly k of them are >= th: the k-th largest, or a
 // prefix of it as soon as the bin holding it holds exactly the elements still wanted
-// (without ties at the boundary, after the two key bytes).  hist: 2 x 256 ints (one per
-// pass in turn, the next one cleared while the current one fills), bc: 3 ints of shared
-// memory.
+// (without ties at the boundary, after the two key bytes).  The first 8-bit pass runs over
+// the registers; the elements of its boundary bin (usually a small fraction) are then
+// listed in shared memory and the later passes run over that list.  hist: 2 x 256 ints
+// (one per pass in turn, the next one cleared while the current one fills), bc: 3 ints,
+// list: room for every element of the CTA, nlist: 1 int, all shared memory.
 template <int NMAX>
-__device__ uint32_t select_kth(const uint32_t (&c)[NMAX], int n, int k, int *hist, int *bc) {
+__device__ uint32_t select_kth(const uint32_t (&c)[NMAX], int n, int k, int *hist, int *bc,
+                               uint32_t *list, int *nlist) {
   for (int b = threadIdx.x; b < 256; b += kTopkThreads) hist[b] = 0;
+  if (threadIdx.x == 0) *nlist = 0;
   __syncthreads();
-  uint32_t prefix = 0;
-  int remaining = k;
+#pragma unroll
+  for (int i = 0; i < NMAX; ++i)
+    if (i < n) atomicAdd(&hist[c[i] >> 24], 1);
+  for (int b = threadIdx.x; b < 256; b += kTopkThreads) hist[256 + b] = 0;
+  __syncthreads();
+  if (threadIdx.x < 32) find_bin(hist, k, bc);
+  __syncthreads();
+  uint32_t prefix = (uint32_t)bc[0] << 24;
+  int remaining = bc[1];
+  if (bc[2] == remaining) return prefix;            // the bin is taken whole: done
+#pragma unroll
+  for (int i = 0; i < NMAX; ++i)
+    if (i < n && (c[i] >> 24) == (prefix >> 24)) list[atomicAdd(nlist, 1)] = c[i];
+  __syncthreads();
+  const int T = *nlist;
 #pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
+  for (int pass = 1; pass < 4; ++pass) {
     int *h = hist + 256 * (pass & 1);
     int *hn = hist + 256 * ((pass + 1) & 1);
     const int shift = 24 - 8 * pass;
-    const uint32_t above = pass == 0 ? 0u : 0xffffffffu << (shift + 8);   // bits already fixed
-#pragma unroll
-    for (int i = 0; i < NMAX; ++i)
-      if (i < n && ((c[i] ^ prefix) & above) == 0u) atomicAdd(&h[(c[i] >> shift) & 0xffu], 1);
+    const uint32_t above = 0xffffffffu << (shift + 8);   // bits already fixed
+    for (int j = threadIdx.x; j < T; j += kTopkThreads) {
+      const uint32_t v = list[j];
+      if (((v ^ prefix) & above) == 0u) atomicAdd(&h[(v >> shift) & 0xffu], 1);
+    }
     for (int b = threadIdx.x; b < 256; b += kTopkThreads) hn[b] = 0;
     __syncthreads();
     if (threadIdx.x < 32) find_bin(h, remaining, bc);
@@ -168,6 +187,8 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const uint16_t *_
   __shared__ int hist[2 * 256];
   __shared__ int bc[3];
   __shared__ int nsel;
+  __shared__ int nlist;
+  __shared__ uint32_t list[kTopkMaxVec * 8 * kTopkThreads];   // >= kTopkMaxSlices * kTopkMaxK
   __shared__ int last;
   __shared__ uint32_t sel[kTopkMaxK];
   griddep_wait();
@@ -194,7 +215,7 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const uint16_t *_
         c[8 * e + j] = (key << 16) | (0xffffu - (uint32_t)(lp + j));
       }
     }
-    const uint32_t th = select_kth(c, 8 * nvec, k, hist, bc);
+    const uint32_t th = select_kth(c, 8 * nvec, k, hist, bc, list, &nlist);
     if (threadIdx.x == 0) nsel = 0;
     __syncthreads();
 #pragma unroll
@@ -229,7 +250,7 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const uint16_t *_
     c[i] = q < total ? ((uint32_t)(__ldcg(rc + q) >> 24) << 16) | (0xffffu - (uint32_t)q) : 0u;
   }
   const int nmine = total > threadIdx.x ? (total - 1 - (int)threadIdx.x) / kTopkThreads + 1 : 0;
-  const uint32_t th = select_kth(c, nmine, k, hist, bc);
+  const uint32_t th = select_kth(c, nmine, k, hist, bc, list, &nlist);
   if (threadIdx.x == 0) nsel = 0;
   __syncthreads();
 #pragma unroll
