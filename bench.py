@@ -660,6 +660,7 @@ NCU_CASES = {
     "ffn_up_w4a8_m64": ("w4a8", 64, 34816, 5120, 4),
     "lm_head_w8a16_m16": ("w8a16", 16, 248320, 5120, 8),
     "prefill_w4a16_m2048": ("w4a16", 2048, 34816, 5120, 4),
+    "prefill_w4a8_m2048": ("w4a8", 2048, 34816, 5120, 4),
     # top-k (k = 64) over M rows of N logits: ("topk", M, N, k, 0)
     "topk_m64": ("topk", 64, 248320, 64, 0),
 }

@@ -632,6 +632,18 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
           else if constexpr (W == 16) tmem_ld16(tacc + (uint32_t)(q * BN + cc), v[q]);
           else tmem_ld8(tacc + (uint32_t)(q * BN + cc), v[q]);
         }
+        // Wide tiles (one issuer, 32 columns per TMEM load; the epilogue holds up the
+        // next tile's MMAs there) load the token scales of the 32 columns before using
+        // any, so that their latencies overlap; narrow tiles read them as they go
+        // (measured faster for those).
+        constexpr bool kBatchScales = TOKSCALE && !QIN && BN >= 128;
+        float tsc[W];
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+          tsc[j] = 1.0f;
+          if constexpr (kBatchScales)
+            if (!part && cc + j < mv) tsc[j] = __ldg(a.xs + m0 + cc + j);
+        }
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < W; ++j) {
@@ -644,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
               part[(cc + j) * kRows + row] = acc;
             } else {
               const int m = m0 + cc + j;
-              const float val = QIN ? acc * sxs[m] : TOKSCALE ? acc * __ldg(a.xs + m) : acc;
+              const float val = QIN ? acc * sxs[m] : kBatchScales ? acc * tsc[j] : TOKSCALE ? acc * __ldg(a.xs + m) : acc;
               a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
             }
           }
