@@ -199,3 +199,60 @@ def test_counter_region_is_shared_by_every_plan():
 def test_w4a8_workspace_holds_widened_codes():
     p = q.plan(1, 8192, 34816, 5120, 152)
     assert p.ws_bytes >= 8192 * 5120 * 2
+
+
+def _topk_expected_ws(M, N, k):
+    """The slice plan restated: slices of 2048 or 4096 positions, at most 64, covering N;
+    workspace = M counters (256-byte aligned) + M x slices x k 8-byte candidates."""
+    slices = min(64, max(1, -(-N // 2048)))
+    per = -(-N // slices)
+    slice_len = -(-per // 2048) * 2048
+    slices = -(-N // slice_len)
+    assert slice_len <= 4096 and slices <= 64 and slices * slice_len >= N
+    counters = -(-(M * 4) // 256) * 256
+    return counters, counters + M * slices * k * 8
+
+
+@pytest.mark.parametrize("M,N,k", [(1, 248320, 64), (64, 248320, 64), (3, 4096, 1), (2, 2056, 17),
+                                   (5, 8, 8), (7, 262144, 50), (1, 131080, 64)])
+def test_topk_workspace_sizes(M, N, k):
+    L = q.lib()
+    zero, total = _topk_expected_ws(M, N, k)
+    assert L.topk_workspace_zero_bytes(M, N, k) == zero
+    assert L.topk_workspace_bytes(M, N, k) == total
+
+
+def test_topk_and_gather_argument_errors_before_device():
+    L = q.lib()
+    n = ctypes.c_void_p(0)
+    # unsupported top-k shapes: k out of [1, 64], k > N, N not a multiple of 8, N too large
+    for M, N, k in [(1, 256, 0), (1, 256, 65), (1, 16, 17), (1, 260, 4), (1, 262144 + 8, 4)]:
+        assert L.topk_workspace_bytes(M, N, k) == 0
+        assert L.topk_logits(FAKE, M, N, k, FAKE, FAKE, FAKE, 1 << 20, n) == q.QW_ERR_UNSUPPORTED_SHAPE
+    assert L.topk_logits(FAKE, -1, 256, 4, FAKE, FAKE, FAKE, 1 << 20, n) == q.QW_ERR_INVALID_ARG
+    assert L.topk_logits(n, 0, 256, 4, n, n, n, 0, n) == q.QW_OK             # no rows: nothing to do
+    assert L.topk_logits(n, 2, 256, 4, FAKE, FAKE, FAKE, 1 << 20, n) == q.QW_ERR_INVALID_ARG
+    assert L.topk_logits(MIS, 2, 256, 4, FAKE, FAKE, FAKE, 1 << 20, n) == q.QW_ERR_ALIGNMENT
+    need = L.topk_workspace_bytes(2, 256, 4)
+    assert L.topk_logits(FAKE, 2, 256, 4, FAKE, FAKE, FAKE, need - 1, n) == q.QW_ERR_WORKSPACE
+    assert L.topk_logits(FAKE, 2, 256, 4, FAKE, FAKE, n, 0, n) == q.QW_ERR_WORKSPACE
+    # gather: shapes, pointers, alignment
+    assert L.embed_gather_w8(FAKE, -1, FAKE, 256, 256, FAKE, n) == q.QW_ERR_INVALID_ARG
+    assert L.embed_gather_w8(FAKE, 4, FAKE, 200, 256, FAKE, n) == q.QW_ERR_UNSUPPORTED_SHAPE
+    assert L.embed_gather_w8(FAKE, 4, FAKE, 256, 0, FAKE, n) == q.QW_ERR_UNSUPPORTED_SHAPE
+    assert L.embed_gather_w8(n, 0, n, 256, 256, n, n) == q.QW_OK                # no tokens
+    assert L.embed_gather_w8(n, 4, FAKE, 256, 256, FAKE, n) == q.QW_ERR_INVALID_ARG
+    assert L.embed_gather_w8(FAKE, 4, MIS, 256, 256, FAKE, n) == q.QW_ERR_ALIGNMENT
+    # the fused W4A8 entry point shares the GEMM checks
+    assert L.qgemm_w4a8_fused(FAKE, FAKE, 4, 512, 100, FAKE, n, 0, n) == q.QW_ERR_UNSUPPORTED_SHAPE
+    assert L.qgemm_w4a8_fused(n, FAKE, 4, 512, 256, FAKE, n, 0, n) == q.QW_ERR_INVALID_ARG
+    assert L.qgemm_w4a8_fused(n, n, 0, 512, 256, n, n, 0, n) == q.QW_OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_next_rows_report_arch_without_device():
+    L = q.lib()
+    n = ctypes.c_void_p(0)
+    need = L.topk_workspace_bytes(2, 256, 4)
+    assert L.topk_logits(FAKE, 2, 256, 4, FAKE, FAKE, FAKE, need, n) == q.QW_ERR_ARCH
+    assert L.embed_gather_w8(FAKE, 4, FAKE, 256, 256, FAKE, n) == q.QW_ERR_ARCH
