@@ -72,12 +72,14 @@ cudaError_t launch_embed_gather(const int32_t *ids, int T, const void *packed, i
 // order-preserving 16-bit integer (-0 taken as +0, so the two tie); positions past N get
 // key 0, which no finite fp16 value maps to.  Within a slice of at most 4096 positions an
 // element is the 32-bit composite  key16 << 16 | (0xffff - local position), unique and in
-// exactly that order.  The slice's k largest are found by radix selection (8-bit passes,
-// histograms in shared memory) and listed in order in the workspace as 40-bit global
-// composites  key16 << 24 | (2^24 - 1 - index).  The last slice CTA of a row selects
-// again over the row's S k candidates as  key16 << 16 | (0xffff - slot): slices cover
-// ascending index ranges and list their candidates in order, so among equal keys the
-// smaller slot is the smaller index.
+// exactly that order.  A slice finds its k largest by radix selection: a first 8-bit pass
+// over the top byte of the keys (computed two at a time from the packed fp16 words), then
+// only the elements above the boundary bin (all taken) and in it (listed in shared memory
+// for the next 8-bit passes) become composites.  It lists its winners in order in the
+// workspace as 40-bit global composites  key16 << 24 | (2^24 - 1 - index).  The last slice
+// CTA of a row selects again, the same way, over the row's S k candidates as
+// key16 << 16 | (0xffff - slot): slices cover ascending index ranges and list their
+// candidates in order, so among equal keys the smaller slot is the smaller index.
 constexpr int kTopkThreads = 256;
 constexpr int kTopkMaxK = 64;
 constexpr int kTopkMaxSlices = 64;
@@ -85,9 +87,15 @@ constexpr int kTopkMaxVec = 2;                 // 16-byte vectors per thread per
 constexpr int kTopkMerge = kTopkMaxSlices * kTopkMaxK / kTopkThreads;   // candidates per thread
 static_assert(kTopkMaxSlices * kTopkMaxK <= kTopkMaxVec * 8 * kTopkThreads, "one list serves both selections");
 
-__device__ __forceinline__ uint32_t order_key(uint16_t h) {
-  if (h == 0x8000u) h = 0;                      // -0 ties with +0
-  return (h & 0x8000u) ? (uint32_t)(~h & 0xffffu) : (uint32_t)(h | 0x8000u);
+// Two order keys from a word holding two fp16 values (low half = the lower position):
+// -0 becomes +0 (x + 0 is exact for every other value), then a negative value's bits are
+// inverted and a non-negative value's sign bit is set.
+__device__ __forceinline__ uint32_t order_keys2(uint32_t w) {
+  __half2 h = *reinterpret_cast<const __half2 *>(&w);
+  h = __hadd2(h, __float2half2_rn(0.0f));
+  const uint32_t x = *reinterpret_cast<const uint32_t *>(&h);
+  const uint32_t s = (x >> 15) & 0x00010001u;     // the two sign bits, at bits 0 and 16
+  return x ^ (s * 0x7fffu + 0x80008000u);         // 0xffff or 0x8000 per half
 }
 
 __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t index) {
@@ -127,54 +135,87 @@ __device__ __forceinline__ void find_bin(const int *hist, int remaining, int *bc
   }
 }
 
-// Radix selection over the CTA: every thread holds n distinct 32-bit composites in c[];
-// returns a threshold th such that exactly k of them are >= th: the k-th largest, or a
-// prefix of it as soon as the bin holding it holds exactly the elements still wanted
-// (without ties at the boundary, after the two key bytes).  The first 8-bit pass runs over
-// the registers; the elements of its boundary bin (usually a small fraction) are then
-// listed in shared memory and the later passes run over that list.  hist: 2 x 256 ints
-// (one per pass in turn, the next one cleared while the current one fills), bc: 3 ints,
-// list: room for every element of the CTA, nlist: 1 int, all shared memory.
-template <int NMAX>
-__device__ uint32_t select_kth(const uint32_t (&c)[NMAX], int n, int k, int *hist, int *bc,
-                               uint32_t *list, int *nlist) {
-  for (int b = threadIdx.x; b < 256; b += kTopkThreads) hist[b] = 0;
-  if (threadIdx.x == 0) *nlist = 0;
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < NMAX; ++i)
-    if (i < n) atomicAdd(&hist[c[i] >> 24], 1);
-  for (int b = threadIdx.x; b < 256; b += kTopkThreads) hist[256 + b] = 0;
-  __syncthreads();
-  if (threadIdx.x < 32) find_bin(hist, k, bc);
-  __syncthreads();
-  uint32_t prefix = (uint32_t)bc[0] << 24;
-  int remaining = bc[1];
-  if (bc[2] == remaining) return prefix;            // the bin is taken whole: done
-#pragma unroll
-  for (int i = 0; i < NMAX; ++i)
-    if (i < n && (c[i] >> 24) == (prefix >> 24)) list[atomicAdd(nlist, 1)] = c[i];
-  __syncthreads();
-  const int T = *nlist;
+// The shared state of one selection: hist 2 x 256 ints (one per pass in turn, the next
+// cleared while the current one fills), bc 3 ints, the boundary-bin list and the winners.
+struct TopkSmem {
+  int hist[2 * 256];
+  int bc[3];
+  int nlist, nsel;
+  uint32_t list[kTopkMaxVec * 8 * kTopkThreads];   // >= kTopkMaxSlices * kTopkMaxK
+  uint32_t sel[kTopkMaxK];
+};
+
+// Called by the whole CTA after the first pass (over the top byte) found the boundary bin
+// b0 with r0 of its elements still wanted, every element of the CTA above b0 already in
+// sel and every element in b0 in the list (T of them, all distinct composites with top
+// byte b0), hist[256..511] zero.  Unless the bin is taken whole, the next 8-bit passes run
+// over the list; its elements at or above the resulting threshold join sel, which then
+// holds exactly k composites.
+__device__ void finish_select(TopkSmem &sm, uint32_t b0, int r0, bool whole) {
+  const int T = sm.nlist;
+  if (whole) {
+    for (int j = threadIdx.x; j < T; j += kTopkThreads) sm.sel[atomicAdd(&sm.nsel, 1)] = sm.list[j];
+    __syncthreads();
+    return;
+  }
+  uint32_t prefix = b0 << 24;
+  int remaining = r0;
 #pragma unroll 1
   for (int pass = 1; pass < 4; ++pass) {
-    int *h = hist + 256 * (pass & 1);
-    int *hn = hist + 256 * ((pass + 1) & 1);
+    int *h = sm.hist + 256 * (pass & 1);
+    int *hn = sm.hist + 256 * ((pass + 1) & 1);
     const int shift = 24 - 8 * pass;
     const uint32_t above = 0xffffffffu << (shift + 8);   // bits already fixed
     for (int j = threadIdx.x; j < T; j += kTopkThreads) {
-      const uint32_t v = list[j];
+      const uint32_t v = sm.list[j];
       if (((v ^ prefix) & above) == 0u) atomicAdd(&h[(v >> shift) & 0xffu], 1);
     }
     for (int b = threadIdx.x; b < 256; b += kTopkThreads) hn[b] = 0;
     __syncthreads();
-    if (threadIdx.x < 32) find_bin(h, remaining, bc);
+    if (threadIdx.x < 32) find_bin(h, remaining, sm.bc);
     __syncthreads();
-    prefix |= (uint32_t)bc[0] << shift;
-    remaining = bc[1];
-    if (bc[2] == remaining) break;                   // the bin is taken whole: done
+    prefix |= (uint32_t)sm.bc[0] << shift;
+    remaining = sm.bc[1];
+    if (sm.bc[2] == remaining) break;                 // the bin is taken whole: done
   }
-  return prefix;
+  for (int j = threadIdx.x; j < T; j += kTopkThreads)
+    if (sm.list[j] >= prefix) sm.sel[atomicAdd(&sm.nsel, 1)] = sm.list[j];
+  __syncthreads();
+}
+
+// First pass over register composites c[0..n) (at least k of them in the CTA): histogram
+// of the top byte, boundary bin, then the split into winners and list; returns with sel
+// holding the k largest.
+template <int NMAX>
+__device__ void select_regs(const uint32_t (&c)[NMAX], int n, int k, TopkSmem &sm) {
+  for (int b = threadIdx.x; b < 512; b += kTopkThreads) sm.hist[b] = 0;
+  if (threadIdx.x == 0) sm.nlist = sm.nsel = 0;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < NMAX; ++i)
+    if (i < n) atomicAdd(&sm.hist[c[i] >> 24], 1);
+  __syncthreads();
+  if (threadIdx.x < 32) find_bin(sm.hist, k, sm.bc);
+  __syncthreads();
+  const uint32_t b0 = (uint32_t)sm.bc[0];
+  const int r0 = sm.bc[1];
+  const bool whole = sm.bc[2] == r0;
+#pragma unroll
+  for (int i = 0; i < NMAX; ++i) {
+    if (i >= n) continue;
+    const uint32_t tb = c[i] >> 24;
+    if (tb > b0) sm.sel[atomicAdd(&sm.nsel, 1)] = c[i];
+    else if (tb == b0) sm.list[atomicAdd(&sm.nlist, 1)] = c[i];
+  }
+  __syncthreads();
+  finish_select(sm, b0, r0, whole);
+}
+
+// sel's k distinct composites in decreasing order: the rank of each among them.
+__device__ __forceinline__ int rank_of(const uint32_t *sel, int k, int a) {
+  int rank = 0;
+  for (int b = 0; b < k; ++b) rank += sel[b] > sel[a];
+  return rank;
 }
 
 // grid (slices, rows).  ws: [M] int counters (zero between calls), then candidates
@@ -184,13 +225,8 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const uint16_t *_
                                                                 int k, int slice_len, uint16_t *vals,
                                                                 int32_t *idx, int *counters,
                                                                 uint64_t *cand) {
-  __shared__ int hist[2 * 256];
-  __shared__ int bc[3];
-  __shared__ int nsel;
-  __shared__ int nlist;
-  __shared__ uint32_t list[kTopkMaxVec * 8 * kTopkThreads];   // >= kTopkMaxSlices * kTopkMaxK
+  __shared__ TopkSmem sm;
   __shared__ int last;
-  __shared__ uint32_t sel[kTopkMaxK];
   griddep_wait();
   griddep_launch_dependents();
   const int m = blockIdx.y, sl = blockIdx.x, S = gridDim.x;
@@ -199,34 +235,54 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const uint16_t *_
 
   // ---- this slice: its k best (padding past N included when the slice is short)
   {
-    uint32_t c[kTopkMaxVec * 8];
+    uint32_t kw[kTopkMaxVec * 4];                     // order keys, two per word
     const int base = sl * slice_len;
     const int nvec = slice_len / (8 * kTopkThreads);
 #pragma unroll
     for (int e = 0; e < kTopkMaxVec; ++e) {
       const int lp = 8 * (threadIdx.x + kTopkThreads * e);
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
       const bool in = e < nvec && base + lp < N;    // N % 8 == 0: a vector is all in or all out
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (in) v = __ldg(reinterpret_cast<const uint4 *>(row + base + lp));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      kw[4 * e + 0] = in ? order_keys2(v.x) : 0u;
+      kw[4 * e + 1] = in ? order_keys2(v.y) : 0u;
+      kw[4 * e + 2] = in ? order_keys2(v.z) : 0u;
+      kw[4 * e + 3] = in ? order_keys2(v.w) : 0u;
+    }
+    for (int b = threadIdx.x; b < 512; b += kTopkThreads) sm.hist[b] = 0;
+    if (threadIdx.x == 0) sm.nlist = sm.nsel = 0;
+    __syncthreads();
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t key = in ? order_key((uint16_t)(w[j >> 1] >> (16 * (j & 1)))) : 0u;
-        c[8 * e + j] = (key << 16) | (0xffffu - (uint32_t)(lp + j));
+    for (int w = 0; w < kTopkMaxVec * 4; ++w)
+      if (w < 4 * nvec) {
+        atomicAdd(&sm.hist[(kw[w] >> 8) & 0xffu], 1);
+        atomicAdd(&sm.hist[kw[w] >> 24], 1);
+      }
+    __syncthreads();
+    if (threadIdx.x < 32) find_bin(sm.hist, k, sm.bc);
+    __syncthreads();
+    const uint32_t b0 = (uint32_t)sm.bc[0];
+    const int r0 = sm.bc[1];
+    const bool whole = sm.bc[2] == r0;
+#pragma unroll
+    for (int w = 0; w < kTopkMaxVec * 4; ++w) {
+      if (w >= 4 * nvec) continue;
+      const uint32_t pos = (uint32_t)(8 * (threadIdx.x + kTopkThreads * (w >> 2)) + 2 * (w & 3));
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const uint32_t key = hf ? kw[w] >> 16 : kw[w] & 0xffffu;
+        const uint32_t tb = key >> 8;
+        if (tb < b0) continue;
+        const uint32_t c = (key << 16) | (0xffffu - (pos + hf));
+        if (tb > b0) sm.sel[atomicAdd(&sm.nsel, 1)] = c;
+        else sm.list[atomicAdd(&sm.nlist, 1)] = c;
       }
     }
-    const uint32_t th = select_kth(c, 8 * nvec, k, hist, bc, list, &nlist);
-    if (threadIdx.x == 0) nsel = 0;
     __syncthreads();
-#pragma unroll
-    for (int i = 0; i < kTopkMaxVec * 8; ++i)
-      if (i < 8 * nvec && c[i] >= th) sel[atomicAdd(&nsel, 1)] = c[i];
-    __syncthreads();
-    for (int a = threadIdx.x; a < k; a += kTopkThreads) {     // listed in order
-      int rank = 0;
-      for (int b = 0; b < k; ++b) rank += sel[b] > sel[a];
-      rowcand[(size_t)sl * k + rank] = composite(sel[a] >> 16, (uint32_t)base + (0xffffu - (sel[a] & 0xffffu)));
-    }
+    finish_select(sm, b0, r0, whole);
+    for (int a = threadIdx.x; a < k; a += kTopkThreads)     // listed in order
+      rowcand[(size_t)sl * k + rank_of(sm.sel, k, a)] =
+          composite(sm.sel[a] >> 16, (uint32_t)base + (0xffffu - (sm.sel[a] & 0xffffu)));
   }
 
   // ---- publish; the last slice CTA of the row merges
@@ -250,19 +306,12 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const uint16_t *_
     c[i] = q < total ? ((uint32_t)(__ldcg(rc + q) >> 24) << 16) | (0xffffu - (uint32_t)q) : 0u;
   }
   const int nmine = total > threadIdx.x ? (total - 1 - (int)threadIdx.x) / kTopkThreads + 1 : 0;
-  const uint32_t th = select_kth(c, nmine, k, hist, bc, list, &nlist);
-  if (threadIdx.x == 0) nsel = 0;
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < kTopkMerge; ++i)
-    if (i < nmine && c[i] >= th) sel[atomicAdd(&nsel, 1)] = c[i];
-  __syncthreads();
+  select_regs(c, nmine, k, sm);
   // rank sort of the k winners (all distinct), largest first
   for (int a = threadIdx.x; a < k; a += kTopkThreads) {
-    int rank = 0;
-    for (int b = 0; b < k; ++b) rank += sel[b] > sel[a];
-    const uint64_t g = __ldcg(rc + (0xffffu - (sel[a] & 0xffffu)));
+    const uint64_t g = __ldcg(rc + (0xffffu - (sm.sel[a] & 0xffffu)));
     const int n = 0xffffff - (int)(g & 0xffffffu);
+    const int rank = rank_of(sm.sel, k, a);
     idx[(size_t)m * k + rank] = n;
     vals[(size_t)m * k + rank] = row[n];
   }
