@@ -15,10 +15,13 @@
 namespace qw {
 
 // ---------------------------------------------------------------- gather --
-// One CTA per token.  Feature k of table row v sits in chunk (v / 128, k / 128) of the
+// One CTA per token, kGatherPer 16-feature pieces per thread with all their loads issued
+// before any is used.  Feature k of table row v sits in chunk (v / 128, k / 128) of the
 // packed table, slice (k % 128) / 16, at byte (v % 128) * 16 + k % 16, stored as
 // code XOR 0x80; the row's fp16 scale follows the slices.  out = fp16(code * scale),
 // one rounding (__hmul_rn of two exact fp16 operands).
+constexpr int kGatherPer = 2;
+
 __global__ void __launch_bounds__(256) embed_gather_kernel(const int32_t *__restrict__ ids,
                                                            const uint8_t *__restrict__ packed, int V,
                                                            int D, uint16_t *__restrict__ out,
@@ -36,32 +39,49 @@ __global__ void __launch_bounds__(256) embed_gather_kernel(const int32_t *__rest
   }
   const int r = v % kRows;
   const uint8_t *tile = packed + (size_t)(v / kRows) * G * kChunkW8;
-  for (int p = threadIdx.x; p < G * 8; p += blockDim.x) {       // 16 features per piece
-    const int g = p >> 3, j = p & 7;
-    const uint8_t *chunk = tile + (size_t)g * kChunkW8;
-    const uint4 c = __ldg(reinterpret_cast<const uint4 *>(chunk + j * 2048 + r * 16));
-    const __half s = __ushort_as_half(__ldg(reinterpret_cast<const unsigned short *>(chunk + 16384 + r * 2)));
-    const uint32_t w[4] = {c.x ^ 0x80808080u, c.y ^ 0x80808080u, c.z ^ 0x80808080u, c.w ^ 0x80808080u};
-    uint32_t o[8];
+  for (int p0 = threadIdx.x; p0 < G * 8; p0 += kGatherPer * blockDim.x) {
+    uint4 c[kGatherPer];
+    __half s[kGatherPer];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int q0 = (int)(int8_t)((w[i] >> (16 * h)) & 0xffu);
-        const int q1 = (int)(int8_t)((w[i] >> (16 * h + 8)) & 0xffu);
-        const __half a = __hmul_rn(__int2half_rn(q0), s), b = __hmul_rn(__int2half_rn(q1), s);
-        o[2 * i + h] = (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
-      }
+    for (int u = 0; u < kGatherPer; ++u) {
+      const int p = p0 + u * blockDim.x;              // 16 features per piece
+      if (p >= G * 8) break;
+      const uint8_t *chunk = tile + (size_t)(p >> 3) * kChunkW8;
+      c[u] = __ldg(reinterpret_cast<const uint4 *>(chunk + (p & 7) * 2048 + r * 16));
+      s[u] = __ushort_as_half(__ldg(reinterpret_cast<const unsigned short *>(chunk + 16384 + r * 2)));
     }
-    uint4 *dst = orow + (size_t)(g * kGroup + j * 16) / 8;
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+    for (int u = 0; u < kGatherPer; ++u) {
+      const int p = p0 + u * blockDim.x;
+      if (p >= G * 8) break;
+      const uint32_t w[4] = {c[u].x ^ 0x80808080u, c[u].y ^ 0x80808080u, c[u].z ^ 0x80808080u,
+                             c[u].w ^ 0x80808080u};
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int q0 = (int)(int8_t)((w[i] >> (16 * h)) & 0xffu);
+          const int q1 = (int)(int8_t)((w[i] >> (16 * h + 8)) & 0xffu);
+          const __half a = __hmul_rn(__int2half_rn(q0), s[u]), b = __hmul_rn(__int2half_rn(q1), s[u]);
+          o[2 * i + h] = (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+        }
+      }
+      uint4 *dst = orow + (size_t)((p >> 3) * kGroup + (p & 7) * 16) / 8;
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
   }
 }
 
 cudaError_t launch_embed_gather(const int32_t *ids, int T, const void *packed, int V, int D,
                                 uint16_t *out, int *err, cudaStream_t st) {
-  cudaError_t e = launch_pdl(reinterpret_cast<const void *>(embed_gather_kernel), dim3(T), dim3(256), 0,
+  // kGatherPer pieces of 16 features per thread: D / 32 threads, in whole warps, 32..256
+  int threads = (D / 16 + kGatherPer - 1) / kGatherPer;
+  threads = (threads + 31) / 32 * 32;
+  if (threads > 256) threads = 256;
+  if (threads < 32) threads = 32;
+  cudaError_t e = launch_pdl(reinterpret_cast<const void *>(embed_gather_kernel), dim3(T), dim3(threads), 0,
                              st, ids, static_cast<const uint8_t *>(packed), V, D, out, err);
   count_launch();
   return e;
