@@ -256,3 +256,51 @@ def test_next_rows_report_arch_without_device():
     need = L.topk_workspace_bytes(2, 256, 4)
     assert L.topk_logits(FAKE, 2, 256, 4, FAKE, FAKE, FAKE, need, n) == q.QW_ERR_ARCH
     assert L.embed_gather_w8(FAKE, 4, FAKE, 256, 256, FAKE, n) == q.QW_ERR_ARCH
+
+
+def _check_partition(p):
+    """Every (tile, group) chunk belongs to exactly one segment of one CTA; a segment that
+    cuts a tile has a partial slot of its own CTA (2p or 2p + 1); a cut tile's pieces come
+    from consecutive CTAs in K order and cover its groups without gaps."""
+    owner = {}
+    slots = set()
+    pieces = {}
+    for cta in range(p.grid):
+        for tile, g0, g1, slot in q.plan_segments(p, cta):
+            assert 0 <= tile < p.tiles and 0 <= g0 < g1 <= p.groups
+            for g in range(g0, g1):
+                assert (tile, g) not in owner
+                owner[(tile, g)] = cta
+            if g0 == 0 and g1 == p.groups:
+                assert slot == -1
+            else:
+                assert p.stream_k and slot in (2 * cta, 2 * cta + 1) and slot not in slots
+                slots.add(slot)
+                pieces.setdefault(tile, []).append((g0, g1, cta))
+    assert len(owner) == p.chunks
+    for tile, ps in pieces.items():
+        ps.sort()
+        assert ps[0][0] == 0 and ps[-1][1] == p.groups
+        for (a0, a1, ca), (b0, b1, cb) in zip(ps, ps[1:]):
+            assert a1 == b0 and cb == ca + 1
+
+
+def test_schedule_partition_random_shapes():
+    """Seeded random shapes across all four modes, token counts 1..9000, widths up to
+    2^18 rows, depths up to 2^15 and SM counts 1..152: the chunk partition invariants hold
+    and the plan fits the device limits."""
+    import random
+    rng = random.Random(20261202)
+    for _ in range(120):
+        mode = rng.randrange(4)
+        M = rng.choice([1, 2, 3, 4, 5, 8, 15, 16, 17, 31, 33, 64, 65, 100, 128, 129, 255, 300, 512,
+                        1000, 2048, 4097, 9000])
+        N = 128 * rng.choice([1, 2, 3, 5, 7, 40, 41, 96, 272, 1024, 1940])
+        K = 128 * rng.choice([1, 2, 3, 5, 8, 40, 41, 136])
+        sms = rng.choice([1, 2, 7, 64, 100, 148, 152])
+        p = q.plan(mode, M, N, K, sms)
+        if p.chunks > 200_000:                    # keep the CPU check quick
+            continue
+        assert 1 <= p.grid <= sms and p.smem_bytes <= 232448 and p.stages >= 2
+        assert p.bn >= min(M, 256) and p.token_tiles == -(-M // p.bn)
+        _check_partition(p)
