@@ -18,6 +18,10 @@ scales, int8 per-token activations), item 1 (int8 group-128 requantization,
   Frobenius error.
 * ``half_to_double`` / ``double_to_half`` -- binary16 conversions written from
   the format definition.
+* ``attn_int8qk(q, k, v)`` (``oracle/attention.py``, numpy) -- int8-QK causal
+  prefill attention, from the page's paragraph "int8-QK prefill attention": K
+  smoothed by its per-head channel mean, per-row int8 Q and K, binary64 softmax
+  and P.V.
 
 Every function is pinned by ``tests/test_oracle_*.py`` against brute force in
 exact rational arithmetic, closed forms and the invariants the pages imply.
@@ -29,6 +33,8 @@ import os
 import subprocess
 
 import numpy as np
+
+from .attention import attn_int8qk, quant_rows_f32, smooth_k  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")

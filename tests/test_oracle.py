@@ -319,3 +319,116 @@ def test_topk_closed_forms():
     assert list(idx[0]) == [0, 2, 3, 1]
     _, idx = oracle.topk(np.full((2, 50), 3.0, np.float16), 8)
     assert (idx == np.arange(8)).all()
+
+
+# ---- int8-QK prefill attention (the page's paragraph "int8-QK prefill attention") ----
+
+def test_attn_row_quantizer_is_the_activation_quantizer():
+    """Q and smoothed K are quantized with the activation quantizer's arithmetic: on fp16
+    rows (including a zero row and exact ties) the attention oracle's row quantizer and the
+    C quantizer agree bit for bit."""
+    rng = np.random.default_rng(41)
+    x = (rng.standard_normal((9, 96)) * 3).astype(np.float16)
+    x[3] = 0
+    x[4, :] = 0
+    x[4, 0], x[4, 1], x[4, 2] = 127.0, 0.5, -1.5          # s = 1: halves round to even
+    q1, s1 = oracle.quant_rows_f32(x.astype(np.float32))
+    q2, s2 = oracle.quant_act_int8(x)
+    assert np.array_equal(q1, q2) and np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
+    assert q1[4, 1] == 0 and q1[4, 2] == -2
+
+
+def test_attn_row_quantizer_divides():
+    """Rows built where a reciprocal multiply would give another code than the IEEE divide
+    (elements x with rne(x * (1/s)) != rne(x / s) for their row's scale): the attention
+    oracle's row quantizer matches the C quantizer bit for bit on them."""
+    allv = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    pos = np.sort(allv[np.isfinite(allv) & (allv > 0)].astype(np.float32))
+    rows = []
+    for a in pos[(pos > 0.05) & (pos < 60)][::7]:
+        xs = pos[pos <= a]
+        s = np.float32(a / np.float32(127.0))
+        odd = xs[np.rint(xs / s) != np.rint(xs * (np.float32(1.0) / s))]
+        if len(odd):
+            row = np.zeros(32, np.float32)
+            row[0] = a
+            row[1:1 + min(31, len(odd))] = odd[:31]
+            rows.append(row)
+        if len(rows) == 12:
+            break
+    x = np.array(rows, np.float32).astype(np.float16)
+    q1, s1 = oracle.quant_rows_f32(x.astype(np.float32))
+    q2, s2 = oracle.quant_act_int8(x)
+    assert np.array_equal(q1, q2) and np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
+
+
+def test_attn_two_keys_closed_form():
+    """Two keys, d = 4: codes and scales come out exact (amax = 127 * 2^-6), so the score
+    gap is 2 * 127^2 * 2^-6 * 2^-6 / sqrt(4) and the second query's output is the logistic
+    mix of the two values; the first query sees only the first key (causal)."""
+    a = 127.0 / 64.0                                       # exact in fp16
+    k = np.zeros((2, 1, 4), np.float16)
+    k[0, 0, 0], k[1, 0, 0] = -a, a                         # channel mean 0: smoothing is a no-op
+    q = np.zeros((2, 1, 4), np.float16)
+    q[0, 0, 1] = 1.0
+    q[1, 0, 0] = a
+    v = np.array([[[1.0, -2.0, 0.5, 3.0]], [[-1.0, 4.0, 0.25, 0.0]]], np.float16)
+    o = oracle.attn_int8qk(q, k, v, out_f64=True)
+    gap = 2 * 127 * 127 * 2.0 ** -12 / 2.0
+    p1 = 1.0 / (1.0 + np.exp(-gap))
+    want = (1 - p1) * v[0, 0].astype(np.float64) + p1 * v[1, 0].astype(np.float64)
+    assert np.array_equal(o[0, 0], v[0, 0].astype(np.float64))
+    assert np.allclose(o[1, 0], want, rtol=1e-13, atol=1e-15)
+
+
+def test_attn_channel_offsets_are_invisible():
+    """Smoothing removes any per-channel offset of K: with integer keys, integer offsets and
+    S a power of two every step is exact, so the outputs are bit-identical (an oracle that
+    skipped the smoothing, or averaged over channels, would differ)."""
+    rng = np.random.default_rng(42)
+    S, T, Hq, Hkv, d = 16, 8, 4, 2, 32
+    k = rng.integers(-8, 9, (S, Hkv, d)).astype(np.float16)
+    off = rng.integers(-100, 101, (1, Hkv, d)).astype(np.float16)
+    q = rng.standard_normal((T, Hq, d)).astype(np.float16)
+    v = rng.standard_normal((S, Hkv, d)).astype(np.float16)
+    o1 = oracle.attn_int8qk(q, k, v)
+    o2 = oracle.attn_int8qk(q, (k + off).astype(np.float16), v)
+    assert np.array_equal(o1.view(np.uint16), o2.view(np.uint16))
+    o3 = oracle.attn_int8qk(q, (k * 3).astype(np.float16), v)   # not an offset: must differ
+    assert not np.array_equal(o1.view(np.uint16), o3.view(np.uint16))
+
+
+def test_attn_causal_mask_and_grouped_heads():
+    """One-hot value rows tagged with their KV head: query 0 returns value 0 exactly, query 1
+    carries no weight on key 2 however large its score, query 2 puts most of it there; query
+    head h reads KV head h // 2 (the tag comes back exactly)."""
+    S, T, Hq, Hkv, d = 3, 3, 4, 2, 8
+    k = np.zeros((S, Hkv, d), np.float16)
+    k[2, :, 0] = 60.0
+    q = np.zeros((T, Hq, d), np.float16)
+    q[:, :, 0] = 2.0
+    v = np.zeros((S, Hkv, d), np.float16)
+    for j in range(S):
+        v[j, :, j] = 1.0
+    for g in range(Hkv):
+        v[:, g, 7] = g + 1
+    o = oracle.attn_int8qk(q, k, v, out_f64=True)
+    for h in range(Hq):
+        assert np.array_equal(o[0, h], v[0, h // 2].astype(np.float64))
+        assert o[1, h, 2] == 0.0 and abs(o[1, h, 0] + o[1, h, 1] - 1.0) < 1e-15
+        assert o[2, h, 2] > 0.99
+        assert np.allclose(o[:, h, 7], h // 2 + 1, rtol=0, atol=1e-12)
+
+
+def test_attn_uniform_when_keys_equal():
+    """Equal keys smooth to zero (scale 0, codes 0): every visible key gets the same
+    weight, so query i returns the mean of values 0 .. S - T + i."""
+    rng = np.random.default_rng(43)
+    S, T, H, d = 12, 5, 2, 16
+    k = np.repeat(rng.standard_normal((1, H, d)).astype(np.float16), S, axis=0)
+    q = rng.standard_normal((T, H, d)).astype(np.float16)
+    v = rng.standard_normal((S, H, d)).astype(np.float16)
+    o = oracle.attn_int8qk(q, k, v, out_f64=True)
+    for i in range(T):
+        n = S - T + i + 1
+        assert np.allclose(o[i], v[:n].astype(np.float64).mean(axis=0), rtol=0, atol=1e-13)
