@@ -122,6 +122,23 @@ def _need(t, dtype, name, ndim=None):
         raise ValueError(f"{name} must have {ndim} dimensions")
 
 
+def _need_shape(t, shape, name):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _need_packed(packed, nbytes, like, name="packed"):
+    """A packed weight buffer: a contiguous uint8 CUDA tensor on `like`'s device holding at
+    least the nbytes the layout needs for the given shape (the kernels read all of them)."""
+    _need(packed, torch.uint8, name)
+    if packed.device != like.device:
+        raise ValueError(f"{name} is on {packed.device}, the activations on {like.device}")
+    if nbytes <= 0:
+        return                          # an unsupported shape: the library rejects it
+    if packed.numel() < nbytes:
+        raise ValueError(f"{name} holds {packed.numel()} bytes, the layout needs {nbytes}")
+
+
 # ------------------------------------------------------------------ packing --
 def qpack_w4_bytes(N: int, K: int) -> int:
     return int(lib().qpack_w4_bytes(N, K))
@@ -136,8 +153,11 @@ def _pack(bits, codes, scales, out=None):
     _need(scales, torch.float16, "scales", 2)
     N, K = codes.shape
     nbytes = (qpack_w4_bytes if bits == 4 else qpack_w8_bytes)(N, K)
+    _need_shape(scales, (N, K // 128), "scales")
     if out is None:
         out = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=codes.device)
+    elif nbytes > 0:
+        _need_packed(out, nbytes, codes, "out")
     fn = lib().qpack_w4 if bits == 4 else lib().qpack_w8
     with torch.cuda.device(codes.device):
         _check(fn(_ptr(codes), _ptr(scales), N, K, _ptr(out), _stream(codes)))
@@ -161,8 +181,12 @@ def quant_act_int8(x: torch.Tensor, xq: torch.Tensor | None = None, xs: torch.Te
     M, K = x.shape
     if xq is None:
         xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    _need(xq, torch.int8, "xq", 2)
+    _need_shape(xq, (M, K), "xq")
     if xs is None:
         xs = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _need(xs, torch.float32, "xs", 1)
+    _need_shape(xs, (M,), "xs")
     with torch.cuda.device(x.device):
         _check(lib().quant_act_int8(_ptr(x), M, K, _ptr(xq), _ptr(xs), _stream(x)))
     return xq, xs
@@ -217,6 +241,8 @@ def qgemm_w4a16(x, packed, N: int, K: int, y=None, ws: Workspace | None = None):
     if x.shape[1] != K:
         raise ValueError("x.shape[1] != K")
     y = _out(y, M, N, x.device)
+    if M and N:
+        _need_packed(packed, qpack_w4_bytes(N, K), x)
     wbuf, wbytes = _ws_for(x, MODE_W4A16, M, N, K, ws)
     with torch.cuda.device(x.device):
         _check(lib().qgemm_w4a16(_ptr(x), _ptr(packed), M, N, K, _ptr(y), _ptr(wbuf), wbytes,
@@ -232,6 +258,8 @@ def qgemm_w4a8(xq, xs, packed, N: int, K: int, y=None, ws: Workspace | None = No
     if xq.shape[1] != K or xs.shape[0] != M:
         raise ValueError("shape mismatch")
     y = _out(y, M, N, xq.device)
+    if M and N:
+        _need_packed(packed, qpack_w4_bytes(N, K), xq)
     wbuf, wbytes = _ws_for(xq, MODE_W4A8, M, N, K, ws)
     with torch.cuda.device(xq.device):
         _check(lib().qgemm_w4a8(_ptr(xq), _ptr(xs), _ptr(packed), M, N, K, _ptr(y), _ptr(wbuf),
@@ -247,6 +275,8 @@ def qgemm_w4a8_fused(x, packed, N: int, K: int, y=None, ws: Workspace | None = N
     if x.shape[1] != K:
         raise ValueError("x.shape[1] != K")
     y = _out(y, M, N, x.device)
+    if M and N:
+        _need_packed(packed, qpack_w4_bytes(N, K), x)
     wbuf, wbytes = _ws_for(x, MODE_W4A8_FUSED, M, N, K, ws)
     with torch.cuda.device(x.device):
         _check(lib().qgemm_w4a8_fused(_ptr(x), _ptr(packed), M, N, K, _ptr(y), _ptr(wbuf), wbytes,
@@ -261,6 +291,8 @@ def qgemm_w8a16(x, packed, N: int, K: int, y=None, ws: Workspace | None = None):
     if x.shape[1] != K:
         raise ValueError("x.shape[1] != K")
     y = _out(y, M, N, x.device)
+    if M and N:
+        _need_packed(packed, qpack_w8_bytes(N, K), x)
     wbuf, wbytes = _ws_for(x, MODE_W8A16, M, N, K, ws)
     with torch.cuda.device(x.device):
         _check(lib().qgemm_w8a16(_ptr(x), _ptr(packed), M, N, K, _ptr(y), _ptr(wbuf), wbytes,
@@ -276,6 +308,9 @@ def embed_gather_w8(ids, packed, V: int, D: int, out=None):
     if out is None:
         out = torch.empty((T, D), dtype=torch.float16, device=ids.device)
     _need(out, torch.float16, "out", 2)
+    _need_shape(out, (T, D), "out")
+    if T:
+        _need_packed(packed, qpack_w8_bytes(V, D), ids)
     with torch.cuda.device(ids.device):
         _check(lib().embed_gather_w8(_ptr(ids), T, _ptr(packed), V, D, _ptr(out), _stream(ids)))
     return out
@@ -311,6 +346,8 @@ def qgemm_w4a16_noalloc(x, packed, N: int, K: int, y=None):
     if x.shape[1] != K:
         raise ValueError("x.shape[1] != K")
     y = _out(y, M, N, x.device)
+    if M and N:
+        _need_packed(packed, qpack_w4_bytes(N, K), x)
     with torch.cuda.device(x.device):
         _check(lib().qgemm_w4a16_noalloc(_ptr(x), _ptr(packed), M, N, K, _ptr(y), _stream(x)))
     return y

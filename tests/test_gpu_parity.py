@@ -505,3 +505,29 @@ def test_weights_immutable_option_back_to_back(q):
         assert q.device_error() == 0
     finally:
         q.set_weights_immutable(False)
+
+
+@pytest.mark.gpu
+def test_binding_rejects_short_or_misshapen_buffers(q):
+    """The binding checks every caller-supplied buffer against the shapes before anything
+    is launched: a packed table smaller than N x K needs, outputs of the wrong shape."""
+    p = synth.make_problem(2, 256, 256, seed=77)
+    packed = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
+    x = p.x.to(DEV)
+    with pytest.raises(ValueError):
+        q.qgemm_w4a16(x, packed, 512, 256)                  # N = 512 needs twice the bytes
+    with pytest.raises(ValueError):
+        q.qgemm_w8a16(x, packed, 256, 256)                  # an int8 table needs more
+    with pytest.raises(ValueError):
+        q.qgemm_w4a16(x, packed[:100], 256, 256)
+    with pytest.raises(ValueError):
+        q.quant_act_int8(x, xq=torch.empty((2, 128), dtype=torch.int8, device=DEV))
+    with pytest.raises(ValueError):
+        q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV), out=torch.empty(64, dtype=torch.uint8, device=DEV))
+    ids = torch.tensor([0, 1], dtype=torch.int32, device=DEV)
+    with pytest.raises(ValueError):
+        q.embed_gather_w8(ids, packed, 256, 256)            # a W4 buffer is too small for W8
+    torch.cuda.synchronize()
+    assert q.device_error() == 0
+    y = q.qgemm_w4a16(x, packed, 256, 256)                  # the right sizes still run
+    assert y.shape == (2, 256)
