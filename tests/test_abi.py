@@ -303,4 +303,8 @@ def test_schedule_partition_random_shapes():
             continue
         assert 1 <= p.grid <= sms and p.smem_bytes <= 232448 and p.stages >= 2
         assert p.bn >= min(M, 256) and p.token_tiles == -(-M // p.bn)
+        # the weight ring is split into one half per chunk parity, each slot with a single
+        # producer filling it in order: an odd depth would let a parity wait alias (ABA)
+        assert p.stages % 2 == 0 and 4 <= p.stages <= 16, p.stages
+        assert 2 <= p.act_stages <= 4 and p.act_block in (1, 2, 4)
         _check_partition(p)
