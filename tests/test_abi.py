@@ -22,7 +22,8 @@ def built():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as fh:
+        text = fh.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
     return sorted(set(n for n in names if n not in ("if", "while", "sizeof")))
@@ -47,7 +48,8 @@ def test_packed_sizes():
 
 
 def test_lm_head_size_matches_pages():
-    g = json.load(open(os.path.join(ROOT, "tests", "golden", "lm_head_bytes.json")))
+    with open(os.path.join(ROOT, "tests", "golden", "lm_head_bytes.json")) as fh:
+        g = json.load(fh)
     gb = q.qpack_w8_bytes(g["rows"], g["K"]) / 1e9
     lo, hi = g["accept_GB"]
     assert lo <= gb <= hi
