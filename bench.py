@@ -659,6 +659,9 @@ NCU_CASES = {
     "proj_w4a8_fused_m4": ("w4a8f", 4, 5120, 5120, 4),
     "ffn_up_w4a8_m64": ("w4a8", 64, 34816, 5120, 4),
     "lm_head_w8a16_m16": ("w8a16", 16, 248320, 5120, 8),
+    "lm_head_w4a16_m1": ("w4a16", 1, 248320, 5120, 4),
+    "lm_head_w4a16_m16": ("w4a16", 16, 248320, 5120, 4),
+    "ffn_up_w4a16_m64": ("w4a16", 64, 34816, 5120, 4),
     "prefill_w4a16_m2048": ("w4a16", 2048, 34816, 5120, 4),
     "prefill_w4a8_m2048": ("w4a8", 2048, 34816, 5120, 4),
     # top-k (k = 64) over M rows of N logits: ("topk", M, N, k, 0)

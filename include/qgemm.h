@@ -27,7 +27,12 @@
  *     word; qw_device_error() reads and clears it.
  *   - Shapes: K and N must be positive multiples of 128.  M = 0 or N = 0 is
  *     an empty problem and returns QW_OK without enqueuing work.
- *   - Every pointer must be 16-byte aligned.
+ *   - Alignment, checked on every call (QW_ERR_ALIGNMENT otherwise): GEMM
+ *     activations (x, xq), packed weights, weight codes, quantizer input x and
+ *     logits 16 bytes; workspaces 256 bytes; quant_act_int8's xq 8 bytes;
+ *     embed_gather_w8's output 16 bytes; every other fp16 array (outputs y and
+ *     vals, weight scales) 2 bytes, binary32 token scales and int32 ids/indices
+ *     4 bytes (their element sizes).
  *   - The device must be compute capability 10.3 (GB300); otherwise QW_ERR_ARCH.
  *   - There is no CPU fallback: every computing call runs hand-written CUDA
  *     kernels on the current device.
@@ -49,7 +54,7 @@ enum {
     QW_OK = 0,
     QW_ERR_INVALID_ARG = -1,        /* null pointer, negative size */
     QW_ERR_UNSUPPORTED_SHAPE = -2,  /* K or N not a multiple of 128, or too large */
-    QW_ERR_ALIGNMENT = -3,          /* a pointer is not 16-byte aligned */
+    QW_ERR_ALIGNMENT = -3,          /* a pointer is below its required alignment */
     QW_ERR_WORKSPACE = -4,          /* workspace missing or smaller than required */
     QW_ERR_ARCH = -5,               /* no device, or the device is not sm_103 */
     QW_ERR_CUDA = -6,               /* a CUDA runtime call failed */
@@ -76,12 +81,20 @@ enum { QW_MODE_W4A16 = 0, QW_MODE_W4A8 = 1, QW_MODE_W8A16 = 2, QW_MODE_W4A8_FUSE
  *   packed  device buffer of qpack_w4_bytes(N, K) / qpack_w8_bytes(N, K) bytes,
  *           written completely.  Its layout, chunk (t, g) for row tile
  *           t = n/128 and group g = k/128 at byte offset (t*(K/128)+g)*CHUNK:
- *             W4: CHUNK = 8448.  Bytes [0, 8192): for slice j in 0..3 and row
- *                 r in 0..127, 16 bytes at j*2048 + r*16 hold the 32 codes
- *                 k = 128g + 32j + 8i + e (word i = 0..3, e = 0..7) of row
- *                 128t + r, as nibbles (code + 8) at bit 4*p of word i where
- *                 p = 4*(e % 2) + e/2.  Bytes [8192, 8448): the 128 scales of
- *                 the rows, fp16, in row order.
+ *             W4: CHUNK = 8448, in the fragment order of a warp-level
+ *                 16 x 16 tensor-core tile (rows R and R + 8 of a 16-row block
+ *                 share a word).  Bytes [0, 8192): 512 vectors of 16 bytes;
+ *                 vector (b, h, c, i) (row block b = 0..7, K half h = 0..1,
+ *                 c = 0..3, i = 0..7) at byte 16*(((b*2 + h)*4 + c)*8 + (i XOR 2c)).
+ *                 With R = 128t +
+ *                 16b + i and k0 = 128g + 16*(4h + w) + 2c, word w = 0..3 of the
+ *                 vector holds 8 nibbles (code + 8); nibble p at bit 4p:
+ *                   p = 0, 4: row R,     k0 and k0 + 1
+ *                   p = 1, 5: row R,     k0 + 8 and k0 + 9
+ *                   p = 2, 6: row R + 8, k0 and k0 + 1
+ *                   p = 3, 7: row R + 8, k0 + 8 and k0 + 9.
+ *                 Bytes [8192, 8448): scale pairs, pair b*8 + i = (scale of row
+ *                 R, scale of row R + 8), fp16.
  *             W8: CHUNK = 16640.  Bytes [0, 16384): for slice j in 0..7 and row
  *                 r, 16 bytes at j*2048 + r*16 hold codes k = 128g + 16j + b
  *                 (b = 0..15, byte b) stored as (code XOR 0x80).  Bytes
@@ -188,10 +201,11 @@ int topk_logits(const uint16_t *logits, int M, int N, int k, uint16_t *vals, int
  * item 4: activations quantized to int8 per token, int4 weights).
  *   x [M, K] fp16, device, 16-byte aligned.  Other arguments as qgemm_w4a16;
  *   the workspace is qgemm_workspace_bytes(QW_MODE_W4A8_FUSED, M, N, K).
- * When M <= 16 and the M fp16 rows take at most 48 KB (M*K*2 bytes), one kernel
- * copies the rows into shared memory, computes the token scales and quantizes
- * there, so no int8 activations are written; otherwise the quantizer writes its
- * codes and scales into the workspace and the W4A8 GEMM follows.  Async.
+ * When M <= 8 and the M fp16 rows take at most 96 KB (M*K*2 bytes), one kernel
+ * finds the token scales (every CTA reads the whole rows) and quantizes each
+ * activation tile in shared memory, so no int8 activations are written;
+ * otherwise the quantizer writes its codes and scales into the workspace and the
+ * W4A8 GEMM follows.  Async.
  * Returns as qgemm_w4a8.
  * ------------------------------------------------------------------------ */
 int qgemm_w4a8_fused(const uint16_t *x, const void *packed_w4, int M, int N, int K, uint16_t *y,
@@ -205,14 +219,17 @@ int qgemm_w4a8_fused(const uint16_t *x, const void *packed_w4, int M, int N, int
  * allowed).  The source pages have no counterpart to this entry point.
  *
  * Same arguments and result as qgemm_w4a16 minus the workspace: the scratch
- * memory is a fixed 4 MiB array inside the library on every GPU that loads it
- * (held until the process exits).  That covers M <= 16 at any N and K, and
- * shapes with at least 32 x (number of SMs) output tiles; a shape that needs
- * more returns QW_ERR_WORKSPACE with the sizes in qw_last_error_string().
- * The call allocates nothing.  Its first call on a device sets up that device's
- * scratch (looks up its address and clears it, synchronously), so make that
- * first call outside any stream capture.  Every call on a device shares the
- * same scratch: calls that may overlap on the GPU race and must be serialized
+ * memory is a fixed array of 5 MiB + 40 KiB inside the library on every GPU that
+ * loads it (held until the process exits).  That covers M <= 16 at any N and K on
+ * any device of up to 160 SMs, and shapes whose schedule assigns whole tiles (at
+ * least 32 x (number of SMs) output tiles); a shape that needs more returns
+ * QW_ERR_WORKSPACE, with the sizes in qw_last_error_string(), before any device
+ * work.  The call allocates nothing.  Every call looks up the array's device
+ * address (cudaGetSymbolAddress, no allocation); the first call on a device, and
+ * the first call after a device reset reloaded the library's module, sets the
+ * scratch up: it clears it and waits for the device (cudaDeviceSynchronize), so
+ * make that first call outside any stream capture.  Every call on a device shares
+ * the same scratch: calls that may overlap on the GPU race and must be serialized
  * by the caller.  After QW_ERR_TIMEOUT the scratch may hold stale counters and
  * the process should stop using this entry point.
  * ------------------------------------------------------------------------ */
@@ -244,16 +261,55 @@ int qw_get_option(int option);
  * Diagnostics.
  *   qw_last_error_string  text of the last host-side error of the calling
  *                         thread ("" if none).  Never NULL.
- *   qw_device_error       synchronizes the current device, returns the device
- *                         error word (QW_OK, QW_ERR_TIMEOUT or
- *                         QW_ERR_BAD_CODES) and clears it.  QW_ERR_CUDA if the
- *                         read itself fails.
+ *   qw_device_error       waits for the work enqueued on `stream` (stream-ordered
+ *                         read), returns the device error word of the current
+ *                         device (QW_OK, QW_ERR_TIMEOUT, QW_ERR_BAD_CODES or
+ *                         QW_ERR_BAD_INDEX) and clears it.  The word is one per
+ *                         device: it also holds errors of kernels on other streams
+ *                         that completed before the read.  QW_ERR_CUDA if the read
+ *                         itself fails.
  *   qw_num_kernel_launches  number of kernels this library has enqueued in
  *                         this process (all devices, all threads).
  * ------------------------------------------------------------------------ */
 const char *qw_last_error_string(void);
-int qw_device_error(void);
+int qw_device_error(qw_stream_t stream);
 long long qw_num_kernel_launches(void);
+
+/* ------------------------------------------------------------------------
+ * Measurement and verification tools (not on the GEMM's path).
+ *
+ *   qw_diag_mma_peak  dense rate of the warp-level tensor-core MMA (mma.sync):
+ *       kind 0 f16 x f16 -> f32 (m16n8k16), 1 s8 x s8 -> s32 (m16n8k32),
+ *       2 e4m3 x e4m3 -> f32 (m16n8k32), 3 s4 x s4 -> s32 (m16n8k64).  sm_103a has
+ *       no int8 tcgen05 MMA, so kind 1 measures the int8 tensor-core rate that the
+ *       W4A8 mode ("In full" item 4: int8 tensor cores) is reported against.
+ *       Launches `ctas` CTAs of 256 threads; every warp issues iters x 8 independent
+ *       MMAs on register operands.  sink: ctas*256 binary32, device (written so the
+ *       work is kept).  *ops (host) = 2*m*n*k per MMA x the MMAs of the launch; the
+ *       caller times the launch.  Async.
+ *   qw_diag_tc_probe  tcgen05.mma timing at the GEMM's shapes: `grid` CTAs (<= SMs,
+ *       one per SM); lane 0 of warps 0..issuers-1 each stream `chunks` chunks of a
+ *       128 x n x 128 product (kind 0: kind::f16, 8 MMAs of K = 16; kind 1:
+ *       kind::f8f6f4 with e4m3 operands, 4 MMAs of K = 32) into its own
+ *       accumulator, A from TMEM (a_tmem = 1) or shared memory.  window 0: one
+ *       commit at the end; w >= 1: a commit per chunk, chunk c first waiting for
+ *       chunk c - w's commit (a ring of w operand slots).  n*issuers <= 256,
+ *       window <= 8.  out: device, grid*4*4 uint64; per (CTA, issuer): issue ns,
+ *       wait ns, total ns, chunks done.  Async.
+ *   qw_diag_f8f6f4_gemm  d[r][j] = sum_k a[r][k] * b[j][k] (r < 128, j < 16) on
+ *       tcgen05 kind::f8f6f4, e4m3 operands given as bytes (a [128][K], b [16][K],
+ *       row-major, device, 16-byte aligned), A from TMEM (a_tmem = 1) or shared
+ *       memory, fp32 d [128][16] (device).  K = 128..512, a multiple of 128.  Checks
+ *       whether int4 x int8 products (int4 codes and the two 4-bit halves of the
+ *       int8 codes are exact in e4m3) accumulate exactly.  Async.
+ * Return QW_OK, QW_ERR_INVALID_ARG, QW_ERR_ALIGNMENT, QW_ERR_ARCH or QW_ERR_CUDA;
+ * a bounded wait that runs out records QW_ERR_TIMEOUT (read by qw_device_error).
+ * ------------------------------------------------------------------------ */
+int qw_diag_mma_peak(int kind, int ctas, int iters, float *sink, double *ops, qw_stream_t stream);
+int qw_diag_tc_probe(int kind, int a_tmem, int n, int issuers, int chunks, int window,
+                     unsigned long long *out, int grid, qw_stream_t stream);
+int qw_diag_f8f6f4_gemm(const uint8_t *a, const uint8_t *b, int K, int a_tmem, float *d,
+                        qw_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Schedule query (host only, no device access): how a qgemm call of this shape
@@ -275,6 +331,8 @@ typedef struct {
     int act_stages;         /* activation ring depth in shared memory (blocks) */
     int act_block;          /* K groups per activation block (one tensor copy) */
     int fused;              /* QW_MODE_W4A8_FUSED: 1 when the quantizer runs inside the GEMM */
+    int decode_teams;       /* > 0: int4 weights and M <= 16 run on the decode-batch kernel
+                               (warp-level MMA), with this many teams of four warps */
 } qw_plan_t;
 
 int qw_plan(int mode, int M, int N, int K, int num_sms, qw_plan_t *out);

@@ -42,7 +42,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("bn", _i), ("token_tiles", _i), ("row_tiles", _i), ("groups", _i),
                 ("tiles", _ll), ("chunks", _ll), ("grid", _i), ("stream_k", _i), ("stages", _i),
                 ("smem_bytes", _i), ("ws_bytes", _sz), ("ws_zero_bytes", _sz),
-                ("act_stages", _i), ("act_block", _i), ("fused", _i)]
+                ("act_stages", _i), ("act_block", _i), ("fused", _i), ("decode_teams", _i)]
 
 
 SIGNATURES = {
@@ -63,10 +63,13 @@ SIGNATURES = {
     "qgemm_w8a16": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "qgemm_w4a16_noalloc": (_i, [_p, _p, _i, _i, _i, _p, _p]),
     "qw_last_error_string": (ctypes.c_char_p, []),
-    "qw_device_error": (_i, []),
+    "qw_device_error": (_i, [_p]),
     "qw_num_kernel_launches": (_ll, []),
     "qw_set_option": (_i, [_i, _i]),
     "qw_get_option": (_i, [_i]),
+    "qw_diag_mma_peak": (_i, [_i, _i, _i, _p, ctypes.POINTER(ctypes.c_double), _p]),
+    "qw_diag_tc_probe": (_i, [_i, _i, _i, _i, _i, _i, _p, _i, _p]),
+    "qw_diag_f8f6f4_gemm": (_i, [_p, _p, _i, _i, _p, _p]),
     "qw_plan": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(Plan)]),
     "qw_plan_segments": (_i, [ctypes.POINTER(Plan), _i, _i, _p, _p, _p, _p]),
 }
@@ -354,9 +357,12 @@ def qgemm_w4a16_noalloc(x, packed, N: int, K: int, y=None):
 
 
 # -------------------------------------------------------------- diagnostics --
-def device_error() -> int:
-    """Synchronize and return (and clear) the device error word of the current device."""
-    return int(lib().qw_device_error())
+def device_error(stream=None) -> int:
+    """Wait for the work enqueued on `stream` (default: the current stream of the current
+    device), then return and clear the device error word of the current device."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(lib().qw_device_error(ctypes.c_void_p(stream.cuda_stream)))
 
 
 QW_OPT_WEIGHTS_IMMUTABLE = 1
@@ -371,6 +377,48 @@ def set_weights_immutable(flag: bool = True):
 
 def num_kernel_launches() -> int:
     return int(lib().qw_num_kernel_launches())
+
+
+# ----------------------------------------------------- measurement tools --
+MMA_KINDS = {"f16": 0, "s8": 1, "e4m3": 2, "s4": 3}
+
+
+def diag_mma_peak(kind: str, ctas: int, iters: int, device=None):
+    """Launch the mma.sync rate microbenchmark on the current stream; returns
+    (ops of the launch, sink tensor).  The caller times the launch."""
+    dev = torch.device(device or "cuda")
+    sink = torch.empty(ctas * 256, dtype=torch.float32, device=dev)
+    ops = ctypes.c_double(0.0)
+    with torch.cuda.device(dev):
+        _check(lib().qw_diag_mma_peak(MMA_KINDS[kind], ctas, iters, _ptr(sink), ctypes.byref(ops),
+                                      _stream(sink)))
+    return ops.value, sink
+
+
+def diag_tc_probe(kind: int, a_tmem: bool, n: int, issuers: int, chunks: int, window: int, grid: int,
+                  device=None):
+    """tcgen05.mma timing probe; returns the device tensor [grid, 4, 4] (issue ns, wait ns,
+    total ns, chunks) -- read it after synchronizing."""
+    dev = torch.device(device or "cuda")
+    out = torch.zeros((grid, 4, 4), dtype=torch.int64, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().qw_diag_tc_probe(kind, 1 if a_tmem else 0, n, issuers, chunks, window, _ptr(out), grid,
+                                      _stream(out)))
+    return out
+
+
+def diag_f8f6f4_gemm(a_e4m3, b_e4m3, a_tmem: bool):
+    """d [128, 16] fp32 = a [128, K] . b [16, K]^T on tcgen05 kind::f8f6f4 (e4m3 bytes as uint8)."""
+    _need(a_e4m3, torch.uint8, "a", 2)
+    _need(b_e4m3, torch.uint8, "b", 2)
+    K = a_e4m3.shape[1]
+    if tuple(a_e4m3.shape) != (128, K) or tuple(b_e4m3.shape) != (16, K):
+        raise ValueError("a must be [128, K] and b [16, K]")
+    d = torch.empty((128, 16), dtype=torch.float32, device=a_e4m3.device)
+    with torch.cuda.device(a_e4m3.device):
+        _check(lib().qw_diag_f8f6f4_gemm(_ptr(a_e4m3), _ptr(b_e4m3), K, 1 if a_tmem else 0, _ptr(d),
+                                         _stream(a_e4m3)))
+    return d
 
 
 def plan(mode: int, M: int, N: int, K: int, num_sms: int) -> Plan:

@@ -169,8 +169,10 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (mode == QW_MODE_W4A8_FUSED && P.fused) {
+    // the decode-batch kernel quantizes per token itself: fp16 tiles, as W4A16
     a.xf16 = static_cast<const uint16_t *>(act);
-    e = qw::launch_gemm_w4a8_fused(a, st);
+    if ((rc = encode_act_map(&a.tmap, act, M, K, qw::ms_rows(M), P.xblock, false))) return rc;
+    e = qw::launch_gemm_ms(a, 2, st);
     if (e != cudaSuccess) return fail_cuda(e, "GEMM kernel launch");
     return QW_OK;
   }
@@ -184,9 +186,11 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
     a.xs = s;
     mode = QW_MODE_W4A8;
   }
+  // the decode-batch kernel's activation tiles hold 8 or 16 token rows
+  const int box_rows = P.ms_teams ? qw::ms_rows(M) : P.bn;
   if (mode == QW_MODE_W4A8 && qw::act8_in_kernel(mode, P.bn)) {
-    if ((rc = encode_act_map(&a.tmap, act, M, K, P.bn, P.xblock, true))) return rc;
-    e = qw::launch_gemm_w4a8(a, st);
+    if ((rc = encode_act_map(&a.tmap, act, M, K, box_rows, P.xblock, true))) return rc;
+    e = P.ms_teams ? qw::launch_gemm_ms(a, 1, st) : qw::launch_gemm_w4a8(a, st);
   } else if (mode == QW_MODE_W4A8) {
     uint16_t *wide = reinterpret_cast<uint16_t *>(w + P.ws_counters + P.ws_partials);
     if ((rc = encode_act_map(&a.tmap, wide, M, K, P.bn, P.xblock, false))) return rc;
@@ -194,8 +198,10 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
     if (e != cudaSuccess) return fail_cuda(e, "widen kernel launch");
     e = qw::launch_gemm_w4a8(a, st);
   } else {
-    if ((rc = encode_act_map(&a.tmap, act, M, K, P.bn, P.xblock, false))) return rc;
-    e = mode == QW_MODE_W8A16 ? qw::launch_gemm_w8a16(a, st) : qw::launch_gemm_w4a16(a, st);
+    if ((rc = encode_act_map(&a.tmap, act, M, K, box_rows, P.xblock, false))) return rc;
+    e = mode == QW_MODE_W8A16 ? qw::launch_gemm_w8a16(a, st)
+        : P.ms_teams          ? qw::launch_gemm_ms(a, 0, st)
+                              : qw::launch_gemm_w4a16(a, st);
   }
   if (e != cudaSuccess) return fail_cuda(e, "GEMM kernel launch");
   return QW_OK;
@@ -230,6 +236,15 @@ namespace qw {
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int set_last_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
+int device_info(int *sms, int **err) {
+  DevInfo *d = nullptr;
+  const int rc = current_device(d);
+  if (rc) return rc;
+  if (sms) *sms = d->sms;
+  if (err) *err = d->err;
+  return QW_OK;
+}
 
 cudaError_t ensure_smem_attr(const void *func, int bytes) {
   struct Entry { const void *f; int dev; int bytes; };
@@ -375,17 +390,20 @@ int qgemm_w8a16(const uint16_t *x, const void *packed_w8, int M, int N, int K, u
 
 const char *qw_last_error_string(void) { return tl_err; }
 
-int qw_device_error(void) {
+int qw_device_error(qw_stream_t stream) {
   DevInfo *d = nullptr;
   int rc = current_device(d);
   if (rc) return rc;
-  cudaError_t e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+  // stream-ordered: the read sees every kernel enqueued on `stream` before it (and
+  // whatever else has completed on the device by then), then the word is cleared
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int v = 0;
-  e = cudaMemcpyFromSymbol(&v, g_qw_err, sizeof v);
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_qw_err, sizeof v, 0, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return fail_cuda(e, "read error word");
-  const int zero = 0;
-  e = cudaMemcpyToSymbol(g_qw_err, &zero, sizeof zero);
+  static const int zero = 0;
+  e = cudaMemcpyToSymbolAsync(g_qw_err, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return fail_cuda(e, "clear error word");
   return v;
 }
@@ -425,6 +443,7 @@ int qw_plan(int mode, int M, int N, int K, int num_sms, qw_plan_t *out) {
   out->act_stages = P.xstages;
   out->act_block = P.xblock;
   out->fused = P.fused;
+  out->decode_teams = P.ms_teams;
   return QW_OK;
 }
 

@@ -116,46 +116,54 @@ __global__ void widen_i8_kernel(const int8_t *__restrict__ src, uint16_t *__rest
 }
 
 // --------------------------------------------------------------------------
-// Packers.  One thread per 16-byte slice of a chunk; see qgemm.h for the layout.
+// Packers; see qgemm.h for the layouts.
+//
+// W4: one thread per 16-byte vector of a chunk: the vector at position
+// ((b * 2 + h) * 4 + c) * 8 + (i ^ 2 c) (row block b of 16 rows, K half h, lane quarter
+// c, row i of the block's upper-or-lower eight; the XOR keeps both the row-per-thread and
+// the fragment-per-lane reads free of shared-memory bank conflicts) holds, in word w, the
+// codes of rows R = 16 b + i and R + 8 at the four K offsets k0, k0 + 1, k0 + 8, k0 + 9
+// with k0 = 16 (4 h + w) + 2 c.  Nibble p of a word:
+//   p = 0, 4: (R, k0), (R, k0 + 1)        p = 1, 5: (R, k0 + 8), (R, k0 + 9)
+//   p = 2, 6: (R + 8, k0), (R + 8, k0 + 1) p = 3, 7: (R + 8, k0 + 8), (R + 8, k0 + 9)
+// stored as code + 8.  The scales follow as (R, R + 8) pairs, pair b * 8 + i.
 __global__ void pack_w4_kernel(const int8_t *__restrict__ codes, const uint16_t *__restrict__ scales,
                                int N, int K, uint8_t *__restrict__ packed, int *err) {
   griddep_wait();
   griddep_launch_dependents();
   const int G = K / kGroup;
-  const size_t total = (size_t)N * K / 32;   // 16-byte slices
+  const size_t total = (size_t)N * K / 32;   // 16-byte vectors
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
        idx += (size_t)gridDim.x * blockDim.x) {
     const size_t chunk = idx / 512;
-    const int j = (int)((idx / 128) % 4);
-    const int r = (int)(idx % 128);
+    const int v = (int)(idx % 512);                 // position in the chunk
+    const int c = (v >> 3) & 3, i = (v & 7) ^ (2 * c), h = (v >> 5) & 1, b = v >> 6;
     const size_t t = chunk / G;
     const int g = (int)(chunk % G);
-    const size_t n = t * kRows + r;
-    const int8_t *src = codes + n * K + (size_t)g * kGroup + 32 * j;
-    const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src));
-    const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src + 16));
-    const int8_t *c8a = reinterpret_cast<const int8_t *>(&a);
-    const int8_t *c8b = reinterpret_cast<const int8_t *>(&b);
+    const size_t R = t * kRows + 16 * b + i;
+    const int8_t *lo = codes + R * K + (size_t)g * kGroup;
+    const int8_t *hi = lo + (size_t)8 * K;
     uint32_t wds[4];
     bool bad = false;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int w = 0; w < 4; ++w) {
+      const int k0 = 16 * (4 * h + w) + 2 * c;
+      const int q[8] = {lo[k0], lo[k0 + 8], hi[k0], hi[k0 + 8], lo[k0 + 1], lo[k0 + 9], hi[k0 + 1], hi[k0 + 9]};
       uint32_t wd = 0;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int kk = 8 * i + e;
-        const int c = kk < 16 ? c8a[kk] : c8b[kk - 16];
-        bad |= (c < -8 || c > 7);
-        const uint32_t u = (uint32_t)(c + 8) & 15u;
-        const int p = 4 * (e & 1) + (e >> 1);
-        wd |= u << (4 * p);
+      for (int p = 0; p < 8; ++p) {
+        bad |= (q[p] < -8 || q[p] > 7);
+        wd |= ((uint32_t)(q[p] + 8) & 15u) << (4 * p);
       }
-      wds[i] = wd;
+      wds[w] = wd;
     }
     if (bad) atomicCAS(err, 0, -8);
     uint8_t *dst = packed + chunk * kChunkW4;
-    *reinterpret_cast<uint4 *>(dst + j * 2048 + r * 16) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
-    if (j == 0) *reinterpret_cast<uint16_t *>(dst + 8192 + r * 2) = scales[n * G + g];
+    *reinterpret_cast<uint4 *>(dst + v * 16) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+    if (h == 0 && c == 0) {
+      const uint32_t pair = (uint32_t)scales[R * G + g] | ((uint32_t)scales[(R + 8) * G + g] << 16);
+      *reinterpret_cast<uint32_t *>(dst + 8192 + (b * 8 + i) * 4) = pair;
+    }
   }
 }
 

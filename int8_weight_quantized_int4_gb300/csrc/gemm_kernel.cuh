@@ -76,27 +76,26 @@ static_assert(kAmaxSlot + 4 * 4 * kMaxFusedRows <= kSmemReserve - 1024, "barrier
 
 // ---- dequantization: packed codes -> 32 half2 (64 fp16 values q*s) per thread ----
 
-// W4: two 16-byte slices (64 codes) of one row; nibble (q + 8) at bit 4p of each
-// word holds element e = 2*(p % 4) + p / 4, so the masks below yield (k, k+1) pairs.
-__device__ __forceinline__ void dequant_w4(const uint4 (&v)[2], __half2 s2, uint32_t (&o)[32]) {
+// W4: the four 16-byte vectors (lane quarters c = 0..3) of one K half of row R (see
+// the packer): word w of vector c holds the codes at k0 = 16 w + 2 c (+ 64 h), k0 + 1
+// (nibbles 0 and 4) and k0 + 8, k0 + 9 (nibbles 1 and 5) of the row block's lower row;
+// the upper row (R % 16 >= 8) reads the same word shifted right by 8.  TMEM column
+// (k0 - 64 h) / 2 = 8 w + c holds the pair (k0, k0 + 1), column 8 w + c + 4 the pair
+// (k0 + 8, k0 + 9).
+__device__ __forceinline__ void dequant_w4(const uint4 (&v)[4], int sh, __half2 s2, uint32_t (&o)[32]) {
   const __half2 k1032 = __float2half2_rn(1032.0f);
   const __half2 k16th = __float2half2_rn(0.0625f);
   const __half2 km72 = __float2half2_rn(-72.0f);
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t w[4] = {v[c].x >> sh, v[c].y >> sh, v[c].z >> sh, v[c].w >> sh};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = w[i], hi = w[i] >> 8;
       // (1024 + u) - 1032 = q  and  (1024 + 16u)/16 - 72 = q, both exact in fp16
-      const __half2 q0 = __hsub2(u32_as_h2(lop3_and_or(lo, 0x000f000fu, 0x64006400u)), k1032);
-      const __half2 q1 = __hfma2(u32_as_h2(lop3_and_or(lo, 0x00f000f0u, 0x64006400u)), k16th, km72);
-      const __half2 q2 = __hsub2(u32_as_h2(lop3_and_or(hi, 0x000f000fu, 0x64006400u)), k1032);
-      const __half2 q3 = __hfma2(u32_as_h2(lop3_and_or(hi, 0x00f000f0u, 0x64006400u)), k16th, km72);
-      o[16 * j + 4 * i + 0] = h2_as_u32(__hmul2_rn(q0, s2));
-      o[16 * j + 4 * i + 1] = h2_as_u32(__hmul2_rn(q1, s2));
-      o[16 * j + 4 * i + 2] = h2_as_u32(__hmul2_rn(q2, s2));
-      o[16 * j + 4 * i + 3] = h2_as_u32(__hmul2_rn(q3, s2));
+      const __half2 q0 = __hsub2(u32_as_h2(lop3_and_or(w[i], 0x000f000fu, 0x64006400u)), k1032);
+      const __half2 q1 = __hfma2(u32_as_h2(lop3_and_or(w[i], 0x00f000f0u, 0x64006400u)), k16th, km72);
+      o[8 * i + c] = h2_as_u32(__hmul2_rn(q0, s2));
+      o[8 * i + c + 4] = h2_as_u32(__hmul2_rn(q1, s2));
     }
   }
 }
@@ -466,11 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             if constexpr (WBITS == 4) {
-              uint4 v[2];
-              v[0] = *reinterpret_cast<const uint4 *>(wc + (2 * h) * 2048 + row * 16);
-              v[1] = *reinterpret_cast<const uint4 *>(wc + (2 * h + 1) * 2048 + row * 16);
-              const __half sc = *reinterpret_cast<const __half *>(wc + 8192 + row * 2);
-              dequant_w4(v, __half2half2(sc), o[h]);
+              // row = 16 b + i (+ 8 for the upper eight rows of block b)
+              const int rb = row >> 4, ri = row & 7, up = (row >> 3) & 1;
+              uint4 v[4];
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                v[c] = *reinterpret_cast<const uint4 *>(wc + (((rb * 2 + h) * 4 + c) * 8 + (ri ^ (2 * c))) * 16);
+              const __half sc = *reinterpret_cast<const __half *>(wc + 8192 + (rb * 8 + ri) * 4 + up * 2);
+              dequant_w4(v, up * 8, __half2half2(sc), o[h]);
             } else {
               uint4 v[4];
 #pragma unroll

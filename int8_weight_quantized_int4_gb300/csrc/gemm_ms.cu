@@ -1,0 +1,27 @@
+// gemm_ms.cu -- instantiations of the decode-batch kernel (warp-level MMA): W4A16, W4A8
+// from int8 activations (widened in shared memory) and W4A8 from fp16 activations
+// (quantized per token in the kernel, up to 8 tokens); one or two tiles of 8 tokens.
+#include "gemm_ms.cuh"
+
+namespace qw {
+
+template <int NT8, int AMODE>
+static cudaError_t run_ms(const GemmArgs &a, cudaStream_t st) {
+  auto *k = qgemm_ms_kernel<NT8, AMODE>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(k), a.P.smem_bytes);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(reinterpret_cast<const void *>(k), dim3(a.P.grid), dim3(ms_threads()),
+                 (size_t)a.P.smem_bytes, st, a);
+  count_launch();
+  return e;
+}
+
+cudaError_t launch_gemm_ms(const GemmArgs &a, int act, cudaStream_t st) {
+  if (!a.P.ms_teams || a.P.ms_teams != ms_teams(a.P.M) || a.P.bn != kMsMaxTokens) return cudaErrorInvalidValue;
+  const bool one = a.P.M <= 8;
+  if (act == kActQuant) return one ? run_ms<1, kActQuant>(a, st) : cudaErrorInvalidValue;
+  if (act == kActI8) return one ? run_ms<1, kActI8>(a, st) : run_ms<2, kActI8>(a, st);
+  return one ? run_ms<1, kActF16>(a, st) : run_ms<2, kActF16>(a, st);
+}
+
+}  // namespace qw

@@ -26,6 +26,9 @@ struct GemmArgs {
 void count_launch();
 // Record a host-side error for qw_last_error_string(); returns `code`.
 int set_last_error(int code, const char *msg);
+// Check the current device (sm_103) and return its SM count and the address of its
+// device error word; QW_OK or a QW_ERR_* code (recorded for qw_last_error_string()).
+int device_info(int *sms, int **err);
 
 // Launch `func` with programmatic stream serialization: it may start while the
 // preceding kernel on the stream finishes; every kernel of this library executes
@@ -71,7 +74,9 @@ cudaError_t launch_topk(const uint16_t *logits, int M, int N, int k, uint16_t *v
 
 cudaError_t launch_gemm_w4a16(const GemmArgs &a, cudaStream_t st);
 cudaError_t launch_gemm_w4a8(const GemmArgs &a, cudaStream_t st);
-cudaError_t launch_gemm_w4a8_fused(const GemmArgs &a, cudaStream_t st);
 cudaError_t launch_gemm_w8a16(const GemmArgs &a, cudaStream_t st);
+// decode batches (plan.ms_teams > 0); act: 0 fp16 activations (W4A16), 1 int8 codes and
+// token scales (W4A8), 2 fp16 activations quantized per token in the kernel (W4A8)
+cudaError_t launch_gemm_ms(const GemmArgs &a, int act, cudaStream_t st);
 
 }  // namespace qw

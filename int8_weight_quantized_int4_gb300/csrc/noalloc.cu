@@ -20,22 +20,29 @@
 #include <cuda_runtime.h>
 #include "qgemm.h"
 #include "launch.h"
+#include "schedule.h"
 
 namespace {
 
-// 4 MiB per device: enough for decode batches of up to 16 tokens at any N and K
-// (stream-K partial sums of 16 tokens per CTA), and for large batches whose
-// schedule assigns whole tiles (only the tile counters are used).
-constexpr size_t kScratchBytes = (size_t)4 << 20;
+// The largest stream-K plan of a token tile of 16 (M <= 16): binary32 partial sums of
+// two 16 x 128 tiles per CTA for up to kMaxGrid CTAs, after the fixed tile-counter
+// region of every workspace.  Plans that assign whole tiles use only the counters.
+constexpr size_t kCounterBytes = (size_t)qw::kStreamKMaxTilesPerSm * qw::kMaxGrid * 4;
+constexpr size_t kScratchBytes =
+    (kCounterBytes + 255) / 256 * 256 + (size_t)2 * qw::kMaxGrid * 16 * qw::kRows * 4;   // 5 MiB + 40 KiB
+static_assert(kScratchBytes == ((size_t)5 << 20) + ((size_t)40 << 10), "scratch size");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 void *g_scratch_ptr[kMaxDevices];   // device address of the array, per device (null until set up)
 
-// Once per device, with that device current: look up the array's device address
-// (the host-side symbol is only a stand-in and must never reach a kernel) and
-// clear it.
+// With the device current: look up the array's device address (the host-side symbol
+// is only a stand-in and must never reach a kernel).  The lookup allocates nothing
+// and runs on every call, so that a module reloaded after a device reset is seen: a
+// new address is set up again.  Set-up clears the array and waits for the clear
+// (cudaMemset runs on the legacy default stream, which does not order work on
+// non-blocking streams), so no kernel of the first call can see it half-done.
 int scratch_for_current_device(void **out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -43,22 +50,23 @@ int scratch_for_current_device(void **out) {
     cudaGetLastError();
     return qw::set_last_error(QW_ERR_ARCH, "qgemm_w4a16_noalloc: no usable CUDA device");
   }
+  void *p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p) {
+    cudaGetLastError();
+    return qw::set_last_error(QW_ERR_CUDA, "qgemm_w4a16_noalloc: cudaGetSymbolAddress failed");
+  }
   std::lock_guard<std::mutex> lk(g_setup_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p) {
-      cudaGetLastError();
-      return qw::set_last_error(QW_ERR_CUDA, "qgemm_w4a16_noalloc: cudaGetSymbolAddress failed");
-    }
+  if (g_scratch_ptr[dev] != p) {
     e = cudaMemset(p, 0, kScratchBytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
       cudaGetLastError();
       return qw::set_last_error(QW_ERR_CUDA, "qgemm_w4a16_noalloc: clearing the scratch failed");
     }
     g_scratch_ptr[dev] = p;
   }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return QW_OK;
 }
 
@@ -68,11 +76,11 @@ extern "C" int qgemm_w4a16_noalloc(const uint16_t *x, const void *packed_w4, int
                                    uint16_t *y, qw_stream_t stream) {
   if (M < 0 || N < 0 || K < 0)
     return qw::set_last_error(QW_ERR_INVALID_ARG, "qgemm_w4a16_noalloc: negative size");
-  if (M == 0 || N == 0) return qgemm_w4a16(x, packed_w4, M, N, K, y, nullptr, 0, stream);
-  void *scratch = nullptr;
-  int rc = scratch_for_current_device(&scratch);
-  if (rc) return rc;
+  if (M == 0 || N == 0 || K == 0 || K % 128 || N % 128)   // rejected or empty: no scratch involved
+    return qgemm_w4a16(x, packed_w4, M, N, K, y, nullptr, 0, stream);
+  // the size check comes before any device work
   const size_t need = qgemm_workspace_bytes(QW_MODE_W4A16, M, N, K);
+  if (need == 0) return qgemm_w4a16(x, packed_w4, M, N, K, y, nullptr, 0, stream);
   if (need > kScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof msg,
@@ -81,5 +89,8 @@ extern "C" int qgemm_w4a16_noalloc(const uint16_t *x, const void *packed_w4, int
              M, N, K, need, kScratchBytes);
     return qw::set_last_error(QW_ERR_WORKSPACE, msg);
   }
+  void *scratch = nullptr;
+  int rc = scratch_for_current_device(&scratch);
+  if (rc) return rc;
   return qgemm_w4a16(x, packed_w4, M, N, K, y, scratch, kScratchBytes, stream);
 }

@@ -32,7 +32,7 @@ constexpr int kGroup = 128;        // K per group / per chunk
 constexpr int kChunkW4 = 8192 + 256;
 constexpr int kChunkW8 = 16384 + 256;
 constexpr int kTokenSuperTiles = 16;   // token tiles kept hot in L2 together
-constexpr int kMaxGrid = 256;          // persistent CTAs at most (one per SM)
+constexpr int kMaxGrid = 320;          // persistent CTAs at most (one per SM, two for the decode kernel)
 
 struct Plan {
   int mode, M, N, K;
@@ -44,7 +44,10 @@ struct Plan {
   int xblock;                    // chunks per activation block (one tensor copy)
   int smem_bytes;
   int fused;                     // W4A8 with the per-token quantizer inside the GEMM
-  int rows_bytes;                // fused: shared-memory copy of the M fp16 rows
+  int rows_bytes;                // unused (0)
+  int ms_teams;                  // > 0: the warp-level MMA kernel for decode batches (M <= 16),
+                                 // with this many teams of warps (one chunk per team at a time)
+  int ms_red_bytes;              // its shared-memory buffer for the teams' partial sums
   float grid_per_chunk;          // grid / chunks, to estimate a chunk's owner
   size_t ws_counters, ws_partials, ws_act, ws_quant, ws_bytes, ws_zero;
   int begin[kMaxGrid + 1];       // stream-K: first chunk of each CTA (begin[grid] = chunks)
@@ -144,9 +147,12 @@ QW_HD int chunk_bytes(int mode) { return mode == 2 ? kChunkW8 : kChunkW4; }
 // fp16 rows fit in shared memory next to the pipeline (at most kFusedRowsMax bytes,
 // token tiles of 16); otherwise it runs the standalone quantizer into the workspace
 // and then the mode-1 GEMM.
-constexpr int kFusedRowsMax = 48 * 1024;
+// Mode 3 quantizes inside the decode-batch kernel for up to eight tokens whose fp16 rows
+// take at most kFusedRowsMax bytes (every CTA reads them all to find the token scales);
+// otherwise it runs the standalone quantizer into the workspace and then the mode-1 GEMM.
+constexpr int kFusedRowsMax = 96 * 1024;
 QW_HD bool quant_in_kernel(int mode, int M, int K) {
-  return mode == 3 && M >= 1 && M <= 16 && (long long)M * K * 2 <= kFusedRowsMax;
+  return mode == 3 && M >= 1 && M <= 8 && (long long)M * K * 2 <= kFusedRowsMax;
 }
 
 // W4A8 widens int8 activation codes to fp16 inside the GEMM (through a staging
@@ -168,19 +174,62 @@ QW_HD int xstage_bytes(int mode, int bn) {
   return act_block(bn) * (bn * kGroup * 2 + (act8_in_kernel(mode, bn) ? bn * kGroup : 0));
 }
 
+// Decode batches (M <= kMsMaxTokens, int4 weights, fp16 or int8 activations) run on the
+// warp-level MMA kernel: kMsTeams teams of warps, each team computing whole 128 x 128
+// chunks, the dequantized weights going from registers straight into the MMA.  Its CTA
+// takes at most half an SM (shared memory, registers), so that the next layer's CTAs
+// can start on an SM while this layer's finish there.
+constexpr int kMsMaxTokens = 16;
+constexpr int kMsComputeWarps = 8;
+constexpr int kMsRedStride = 132;        // floats per token row of a team's sum buffer
+constexpr int kMsSmemLimit = 113 * 1024; // two CTAs per SM
+// Launches of at least this many chunks per SM run two decode CTAs per SM (more warps
+// streaming at once); shorter ones one, leaving the SM's other half to the next layer.
+constexpr int kMsLongChunksPerSm = 32;
+QW_HD bool ms_kernel(int mode, int M) {
+  return (mode == 0 || mode == 1 || mode == 3) && M >= 1 && M <= kMsMaxTokens;
+}
+// token rows of its activation tiles: 8 (one tile of eight tokens) or 16
+QW_HD int ms_rows(int M) { return M <= 8 ? 8 : 16; }
+// 16-row blocks of a chunk per warp: 4 for eight tokens, 2 for sixteen (registers)
+QW_HD int ms_row_blocks(int M) { return M <= 8 ? 4 : 2; }
+// teams (each computing one chunk at a time): 8 row blocks / row blocks per warp warps each
+QW_HD int ms_teams(int M) { return kMsComputeWarps * ms_row_blocks(M) / 8; }
+// the teams other than the first leave their sums here at the end of a tile segment
+QW_HD int ms_red_bytes(int M) { return (ms_teams(M) - 1) * ms_rows(M) * kMsRedStride * 4; }
+// activation slot: act_block(16) = 4 K groups of ms_rows(M) x 128 fp16 (+ int8 staging)
+QW_HD int ms_xstage_bytes(int mode, int M) {
+  return 4 * ms_rows(M) * kGroup * (mode == 1 ? 3 : 2);
+}
+// shared-memory floats of the in-kernel quantizer: per-warp amax [8][8], scales [8] and
+// reciprocals [8]
+constexpr int kMsQuantFloats = 8 * 8 + 8 + 8;
+// ring depths: three activation blocks when that leaves eight weight slots, else two;
+// the weight slots (at most kMaxWStages) split evenly between the teams
+QW_HD bool ms_ring_depths(int mode, int M, int &xst, int &wst) {
+  const int xb = ms_xstage_bytes(mode, M), wb = (int)align_up((size_t)kChunkW4, 128);
+  for (int x = 3; x >= 2; --x) {
+    int w = (kMsSmemLimit - kSmemReserve - ms_red_bytes(M) - kMsQuantFloats * 4 - x * xb) / wb;
+    if (w > kMaxWStages) w = kMaxWStages;
+    w -= w % ms_teams(M);
+    if (w >= 8 || (x == 2 && w >= 2 * ms_teams(M))) { xst = x; wst = w; return true; }
+  }
+  return false;
+}
+
 // Ring depths: the deepest activation ring (at most kMaxXStages, or 3 for token
 // tiles up to 64 whose blocks already span several groups -- except the fused W4A8
 // mode, whose quantized blocks are all written up front -- at least 2) that still
 // leaves four weight slots; the weight ring takes the rest (at most kMaxWStages),
 // rounded down to an even count (half per dequant group).  Returns false when
 // even 2 + 4 slots do not fit.
-QW_HD bool ring_depths(int mode, int bn, int &xst, int &wst, int extra = 0) {
+QW_HD bool ring_depths(int mode, int bn, int &xst, int &wst, int extra = 0, int split = 2) {
   const int xb = xstage_bytes(mode, bn), wb = wstage_bytes(mode);
   for (int x = (bn <= 64 && mode != 3) ? 3 : kMaxXStages; x >= 2; --x) {
     int w = (kSmemLimit - kSmemReserve - extra - x * xb) / wb;
     if (w > kMaxWStages) w = kMaxWStages;
-    w &= ~1;
-    if (w >= 4) { xst = x; wst = w; return true; }
+    w -= w % split;                      // the same number of slots per consumer
+    if (w >= 2 * split) { xst = x; wst = w; return true; }
   }
   return false;
 }
@@ -237,9 +286,9 @@ inline void fill_begin(Plan &P) {
 inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   if (mode < 0 || mode > 3 || M < 0 || N < 0 || K < 0 || num_sms < 1) return -1;
   if (N % kRows || K % kGroup) return -2;
-  if (num_sms > kMaxGrid) num_sms = kMaxGrid;
+  if (num_sms > kMaxGrid / 2) num_sms = kMaxGrid / 2;
   P.fused = quant_in_kernel(mode, M, K) ? 1 : 0;
-  P.rows_bytes = P.fused ? (int)align_up((size_t)M * K * 2, 1024) : 0;
+  P.rows_bytes = 0;
   // mode 3 outside the fused range is the quantizer followed by a mode-1 plan
   const bool quant_first = mode == 3 && !P.fused;
   if (quant_first) mode = 1;
@@ -253,16 +302,29 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   if (chunks >= (1LL << 30)) return -2;      // 32-bit chunk indices with headroom
   P.tiles = (int)tiles;
   P.chunks = (int)chunks;
-  const bool many = P.tiles >= kStreamKMaxTilesPerSm * num_sms || (P.tiles % num_sms) == 0;
+  // persistent CTAs: one per SM, two for long decode-kernel launches (at most kMaxGrid)
+  int ctas = num_sms;
+  if (ms_kernel(mode, M) && (long long)P.chunks >= (long long)kMsLongChunksPerSm * num_sms) ctas = 2 * num_sms;
+  if (ctas > kMaxGrid) ctas = kMaxGrid;
+  const bool many = P.tiles >= kStreamKMaxTilesPerSm * num_sms || (P.tiles % ctas) == 0;
   P.stream_k = (P.chunks > 0 && !many) ? 1 : 0;
   if (P.chunks == 0) P.grid = 0;
-  else if (P.stream_k) P.grid = P.chunks < num_sms ? P.chunks : num_sms;
-  else P.grid = P.tiles < num_sms ? P.tiles : num_sms;
+  else if (P.stream_k) P.grid = P.chunks < ctas ? P.chunks : ctas;
+  else P.grid = P.tiles < ctas ? P.tiles : ctas;
   fill_begin(P);
   P.xblock = act_block(P.bn);
-  if (!ring_depths(mode, P.bn, P.xstages, P.stages, P.rows_bytes)) return -2;
-  P.smem_bytes = P.xstages * xstage_bytes(mode, P.bn) + P.stages * wstage_bytes(mode) + P.rows_bytes +
-                 kSmemReserve;
+  P.ms_teams = ms_kernel(mode, M) ? ms_teams(M) : 0;
+  if (P.ms_teams) {
+    P.ms_red_bytes = ms_red_bytes(M);
+    if (!ms_ring_depths(mode, M, P.xstages, P.stages)) return -2;
+    P.smem_bytes = P.xstages * ms_xstage_bytes(mode, M) + P.stages * wstage_bytes(mode) + P.ms_red_bytes +
+                   kMsQuantFloats * 4 + kSmemReserve;
+  } else {
+    P.ms_red_bytes = 0;
+    if (!ring_depths(mode, P.bn, P.xstages, P.stages, P.rows_bytes)) return -2;
+    P.smem_bytes = P.xstages * xstage_bytes(mode, P.bn) + P.stages * wstage_bytes(mode) + P.rows_bytes +
+                   kSmemReserve;
+  }
   // Tile counters live in a fixed region at the start of every workspace, sized for
   // the largest stream-K plan (fewer than kStreamKMaxTilesPerSm tiles per SM), so
   // that no plan's partials or widened activations ever overlap another plan's

@@ -80,6 +80,43 @@ def test_argument_errors_before_device():
     assert L.qpack_w8(FAKE, FAKE, 128, 130, FAKE, n) == q.QW_ERR_UNSUPPORTED_SHAPE
 
 
+def test_alignment_rules_match_header():
+    """Each alignment the header states is checked on the host before any device access:
+    one pointer at a time is moved off its boundary by the smallest step that breaks it."""
+    L = q.lib()
+    n = ctypes.c_void_p(0)
+    B = 1 << 20
+
+    def at(off):
+        return ctypes.c_void_p(B + off)
+
+    A = q.QW_ERR_ALIGNMENT
+    # GEMMs: activations and packed weights 16 B, workspace 256 B, y 2 B, xs 4 B
+    assert L.qgemm_w4a16(at(8), at(0), 4, 512, 256, at(0), at(0), B, n) == A
+    assert L.qgemm_w4a16(at(0), at(8), 4, 512, 256, at(0), at(0), B, n) == A
+    assert L.qgemm_w4a16(at(0), at(0), 4, 512, 256, at(1), at(0), B, n) == A
+    assert L.qgemm_w4a16(at(0), at(0), 4, 512, 256, at(0), at(128), B, n) == A
+    assert L.qgemm_w4a8(at(0), at(2), at(0), 4, 512, 256, at(0), at(0), B, n) == A
+    assert L.qgemm_w4a8_fused(at(8), at(0), 4, 512, 256, at(0), at(0), B, n) == A
+    # y at 2 bytes and xs at 4 bytes are accepted (past the checks: no device here)
+    ok = (q.QW_OK, q.QW_ERR_ARCH, q.QW_ERR_WORKSPACE)
+    assert L.qgemm_w4a8(at(0), at(4), at(0), 4, 512, 256, at(2), at(0), B, n) in ok
+    # packing: codes and packed 16 B, scales 2 B
+    assert L.qpack_w4(at(8), at(0), 128, 128, at(0), n) == A
+    assert L.qpack_w4(at(0), at(1), 128, 128, at(0), n) == A
+    assert L.qpack_w8(at(0), at(0), 128, 128, at(8), n) == A
+    # quantizer: x 16 B, xq 8 B, xs 4 B
+    assert L.quant_act_int8(at(8), 2, 16, at(0), at(0), n) == A
+    assert L.quant_act_int8(at(0), 2, 16, at(4), at(0), n) == A
+    assert L.quant_act_int8(at(0), 2, 16, at(0), at(2), n) == A
+    # gather: ids 4 B, table and output 16 B; top-k: logits 16 B, vals 2 B, idx 4 B, ws 256 B
+    assert L.embed_gather_w8(at(2), 4, at(0), 256, 256, at(0), n) == A
+    assert L.embed_gather_w8(at(0), 4, at(0), 256, 256, at(8), n) == A
+    assert L.topk_logits(at(0), 2, 256, 4, at(1), at(0), at(0), B, n) == A
+    assert L.topk_logits(at(0), 2, 256, 4, at(0), at(2), at(0), B, n) == A
+    assert L.topk_logits(at(0), 2, 256, 4, at(0), at(0), at(128), B, n) == A
+
+
 def test_options_host_only():
     L = q.lib()
     assert L.qw_get_option(q.QW_OPT_WEIGHTS_IMMUTABLE) == 0
@@ -303,7 +340,10 @@ def test_schedule_partition_random_shapes():
         p = q.plan(mode, M, N, K, sms)
         if p.chunks > 200_000:                    # keep the CPU check quick
             continue
-        assert 1 <= p.grid <= sms and p.smem_bytes <= 232448 and p.stages >= 2
+        # one CTA per SM; the decode-batch kernel (half an SM each) runs two for long launches
+        assert 1 <= p.grid <= (2 * sms if p.decode_teams else sms) and p.smem_bytes <= 232448 and p.stages >= 2
+        if p.decode_teams:
+            assert p.smem_bytes <= 113 * 1024 and M <= 16 and mode in (0, 1, 3)
         assert p.bn >= min(M, 256) and p.token_tiles == -(-M // p.bn)
         # the weight ring is split into one half per chunk parity, each slot with a single
         # producer filling it in order: an odd depth would let a parity wait alias (ABA)
