@@ -283,10 +283,12 @@ long long qw_num_kernel_launches(void);
  *       2 e4m3 x e4m3 -> f32 (m16n8k32), 3 s4 x s4 -> s32 (m16n8k64).  sm_103a has
  *       no int8 tcgen05 MMA, so kind 1 measures the int8 tensor-core rate that the
  *       W4A8 mode ("In full" item 4: int8 tensor cores) is reported against.
- *       Launches `ctas` CTAs of 256 threads; every warp issues iters x 8 independent
- *       MMAs on register operands.  sink: ctas*256 binary32, device (written so the
- *       work is kept).  *ops (host) = 2*m*n*k per MMA x the MMAs of the launch; the
- *       caller times the launch.  Async.
+ *       Launches `ctas` CTAs of 256 threads; every thread keeps `chains` (1, 2, 4
+ *       or 8) independent accumulators and its warp issues iters x chains MMAs on
+ *       register operands (8 chains measure the rate, 1 the latency of dependent
+ *       MMAs).  sink: ctas*256 binary32, device (written so the work is kept).
+ *       *ops (host) = 2*m*n*k per MMA x the MMAs of the launch; the caller times
+ *       the launch.  Async.
  *   qw_diag_tc_probe  tcgen05.mma timing at the GEMM's shapes: `grid` CTAs (<= SMs,
  *       one per SM); lane 0 of warps 0..issuers-1 each stream `chunks` chunks of a
  *       128 x n x 128 product (kind 0: kind::f16, 8 MMAs of K = 16; kind 1:
@@ -305,7 +307,8 @@ long long qw_num_kernel_launches(void);
  * Return QW_OK, QW_ERR_INVALID_ARG, QW_ERR_ALIGNMENT, QW_ERR_ARCH or QW_ERR_CUDA;
  * a bounded wait that runs out records QW_ERR_TIMEOUT (read by qw_device_error).
  * ------------------------------------------------------------------------ */
-int qw_diag_mma_peak(int kind, int ctas, int iters, float *sink, double *ops, qw_stream_t stream);
+int qw_diag_mma_peak(int kind, int ctas, int iters, int chains, float *sink, double *ops,
+                     qw_stream_t stream);
 int qw_diag_tc_probe(int kind, int a_tmem, int n, int issuers, int chunks, int window,
                      unsigned long long *out, int grid, qw_stream_t stream);
 int qw_diag_f8f6f4_gemm(const uint8_t *a, const uint8_t *b, int K, int a_tmem, float *d,

@@ -67,7 +67,7 @@ SIGNATURES = {
     "qw_num_kernel_launches": (_ll, []),
     "qw_set_option": (_i, [_i, _i]),
     "qw_get_option": (_i, [_i]),
-    "qw_diag_mma_peak": (_i, [_i, _i, _i, _p, ctypes.POINTER(ctypes.c_double), _p]),
+    "qw_diag_mma_peak": (_i, [_i, _i, _i, _i, _p, ctypes.POINTER(ctypes.c_double), _p]),
     "qw_diag_tc_probe": (_i, [_i, _i, _i, _i, _i, _i, _p, _i, _p]),
     "qw_diag_f8f6f4_gemm": (_i, [_p, _p, _i, _i, _p, _p]),
     "qw_plan": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(Plan)]),
@@ -383,14 +383,14 @@ def num_kernel_launches() -> int:
 MMA_KINDS = {"f16": 0, "s8": 1, "e4m3": 2, "s4": 3}
 
 
-def diag_mma_peak(kind: str, ctas: int, iters: int, device=None):
-    """Launch the mma.sync rate microbenchmark on the current stream; returns
-    (ops of the launch, sink tensor).  The caller times the launch."""
+def diag_mma_peak(kind: str, ctas: int, iters: int, chains: int = 8, device=None):
+    """Launch the mma.sync rate (chains=8) or latency (chains=1) microbenchmark on the
+    current stream; returns (ops of the launch, sink tensor).  The caller times it."""
     dev = torch.device(device or "cuda")
     sink = torch.empty(ctas * 256, dtype=torch.float32, device=dev)
     ops = ctypes.c_double(0.0)
     with torch.cuda.device(dev):
-        _check(lib().qw_diag_mma_peak(MMA_KINDS[kind], ctas, iters, _ptr(sink), ctypes.byref(ops),
+        _check(lib().qw_diag_mma_peak(MMA_KINDS[kind], ctas, iters, chains, _ptr(sink), ctypes.byref(ops),
                                       _stream(sink)))
     return ops.value, sink
 

@@ -75,10 +75,12 @@ __device__ __forceinline__ void mma_sync_op(uint32_t (&d)[4], const uint32_t (&a
 }
 
 constexpr int kPeakThreads = 256;
-constexpr int kPeakChains = 8;   // independent accumulators per thread
 
-template <int KIND>
+// CHAINS independent accumulators per thread: 8 saturate the pipe (rate), 1 exposes the
+// latency of one MMA that depends on the previous one
+template <int KIND, int CHAINS>
 __global__ void __launch_bounds__(kPeakThreads) mma_peak_kernel(int iters, float *sink) {
+  constexpr int kPeakChains = CHAINS;
   const uint32_t t = blockIdx.x * kPeakThreads + threadIdx.x;
   uint32_t a[4], b[2];
 #pragma unroll
@@ -335,8 +337,11 @@ __global__ void __launch_bounds__(128, 1) f8f6f4_gemm_kernel(const uint8_t *__re
 }
 
 template <int KIND>
-cudaError_t run_peak(int ctas, int iters, float *sink, cudaStream_t st) {
-  mma_peak_kernel<KIND><<<ctas, kPeakThreads, 0, st>>>(iters, sink);
+cudaError_t run_peak(int ctas, int iters, int chains, float *sink, cudaStream_t st) {
+  if (chains == 1) mma_peak_kernel<KIND, 1><<<ctas, kPeakThreads, 0, st>>>(iters, sink);
+  else if (chains == 2) mma_peak_kernel<KIND, 2><<<ctas, kPeakThreads, 0, st>>>(iters, sink);
+  else if (chains == 4) mma_peak_kernel<KIND, 4><<<ctas, kPeakThreads, 0, st>>>(iters, sink);
+  else mma_peak_kernel<KIND, 8><<<ctas, kPeakThreads, 0, st>>>(iters, sink);
   count_launch();
   return cudaGetLastError();
 }
@@ -346,21 +351,22 @@ cudaError_t run_peak(int ctas, int iters, float *sink, cudaStream_t st) {
 
 extern "C" {
 
-int qw_diag_mma_peak(int kind, int ctas, int iters, float *sink, double *ops, qw_stream_t stream) {
-  if (kind < 0 || kind > 3 || ctas < 1 || ctas > (1 << 20) || iters < 1 || !sink || !ops)
-    return qw::set_last_error(QW_ERR_INVALID_ARG, "qw_diag_mma_peak: bad kind, size or pointer");
+int qw_diag_mma_peak(int kind, int ctas, int iters, int chains, float *sink, double *ops, qw_stream_t stream) {
+  if (kind < 0 || kind > 3 || ctas < 1 || ctas > (1 << 20) || iters < 1 || !sink || !ops ||
+      (chains != 1 && chains != 2 && chains != 4 && chains != 8))
+    return qw::set_last_error(QW_ERR_INVALID_ARG, "qw_diag_mma_peak: bad kind, size, chains or pointer");
   int rc = qw::device_info(nullptr, nullptr);
   if (rc) return rc;
   // flops (or integer ops) of one MMA: 2 m n k
   static const double per_mma[4] = {2.0 * 16 * 8 * 16, 2.0 * 16 * 8 * 32, 2.0 * 16 * 8 * 32, 2.0 * 16 * 8 * 64};
-  *ops = per_mma[kind] * (double)ctas * (qw::kPeakThreads / 32) * (double)iters * qw::kPeakChains;
+  *ops = per_mma[kind] * (double)ctas * (qw::kPeakThreads / 32) * (double)iters * chains;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (kind) {
-    case 0: e = qw::run_peak<0>(ctas, iters, sink, st); break;
-    case 1: e = qw::run_peak<1>(ctas, iters, sink, st); break;
-    case 2: e = qw::run_peak<2>(ctas, iters, sink, st); break;
-    default: e = qw::run_peak<3>(ctas, iters, sink, st); break;
+    case 0: e = qw::run_peak<0>(ctas, iters, chains, sink, st); break;
+    case 1: e = qw::run_peak<1>(ctas, iters, chains, sink, st); break;
+    case 2: e = qw::run_peak<2>(ctas, iters, chains, sink, st); break;
+    default: e = qw::run_peak<3>(ctas, iters, chains, sink, st); break;
   }
   if (e != cudaSuccess) return qw::set_last_error(QW_ERR_CUDA, cudaGetErrorString(e));
   return QW_OK;

@@ -674,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         named_bar_sync(1, kEpiWarps * 32);
         // a cut segment is this CTA's first or its last
         const int cut = i == 0 ? cut_first : cut_last;
-        const int pf = cut & 0xff, pl = (cut >> 8) & 0xff;
+        const int pf = qw::cut_first(cut), pl = qw::cut_last(cut);
         if (ept == 0) {
           const int old = atom_add_acq_rel_gpu(a.counters + sg.tile, 1);
           const int last = (old == pl - pf) ? 1 : 0;
@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     const uint32_t avail = ring_bytes;
     for (int r = 0; r < npend && !aborted; ++r) {
       const int tile = pend_tile[r];
-      const int pf = pend_cut[r] & 0xff, pl = (pend_cut[r] >> 8) & 0xff, pf_slot = pend_cut[r] >> 16;
+      const int pf = qw::cut_first(pend_cut[r]), pl = qw::cut_last(pend_cut[r]), pf_slot = qw::cut_slot(pend_cut[r]);
       int u, t;
       tile_coords(P, tile, u, t);
       const int n = t * kRows + row;

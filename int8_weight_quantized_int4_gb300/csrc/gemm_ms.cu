@@ -5,9 +5,9 @@
 
 namespace qw {
 
-template <int NT8, int AMODE>
+template <int NT8, int AMODE, int RBW = 2>
 static cudaError_t run_ms(const GemmArgs &a, cudaStream_t st) {
-  auto *k = qgemm_ms_kernel<NT8, AMODE>;
+  auto *k = qgemm_ms_kernel<NT8, AMODE, RBW>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(k), a.P.smem_bytes);
   if (e != cudaSuccess) return e;
   e = launch_pdl(reinterpret_cast<const void *>(k), dim3(a.P.grid), dim3(ms_threads()),
@@ -17,10 +17,13 @@ static cudaError_t run_ms(const GemmArgs &a, cudaStream_t st) {
 }
 
 cudaError_t launch_gemm_ms(const GemmArgs &a, int act, cudaStream_t st) {
-  if (!a.P.ms_teams || a.P.ms_teams != ms_teams(a.P.M) || a.P.bn != kMsMaxTokens) return cudaErrorInvalidValue;
-  const bool one = a.P.M <= 8;
+  // teams = 16-row blocks per warp (plan); four only for eight tokens from fp16
+  if ((a.P.ms_teams != 2 && a.P.ms_teams != 4) || a.P.bn != kMsMaxTokens) return cudaErrorInvalidValue;
+  const bool one = a.P.M <= 8, four = a.P.ms_teams == 4;
+  if (four && !(one && act == kActF16)) return cudaErrorInvalidValue;
   if (act == kActQuant) return one ? run_ms<1, kActQuant>(a, st) : cudaErrorInvalidValue;
   if (act == kActI8) return one ? run_ms<1, kActI8>(a, st) : run_ms<2, kActI8>(a, st);
+  if (four) return run_ms<1, kActF16, 4>(a, st);
   return one ? run_ms<1, kActF16>(a, st) : run_ms<2, kActF16>(a, st);
 }
 

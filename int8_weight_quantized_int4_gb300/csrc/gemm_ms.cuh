@@ -19,14 +19,15 @@
 // an SM, so the next layer's CTAs start while this layer's finish):
 //   warp 0, lane 0 : one bulk copy per packed chunk into the weight ring; the ring is
 //                    split into one part per team and a team's chunks fill its part
-//                    in order
+//                    in order.  When the weights may be read ahead of the preceding
+//                    kernel, the chunks beyond the ring are first prefetched into L2.
 //   warp 1, lane 0 : one TMA tensor copy per block of four K groups of the
 //                    activations (8 or 16 token rows, 128-byte swizzle, zero fill past M)
-//   compute warps  : eight, in teams; team j takes the chunks with CTA-wide index
-//                    = j (mod teams), visiting the activation blocks and, in each, only
-//                    its own chunks.  Up to 8 tokens a warp covers four 16-row blocks of
-//                    a chunk (four teams of two warps), up to 16 tokens two (two teams of
-//                    four): more independent MMA chains per warp where registers allow.
+//   compute warps  : eight, in teams; team j takes the chunks with CTA-wide index = j
+//                    (mod teams), visiting the activation blocks and, in each, only its
+//                    own chunks.  A warp covers RBW 16-row blocks of a chunk: two (two
+//                    teams of four warps), or four for long launches of up to 8 tokens
+//                    (four teams of two: more independent MMA chains per warp).
 //                    K step by K step the weights become MMA fragments and accumulate
 //                    into a per-group fp32 sum, which is then scaled by the signed group
 //                    scale (binary32) into the running sum.  At the end of a tile
@@ -113,11 +114,12 @@ __device__ __forceinline__ void frag_w4_zp(uint32_t w, uint32_t (&a)[4]) {
   a[3] = lop3_and_or(x, 0x00f000f0u, 0x64006400u);
 }
 
-template <int NT8, int AMODE>
+template <int NT8, int AMODE, int RBW>
 __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_constant__ GemmArgs a) {
   constexpr bool ACT8 = AMODE == kActI8;
   constexpr bool QIN = AMODE == kActQuant;
-  constexpr int RBW = NT8 == 1 ? 4 : 2;                 // 16-row blocks per warp in a chunk
+  static_assert(RBW == 2 || RBW == 4, "16-row blocks per warp in a chunk");
+  constexpr int KS = 1;                                 // accumulator sets per row block
   constexpr int TW = 8 / RBW;                           // warps per team (a chunk has 8 row blocks)
   constexpr int TEAMS = kMsComputeWarps / TW;
   constexpr int kCompute = kMsComputeWarps;
@@ -233,6 +235,18 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
     // ------------------------------------------------------ weight copies --
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
+      if (early) {
+        // ahead of the preceding kernel: the chunks that will not fit the ring now are
+        // pulled into L2, so that their copies after the wait come from L2, not HBM
+        int c = 0;
+        for (int i = 0; segment(P, cta, i, sg); ++i) {
+          int u, t;
+          tile_coords(P, sg.tile, u, t);
+          const uint8_t *src = a.wpack + ((size_t)t * P.G + sg.g0) * kChunkW4;
+          for (int g = sg.g0; g < sg.g1; ++g, ++c, src += kChunkW4)
+            if (c >= SW) prefetch_l2(src, kChunkW4);
+        }
+      }
       int s[TEAMS], cidx = 0;
       uint32_t ph[TEAMS];
 #pragma unroll
@@ -357,15 +371,19 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
           uint32_t sc2[RBW];
 #pragma unroll
           for (int r = 0; r < RBW; ++r) sc2[r] = lds32(wc + soff + (uint32_t)(r * 32));
-          float ga[RBW][NT8][4], gz[NT8][4];
+          // KS accumulator sets (K step % KS): MMAs on one accumulator form a dependent
+          // chain, and more sets shorten it
+          float ga[KS][RBW][NT8][4], gz[KS][NT8][4];
 #pragma unroll
-          for (int jt = 0; jt < NT8; ++jt)
+          for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              gz[jt][e] = 0.0f;
+            for (int jt = 0; jt < NT8; ++jt)
 #pragma unroll
-              for (int r = 0; r < RBW; ++r) ga[r][jt][e] = 0.0f;
-            }
+              for (int e = 0; e < 4; ++e) {
+                gz[ks][jt][e] = 0.0f;
+#pragma unroll
+                for (int r = 0; r < RBW; ++r) ga[ks][r][jt][e] = 0.0f;
+              }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {                  // K steps 4 h .. 4 h + 3
             uint4 v[RBW];
@@ -389,7 +407,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
                 const int wd = (2 * sp2 + kk);           // word of the vector = K step % 4
                 if constexpr (kZP) {
 #pragma unroll
-                  for (int jt = 0; jt < NT8; ++jt) mma_16816(gz[jt], zp, bf[kk][jt][0], bf[kk][jt][1]);
+                  for (int jt = 0; jt < NT8; ++jt) mma_16816(gz[kk % KS][jt], zp, bf[kk][jt][0], bf[kk][jt][1]);
                 }
 #pragma unroll
                 for (int r = 0; r < RBW; ++r) {
@@ -398,7 +416,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
                   if constexpr (kZP) frag_w4_zp(w, af);
                   else frag_w4(w, af);
 #pragma unroll
-                  for (int jt = 0; jt < NT8; ++jt) mma_16816(ga[r][jt], af, bf[kk][jt][0], bf[kk][jt][1]);
+                  for (int jt = 0; jt < NT8; ++jt) mma_16816(ga[kk % KS][r][jt], af, bf[kk][jt][0], bf[kk][jt][1]);
                 }
               }
             }
@@ -412,8 +430,12 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
 #pragma unroll
             for (int jt = 0; jt < NT8; ++jt)
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                acc[r][jt][e] = fmaf(e < 2 ? sf.x : sf.y, kZP ? ga[r][jt][e] + gz[jt][e] : ga[r][jt][e], acc[r][jt][e]);
+              for (int e = 0; e < 4; ++e) {
+                float gs = 0.0f;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) gs += kZP ? ga[ks][r][jt][e] + gz[ks][jt][e] : ga[ks][r][jt][e];
+                acc[r][jt][e] = fmaf(e < 2 ? sf.x : sf.y, gs, acc[r][jt][e]);
+              }
           }
         }
         __syncwarp();
@@ -469,7 +491,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
       named_bar_sync(1, kCThreads);
       if (part && !aborted) {
         const int cut = i == 0 ? cut_first : cut_last;
-        const int pf = cut & 0xff, pl = (cut >> 8) & 0xff;
+        const int pf = qw::cut_first(cut), pl = qw::cut_last(cut);
         if (ct == 0) {
           const int old = atom_add_acq_rel_gpu(a.counters + sg.tile, 1);
           const int last = (old == pl - pf) ? 1 : 0;
@@ -489,7 +511,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
     // these reads after their release), summed in CTA order
     for (int r = 0; r < npend && !aborted; ++r) {
       const int tile = pend_tile[r];
-      const int pf = pend_cut[r] & 0xff, pl = (pend_cut[r] >> 8) & 0xff, pf_slot = pend_cut[r] >> 16;
+      const int pf = qw::cut_first(pend_cut[r]), pl = qw::cut_last(pend_cut[r]), pf_slot = qw::cut_slot(pend_cut[r]);
       int u, t;
       tile_coords(P, tile, u, t);
       const int mv = P.M < kMsMaxTokens ? P.M : kMsMaxTokens;

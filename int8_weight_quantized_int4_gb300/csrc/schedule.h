@@ -52,11 +52,19 @@ struct Plan {
   size_t ws_counters, ws_partials, ws_act, ws_quant, ws_bytes, ws_zero;
   int begin[kMaxGrid + 1];       // stream-K: first chunk of each CTA (begin[grid] = chunks)
   // stream-K: for CTA p's first ([p][0]) and last ([p][1]) segment, when that segment
-  // is a cut tile, its contributors packed as  p_first | p_last << 8 | slot << 16
-  // (slot = partial slot of p_first; the others use 2 p'), else 0.  Lets a kernel
-  // find the partials of a cut tile without searching the begin table.
+  // is a cut tile, its contributors packed by cut_pack (p_first, p_last and the partial
+  // slot of p_first; the others use 2 p'), else 0.  Lets a kernel find the partials of a
+  // cut tile without searching the begin table.
   int cut[kMaxGrid][2];
 };
+
+// cut-tile contributors: p_first and p_last in 10 bits each (kMaxGrid <= 1024), the
+// partial slot of p_first (< 2 kMaxGrid) in the upper 12 bits
+static_assert(kMaxGrid <= 1024, "cut packing");
+QW_HD int cut_pack(int pf, int pl, int slot) { return pf | (pl << 10) | (slot << 20); }
+QW_HD int cut_first(int c) { return c & 0x3ff; }
+QW_HD int cut_last(int c) { return (c >> 10) & 0x3ff; }
+QW_HD int cut_slot(int c) { return (int)((unsigned)c >> 20); }
 
 struct Seg {
   int tile;
@@ -191,12 +199,13 @@ QW_HD bool ms_kernel(int mode, int M) {
 }
 // token rows of its activation tiles: 8 (one tile of eight tokens) or 16
 QW_HD int ms_rows(int M) { return M <= 8 ? 8 : 16; }
-// 16-row blocks of a chunk per warp: 4 for eight tokens, 2 for sixteen (registers)
-QW_HD int ms_row_blocks(int M) { return M <= 8 ? 4 : 2; }
-// teams (each computing one chunk at a time): 8 row blocks / row blocks per warp warps each
-QW_HD int ms_teams(int M) { return kMsComputeWarps * ms_row_blocks(M) / 8; }
+// 16-row blocks of a chunk per warp: 4 for long launches of up to 8 tokens from fp16
+// activations (more independent MMA chains per warp), else 2.  A team computes one chunk
+// at a time with 8 / (row blocks per warp) warps, so there are as many teams as row blocks
+// per warp.
+QW_HD int ms_row_blocks(int mode, int M, bool long_launch) { return long_launch && mode == 0 && M <= 8 ? 4 : 2; }
 // the teams other than the first leave their sums here at the end of a tile segment
-QW_HD int ms_red_bytes(int M) { return (ms_teams(M) - 1) * ms_rows(M) * kMsRedStride * 4; }
+QW_HD int ms_red_bytes(int M, int teams) { return (teams - 1) * ms_rows(M) * kMsRedStride * 4; }
 // activation slot: act_block(16) = 4 K groups of ms_rows(M) x 128 fp16 (+ int8 staging)
 QW_HD int ms_xstage_bytes(int mode, int M) {
   return 4 * ms_rows(M) * kGroup * (mode == 1 ? 3 : 2);
@@ -206,13 +215,13 @@ QW_HD int ms_xstage_bytes(int mode, int M) {
 constexpr int kMsQuantFloats = 8 * 8 + 8 + 8;
 // ring depths: three activation blocks when that leaves eight weight slots, else two;
 // the weight slots (at most kMaxWStages) split evenly between the teams
-QW_HD bool ms_ring_depths(int mode, int M, int &xst, int &wst) {
+QW_HD bool ms_ring_depths(int mode, int M, int teams, int &xst, int &wst) {
   const int xb = ms_xstage_bytes(mode, M), wb = (int)align_up((size_t)kChunkW4, 128);
   for (int x = 3; x >= 2; --x) {
-    int w = (kMsSmemLimit - kSmemReserve - ms_red_bytes(M) - kMsQuantFloats * 4 - x * xb) / wb;
+    int w = (kMsSmemLimit - kSmemReserve - ms_red_bytes(M, teams) - kMsQuantFloats * 4 - x * xb) / wb;
     if (w > kMaxWStages) w = kMaxWStages;
-    w -= w % ms_teams(M);
-    if (w >= 8 || (x == 2 && w >= 2 * ms_teams(M))) { xst = x; wst = w; return true; }
+    w -= w % teams;
+    if (w >= 8 || (x == 2 && w >= 2 * teams)) { xst = x; wst = w; return true; }
   }
   return false;
 }
@@ -277,7 +286,7 @@ inline void fill_begin(Plan &P) {
       if (s.slot < 0) continue;
       int pf, pl;
       tile_contributors(P, s.tile, pf, pl);
-      P.cut[p][e] = pf | (pl << 8) | (partial_slot(P, pf, s.tile) << 16);
+      P.cut[p][e] = cut_pack(pf, pl, partial_slot(P, pf, s.tile));
     }
   }
 }
@@ -313,10 +322,10 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   else P.grid = P.tiles < ctas ? P.tiles : ctas;
   fill_begin(P);
   P.xblock = act_block(P.bn);
-  P.ms_teams = ms_kernel(mode, M) ? ms_teams(M) : 0;
+  P.ms_teams = ms_kernel(mode, M) ? ms_row_blocks(mode, M, ctas > num_sms) : 0;
   if (P.ms_teams) {
-    P.ms_red_bytes = ms_red_bytes(M);
-    if (!ms_ring_depths(mode, M, P.xstages, P.stages)) return -2;
+    P.ms_red_bytes = ms_red_bytes(M, P.ms_teams);
+    if (!ms_ring_depths(mode, M, P.ms_teams, P.xstages, P.stages)) return -2;
     P.smem_bytes = P.xstages * ms_xstage_bytes(mode, M) + P.stages * wstage_bytes(mode) + P.ms_red_bytes +
                    kMsQuantFloats * 4 + kSmemReserve;
   } else {

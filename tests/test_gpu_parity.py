@@ -228,6 +228,18 @@ def test_ffn_pair_m64_w4a8(q):
     assert max(e_up.values()) <= TOL and max(e_dn.values()) <= TOL, (e_up, e_dn)
 
 
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_decode_long_launch_two_ctas_per_sm(q, M):
+    """A decode-sized batch over enough chunks that the schedule runs two CTAs per SM
+    (more than 256 CTAs): every output against the oracle."""
+    p = synth.make_problem(M, 16384, 5120, seed=470 + M, outlier_frac=0.01)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    pl = q.plan(q.MODE_W4A16, M, p.N, p.K, sms)
+    assert pl.decode_teams > 0 and pl.grid > sms, (pl.grid, pl.decode_teams)
+    e = run_modes(q, p, ("w4a16", "w4a8"))
+    assert max(e.values()) <= TOL, e
+
+
 @pytest.mark.slow
 def test_prefill_8192_sampled(q):
     p = synth.prefill(8192)
