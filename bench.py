@@ -6,7 +6,7 @@ M in {1, 4, 16, 64} tokens, in both modes -- W4A16, and W4A8 with per-token
 int8 activation quantization -- over 32 distinct packed weight matrices (one
 per "layer", 432 MB in total, so every GEMM streams its weights from HBM, not
 L2).  One step = every (mode, M) over all 32 layers: 128 W4A16 GEMMs plus 128
-x (quantize, widen, W4A8 GEMM).  Each (mode, M) block is captured once as a
+W4A8 layers from fp16 (one kernel up to 16 tokens; quantizer, widening and GEMM at 64).  Each (mode, M) block is captured once as a
 CUDA graph through the library's public calls and replayed; CUDA events on the
 launching stream time every block.
 
@@ -55,13 +55,14 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "qgemm_tc_kernel_proj_w4a16_m16.md")
-KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "schedule.h")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "qgemm_ms_kernel_proj_w4a16_m16.md")
+KERNEL_SOURCES = ("gemm_ms.cuh", "gemm_kernel.cuh", "ptx.cuh", "schedule.h")
 
 
 def profiled_traffic():
-    """DRAM bytes (read + write) of one headline GEMM launch, from the committed ncu
-    summary, provided the kernel sources still hash to what was profiled; else None."""
+    """DRAM bytes (read + write) of one M = 16 projection launch of the decode-batch
+    kernel, from the committed ncu summary, provided the kernel sources still hash to
+    what was profiled; else None."""
     try:
         text = open(TRAFFIC_PROFILE).read()
     except OSError:
@@ -333,6 +334,7 @@ def run_ours(args):
             else:
                 g.replay()
 
+    blocks_default = []
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step(gl=graphs_default)
@@ -340,7 +342,7 @@ def run_ours(args):
         d0.record(stream)
         nd = max(3, args.steps // 4)
         for _ in range(nd):
-            step(gl=graphs_default)
+            step(blocks_default, gl=graphs_default)
         d1.record(stream)
         for _ in range(args.warmup):
             step()
@@ -368,49 +370,62 @@ def run_ours(args):
     ms_per_step = elapsed_ms / args.steps
     value = ws_n * step_wbytes * args.steps / (elapsed_ms / 1e3) / 1e9
 
-    # ---- per (mode, M) figures from the block events
-    per = {}
-    for mode, M, s, e in blocks:
-        per.setdefault((mode, M), []).append(s.elapsed_time(e))
-    per_m = {}
+    # ---- per (mode, M) figures from the block events, for the headline mode (weights
+    #      declared immutable) and for the library default
+    def per_m_table(blist):
+        per = {}
+        for mode, M, s, e in blist:
+            per.setdefault((mode, M), []).append(s.elapsed_time(e))
+        table = {}
+        for (mode, M), v in per.items():
+            ms = statistics.median(v)
+            us = 1e3 * ms / LAYERS
+            flops = 2.0 * M * N * K
+            act_b = M * K * (2 if mode == "w4a16" else 1) + (4 * M if mode == "w4a8" else 0)
+            alg = w4_bytes(N, K) + act_b + 2 * M * N
+            table[f"{mode}_M{M}"] = {
+                "us_per_layer": round(us, 3), "weight_GBps": round(w4_bytes(N, K) / us / 1e3, 1),
+                "TFLOPS": round(flops / us / 1e6, 2), "alg_GBps": round(alg / us / 1e3, 1),
+                "frac_hbm": round(alg / us / 1e3 / hbm, 4),
+                "kernels_per_layer": 1 if mode == "w4a16" else w4a8_kernels(M, N, K),
+                "kernel": "qgemm_ms_kernel" if M <= 16 else "qgemm_tc_kernel"}
+        return per, table
+
+    per, per_m = per_m_table(blocks)
+    _, per_m_default = per_m_table(blocks_default)
+    # roofline of the dominant kernel: the decode-batch kernel (M <= 16, both modes, about
+    # two thirds of the step's device time), W4A16 launches at M = 1, 4, 16
     roof_bytes = roof_ms = 0.0
     for (mode, M), v in per.items():
-        ms = statistics.median(v)
-        us = 1e3 * ms / LAYERS
-        flops = 2.0 * M * N * K
-        act_b = M * K * (2 if mode == "w4a16" else 1) + (4 * M if mode == "w4a8" else 0)
-        alg = w4_bytes(N, K) + act_b + 2 * M * N
-        per_m[f"{mode}_M{M}"] = {
-            "us_per_layer": round(us, 3), "weight_GBps": round(w4_bytes(N, K) / us / 1e3, 1),
-            "TFLOPS": round(flops / us / 1e6, 2), "alg_GBps": round(alg / us / 1e3, 1),
-            "frac_hbm": round(alg / us / 1e3 / hbm, 4),
-            "kernels_per_layer": 1 if mode == "w4a16" else w4a8_kernels(M, N, K)}
-        if mode == "w4a16":
-            roof_bytes += alg * LAYERS * len(v)
+        if mode == "w4a16" and M <= 16:
+            roof_bytes += (w4_bytes(N, K) + 4 * M * K) * LAYERS * len(v)
             roof_ms += sum(v)
     achieved = roof_bytes / (roof_ms / 1e3) / 1e9
     traffic = profiled_traffic()
-    roofline = {"bound": "hbm", "kernel": "qgemm_tc_kernel (W4A16, M=1..64, K=N=5120)",
+    roofline = {"bound": "hbm", "kernel": "qgemm_ms_kernel (W4A16, M = 1, 4, 16, K = N = 5120)",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "peak_source": pk_src,
+                "frac": round(achieved / hbm, 4), "peak_source": pk_src + " (hbm_gbs)",
                 "traffic": traffic,
-                "traffic_source": ("ncu capture of one M=16 launch, DRAM read + write bytes "
-                                   "(profiles/qgemm_tc_kernel_proj_w4a16_m16.md)" if traffic is not None
+                "traffic_source": ("ncu capture of one M = 16 launch, DRAM read + write bytes"
+                                   if traffic is not None
                                    else "null: kernel sources changed since the last ncu capture"),
                 "per_launch_alg_bytes": "13,516,800 B packed weights + 2MK activation + 2MN output"}
 
     # ---- parity spot check of the timed outputs (the pages' lesson: a kernel can
     #      benchmark beautifully while producing garbage)
     import oracle
-    cols = np.arange(0, N, 37)
     parity = {}
     for M in MS:
-        xc = X[M][LAYERS - 1].cpu()
-        ref16 = oracle.w4a16(xc, p.codes[cols], p.scales[cols])
-        parity[f"w4a16_M{M}"] = parity_err(Y16[M][LAYERS - 1].cpu()[:, cols], ref16)
-        oq, os_ = oracle.quant_act_int8(xc)
-        ref8 = oracle.w4a8(oq, os_, p.codes[cols], p.scales[cols])
-        parity[f"w4a8_M{M}"] = parity_err(Y8[M][LAYERS - 1].cpu()[:, cols], ref8)
+        # every output of the last layer, and a column sample of the first
+        for r, cols in ((LAYERS - 1, np.arange(N)), (0, np.arange(0, N, 7))):
+            xc = X[M][r].cpu()
+            ref16 = oracle.w4a16(xc, p.codes[cols], p.scales[cols])
+            e16 = parity_err(Y16[M][r].cpu()[:, cols], ref16)
+            oq, os_ = oracle.quant_act_int8(xc)
+            ref8 = oracle.w4a8(oq, os_, p.codes[cols], p.scales[cols])
+            e8 = parity_err(Y8[M][r].cpu()[:, cols], ref8)
+            parity[f"w4a16_M{M}"] = max(parity.get(f"w4a16_M{M}", 0.0), e16)
+            parity[f"w4a8_M{M}"] = max(parity.get(f"w4a8_M{M}", 0.0), e8)
 
     # ---- end to end: host (pinned) inputs in, results out, every step
     hx = {M: X[M].cpu().pin_memory() for M in MS}
@@ -457,7 +472,7 @@ def run_ours(args):
                        "weights_immutable_option": True,
                        "value_with_default_option": round(value_default, 1),
                        "parallelism": f"replicas x{ws_n}"},
-            "roofline": roofline, "per_M": per_m, "parity": parity,
+            "roofline": roofline, "per_M": per_m, "per_M_default_option": per_m_default, "parity": parity,
             "gpu_launches": int(launches_per_step * args.steps), "clocks": clk, "e2e": e2e,
             "device_error": derr}
 
@@ -482,6 +497,32 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def mma_rates(q, dev):
+    """Dense rates of the warp-level tensor-core MMA (mma.sync) measured with the
+    library's microbenchmark: every warp issues independent MMAs on register operands
+    (8 chains), two 256-thread CTAs per SM, the best of 3 launches of ~20 ms each."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    res = {}
+    for kind in ("f16", "s8", "e4m3", "s4"):
+        iters = 2000
+        best = 0.0
+        for rep in range(4):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            ops, _ = q.diag_mma_peak(kind, 2 * sms, iters, 8, dev)
+            e.record()
+            torch.cuda.synchronize()
+            ms = s.elapsed_time(e)
+            if rep == 0:
+                iters = max(200, int(iters * 20.0 / max(ms, 1e-3)))
+                continue
+            best = max(best, ops / ms / 1e9)
+        res[kind] = {"TOPS": round(best, 1), "instruction": {
+            "f16": "mma.sync.m16n8k16 f16 -> f32", "s8": "mma.sync.m16n8k32 s8 -> s32",
+            "e4m3": "mma.sync.m16n8k32 e4m3 -> f32", "s4": "mma.sync.m16n8k64 s4 -> s32"}[kind]}
+    return res
+
+
 # ----------------------------------------------------- the other workloads --
 def extras(q, dev, stream, pk, pk_src):
     """FFN pair (M=64, W4A8), prefill (M=8192, both modes), 2048-token prefill chunks on
@@ -490,8 +531,14 @@ def extras(q, dev, stream, pk, pk_src):
     Each timed with CUDA events on graph replays, with a parity spot check."""
     import oracle
     hbm = float(pk["hbm_gbs"])
-    peak16 = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+    # the prefill cells are timed over a few graph replays (milliseconds): burst peak
+    peak16 = float(pk["bf16_tflops"])
+    peak16_sus = float(pk.get("bf16_tflops_sustained", peak16))
     out = {}
+    # measured warp-level MMA rates (the only int8 tensor-core instruction sm_103a has)
+    rates = mma_rates(q, dev)
+    out["mma_sync_peaks"] = rates
+    int8_peak = rates["s8"]["TOPS"]
 
     def timeit(fn, reps):
         g = capture(fn, stream)
@@ -549,10 +596,19 @@ def extras(q, dev, stream, pk, pk_src):
             oq, os_ = oracle.quant_act_int8(xr)
             ref = oracle.w4a8(oq, os_, pp.codes[cols], pp.scales[cols])
         tf = flops / ms / 1e9
-        out[f"prefill_m8192_{mode}"] = {
-            "ms": round(ms, 3), "TFLOPS": round(tf, 1), "frac_f16_peak": round(tf / peak16, 4),
-            "f16_peak_TFLOPS": peak16, "peak_source": pk_src + " (bf16 sustained; fp16 dense rate is the same)",
-            "int8_peak": None, "parity": parity_err(y.cpu().numpy()[rows][:, cols], ref)}
+        entry = {"ms": round(ms, 3), "TFLOPS": round(tf, 1), "frac_f16_peak": round(tf / peak16, 4),
+                 "f16_peak_TFLOPS": peak16,
+                 "peak_source": pk_src + " bf16_tflops (burst: the cell is a few ms of graph replays; "
+                                         "the dense fp16 rate equals bf16)",
+                 "frac_f16_sustained_peak": round(tf / peak16_sus, 4),
+                 "parity": parity_err(y.cpu().numpy()[rows][:, cols], ref)}
+        if mode == "w4a8":
+            # the int8 x int4 products run exactly on the fp16 tensor path; against the
+            # measured int8 tensor rate (mma.sync s8) the fraction exceeds 1
+            entry.update({"TOPS": round(tf, 1), "int8_peak": round(int8_peak, 1),
+                          "int8_peak_source": "mma.sync m16n8k32 s8 microbenchmark in this run",
+                          "frac_int8_peak": round(tf / int8_peak, 3)})
+        out[f"prefill_m8192_{mode}"] = entry
     del pkd, x, y, wsp
     torch.cuda.empty_cache()
 
@@ -581,6 +637,7 @@ def extras(q, dev, stream, pk, pk_src):
             tf = flops / ms / 1e9
             out[f"prefill_chunk_m2048_{name}_{mode}"] = {
                 "us": round(ms * 1e3, 1), "TFLOPS": round(tf, 1), "frac_f16_peak": round(tf / peak16, 4),
+                "peak": "bf16_tflops burst",
                 "N": prob.N, "K": prob.K, "parity": parity_err(y.cpu().numpy()[rows][:, cols], ref)}
         del pkd, x, y, wsp
     torch.cuda.empty_cache()
@@ -642,10 +699,10 @@ def extras(q, dev, stream, pk, pk_src):
         lg = synth.logits(M, lh.N, seed=50 + M).to(dev)
         ms = timeit(lambda: q.topk_logits(lg, 64), 20)
         entry = {"us": round(ms * 1e3, 2), "GBps": round(2 * M * lh.N / ms / 1e6, 1), "k": 64}
-        if M == 1:
-            v, i = q.topk_logits(lg, 64)
-            ov, oi = oracle.topk(lg.cpu().numpy(), 64)
-            entry["exact"] = bool(np.array_equal(i.cpu().numpy().astype(np.int64), oi))
+        v, i = q.topk_logits(lg, 64)
+        ov, oi = oracle.topk(lg.cpu().numpy(), 64)
+        entry["exact"] = bool(np.array_equal(i.cpu().numpy().astype(np.int64), oi) and
+                              np.array_equal(v.cpu().numpy().view(np.uint16), ov.view(np.uint16)))
         out[f"topk_logits_M{M}_N{lh.N}"] = entry
     return out
 
@@ -666,6 +723,8 @@ NCU_CASES = {
     "prefill_w4a8_m2048": ("w4a8", 2048, 34816, 5120, 4),
     # top-k (k = 64) over M rows of N logits: ("topk", M, N, k, 0)
     "topk_m64": ("topk", 64, 248320, 64, 0),
+    # dequant-on-gather of T rows from the int8 group-128 table: ("gather", T, V, D, 8)
+    "embed_gather_t2048": ("gather", 2048, 248320, 5120, 8),
 }
 
 
@@ -678,6 +737,16 @@ def run_ncu_case(name):
     mode, M, N, K, bits = NCU_CASES[name]
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
+    if mode == "gather":
+        p = synth.make_problem(1, N, K, seed=5, bits=8, scale_lo=0.001, scale_hi=0.01)
+        packed = q.qpack_w8(p.codes.to(dev), p.scales.to(dev))
+        ids = synth.token_ids(M, N, seed=40 + M).to(dev)
+        for _ in range(4):
+            out = q.embed_gather_w8(ids, packed, N, K)
+        torch.cuda.synchronize()
+        assert q.device_error() == 0
+        print(json.dumps({"ncu_case": name, "T": M, "V": N, "D": K, "absmax": float(out.float().abs().max())}))
+        return
     if mode == "topk":
         lg = synth.logits(M, N, seed=50 + M).to(dev)
         for _ in range(4):
@@ -707,6 +776,94 @@ def run_ncu_case(name):
                       "y_absmax": float(y.float().abs().max())}))
 
 
+def e4m3_of_int(v):
+    """The e4m3 byte of each integer (|v| <= 448 with at most 4 significant bits, which
+    every int4 code and every 16 h, l half of an int8 code satisfies), from the format:
+    sign, 4-bit exponent biased by 7, 3-bit mantissa."""
+    v = np.asarray(v, dtype=np.int64)
+    sign = (v < 0).astype(np.uint8) << 7
+    a = np.abs(v)
+    out = np.zeros(a.shape, np.uint8)
+    nz = a > 0
+    e = np.floor(np.log2(np.maximum(a, 1))).astype(np.int64)
+    m = a * 8 // (1 << e) - 8
+    if not np.all((a[nz] * 8) % (1 << e[nz]) == 0):
+        raise ValueError("value needs more than 4 significant bits")
+    out[nz] = (((e[nz] + 7) << 3) | m[nz]).astype(np.uint8)
+    return out | sign
+
+
+def run_diag(args):
+    """Measurement tools behind the design choices: warp-level MMA rates (8 chains) and
+    latencies (1 chain), tcgen05.mma issue time and completion latency at the GEMM's
+    shapes, and whether int4 x int8 products split into e4m3 terms come out exact on
+    tcgen05 kind::f8f6f4.  One JSON line."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import int8_weight_quantized_int4_gb300 as q
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {"sms": sms, "mma_sync": {}, "tcgen05": {}, "f8f6f4_exact": {}}
+    clocks = Clocks(0)
+    clocks.start()
+    for kind in ("f16", "s8", "e4m3", "s4"):
+        for chains in (8, 1):
+            iters, best, per_iter = 2000, 0.0, 0.0
+            for rep in range(4):
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record()
+                ops, _ = q.diag_mma_peak(kind, 2 * sms if chains == 8 else sms, iters, chains, dev)
+                e.record()
+                torch.cuda.synchronize()
+                ms = s.elapsed_time(e)
+                if rep == 0:
+                    iters = max(200, int(iters * 20.0 / max(ms, 1e-3)))
+                    continue
+                if ops / ms / 1e9 > best:
+                    best, per_iter = ops / ms / 1e9, ms * 1e6 / iters
+            out["mma_sync"][f"{kind}_chains{chains}"] = {"TOPS": round(best, 1), "ns_per_iteration": round(per_iter, 2)}
+    for name, kind, a_tmem, n, issuers, chunks, window in (
+            ("f16_A_tmem_n16_1issuer_wait_each", 0, 1, 16, 1, 64, 1),
+            ("f16_A_tmem_n16_4issuers_no_wait", 0, 1, 16, 4, 256, 0),
+            ("f16_A_smem_n16_1issuer_wait_each", 0, 0, 16, 1, 64, 1),
+            ("f8f6f4_A_tmem_n16_1issuer_wait_each", 1, 1, 16, 1, 64, 1),
+            ("f16_A_tmem_n256_dense", 0, 1, 256, 1, 2048, 0),
+            ("f8f6f4_A_tmem_n256_dense", 1, 1, 256, 1, 2048, 0)):
+        q.diag_tc_probe(kind, a_tmem, n, issuers, chunks, window, sms)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        o = q.diag_tc_probe(kind, a_tmem, n, issuers, chunks, window, sms)
+        e.record()
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e)
+        a = o.cpu().numpy().astype(np.float64)[:, :issuers, :]
+        done = a[..., 3].sum()
+        nmma = 8 if kind == 0 else 4
+        out["tcgen05"][name] = {
+            "issue_ns_per_mma": round(float(a[..., 0].sum() / done / nmma), 1),
+            "wait_ns_per_chunk": round(float(a[..., 1].sum() / done), 1),
+            "ns_per_chunk_per_cta": round(float(a[..., 2].max(axis=1).mean() / (chunks * issuers)), 1),
+            "TFLOPS": round(2.0 * 128 * n * 128 * chunks * issuers * sms / ms / 1e9, 1)}
+    rng = np.random.default_rng(0)
+    for K in (256, 512):
+        qw = rng.integers(-8, 8, (128, K // 2))
+        qa = rng.integers(-127, 128, (16, K // 2))
+        A = np.repeat(qw, 2, axis=1)
+        B = np.stack([16 * (qa >> 4), qa & 15], axis=2).reshape(16, K)
+        ref = qw.astype(np.int64) @ qa.T.astype(np.int64)
+        for a_tmem in (0, 1):
+            d = q.diag_f8f6f4_gemm(torch.from_numpy(e4m3_of_int(A)).to(dev), torch.from_numpy(e4m3_of_int(B)).to(dev),
+                                   bool(a_tmem))
+            torch.cuda.synchronize()
+            out["f8f6f4_exact"][f"K{K}_A_{'tmem' if a_tmem else 'smem'}"] = bool(
+                np.array_equal(d.cpu().numpy().astype(np.float64), ref.astype(np.float64)))
+    out["clocks"] = clocks.stop()
+    out["device_error"] = q.device_error()
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--ncu-case", choices=sorted(NCU_CASES), default=None,
@@ -717,10 +874,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--diag", action="store_true", help="run the MMA microbenchmarks and probes and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.ncu_case:
+    if args.diag:
+        run_diag(args)
+    elif args.ncu_case:
         run_ncu_case(args.ncu_case)
     elif args.impl == "reference":
         run_reference(args)

@@ -201,7 +201,7 @@ int topk_logits(const uint16_t *logits, int M, int N, int k, uint16_t *vals, int
  * item 4: activations quantized to int8 per token, int4 weights).
  *   x [M, K] fp16, device, 16-byte aligned.  Other arguments as qgemm_w4a16;
  *   the workspace is qgemm_workspace_bytes(QW_MODE_W4A8_FUSED, M, N, K).
- * When M <= 8 and the M fp16 rows take at most 96 KB (M*K*2 bytes), one kernel
+ * When M <= 4 and the M fp16 rows take at most 48 KB (M*K*2 bytes), one kernel
  * finds the token scales (every CTA reads the whole rows) and quantizes each
  * activation tile in shared memory, so no int8 activations are written;
  * otherwise the quantizer writes its codes and scales into the workspace and the

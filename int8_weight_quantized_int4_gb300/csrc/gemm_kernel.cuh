@@ -199,8 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   constexpr uint32_t kXChunk = BN * kGroup * 2;          // one fp16 tile (two swizzled halves)
   constexpr uint32_t kXStage = kXBlock * (kXChunk + (kAct8 ? BN * kGroup : 0));
   constexpr uint32_t kXBytes = kXBlock * (kAct8 ? BN * kGroup : kXChunk);   // per copy
+  // MMA issuers, one accumulator each: a tcgen05.mma holds its issuing thread ~73 ns
+  // whatever its N, so a chunk's 8 MMAs take one thread ~0.6 us -- several issuers keep
+  // the weight stream going; TMEM holds issuers x accumulator sets x BN columns plus the
+  // A ring.
   constexpr int kNAcc = BN <= 128 ? 2 : 1;             // accumulator sets (double buffer)
-  constexpr int kIssuers = BN <= 32 ? 4 : BN <= 64 ? 2 : 1;   // one accumulator each
+  constexpr int kIssuers = BN <= 32 ? 4 : BN <= 64 ? 2 : 1;
   static_assert(kIssuers <= kMaxIssuers && (kIssuers & (kIssuers - 1)) == 0, "issuers");
   // W4A8 widening: the two widen warps, plus the two issuer warps left idle when a
   // token tile needs at most two issuers

@@ -151,9 +151,9 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
   const uint32_t wbase = sbase + (uint32_t)SX * kXStage;
   const uint32_t rbase = wbase + (uint32_t)SW * kWStage;
   float *red = reinterpret_cast<float *>(gbase + (rbase - sbase));
-  // in-kernel quantizer: per-warp amax [8 warps][8 tokens], scales [8], reciprocals [8]
+  // in-kernel quantizer: per-warp amax [8 warps][16 tokens], scales [16], reciprocals [16]
   float *qamax = red + P.ms_red_bytes / 4;
-  float *qsc = qamax + 64, *qrc = qsc + 8;
+  float *qsc = qamax + 128, *qrc = qsc + 16;
   const uint32_t bars = rbase + (uint32_t)P.ms_red_bytes + (uint32_t)kMsQuantFloats * 4;
   uint8_t *gbars = gbase + (bars - sbase);
   auto wfull_bar = [&](int s) { return bars + 8u * s; };
@@ -200,28 +200,37 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
     // of every row, then thread m combines the shares of row m
     if (warp >= kMsWarpC0) {
       const int cw = warp - kMsWarpC0, nv = P.K / 8;
+      constexpr int kBatch = 8;                     // loads in flight per thread
       for (int m = 0; m < P.M; ++m) {
         const uint4 *xr = reinterpret_cast<const uint4 *>(a.xf16 + (size_t)m * P.K);
         float amax = 0.0f;
-        for (int v = cw * 32 + lane; v < nv; v += kMsComputeWarps * 32) {
-          const uint4 w = __ldg(xr + v);
-          const __half2 *h = reinterpret_cast<const __half2 *>(&w);
+        for (int v0 = cw * 32 + lane; v0 < nv; v0 += kBatch * kMsComputeWarps * 32) {
+          uint4 w[kBatch];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(h[e]);
-            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+          for (int b = 0; b < kBatch; ++b) {
+            const int v = v0 + b * kMsComputeWarps * 32;
+            w[b] = v < nv ? __ldg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            const __half2 *h = reinterpret_cast<const __half2 *>(&w[b]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __half22float2(h[e]);
+              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
           }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if (lane == 0) qamax[cw * 8 + m] = amax;
+        if (lane == 0) qamax[cw * 16 + m] = amax;
       }
       named_bar_sync(2, kMsComputeWarps * 32);
       const int ct = threadIdx.x - kMsWarpC0 * 32;
       if (ct < P.M) {
         float amax = qamax[ct];
 #pragma unroll
-        for (int w = 1; w < kMsComputeWarps; ++w) amax = fmaxf(amax, qamax[w * 8 + ct]);
+        for (int w = 1; w < kMsComputeWarps; ++w) amax = fmaxf(amax, qamax[w * 16 + ct]);
         const float sc = amax == 0.0f ? 0.0f : __fdiv_rn(amax, 127.0f);
         qsc[ct] = sc;
         qrc[ct] = sc == 0.0f ? 0.0f : __frcp_rn(sc);
@@ -339,9 +348,10 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
               widen_chunk<BNX, kCThreads>(xb + j * kXChunk, xb + kXBlock * kXChunk + j * (BNX * kGroup), ct,
                                           P.M < BNX ? P.M : BNX);
             } else {
-              // unit: four values 4 c .. 4 c + 3 of row r of group j (M <= 8, so one pass)
-              const int r = ct >> 5, c = ct & 31;
-              if (r < P.M) {
+              // unit: four values 4 c .. 4 c + 3 of row r of group j
+              for (int un = ct; un < P.M * 32; un += kCThreads) {
+              const int r = un >> 5, c = un & 31;
+              {
                 uint8_t *q = xb + j * kXChunk + (c >> 4) * (BNX * 128) + r * 128 +
                              ((((c >> 1) & 7) ^ (r & 7)) << 4) + ((c & 1) << 3);
                 const uint2 v = *reinterpret_cast<const uint2 *>(q);
@@ -358,6 +368,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
                   o[e] = h2_as_u32(__halves2half2(__int2half_rn(q0), __int2half_rn(q1)));
                 }
                 *reinterpret_cast<uint2 *>(q) = make_uint2(o[0], o[1]);
+              }
               }
             }
           }

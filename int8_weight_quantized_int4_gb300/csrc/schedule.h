@@ -155,12 +155,13 @@ QW_HD int chunk_bytes(int mode) { return mode == 2 ? kChunkW8 : kChunkW4; }
 // fp16 rows fit in shared memory next to the pipeline (at most kFusedRowsMax bytes,
 // token tiles of 16); otherwise it runs the standalone quantizer into the workspace
 // and then the mode-1 GEMM.
-// Mode 3 quantizes inside the decode-batch kernel for up to eight tokens whose fp16 rows
-// take at most kFusedRowsMax bytes (every CTA reads them all to find the token scales);
+// Mode 3 quantizes inside the decode-batch kernel for up to 4 tokens whose fp16 rows
+// take at most kFusedRowsMax bytes (every CTA reads them all from L2 to find the token
+// scales, which costs more than a separate quantizer launch for larger batches);
 // otherwise it runs the standalone quantizer into the workspace and then the mode-1 GEMM.
-constexpr int kFusedRowsMax = 96 * 1024;
+constexpr int kFusedRowsMax = 48 * 1024;
 QW_HD bool quant_in_kernel(int mode, int M, int K) {
-  return mode == 3 && M >= 1 && M <= 8 && (long long)M * K * 2 <= kFusedRowsMax;
+  return mode == 3 && M >= 1 && M <= 4 && (long long)M * K * 2 <= kFusedRowsMax;
 }
 
 // W4A8 widens int8 activation codes to fp16 inside the GEMM (through a staging
@@ -210,9 +211,9 @@ QW_HD int ms_red_bytes(int M, int teams) { return (teams - 1) * ms_rows(M) * kMs
 QW_HD int ms_xstage_bytes(int mode, int M) {
   return 4 * ms_rows(M) * kGroup * (mode == 1 ? 3 : 2);
 }
-// shared-memory floats of the in-kernel quantizer: per-warp amax [8][8], scales [8] and
-// reciprocals [8]
-constexpr int kMsQuantFloats = 8 * 8 + 8 + 8;
+// shared-memory floats of the in-kernel quantizer: per-warp amax [8][16], scales [16] and
+// reciprocals [16]
+constexpr int kMsQuantFloats = 8 * 16 + 16 + 16;
 // ring depths: three activation blocks when that leaves eight weight slots, else two;
 // the weight slots (at most kMaxWStages) split evenly between the teams
 QW_HD bool ms_ring_depths(int mode, int M, int teams, int &xst, int &wst) {

@@ -321,7 +321,7 @@ def test_signed_scales_sign_fold_equivalence(q):
                                    (17, 640, 640), (64, 640, 1024)])
 def test_w4a8_fused_bit_identical_to_two_step(q, M, N, K):
     """qgemm_w4a8_fused(x) equals qgemm_w4a8(quant_act_int8(x)) bit for bit -- inside
-    one kernel (M <= 8 and M*K*2 <= 96 KB) and through the quantizer-then-GEMM
+    one kernel (M <= 4 and M*K*2 <= 48 KB) and through the quantizer-then-GEMM
     path -- and meets the tolerance against the oracle."""
     p = synth.make_problem(M, N, K, seed=11 + M, outlier_frac=0.01)
     x = _special_rows(p.x) if M >= 4 else p.x
@@ -333,7 +333,7 @@ def test_w4a8_fused_bit_identical_to_two_step(q, M, N, K):
     torch.cuda.synchronize()
     assert q.device_error() == 0
     pl = q.plan(q.MODE_W4A8_FUSED, M, N, K, torch.cuda.get_device_properties(DEV).multi_processor_count)
-    assert pl.fused == (1 if (M <= 8 and M * K * 2 <= 96 * 1024) else 0)
+    assert pl.fused == (1 if (M <= 4 and M * K * 2 <= 48 * 1024) else 0)
     assert np.array_equal(bits(y1), bits(y2))
     oq, os_ = oracle.quant_act_int8(x.numpy())
     assert nerr(y1, oracle.w4a8(oq, os_, p.codes, p.scales)) <= TOL
