@@ -250,10 +250,19 @@ int qgemm_w4a16_noalloc(const uint16_t *x, const void *packed_w4, int M, int N, 
  *   then streams and dequantizes its weights before that kernel completes, so
  *   consecutive layers overlap.  Leave it 0 when a weight-writing kernel (e.g.
  *   qpack_*) may directly precede a GEMM on the same stream.
+ *
+ *   QW_OPT_WAIT_LIMIT_US (default 4000000, i.e. 4 s; 0 .. 4000000).  The time
+ *   limit, in microseconds, of every wait inside a GEMM kernel (a pipeline stage
+ *   waiting for another).  A wait that runs past it ends the kernel early with
+ *   QW_ERR_TIMEOUT in the device error word (qw_device_error) and an undefined
+ *   y; the workspace must then be zero-filled again.  A test hook: lowering it
+ *   (0 makes every wait that is not already satisfied when first checked give
+ *   up) drives an unmodified kernel through that path.  Leave it at the default
+ *   otherwise.
  *   qw_set_option returns QW_OK or QW_ERR_INVALID_ARG; qw_get_option returns the
  *   value or QW_ERR_INVALID_ARG.
  * ------------------------------------------------------------------------ */
-enum { QW_OPT_WEIGHTS_IMMUTABLE = 1 };
+enum { QW_OPT_WEIGHTS_IMMUTABLE = 1, QW_OPT_WAIT_LIMIT_US = 2 };
 int qw_set_option(int option, int value);
 int qw_get_option(int option);
 

@@ -216,6 +216,11 @@ class Workspace:
             self.buf = torch.zeros(need, dtype=torch.uint8, device=self.device)
         return self.buf, self.buf.numel()
 
+    def zero(self):
+        """Zero-fill the buffer again (needed after a call that ended in QW_ERR_TIMEOUT)."""
+        if self.buf is not None:
+            self.buf.zero_()
+
 
 _default_ws = {}
 
@@ -373,6 +378,17 @@ def set_weights_immutable(flag: bool = True):
     precedes a GEMM on its stream, letting each GEMM stream its weights while the
     preceding kernel finishes (see include/qgemm.h)."""
     _check(lib().qw_set_option(QW_OPT_WEIGHTS_IMMUTABLE, 1 if flag else 0))
+
+
+QW_OPT_WAIT_LIMIT_US = 2
+DEFAULT_WAIT_LIMIT_US = 4_000_000
+
+
+def set_wait_limit_us(us: int | None = None):
+    """Test hook: the time limit of every wait inside the GEMM kernels launched from now
+    on, in microseconds (None restores the 4 s default).  A kernel whose wait runs past
+    it ends early with QW_ERR_TIMEOUT in the device error word."""
+    _check(lib().qw_set_option(QW_OPT_WAIT_LIMIT_US, DEFAULT_WAIT_LIMIT_US if us is None else int(us)))
 
 
 def num_kernel_launches() -> int:

@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 #include "qgemm.h"
 #include "launch.h"
+#include "ptx.cuh"
 #include "schedule.h"
 
 // Per-device error word written by the kernels (pipeline timeouts, bad codes).
@@ -21,6 +22,10 @@ namespace {
 thread_local char tl_err[512];
 std::atomic<long long> g_launches{0};
 std::atomic<int> g_opt_weights_immutable{0};
+// QW_OPT_WAIT_LIMIT_US: the kernels' default limit unless a test lowers it
+constexpr int kDefaultWaitLimitUs = 4000000;
+static_assert(1000ull * kDefaultWaitLimitUs == qw::kWaitLimitNs, "default wait limit");
+std::atomic<int> g_opt_wait_limit_us{kDefaultWaitLimitUs};
 
 int fail(int code, const char *fmt, ...) {
   va_list ap;
@@ -166,6 +171,7 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
   a.partials = P.ws_partials ? reinterpret_cast<float *>(w + P.ws_counters) : nullptr;
   a.err = d->err;
   a.early_weights = g_opt_weights_immutable.load(std::memory_order_relaxed);
+  a.wait_ns = 1000ull * (unsigned long long)g_opt_wait_limit_us.load(std::memory_order_relaxed);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (mode == QW_MODE_W4A8_FUSED && P.fused) {
@@ -411,15 +417,21 @@ int qw_device_error(qw_stream_t stream) {
 long long qw_num_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int qw_set_option(int option, int value) {
-  if (option != QW_OPT_WEIGHTS_IMMUTABLE || (value != 0 && value != 1))
-    return fail(QW_ERR_INVALID_ARG, "unknown option %d or value %d", option, value);
-  g_opt_weights_immutable.store(value, std::memory_order_relaxed);
-  return QW_OK;
+  if (option == QW_OPT_WEIGHTS_IMMUTABLE && (value == 0 || value == 1)) {
+    g_opt_weights_immutable.store(value, std::memory_order_relaxed);
+    return QW_OK;
+  }
+  if (option == QW_OPT_WAIT_LIMIT_US && value >= 0 && value <= kDefaultWaitLimitUs) {
+    g_opt_wait_limit_us.store(value, std::memory_order_relaxed);
+    return QW_OK;
+  }
+  return fail(QW_ERR_INVALID_ARG, "unknown option %d or value %d", option, value);
 }
 
 int qw_get_option(int option) {
-  if (option != QW_OPT_WEIGHTS_IMMUTABLE) return fail(QW_ERR_INVALID_ARG, "unknown option %d", option);
-  return g_opt_weights_immutable.load(std::memory_order_relaxed);
+  if (option == QW_OPT_WEIGHTS_IMMUTABLE) return g_opt_weights_immutable.load(std::memory_order_relaxed);
+  if (option == QW_OPT_WAIT_LIMIT_US) return g_opt_wait_limit_us.load(std::memory_order_relaxed);
+  return fail(QW_ERR_INVALID_ARG, "unknown option %d", option);
 }
 
 int qw_plan(int mode, int M, int N, int K, int num_sms, qw_plan_t *out) {

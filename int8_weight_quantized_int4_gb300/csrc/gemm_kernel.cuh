@@ -63,16 +63,11 @@ constexpr int kBarAEmpty = kBarAFull + 8 * kMaxAStages;
 constexpr int kBarAccFull = kBarAEmpty + 8 * kMaxAStages;
 constexpr int kBarAccEmpty = kBarAccFull + 8 * 2;
 constexpr int kBarRed = kBarAccEmpty + 8 * 2;        // stream-K reduction loads
-constexpr int kBarRows = kBarRed + 8;                // fused W4A8: fp16 rows landed
-constexpr int kBarScales = kBarRows + 8;             // fused W4A8: token scales ready
-constexpr int kTmemSlot = kBarScales + 8;
-constexpr int kAbortSlot = kTmemSlot + 4;
-constexpr int kBcastSlot = kAbortSlot + 4;
-constexpr int kMaxFusedRows = 16;                    // fused W4A8: token rows (one tile of 16)
-constexpr int kScaleSlot = kBcastSlot + 4;           // binary32 [kMaxFusedRows] token scales
-constexpr int kRcpSlot = kScaleSlot + 4 * kMaxFusedRows;    // binary32 [kMaxFusedRows] 1 / scale
-constexpr int kAmaxSlot = kRcpSlot + 4 * kMaxFusedRows;     // binary32 [4 warps][kMaxFusedRows]
-static_assert(kAmaxSlot + 4 * 4 * kMaxFusedRows <= kSmemReserve - 1024, "barrier block too large");
+constexpr int kBarDrain = kBarRed + 8;               // the issuers' last MMAs completed
+constexpr int kWaitSlot = kBarDrain + 8;             // WaitBlock (abort flag, limit, error word)
+constexpr int kTmemSlot = kWaitSlot + (int)sizeof(WaitBlock);
+constexpr int kBcastSlot = kTmemSlot + 4;
+static_assert(kWaitSlot % 8 == 0 && kBcastSlot + 4 <= kSmemReserve - 1024, "barrier block too large");
 
 // ---- dequantization: packed codes -> 32 half2 (64 fp16 values q*s) per thread ----
 
@@ -144,7 +139,7 @@ __device__ __forceinline__ void widen_chunk(uint8_t *btile, const uint8_t *stg, 
 }
 
 // q = clamp(rne(x / s), -127, 127) with x / s the IEEE binary32 quotient, as the
-// standalone quantizer computes it, but without a divide per value: t = x * (1/s)
+// standalone quantizer computes it (used by the decode kernel's in-kernel quantizer), but without a divide per value: t = x * (1/s)
 // (correctly rounded reciprocal and product) is within 3 * 2^-24 * |x/s| <= 2.3e-5 of
 // the quotient, since |x/s| <= 127 (1 + 2^-24).  So rne(t) = rne(x / s) unless t lies
 // within 2^-14 of a half-integer; only those values take the IEEE divide, out of line
@@ -158,43 +153,12 @@ __device__ __forceinline__ int quant_code(float x, float s, float rs) {
   return max(-127, min(127, (int)qf));
 }
 
-// Fused W4A8: quantize rows [0, rows) of one K group from the shared-memory copy of
-// the fp16 activations (row stride K) into the 128-byte-swizzled fp16 tile of the
-// chunk, with the standalone quantizer's arithmetic (quant_code), q = 0 when s = 0;
-// the code is exact in fp16.  rc holds the rows' reciprocal scales.  Work unit: 4
-// consecutive values (8 bytes) of one row.
-template <int BN, int NT>
-__device__ __forceinline__ void quantize_chunk(uint8_t *btile, const uint8_t *rows_smem, int K, int g,
-                                               const float *sc, const float *rc, int t, int rows) {
-  for (int un = t; un < rows * 32; un += NT) {
-    const int r = un >> 5, c = un & 31;             // values k = 4c .. 4c + 3 of group g
-    const uint2 v = *reinterpret_cast<const uint2 *>(rows_smem + ((size_t)r * K + g * kGroup + c * 4) * 2);
-    const float s = sc[r], rs = rc[r];
-    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
-    uint32_t o[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float2 f = __half22float2(h[e]);
-      int q0 = 0, q1 = 0;
-      if (s != 0.0f) {
-        q0 = quant_code(f.x, s, rs);
-        q1 = quant_code(f.y, s, rs);
-      }
-      o[e] = h2_as_u32(__halves2half2(__int2half_rn(q0), __int2half_rn(q1)));
-    }
-    const int kc = c >> 4, cc = (c >> 1) & 7;        // 64-wide half, 16-byte piece in it
-    uint8_t *dst = btile + kc * BN * 128 + r * 128 + ((cc ^ (r & 7)) << 4) + ((c & 1) << 3);
-    *reinterpret_cast<uint2 *>(dst) = make_uint2(o[0], o[1]);
-  }
-}
-
-template <int BN, int WBITS, bool TOKSCALE, bool QIN>
+template <int BN, int WBITS, bool TOKSCALE>
 __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_constant__ GemmArgs a) {
   constexpr uint32_t kChunk = WBITS == 8 ? kChunkW8 : kChunkW4;
   constexpr uint32_t kWStage = (kChunk + 127) / 128 * 128;
   static_assert(kChunk % 128 == 0, "weight slots stay 128-byte aligned");
-  constexpr bool kAct8 = TOKSCALE && BN <= kAct8InKernelMaxBn && !QIN;
-  static_assert(!QIN || (TOKSCALE && BN == 16 && WBITS == 4), "fused quantizer: W4A8, tiles of 16");
+  constexpr bool kAct8 = TOKSCALE && BN <= kAct8InKernelMaxBn;
   constexpr int kXBlock = act_block(BN);                 // chunks per activation copy
   constexpr uint32_t kXChunk = BN * kGroup * 2;          // one fp16 tile (two swizzled halves)
   constexpr uint32_t kXStage = kXBlock * (kXChunk + (kAct8 ? BN * kGroup : 0));
@@ -238,14 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   // activation ring first (1024-byte aligned slots for the swizzle), then weights
   const uint32_t wbase = sbase + (uint32_t)SX * kXStage;
   const uint32_t ring_bytes = (uint32_t)SX * kXStage + (uint32_t)SW * kWStage;
-  const uint32_t rbase = sbase + ring_bytes;                 // fused: fp16 rows
-  uint8_t *grows = gbase + ring_bytes;
-  const uint32_t bars = rbase + (uint32_t)P.rows_bytes;
-  uint8_t *gbars = grows + P.rows_bytes;
-  float *sxs = reinterpret_cast<float *>(gbars + kScaleSlot);    // fused: token scales
-  float *sxr = reinterpret_cast<float *>(gbars + kRcpSlot);      // fused: their reciprocals
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(gbars + kAbortSlot);
+  const uint32_t bars = sbase + ring_bytes;
+  uint8_t *gbars = gbase + ring_bytes;
+  volatile WaitBlock *wctl = reinterpret_cast<volatile WaitBlock *>(gbars + kWaitSlot);
   volatile int *bcast = reinterpret_cast<volatile int *>(gbars + kBcastSlot);
+  // a pipeline wait: bounded by the launch's limit, gives up once the CTA aborts
+  auto pwait = [&](uint32_t bar, uint32_t parity) { return mbar_wait(bar, parity, wctl, a.wait_ns == 0); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -280,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     if (l < SX) {
       mbar_init(xfull_bar(l), 1);
       mbar_init(xempty_bar(l), kIssuers);
-      mbar_init(bfull_bar(l), QIN ? 1 : kWidenW);
+      mbar_init(bfull_bar(l), kWidenW);
     }
     fence_mbar_init();
   } else if (threadIdx.x >= 96 && threadIdx.x < 128) {
@@ -294,15 +256,14 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       mbar_init(accempty_bar(l), kEpiWarps);
     }
     if (l == 2) mbar_init(bars + kBarRed, 1);
-    if (l == 3) mbar_init(bars + kBarRows, 1);
-    if (l == 4) mbar_init(bars + kBarScales, 1);
+    if (l == 3) mbar_init(bars + kBarDrain, kIssuers);
     if (l == 5) {
-      *abort_flag = 0;
+      wait_block_init(wctl, a.wait_ns, a.err);
       *bcast = 0;
     }
     fence_mbar_init();
   }
-  if (!QIN && warp == kWarpAct && lane == 0) prefetch_tensormap(&a.tmap);
+  if (warp == kWarpAct && lane == 0) prefetch_tensormap(&a.tmap);
   if (warp == 0) {
     tmem_alloc(bars + kTmemSlot, kTmemCols);
     tmem_relinquish();
@@ -326,31 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   if (!early) griddep_wait();
   griddep_launch_dependents();
 
-  // Fused W4A8: the activation blocks that fit in the (initially empty) activation
-  // ring are quantized by the epilogue and widen warps together (kQuantThreads
-  // threads, thread index qt), each released to the MMA warps as soon as it is
-  // written; the rest by the widen warps alone as slots free up.
-  constexpr int kQuantThreads = (kEpiWarps + kWidenWarps) * 32;
-  auto quantize_initial_blocks = [&](int qt) {
-    Seg qs;
-    int bi = 0;
-    for (int i = 0; segment(P, cta, i, qs); ++i)
-      for (int g = qs.g0; g < qs.g1 && bi < SX; g += kXBlock, ++bi) {
-        const int nb = qs.g1 - g < kXBlock ? qs.g1 - g : kXBlock;
-        uint8_t *xs = gbase + (size_t)bi * kXStage;
-        for (int j = 0; j < nb; ++j)
-          quantize_chunk<BN, kQuantThreads>(xs + j * kXChunk, grows, P.K, g + j, sxs, sxr, qt, P.M);
-        fence_proxy_async_smem();
-        named_bar_sync(2, kQuantThreads);
-        if (qt == kQuantThreads - kWidenWarps * 32) mbar_arrive(bfull_bar(bi));
-      }
-  };
-
   if (warp == kWarpTma) {
     // ------------------------------------------------------ weight copies --
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int s[2] = {0, 0}, cidx = 0;
+      int s[2] = {0, 0}, nfill[2] = {0, 0}, cidx = 0;
       uint32_t ph[2] = {0, 0};
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
@@ -359,35 +300,34 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         const uint8_t *src = a.wpack + ((size_t)t * P.G + sg.g0) * kChunk;
         for (int g = sg.g0; g < sg.g1; ++g, ++cidx, src += kChunk) {
           const int p = cidx & 1, slot = p * SWH + s[p];
-          if (!mbar_wait(wempty_bar(slot), ph[p] ^ 1u, abort_flag, a.err)) { ok = false; break; }
+          if (!pwait(wempty_bar(slot), ph[p] ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(wfull_bar(slot), kChunk);
           bulk_g2s(w_smem(slot), src, kChunk, wfull_bar(slot), pol);
+          ++nfill[p];
           if (++s[p] == SWH) { s[p] = 0; ph[p] ^= 1u; }
         }
       }
+      // the last fill of every slot has landed before the CTA may exit
+      for (int p = 0; p < 2; ++p)
+        for (int j = 0; j < SWH && j < nfill[p]; ++j)
+          mbar_drain(wfull_bar(p * SWH + j), j < s[p] ? ph[p] : ph[p] ^ 1u, wctl);
     }
   } else if (warp == kWarpAct) {
     // -------------------------------------------------- activation copies --
     // one tensor copy per block of up to kXBlock consecutive groups of a segment;
     // a block that runs past the segment (or past K) brings data nobody reads
-    if (lane == 0 && QIN) {
-      // fused W4A8: one bulk copy per fp16 row (the quantizer needs whole rows)
+    if (lane == 0) {
       if (early) griddep_wait();
-      const uint32_t row_bytes = (uint32_t)P.K * 2;
-      mbar_arrive_expect_tx(bars + kBarRows, row_bytes * (uint32_t)P.M);
-      for (int m = 0; m < P.M; ++m)
-        bulk_g2s_nohint(rbase + (uint32_t)m * row_bytes, a.xf16 + (size_t)m * P.K, row_bytes, bars + kBarRows);
-    } else if (lane == 0) {
-      if (early) griddep_wait();
-      int s = 0;
+      int s = 0, nfill = 0;
       uint32_t ph = 0;
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         int u, t;
         tile_coords(P, sg.tile, u, t);
         for (int g = sg.g0; g < sg.g1; g += kXBlock) {
-          if (!mbar_wait(xempty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
+          if (!pwait(xempty_bar(s), ph ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(xfull_bar(s), kXBytes);
+          ++nfill;
           if constexpr (kAct8) {
             // int8 codes: a 128 x BN x kXBlock box into the staging tiles (unswizzled)
             tma_load_3d(x_smem(s) + kXBlock * kXChunk, &a.tmap, 0, u * BN, g, xfull_bar(s));
@@ -399,32 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
           if (++s == SX) { s = 0; ph ^= 1u; }
         }
       }
+      for (int j = 0; j < SX && j < nfill; ++j) mbar_drain(xfull_bar(j), j < s ? ph : ph ^ 1u, wctl);
     }
   } else if ((warp >= kWarpWiden0 && warp < kWarpWiden0 + kWidenWarps) ||
              (kWidenW > kWidenWarps && warp >= kWarpMma0 + 2)) {
     // ------------------------------------------ W4A8 int8 -> fp16 widening --
-    if constexpr (QIN) {
-      // fused W4A8: these warps produce the activation ring from the row copy, once
-      // the epilogue warps have computed the token scales
-      const int wt = threadIdx.x - kWarpWiden0 * 32;   // 0..63
-      bool ok = mbar_wait(bars + kBarScales, 0, abort_flag, a.err);
-      quantize_initial_blocks(kEpiWarps * 32 + wt);
-      int bi = 0;
-      for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
-        for (int g = sg.g0; g < sg.g1; g += kXBlock, ++bi) {
-          const int s = bi % SX;
-          if (bi < SX) continue;                         // quantized and released above
-          if (!mbar_wait(xempty_bar(s), ((uint32_t)(bi / SX) & 1u) ^ 1u, abort_flag, a.err)) { ok = false; break; }
-          const int nb = sg.g1 - g < kXBlock ? sg.g1 - g : kXBlock;
-          uint8_t *xs = gbase + (size_t)s * kXStage;
-          for (int j = 0; j < nb; ++j)
-            quantize_chunk<BN, kWidenWarps * 32>(xs + j * kXChunk, grows, P.K, g + j, sxs, sxr, wt, P.M);
-          fence_proxy_async_smem();
-          named_bar_sync(3, kWidenWarps * 32);
-          if (wt == 0) mbar_arrive(bfull_bar(s));
-        }
-      }
-    } else if constexpr (kAct8) {
+    if constexpr (kAct8) {
       const int wt = warp < kWarpTma ? threadIdx.x - kWarpWiden0 * 32                 // 0..63
                                      : kWidenWarps * 32 + threadIdx.x - (kWarpMma0 + 2) * 32;
       const int rows = P.M < BN ? P.M : BN;            // a single token tile when widening here
@@ -433,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         for (int g = sg.g0; g < sg.g1; g += kXBlock) {
-          if (!mbar_wait(xfull_bar(s), ph, abort_flag, a.err)) { ok = false; break; }
+          // the lanes leave together (their waits may end differently after an abort)
+          if (!__all_sync(0xffffffffu, pwait(xfull_bar(s), ph))) { ok = false; break; }
           const int nb = sg.g1 - g < kXBlock ? sg.g1 - g : kXBlock;
           uint8_t *xs = gbase + (size_t)s * kXStage;
           for (int j = 0; j < nb; ++j)
@@ -461,8 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       for (int g = sg.g0; g < sg.g1; ++g, ++cidx) {
         if ((cidx & 1) == grp) {
           const int slot = grp * SWH + s, aslot = grp * kAHalf + ai;
-          if (!mbar_wait(aempty_bar(aslot), aph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-          if (!mbar_wait(wfull_bar(slot), ph, abort_flag, a.err)) { ok = false; break; }
+          // the lanes leave together: the TMEM stores below are warp-collective
+          bool got = pwait(aempty_bar(aslot), aph ^ 1u);
+          got = got && pwait(wfull_bar(slot), ph);
+          if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
           const uint8_t *wc = gbase + (size_t)SX * kXStage + (size_t)slot * kWStage;
           const uint32_t tcol = tmem + lane_base + (uint32_t)(aslot * 64);
           uint32_t o[2][32];
@@ -514,20 +437,20 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         const int b = i % kNAcc;
-        if (!mbar_wait(accempty_bar(b), ((i / kNAcc) & 1) ^ 1, abort_flag, a.err)) { ok = false; break; }
+        if (!pwait(accempty_bar(b), ((i / kNAcc) & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(kAccCol0 + (b * kIssuers + q) * BN);
         bool first = true, xready = false, used = false;
         int j = 0;                                     // chunk within the activation block
         for (int g = sg.g0; g < sg.g1; ++g, ++cidx) {
           if (!xready) {
-            if (!mbar_wait((kAct8 || QIN) ? bfull_bar(xs) : xfull_bar(xs), xph, abort_flag, a.err)) { ok = false; break; }
+            if (!pwait(kAct8 ? bfull_bar(xs) : xfull_bar(xs), xph)) { ok = false; break; }
             xready = true;
           }
           if ((cidx & (kIssuers - 1)) == q) {
             const int h = cidx >> 1;                   // position in the parity's half
             const int aslot = (cidx & 1) * kAHalf + h % kAHalf;
-            if (!mbar_wait(afull_bar(aslot), (uint32_t)(h / kAHalf) & 1u, abort_flag, a.err)) { ok = false; break; }
+            if (!pwait(afull_bar(aslot), (uint32_t)(h / kAHalf) & 1u)) { ok = false; break; }
             tc_fence_after();
             // descriptor start addresses advance by (offset >> 4); no carry out of the
             // 14-bit field since shared-memory addresses stay below 256 KB
@@ -552,6 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         }
         if (ok) mma_commit(accfull_bar(b));
       }
+      // every MMA this thread issued has completed before the CTA may exit
+      mma_commit(bars + kBarDrain);
+      mbar_drain(bars + kBarDrain, 0, wctl);
     }
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
     // -------------------------------------------------------- epilogue --
@@ -561,42 +487,6 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     const int ept = threadIdx.x - kWarpEpi0 * 32;   // 0..127
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     int cidx = 0;                                   // CTA-wide index of the segment's first chunk
-    if constexpr (QIN) {
-      // fused W4A8: token scales from the row copy, as the standalone quantizer:
-      // amax = max |x| (binary32, exact), s = amax / 127 (IEEE divide), 0 for a zero row
-      float *scratch = reinterpret_cast<float *>(gbars + kAmaxSlot);
-      if (mbar_wait(bars + kBarRows, 0, abort_flag, a.err)) {
-        const int nv = P.K / 8;
-        for (int m = 0; m < P.M; ++m) {
-          const uint4 *xr = reinterpret_cast<const uint4 *>(grows + (size_t)m * P.K * 2);
-          float amax = 0.0f;
-          for (int v = ept; v < nv; v += kEpiWarps * 32) {
-            const uint4 w = xr[v];
-            const __half2 *h = reinterpret_cast<const __half2 *>(&w);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __half22float2(h[e]);
-              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-            }
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-          if (lane == 0) scratch[(warp - kWarpEpi0) * kMaxFusedRows + m] = amax;
-        }
-      }
-      named_bar_sync(1, kEpiWarps * 32);
-      if (ept < P.M) {
-        float amax = scratch[ept];
-#pragma unroll
-        for (int w = 1; w < kEpiWarps; ++w) amax = fmaxf(amax, scratch[w * kMaxFusedRows + ept]);
-        const float sc = amax == 0.0f ? 0.0f : __fdiv_rn(amax, 127.0f);
-        sxs[ept] = sc;
-        sxr[ept] = sc == 0.0f ? 0.0f : __frcp_rn(sc);
-      }
-      named_bar_sync(1, kEpiWarps * 32);
-      if (ept == 0) mbar_arrive(bars + kBarScales);
-      quantize_initial_blocks(ept);
-    }
     int npend = 0, pend_tile[2] = {0, 0};           // cut tiles this CTA must reduce (<= 2)
     int pend_cut[2] = {0, 0};
     // contributors of this CTA's first and last segment (read now, while the
@@ -611,15 +501,15 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 #pragma unroll
       for (int q = 0; q < kIssuers; ++q) valid[q] = nch >= kIssuers || ((q - cidx) & (kIssuers - 1)) < nch;
       cidx += nch;
-      if constexpr (TOKSCALE && !QIN) {
+      if constexpr (TOKSCALE) {
         // token scales of this tile into L1 while the accumulator is being produced
         int u_, t_;
         tile_coords(P, sg.tile, u_, t_);
         for (int m = u_ * BN + row; m < P.M && m < (u_ + 1) * BN; m += kRows) prefetch_l1(a.xs + m);
       }
-      mbar_wait(accfull_bar(b), (i / kNAcc) & 1, abort_flag, a.err);
-      named_bar_sync(1, kEpiWarps * 32);           // all four warps decide together
-      if (*abort_flag) { aborted = true; break; }
+      const bool got = pwait(accfull_bar(b), (i / kNAcc) & 1);
+      // all four warps decide together, on the OR of their views
+      if (named_bar_or(1, kEpiWarps * 32, !got || wctl->abort)) { aborted = true; break; }
       tc_fence_after();
       int u, t;
       tile_coords(P, sg.tile, u, t);
@@ -639,17 +529,14 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
           else tmem_ld8(tacc + (uint32_t)(q * BN + cc), v[q]);
         }
         // Wide tiles (one issuer, 32 columns per TMEM load; the epilogue holds up the
-        // next tile's MMAs there) load the token scales of the 32 columns before using
-        // any, so that their latencies overlap; narrow tiles read them as they go
-        // (measured faster for those).
-        constexpr bool kBatchScales = TOKSCALE && !QIN && BN >= 128;
-        float tsc[W];
-#pragma unroll
-        for (int j = 0; j < W; ++j) {
-          tsc[j] = 1.0f;
-          if constexpr (kBatchScales)
-            if (!part && cc + j < mv) tsc[j] = __ldg(a.xs + m0 + cc + j);
-        }
+        // next tile's MMAs there) load the 32 columns' token scales before using any,
+        // one per lane, and pass column j's along from lane j; narrow tiles read them
+        // as they go (measured faster for those).
+        constexpr bool kBatchScales = TOKSCALE && BN >= 128;
+        static_assert(!kBatchScales || W == 32, "one token scale per lane");
+        float tsc = 1.0f;
+        if constexpr (kBatchScales)
+          if (!part && cc + lane < mv) tsc = __ldg(a.xs + m0 + cc + lane);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < W; ++j) {
@@ -657,12 +544,13 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 #pragma unroll
           for (int q = 0; q < kIssuers; ++q)
             if (valid[q]) acc += __uint_as_float(v[q][j]);
+          const float sj = kBatchScales ? __shfl_sync(0xffffffffu, tsc, j & 31) : 1.0f;
           if (cc + j < mv) {
             if (part) {
               part[(cc + j) * kRows + row] = acc;
             } else {
               const int m = m0 + cc + j;
-              const float val = QIN ? acc * sxs[m] : kBatchScales ? acc * tsc[j] : TOKSCALE ? acc * __ldg(a.xs + m) : acc;
+              const float val = kBatchScales ? acc * sj : TOKSCALE ? acc * __ldg(a.xs + m) : acc;
               a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
             }
           }
@@ -709,10 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       const int mv = P.M - m0 < BN ? P.M - m0 : BN;
       const int nseg = pl - pf + 1;
       auto put = [&](int m, float acc) {
-        const float val = QIN ? acc * sxs[m] : TOKSCALE ? acc * __ldg(a.xs + m) : acc;
+        const float val = TOKSCALE ? acc * __ldg(a.xs + m) : acc;
         a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
       };
-      if constexpr (TOKSCALE && !QIN)  // warm L1 with this tile's token scales
+      if constexpr (TOKSCALE)  // warm L1 with this tile's token scales
         for (int m = m0 + row; m < m0 + mv; m += kRows) prefetch_l1(a.xs + m);
       if (mv <= 4) {
         // the atomic's acquire (thread 0) and the named barrier order these reads
@@ -752,7 +640,12 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
                             a.partials + (size_t)(p == pf ? pf_slot : 2 * p) * (BN * kRows) + (size_t)j0 * kRows,
                             bytes, bars + kBarRed);
         }
-        if (!mbar_wait(bars + kBarRed, red_phase, abort_flag, a.err)) { aborted = true; break; }
+        const bool got = pwait(bars + kBarRed, red_phase);
+        if (named_bar_or(1, kEpiWarps * 32, !got)) {
+          if (ept == 0) mbar_drain(bars + kBarRed, red_phase, wctl);   // its copies still land
+          aborted = true;
+          break;
+        }
         red_phase ^= 1u;
         // eight tokens at a time so that the shared-memory loads overlap; each
         // token's sum still runs over the contributors in CTA order
@@ -782,13 +675,10 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   }
 
   // --------------------------------------------------------------- teardown --
+  // Every producer has drained what it started (weight and activation copies, the
+  // issuers' MMAs, the reduction copies), so nothing is still writing shared memory
+  // or TMEM, aborted or not.
   __syncthreads();
-  if (*abort_flag) {
-    // let bulk copies and MMAs already issued land before the memory goes away
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 1000000ull) {
-    }
-  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

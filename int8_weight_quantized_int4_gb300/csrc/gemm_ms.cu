@@ -21,7 +21,8 @@ cudaError_t launch_gemm_ms(const GemmArgs &a, int act, cudaStream_t st) {
   if ((a.P.ms_teams != 2 && a.P.ms_teams != 4) || a.P.bn != kMsMaxTokens) return cudaErrorInvalidValue;
   const bool one = a.P.M <= 8, four = a.P.ms_teams == 4;
   if (four && !(one && act == kActF16)) return cudaErrorInvalidValue;
-  if (act == kActQuant) return one ? run_ms<1, kActQuant>(a, st) : run_ms<2, kActQuant>(a, st);
+  // the in-kernel quantizer takes at most 4 tokens (the plan's fused rule)
+  if (act == kActQuant) return a.P.M <= 4 ? run_ms<1, kActQuant>(a, st) : cudaErrorInvalidValue;
   if (act == kActI8) return one ? run_ms<1, kActI8>(a, st) : run_ms<2, kActI8>(a, st);
   if (four) return run_ms<1, kActF16, 4>(a, st);
   return one ? run_ms<1, kActF16>(a, st) : run_ms<2, kActF16>(a, st);

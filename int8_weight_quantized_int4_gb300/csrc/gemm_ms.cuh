@@ -160,11 +160,13 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
   auto wempty_bar = [&](int s) { return bars + 128u + 8u * s; };
   auto xfull_bar = [&](int s) { return bars + 256u + 8u * s; };
   auto xempty_bar = [&](int s) { return bars + 288u + 8u * s; };
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(gbars + 352);
   volatile int *bcast = reinterpret_cast<volatile int *>(gbars + 356);
   // the compute warps' common view of the abort flag, taken by one thread before a
   // named barrier, so that all of them pass the same barriers
   volatile int *decide = reinterpret_cast<volatile int *>(gbars + 360);
+  volatile WaitBlock *wctl = reinterpret_cast<volatile WaitBlock *>(gbars + 368);
+  // a pipeline wait: bounded by the launch's limit, gives up once the CTA aborts
+  auto pwait = [&](uint32_t bar, uint32_t parity) { return mbar_wait(bar, parity, wctl, a.wait_ns == 0); };
   auto w_smem = [&](int s) { return wbase + (uint32_t)s * kWStage; };
   auto x_smem = [&](int s) { return sbase + (uint32_t)s * kXStage; };
 
@@ -180,7 +182,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
       mbar_init(xfull_bar(s), 1);
       mbar_init(xempty_bar(s), kCompute);
     }
-    *abort_flag = 0;
+    wait_block_init(wctl, a.wait_ns, a.err);
     *bcast = 0;
     *decide = 0;
     fence_mbar_init();
@@ -245,21 +247,23 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       if (early) {
-        // ahead of the preceding kernel: the chunks that will not fit the ring now are
-        // pulled into L2, so that their copies after the wait come from L2, not HBM
+        // ahead of the preceding kernel: the next kMsL2AheadChunks chunks that will not
+        // fit the ring now are pulled into L2, so that their copies after the wait come
+        // from L2, not HBM (a bounded number: a long launch pulling all of its chunks
+        // would push its own earlier ones out of L2 before they are copied)
         int c = 0;
-        for (int i = 0; segment(P, cta, i, sg); ++i) {
+        for (int i = 0; c < SW + kMsL2AheadChunks && segment(P, cta, i, sg); ++i) {
           int u, t;
           tile_coords(P, sg.tile, u, t);
           const uint8_t *src = a.wpack + ((size_t)t * P.G + sg.g0) * kChunkW4;
-          for (int g = sg.g0; g < sg.g1; ++g, ++c, src += kChunkW4)
+          for (int g = sg.g0; g < sg.g1 && c < SW + kMsL2AheadChunks; ++g, ++c, src += kChunkW4)
             if (c >= SW) prefetch_l2(src, kChunkW4);
         }
       }
-      int s[TEAMS], cidx = 0;
+      int s[TEAMS], nfill[TEAMS], cidx = 0;
       uint32_t ph[TEAMS];
 #pragma unroll
-      for (int j = 0; j < TEAMS; ++j) s[j] = 0, ph[j] = 0;
+      for (int j = 0; j < TEAMS; ++j) s[j] = 0, nfill[j] = 0, ph[j] = 0;
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         int u, t;
@@ -272,30 +276,40 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
 #pragma unroll
           for (int j = 0; j < TEAMS; ++j)
             if (j == tm) { slot = j * SWT + s[j]; par = ph[j]; }
-          if (!mbar_wait(wempty_bar(slot), par ^ 1u, abort_flag, a.err)) { ok = false; break; }
+          if (!pwait(wempty_bar(slot), par ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(wfull_bar(slot), kChunkW4);
           bulk_g2s(w_smem(slot), src, kChunkW4, wfull_bar(slot), pol);
 #pragma unroll
           for (int j = 0; j < TEAMS; ++j)
-            if (j == tm && ++s[j] == SWT) { s[j] = 0; ph[j] ^= 1u; }
+            if (j == tm) {
+              ++nfill[j];
+              if (++s[j] == SWT) { s[j] = 0; ph[j] ^= 1u; }
+            }
         }
       }
+      // the last fill of every slot has landed before the CTA may exit
+#pragma unroll
+      for (int j = 0; j < TEAMS; ++j)
+        for (int k = 0; k < SWT && k < nfill[j]; ++k)
+          mbar_drain(wfull_bar(j * SWT + k), k < s[j] ? ph[j] : ph[j] ^ 1u, wctl);
     }
   } else if (warp == kMsWarpX) {
     // -------------------------------------------------- activation copies --
     if (lane == 0) {
-      int s = 0;
+      int s = 0, nfill = 0;
       uint32_t ph = 0;
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         for (int g = sg.g0; g < sg.g1; g += kXBlock) {
-          if (!mbar_wait(xempty_bar(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
+          if (!pwait(xempty_bar(s), ph ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(xfull_bar(s), kXBytes);
+          ++nfill;
           if constexpr (ACT8) tma_load_3d(x_smem(s) + kXBlock * kXChunk, &a.tmap, 0, 0, g, xfull_bar(s));
           else tma_load_3d(x_smem(s), &a.tmap, 0, 0, 2 * g, xfull_bar(s));
           if (++s == SX) { s = 0; ph ^= 1u; }
         }
       }
+      for (int k = 0; k < SX && k < nfill; ++k) mbar_drain(xfull_bar(k), k < s ? ph : ph ^ 1u, wctl);
     }
   } else if (warp >= kMsWarpC0) {
     // ------------------------------------------------------------ compute --
@@ -339,7 +353,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
         const int nb = sg.g1 - gb < kXBlock ? sg.g1 - gb : kXBlock;
         // every compute warp waits for every activation block and returns it once;
         // after an abort every wait gives up at once and the loops run out quickly
-        mbar_wait(xfull_bar(xs), xph, abort_flag, a.err);
+        pwait(xfull_bar(xs), xph);
         if constexpr (ACT8 || QIN) {
           // the compute warps together turn the block into fp16 codes, then all wait
           uint8_t *xb = gbase + (size_t)xs * kXStage;
@@ -376,7 +390,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
         }
         for (int j = (tm - cidx) & (TEAMS - 1); j < nb; j += TEAMS) {
           const int slot = tm * SWT + s;
-          mbar_wait(wfull_bar(slot), ph, abort_flag, a.err);
+          pwait(wfull_bar(slot), ph);
           const uint32_t xt = x_smem(xs) + (uint32_t)j * kXChunk;
           const uint32_t wc = w_smem(slot);
           uint32_t sc2[RBW];
@@ -471,7 +485,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
           }
         }
       }
-      if (ct == 0) *decide = *abort_flag;
+      if (ct == 0) *decide = wctl->abort;
       named_bar_sync(1, kCThreads);
       if (*decide) aborted = true;
       int u, t;
@@ -547,13 +561,8 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
   }
 
   // --------------------------------------------------------------- teardown --
+  // both copy threads have drained their copies: nothing still writes shared memory
   __syncthreads();
-  if (*abort_flag) {
-    // let bulk copies already issued land before the shared memory goes away
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 1000000ull) {
-    }
-  }
 }
 
 }  // namespace qw

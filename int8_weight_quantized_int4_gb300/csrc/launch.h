@@ -21,6 +21,7 @@ struct GemmArgs {
   float *partials;          // [2*grid][bn][128] binary32 partial sums (stream-K)
   int *err;                 // device error word
   int early_weights;        // weights may be streamed before the preceding kernel ends
+  unsigned long long wait_ns;   // time limit of a pipeline wait (QW_OPT_WAIT_LIMIT_US)
 };
 
 void count_launch();

@@ -33,6 +33,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
       "r"(bytes)
       : "memory");
 }
+// Non-blocking check of a phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Check of a phase that may block for a short, system-dependent time.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -44,10 +56,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Time limit of every pipeline wait.  A wait that exceeds it raises the CTA's
-// abort flag and records QW_ERR_TIMEOUT (-7) in the device error word; every
-// other wait of the CTA then gives up at its next wake-up (within the suspend
-// hint below), so a broken pipeline ends the kernel instead of hanging the GPU.
+// Time limit of a pipeline wait (the default; the caller may set a shorter one
+// through qw_set_option, which a kernel keeps in its WaitBlock; a limit of 0 also
+// makes the first check of a wait non-blocking, so that any wait whose phase is not
+// complete at that check gives up -- the hook that drives the path below).  A wait that
+// exceeds it raises the CTA's abort flag and records QW_ERR_TIMEOUT (-7) in the
+// device error word; every other wait of the CTA then gives up at its next
+// wake-up (within the suspend hint below), so a broken pipeline ends the kernel
+// instead of hanging the GPU.  The drain waits at the end of a kernel (a producer
+// waiting for its own copies or MMAs to land before the CTA releases its shared
+// memory and TMEM) ignore the abort flag and always take this default limit.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 // try_wait with a suspend-time hint: a waiting thread is parked by the hardware
@@ -65,24 +83,54 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                                   int *err) {
+// A CTA's wait state, in shared memory (written once before the CTA's first
+// barrier, so a wait needs one pointer, not three live registers).
+struct WaitBlock {
+  int abort;                  // the CTA's abort flag
+  int pad;
+  uint64_t limit_ns;          // time limit of one wait (a limit of 0: any wait not
+                              // satisfied at its first poll gives up)
+  int *err;                   // device error word
+};
+
+__device__ __forceinline__ void wait_block_init(volatile WaitBlock *w, uint64_t limit_ns, int *err) {
+  w->abort = 0;
+  w->limit_ns = limit_ns;
+  w->err = err;
+}
+
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile WaitBlock *w) {
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = w->limit_ns;
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      atomicCAS(err, 0, -7);
+    if (w->abort) return false;
+    if (globaltimer_ns() - t0 >= limit) {
+      w->abort = 1;
+      atomicCAS(w->err, 0, -7);
       return false;
     }
+    if (mbar_try_wait_sleep(bar, parity)) return true;
   }
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          int *err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort_flag, err);
+// `no_limit` is the launch's "limit of 0" (a kernel parameter, so no register holds it).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile WaitBlock *w,
+                                          bool no_limit) {
+  if (no_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, w);
+}
+
+// Wait for a phase that completes by itself (copies or MMAs this thread already
+// issued), whatever the abort flag says; after kWaitLimitNs record QW_ERR_TIMEOUT
+// and return.
+static __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity, volatile WaitBlock *w) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_sleep(bar, parity)) {
+    if (globaltimer_ns() - t0 >= kWaitLimitNs) {
+      atomicCAS(w->err, 0, -7);
+      return;
+    }
+  }
 }
 
 // ------------------------------------------------------------ bulk copies --
@@ -182,6 +230,18 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Named barrier with an OR over the participants' predicates: every participant
+// gets the same answer, so a decision taken on it sends all of them the same way.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // --------------------------------------------------------------- tcgen05 --

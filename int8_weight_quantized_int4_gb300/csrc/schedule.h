@@ -44,7 +44,6 @@ struct Plan {
   int xblock;                    // chunks per activation block (one tensor copy)
   int smem_bytes;
   int fused;                     // W4A8 with the per-token quantizer inside the GEMM
-  int rows_bytes;                // unused (0)
   int ms_teams;                  // > 0: the warp-level MMA kernel for decode batches (M <= 16),
                                  // with this many teams of warps (one chunk per team at a time)
   int ms_red_bytes;              // its shared-memory buffer for the teams' partial sums
@@ -195,6 +194,10 @@ constexpr int kMsSmemLimit = 113 * 1024; // two CTAs per SM
 // Launches of at least this many chunks per SM run two decode CTAs per SM (more warps
 // streaming at once); shorter ones one, leaving the SM's other half to the next layer.
 constexpr int kMsLongChunksPerSm = 32;
+// With the weights declared immutable, the weight-copy thread pulls at most this many
+// chunks past its ring into L2 before the preceding kernel ends (304 CTAs x 16 x 8.4 KB
+// = 41 MB, well inside the 129 MB L2).
+constexpr int kMsL2AheadChunks = 16;
 QW_HD bool ms_kernel(int mode, int M) {
   return (mode == 0 || mode == 1 || mode == 3) && M >= 1 && M <= kMsMaxTokens;
 }
@@ -228,15 +231,14 @@ QW_HD bool ms_ring_depths(int mode, int M, int teams, int &xst, int &wst) {
 }
 
 // Ring depths: the deepest activation ring (at most kMaxXStages, or 3 for token
-// tiles up to 64 whose blocks already span several groups -- except the fused W4A8
-// mode, whose quantized blocks are all written up front -- at least 2) that still
+// tiles up to 64 whose blocks already span several groups, at least 2) that still
 // leaves four weight slots; the weight ring takes the rest (at most kMaxWStages),
 // rounded down to an even count (half per dequant group).  Returns false when
 // even 2 + 4 slots do not fit.
-QW_HD bool ring_depths(int mode, int bn, int &xst, int &wst, int extra = 0, int split = 2) {
+QW_HD bool ring_depths(int mode, int bn, int &xst, int &wst, int split = 2) {
   const int xb = xstage_bytes(mode, bn), wb = wstage_bytes(mode);
-  for (int x = (bn <= 64 && mode != 3) ? 3 : kMaxXStages; x >= 2; --x) {
-    int w = (kSmemLimit - kSmemReserve - extra - x * xb) / wb;
+  for (int x = bn <= 64 ? 3 : kMaxXStages; x >= 2; --x) {
+    int w = (kSmemLimit - kSmemReserve - x * xb) / wb;
     if (w > kMaxWStages) w = kMaxWStages;
     w -= w % split;                      // the same number of slots per consumer
     if (w >= 2 * split) { xst = x; wst = w; return true; }
@@ -298,7 +300,6 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   if (N % kRows || K % kGroup) return -2;
   if (num_sms > kMaxGrid / 2) num_sms = kMaxGrid / 2;
   P.fused = quant_in_kernel(mode, M, K) ? 1 : 0;
-  P.rows_bytes = 0;
   // mode 3 outside the fused range is the quantizer followed by a mode-1 plan
   const bool quant_first = mode == 3 && !P.fused;
   if (quant_first) mode = 1;
@@ -331,9 +332,8 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
                    kMsQuantFloats * 4 + kSmemReserve;
   } else {
     P.ms_red_bytes = 0;
-    if (!ring_depths(mode, P.bn, P.xstages, P.stages, P.rows_bytes)) return -2;
-    P.smem_bytes = P.xstages * xstage_bytes(mode, P.bn) + P.stages * wstage_bytes(mode) + P.rows_bytes +
-                   kSmemReserve;
+    if (!ring_depths(mode, P.bn, P.xstages, P.stages)) return -2;
+    P.smem_bytes = P.xstages * xstage_bytes(mode, P.bn) + P.stages * wstage_bytes(mode) + kSmemReserve;
   }
   // Tile counters live in a fixed region at the start of every workspace, sized for
   // the largest stream-K plan (fewer than kStreamKMaxTilesPerSm tiles per SM), so

@@ -126,6 +126,14 @@ def test_options_host_only():
     assert L.qw_set_option(7, 1) == q.QW_ERR_INVALID_ARG
     assert L.qw_set_option(q.QW_OPT_WEIGHTS_IMMUTABLE, 2) == q.QW_ERR_INVALID_ARG
     assert L.qw_get_option(7) == q.QW_ERR_INVALID_ARG
+    # the wait-limit test hook: microseconds, 0 .. the 4 s default
+    assert L.qw_get_option(q.QW_OPT_WAIT_LIMIT_US) == q.DEFAULT_WAIT_LIMIT_US == 4_000_000
+    assert L.qw_set_option(q.QW_OPT_WAIT_LIMIT_US, 0) == q.QW_OK
+    assert L.qw_get_option(q.QW_OPT_WAIT_LIMIT_US) == 0
+    assert L.qw_set_option(q.QW_OPT_WAIT_LIMIT_US, -1) == q.QW_ERR_INVALID_ARG
+    assert L.qw_set_option(q.QW_OPT_WAIT_LIMIT_US, 4_000_001) == q.QW_ERR_INVALID_ARG
+    q.set_wait_limit_us(None)
+    assert L.qw_get_option(q.QW_OPT_WAIT_LIMIT_US) == 4_000_000
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
