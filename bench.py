@@ -642,6 +642,31 @@ def extras(q, dev, stream, pk, pk_src):
         del pkd, x, y, wsp
     torch.cuda.empty_cache()
 
+    def lm_head_topk(mode, x, pk, N, K, gemm_ms, ws):
+        # the lm_head with its top-k fused in, against the plain GEMM alone and against the
+        # GEMM followed by the standalone top-k; exactness of the fused top-k vs the oracle
+        k, M = 64, x.shape[0]
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        v = torch.empty((M, k), dtype=torch.float16, device=dev)
+        i = torch.empty((M, k), dtype=torch.int32, device=dev)
+        wst = q.Workspace(dev)
+        fused = lambda: q.qgemm_lm_head_topk(mode, x, pk, N, K, k, y=y, vals=v, idx=i, ws=wst)  # noqa: E731
+        ms_f = timeit(fused, 10)
+        gemm = q.qgemm_w4a16 if mode == q.MODE_W4A16 else q.qgemm_w8a16
+
+        def separate():
+            gemm(x, pk, N, K, y=y, ws=ws)
+            q.topk_logits(y, k)
+        ms_s = timeit(separate, 10)
+        fused()
+        torch.cuda.synchronize()
+        ov, oi = oracle.topk(y.cpu().numpy(), k)
+        exact = bool(np.array_equal(i.cpu().numpy().astype(np.int64), oi) and
+                     np.array_equal(v.cpu().numpy().view(np.uint16), ov.view(np.uint16)))
+        return {"us": round(ms_f * 1e3, 1), "gemm_us": round(gemm_ms * 1e3, 1),
+                "added_us": round((ms_f - gemm_ms) * 1e3, 2), "separate_us": round(ms_s * 1e3, 1),
+                "k": k, "exact": exact}
+
     # lm_head W8A16: 248,320 x 5120 int8 (1.29 GB > L2)
     lh = synth.lm_head(64)
     pk8 = q.qpack_w8(lh.codes.to(dev), lh.scales.to(dev))
@@ -659,6 +684,8 @@ def extras(q, dev, stream, pk, pk_src):
                                       "frac_hbm": round(alg / ms / 1e6 / hbm, 4),
                                       "TFLOPS": round(2 * M * lh.N * lh.K / ms / 1e9, 2),
                                       "parity": parity_err(y.cpu()[:, cols], ref)}
+        if M in (1, 16, 64):
+            out[f"lm_head_topk_w8a16_M{M}"] = lm_head_topk(q.MODE_W8A16, x, pk8, lh.N, lh.K, ms, wsp)
 
     # dequant-on-gather from the same int8 group-128 table (the embedding's format)
     for T in (64, 2048):
@@ -691,6 +718,7 @@ def extras(q, dev, stream, pk, pk_src):
                                       "frac_hbm": round(alg / ms / 1e6 / hbm, 4),
                                       "TFLOPS": round(2 * M * l4.N * l4.K / ms / 1e9, 2),
                                       "parity": parity_err(y.cpu()[:, cols4], ref)}
+        out[f"lm_head_topk_w4a16_M{M}"] = lm_head_topk(q.MODE_W4A16, x, pk4, l4.N, l4.K, ms, wsp)
     del pk4, l4
     torch.cuda.empty_cache()
 

@@ -196,6 +196,31 @@ int topk_logits(const uint16_t *logits, int M, int N, int k, uint16_t *vals, int
                 size_t ws_bytes, qw_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * qgemm_lm_head_topk -- the lm_head with the sampler's top-k fused in: the
+ * logits y = x . W^T of qgemm_w4a16 (mode QW_MODE_W4A16, the GPTQ-int4 head of
+ * the serving README's step table) or qgemm_w8a16 (QW_MODE_W8A16, the int8
+ * group-128 head, "In full" item 1), bit-identical to those calls, and per row
+ * of y its k largest values as topk_logits gives them ("In full" item 6).
+ * The GEMM's epilogue records each token's largest logit in every 128-row
+ * tile; one small kernel then selects among the tiles that can hold the top k
+ * (those whose maximum is at least the k-th largest tile maximum).
+ *   x [M, K] fp16 and packed (qpack_w4 or qpack_w8 bytes) as the GEMM;
+ *   y [M, N] fp16 logits, written;  vals [M, k] fp16, idx [M, k] int32.
+ *   1 <= k <= min(64, N), N <= 262144 (and the GEMM's shape rules).  NaN
+ *   logits are out of contract.
+ *   ws: qgemm_lm_head_topk_workspace_bytes(mode, M, N, K, k) bytes, 256-byte
+ *   aligned, zero-filled once; the first ..._workspace_zero_bytes stay zero
+ *   after every call that returns QW_OK (zero-fill again after QW_ERR_TIMEOUT).
+ * Two launches, async.  Returns as qgemm_w4a16, or QW_ERR_INVALID_ARG for another
+ * mode or k.
+ * ------------------------------------------------------------------------ */
+size_t qgemm_lm_head_topk_workspace_bytes(int mode, int M, int N, int K, int k);
+size_t qgemm_lm_head_topk_workspace_zero_bytes(int mode, int M, int N, int K, int k);
+int qgemm_lm_head_topk(int mode, const uint16_t *x, const void *packed, int M, int N, int K, int k,
+                       uint16_t *y, uint16_t *vals, int32_t *idx, void *ws, size_t ws_bytes,
+                       qw_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * qgemm_w4a8_fused -- the W4A8 layer from fp16 activations: y is bit-identical
  * to quant_act_int8(x) followed by qgemm_w4a8 on the same weights ("In full"
  * item 4: activations quantized to int8 per token, int4 weights).

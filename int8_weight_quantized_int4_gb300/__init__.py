@@ -62,6 +62,9 @@ SIGNATURES = {
     "topk_logits": (_i, [_p, _i, _i, _i, _p, _p, _p, _sz, _p]),
     "qgemm_w8a16": (_i, [_p, _p, _i, _i, _i, _p, _p, _sz, _p]),
     "qgemm_w4a16_noalloc": (_i, [_p, _p, _i, _i, _i, _p, _p]),
+    "qgemm_lm_head_topk_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "qgemm_lm_head_topk_workspace_zero_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "qgemm_lm_head_topk": (_i, [_i, _p, _p, _i, _i, _i, _i, _p, _p, _p, _p, _sz, _p]),
     "qw_last_error_string": (ctypes.c_char_p, []),
     "qw_device_error": (_i, [_p]),
     "qw_num_kernel_launches": (_ll, []),
@@ -216,6 +219,14 @@ class Workspace:
             self.buf = torch.zeros(need, dtype=torch.uint8, device=self.device)
         return self.buf, self.buf.numel()
 
+    def get_bytes(self, need: int):
+        """The buffer, grown to at least `need` bytes (zero-filled when grown)."""
+        if need == 0:
+            return None, 0
+        if self.buf is None or self.buf.numel() < need:
+            self.buf = torch.zeros(need, dtype=torch.uint8, device=self.device)
+        return self.buf, self.buf.numel()
+
     def zero(self):
         """Zero-fill the buffer again (needed after a call that ended in QW_ERR_TIMEOUT)."""
         if self.buf is not None:
@@ -325,6 +336,37 @@ def embed_gather_w8(ids, packed, V: int, D: int, out=None):
 
 
 _topk_ws = {}
+
+
+def qgemm_lm_head_topk(mode: int, x, packed, N: int, K: int, k: int, y=None, vals=None, idx=None,
+                       ws: Workspace | None = None):
+    """The lm_head (MODE_W4A16 on qpack_w4 bytes or MODE_W8A16 on qpack_w8 bytes) with the
+    top-k of each row fused in: returns (y [M,N] fp16 logits, vals [M,k] fp16, idx [M,k] int32),
+    y bit-identical to the plain GEMM and (vals, idx) equal to topk_logits(y, k)."""
+    _need(x, torch.float16, "x", 2)
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("x.shape[1] != K")
+    y = _out(y, M, N, x.device)
+    if vals is None:
+        vals = torch.empty((M, k), dtype=torch.float16, device=x.device)
+    if idx is None:
+        idx = torch.empty((M, k), dtype=torch.int32, device=x.device)
+    _need(vals, torch.float16, "vals", 2)
+    _need(idx, torch.int32, "idx", 2)
+    _need_shape(vals, (M, k), "vals")
+    _need_shape(idx, (M, k), "idx")
+    if M and N:
+        _need_packed(packed, (qpack_w8_bytes if mode == MODE_W8A16 else qpack_w4_bytes)(N, K), x)
+    if ws is None:
+        key = (x.device, torch.cuda.current_stream(x.device).cuda_stream, "lm_head_topk")
+        ws = _default_ws.setdefault(key, Workspace(x.device))
+    with torch.cuda.device(x.device):
+        need = int(lib().qgemm_lm_head_topk_workspace_bytes(mode, M, N, K, k))
+        wbuf, wbytes = ws.get_bytes(need)
+        _check(lib().qgemm_lm_head_topk(mode, _ptr(x), _ptr(packed), M, N, K, k, _ptr(y), _ptr(vals),
+                                        _ptr(idx), _ptr(wbuf), wbytes, _stream(x)))
+    return y, vals, idx
 
 
 def topk_logits(logits, k: int):

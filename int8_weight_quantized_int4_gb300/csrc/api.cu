@@ -141,7 +141,7 @@ int check_shape(int M, int N, int K) {
 }
 
 int gemm_common(int mode, const void *act, const float *xs, const void *packed, int M, int N, int K,
-                uint16_t *y, void *ws, size_t ws_bytes, qw_stream_t stream) {
+                uint16_t *y, void *ws, size_t ws_bytes, qw_stream_t stream, uint32_t *tile_max = nullptr) {
   int rc = check_shape(M, N, K);
   if (rc) return rc;
   if (M == 0 || N == 0) return QW_OK;
@@ -172,6 +172,7 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
   a.err = d->err;
   a.early_weights = g_opt_weights_immutable.load(std::memory_order_relaxed);
   a.wait_ns = 1000ull * (unsigned long long)g_opt_wait_limit_us.load(std::memory_order_relaxed);
+  a.tile_max = tile_max;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (mode == QW_MODE_W4A8_FUSED && P.fused) {
@@ -392,6 +393,49 @@ int qgemm_w4a8_fused(const uint16_t *x, const void *packed_w4, int M, int N, int
 int qgemm_w8a16(const uint16_t *x, const void *packed_w8, int M, int N, int K, uint16_t *y, void *ws,
                 size_t ws_bytes, qw_stream_t stream) {
   return gemm_common(QW_MODE_W8A16, x, nullptr, packed_w8, M, N, K, y, ws, ws_bytes, stream);
+}
+
+// ---- lm_head with top-k: workspace = [tile maxima M x N/128 uint32, zero][GEMM workspace]
+static int lm_head_topk_shape(int mode, int M, int N, int K, int k) {
+  if (mode != QW_MODE_W4A16 && mode != QW_MODE_W8A16)
+    return fail(QW_ERR_INVALID_ARG, "mode %d: the lm_head with top-k takes QW_MODE_W4A16 or QW_MODE_W8A16", mode);
+  int rc = check_shape(M, N, K);
+  if (rc) return rc;
+  if (N > qw::kTopkMaxN) return fail(QW_ERR_UNSUPPORTED_SHAPE, "N=%d above %d", N, qw::kTopkMaxN);
+  if (k < 1 || k > 64 || k > N) return fail(QW_ERR_INVALID_ARG, "k=%d outside 1..min(64, N)", k);
+  return QW_OK;
+}
+static size_t lm_head_tile_bytes(int M, int N) { return qw::align_up((size_t)M * (N / 128) * 4, 256); }
+
+size_t qgemm_lm_head_topk_workspace_bytes(int mode, int M, int N, int K, int k) {
+  if (lm_head_topk_shape(mode, M, N, K, k)) return 0;
+  return lm_head_tile_bytes(M, N) + qgemm_workspace_bytes(mode, M, N, K);
+}
+
+size_t qgemm_lm_head_topk_workspace_zero_bytes(int mode, int M, int N, int K, int k) {
+  if (lm_head_topk_shape(mode, M, N, K, k)) return 0;
+  return lm_head_tile_bytes(M, N) + qgemm_workspace_zero_bytes(mode, M, N, K);
+}
+
+int qgemm_lm_head_topk(int mode, const uint16_t *x, const void *packed, int M, int N, int K, int k, uint16_t *y,
+                       uint16_t *vals, int32_t *idx, void *ws, size_t ws_bytes, qw_stream_t stream) {
+  int rc = lm_head_topk_shape(mode, M, N, K, k);
+  if (rc) return rc;
+  if (M == 0) return QW_OK;
+  if (!vals || !idx) return fail(QW_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned(vals, 2) || !aligned(idx, 4) || (ws && !aligned(ws, 256)))
+    return fail(QW_ERR_ALIGNMENT, "vals 2-byte, idx 4-byte and the workspace 256-byte aligned");
+  const size_t tb = lm_head_tile_bytes(M, N);
+  const size_t need = tb + qgemm_workspace_bytes(mode, M, N, K);
+  if (!ws || ws_bytes < need)
+    return fail(QW_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws ? ws_bytes : (size_t)0);
+  uint32_t *tile_max = static_cast<uint32_t *>(ws);
+  rc = gemm_common(mode, x, nullptr, packed, M, N, K, y, static_cast<uint8_t *>(ws) + tb, ws_bytes - tb, stream,
+                   tile_max);
+  if (rc) return rc;
+  cudaError_t e = qw::launch_topk_tiles(y, M, N, k, tile_max, vals, idx, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "top-k kernel launch");
+  return QW_OK;
 }
 
 const char *qw_last_error_string(void) { return tl_err; }

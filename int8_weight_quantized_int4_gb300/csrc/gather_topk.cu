@@ -107,17 +107,6 @@ constexpr int kTopkMaxVec = 2;                 // 16-byte vectors per thread per
 constexpr int kTopkMerge = kTopkMaxSlices * kTopkMaxK / kTopkThreads;   // candidates per thread
 static_assert(kTopkMaxSlices * kTopkMaxK <= kTopkMaxVec * 8 * kTopkThreads, "one list serves both selections");
 
-// Two order keys from a word holding two fp16 values (low half = the lower position):
-// -0 becomes +0 (x + 0 is exact for every other value), then a negative value's bits are
-// inverted and a non-negative value's sign bit is set.
-__device__ __forceinline__ uint32_t order_keys2(uint32_t w) {
-  __half2 h = *reinterpret_cast<const __half2 *>(&w);
-  h = __hadd2(h, __float2half2_rn(0.0f));
-  const uint32_t x = *reinterpret_cast<const uint32_t *>(&h);
-  const uint32_t s = (x >> 15) & 0x00010001u;     // the two sign bits, at bits 0 and 16
-  return x ^ (s * 0x7fffu + 0x80008000u);         // 0xffff or 0x8000 per half
-}
-
 __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t index) {
   return ((uint64_t)key << 24) | (uint64_t)(0xffffffu - index);
 }
@@ -156,14 +145,17 @@ __device__ __forceinline__ void find_bin(const int *hist, int remaining, int *bc
 }
 
 // The shared state of one selection: hist 2 x 256 ints (one per pass in turn, the next
-// cleared while the current one fills), bc 3 ints, the boundary-bin list and the winners.
-struct TopkSmem {
+// cleared while the current one fills), bc 3 ints, the boundary-bin list (room for every
+// element of the selection) and the winners.
+template <int CAP>
+struct TopkSmemT {
   int hist[2 * 256];
   int bc[3];
   int nlist, nsel;
-  uint32_t list[kTopkMaxVec * 8 * kTopkThreads];   // >= kTopkMaxSlices * kTopkMaxK
+  uint32_t list[CAP];
   uint32_t sel[kTopkMaxK];
 };
+using TopkSmem = TopkSmemT<kTopkMaxVec * 8 * kTopkThreads>;   // >= kTopkMaxSlices * kTopkMaxK
 
 // Called by the whole CTA after the first pass (over the top byte) found the boundary bin
 // b0 with r0 of its elements still wanted, every element of the CTA above b0 already in
@@ -171,7 +163,8 @@ struct TopkSmem {
 // byte b0), hist[256..511] zero.  Unless the bin is taken whole, the next 8-bit passes run
 // over the list; its elements at or above the resulting threshold join sel, which then
 // holds exactly k composites.
-__device__ void finish_select(TopkSmem &sm, uint32_t b0, int r0, bool whole) {
+template <class SM>
+__device__ void finish_select(SM &sm, uint32_t b0, int r0, bool whole) {
   const int T = sm.nlist;
   if (whole) {
     for (int j = threadIdx.x; j < T; j += kTopkThreads) sm.sel[atomicAdd(&sm.nsel, 1)] = sm.list[j];
@@ -206,8 +199,8 @@ __device__ void finish_select(TopkSmem &sm, uint32_t b0, int r0, bool whole) {
 // First pass over register composites c[0..n) (at least k of them in the CTA): histogram
 // of the top byte, boundary bin, then the split into winners and list; returns with sel
 // holding the k largest.
-template <int NMAX>
-__device__ void select_regs(const uint32_t (&c)[NMAX], int n, int k, TopkSmem &sm) {
+template <int NMAX, class SM>
+__device__ void select_regs(const uint32_t (&c)[NMAX], int n, int k, SM &sm) {
   for (int b = threadIdx.x; b < 512; b += kTopkThreads) sm.hist[b] = 0;
   if (threadIdx.x == 0) sm.nlist = sm.nsel = 0;
   __syncthreads();
@@ -335,6 +328,158 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const uint16_t *_
     idx[(size_t)m * k + rank] = n;
     vals[(size_t)m * k + rank] = row[n];
   }
+}
+
+// ------------------------------------------------ top-k from tile maxima --
+// The lm_head with top-k.  The GEMM's epilogue leaves, per token m and 128-row tile t of
+// the logits, the largest order key among the tile's outputs (tile_max[m][t]).  With
+// t_k the k-th largest of those maxima, at least k logits are >= t_k (one per tile of
+// the k best), so every logit of the top k lies in a tile whose maximum is >= t_k: the
+// candidate tiles, exactly k of them unless maxima tie.  One CTA per token:
+//   1. the k largest tile maxima (radix selection over composites key << 16 | 0xffff - t)
+//      give t_k; with at most k tiles every tile is a candidate;
+//   2. the candidate tiles are listed in ascending order (per-warp ballots);
+//   3. the k largest logits of the candidate tiles are selected kTileBatch tiles at a
+//      time, the winners so far (all at smaller indices than the batch) listed first in
+//      index order, so that list positions follow the indices and the composites
+//      key << 16 | 0xffff - position order ties by the smaller index;
+//   4. the winners are written largest first.
+// The tile maxima are cleared on the way (zero again for the next call).
+constexpr int kTileBatch = 64;
+constexpr int kTileSel = (kTileBatch * kRows + kTopkMaxK + kTopkThreads - 1) / kTopkThreads;   // per thread
+constexpr int kMaxTiles = kTopkMaxN / kRows;
+constexpr int kTilesPer = kMaxTiles / kTopkThreads;                                           // 8
+static_assert(kTileSel * kTopkThreads <= 65536 && kMaxTiles <= 65536, "16-bit list positions");
+
+struct TileTopkSmem {
+  TopkSmemT<kTileSel * kTopkThreads> s;
+  uint16_t cand[kMaxTiles];
+  int wcount[kTopkThreads / 32];
+  uint32_t thr;
+  uint32_t run_key[kTopkMaxK], nxt_key[kTopkMaxK];   // winners so far, in index order
+  uint16_t run_val[kTopkMaxK], nxt_val[kTopkMaxK];
+  int run_idx[kTopkMaxK], nxt_idx[kTopkMaxK];
+};
+
+__global__ void __launch_bounds__(kTopkThreads) topk_tiles_kernel(const uint16_t *__restrict__ y, int N, int k,
+                                                                  uint32_t *tile_max, uint16_t *vals,
+                                                                  int32_t *idx) {
+  __shared__ TileTopkSmem sm;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int m = blockIdx.x, T = N / kRows;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint16_t *row = y + (size_t)m * N;
+  uint32_t *tmx = tile_max + (size_t)m * T;
+
+  // ---- 1. the tile maxima (tile tid + 256 i in tk[i]), cleared for the next call
+  uint32_t tk[kTilesPer];
+#pragma unroll
+  for (int i = 0; i < kTilesPer; ++i) {
+    const int t = tid + kTopkThreads * i;
+    tk[i] = t < T ? __ldcg(tmx + t) : 0u;
+  }
+#pragma unroll
+  for (int i = 0; i < kTilesPer; ++i) {
+    const int t = tid + kTopkThreads * i;
+    if (t < T) tmx[t] = 0u;
+  }
+  if (tid == 0) sm.thr = T > k ? 0xffffffffu : 0u;
+  if (T > k) {
+    uint32_t c[kTilesPer];
+#pragma unroll
+    for (int i = 0; i < kTilesPer; ++i) c[i] = (tk[i] << 16) | (0xffffu - (uint32_t)(tid + kTopkThreads * i));
+    select_regs(c, T > tid ? (T - 1 - tid) / kTopkThreads + 1 : 0, k, sm.s);
+    if (tid < k) atomicMin(&sm.thr, sm.s.sel[tid] >> 16);
+  }
+  __syncthreads();
+  const uint32_t thr = sm.thr;
+
+  // ---- 2. candidate tiles, ascending
+  int ncand = 0;
+#pragma unroll
+  for (int i = 0; i < kTilesPer; ++i) {
+    if (kTopkThreads * i >= T) break;                // uniform
+    const int t = tid + kTopkThreads * i;
+    const bool flag = t < T && tk[i] >= thr;
+    const unsigned bal = __ballot_sync(0xffffffffu, flag);
+    if (lane == 0) sm.wcount[warp] = __popc(bal);
+    __syncthreads();
+    int off = ncand, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kTopkThreads / 32; ++w) {
+      off += w < warp ? sm.wcount[w] : 0;
+      tot += sm.wcount[w];
+    }
+    if (flag) sm.cand[off + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)t;
+    ncand += tot;
+    __syncthreads();
+  }
+
+  // ---- 3. the k best logits of the candidate tiles, a batch of tiles at a time
+  int nrun = 0;
+  for (int b0 = 0; b0 < ncand; b0 += kTileBatch) {
+    const int nb = ncand - b0 < kTileBatch ? ncand - b0 : kTileBatch;
+    const int total = nrun + nb * kRows;             // >= 128 > k
+    uint32_t c[kTileSel];
+#pragma unroll
+    for (int e = 0; e < kTileSel; ++e) {
+      const int j = tid + kTopkThreads * e;
+      uint32_t key = 0u;
+      if (j < nrun) {
+        key = sm.run_key[j];
+      } else if (j < total) {
+        const int q = j - nrun;
+        key = order_key16(__ushort_as_half(row[(int)sm.cand[b0 + (q >> 7)] * kRows + (q & (kRows - 1))]));
+      }
+      c[e] = (key << 16) | (0xffffu - (uint32_t)j);
+    }
+    select_regs(c, total > tid ? (total - 1 - tid) / kTopkThreads + 1 : 0, k, sm.s);
+    if (tid < k) {
+      const uint32_t comp = sm.s.sel[tid];
+      const int j = 0xffff - (int)(comp & 0xffffu);
+      uint16_t v;
+      int g;
+      if (j < nrun) {
+        v = sm.run_val[j];
+        g = sm.run_idx[j];
+      } else {
+        const int q = j - nrun;
+        g = (int)sm.cand[b0 + (q >> 7)] * kRows + (q & (kRows - 1));
+        v = row[g];
+      }
+      int r = 0;                                     // rank by list position = by index
+      for (int b = 0; b < k; ++b) r += (0xffff - (int)(sm.s.sel[b] & 0xffffu)) < j;
+      sm.nxt_key[r] = comp >> 16;
+      sm.nxt_val[r] = v;
+      sm.nxt_idx[r] = g;
+    }
+    __syncthreads();
+    if (tid < k) {
+      sm.run_key[tid] = sm.nxt_key[tid];
+      sm.run_val[tid] = sm.nxt_val[tid];
+      sm.run_idx[tid] = sm.nxt_idx[tid];
+    }
+    nrun = k;
+    __syncthreads();
+  }
+
+  // ---- 4. largest first (winners in index order: position breaks ties)
+  if (tid < k) sm.s.sel[tid] = (sm.run_key[tid] << 16) | (0xffffu - (uint32_t)tid);
+  __syncthreads();
+  if (tid < k) {
+    const int r = rank_of(sm.s.sel, k, tid);
+    vals[(size_t)m * k + r] = sm.run_val[tid];
+    idx[(size_t)m * k + r] = sm.run_idx[tid];
+  }
+}
+
+cudaError_t launch_topk_tiles(const uint16_t *y, int M, int N, int k, uint32_t *tile_max, uint16_t *vals,
+                              int32_t *idx, cudaStream_t st) {
+  cudaError_t e = launch_pdl(reinterpret_cast<const void *>(topk_tiles_kernel), dim3(M), dim3(kTopkThreads), 0,
+                             st, y, N, k, tile_max, vals, idx);
+  count_launch();
+  return e;
 }
 
 TopkPlan topk_plan(int M, int N, int k) {

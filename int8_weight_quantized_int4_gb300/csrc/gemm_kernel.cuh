@@ -551,7 +551,10 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
             } else {
               const int m = m0 + cc + j;
               const float val = kBatchScales ? acc * sj : TOKSCALE ? acc * __ldg(a.xs + m) : acc;
-              a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
+              const __half hv = __float2half_rn(val);
+              a.y[(size_t)m * P.N + n] = __half_as_ushort(hv);
+              // the warp holds 32 rows of column m of tile t
+              if (a.tile_max) tile_max_warp(a.tile_max + (size_t)m * P.T + t, order_key16(hv));
             }
           }
         }
@@ -598,7 +601,9 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
       const int nseg = pl - pf + 1;
       auto put = [&](int m, float acc) {
         const float val = TOKSCALE ? acc * __ldg(a.xs + m) : acc;
-        a.y[(size_t)m * P.N + n] = __half_as_ushort(__float2half_rn(val));
+        const __half hv = __float2half_rn(val);
+        a.y[(size_t)m * P.N + n] = __half_as_ushort(hv);
+        if (a.tile_max) tile_max_warp(a.tile_max + (size_t)m * P.T + t, order_key16(hv));   // whole warps call
       };
       if constexpr (TOKSCALE)  // warm L1 with this tile's token scales
         for (int m = m0 + row; m < m0 + mv; m += kRows) prefetch_l1(a.xs + m);

@@ -118,6 +118,7 @@ template <int NT8, int AMODE, int RBW>
 __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_constant__ GemmArgs a) {
   constexpr bool ACT8 = AMODE == kActI8;
   constexpr bool QIN = AMODE == kActQuant;
+  constexpr bool kTileMax = AMODE == kActF16;           // the lm_head's fused top-k is W4A16
   static_assert(RBW == 2 || RBW == 4, "16-row blocks per warp in a chunk");
   constexpr int KS = 1;                                 // accumulator sets per row block
   constexpr int TW = 8 / RBW;                           // warps per team (a chunk has 8 row blocks)
@@ -492,6 +493,9 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
       tile_coords(P, sg.tile, u, t);
       float *part = sg.slot >= 0 ? a.partials + (size_t)sg.slot * PB : nullptr;
       if (tm == 0 && !aborted) {
+        uint32_t tk[NT8][2];                        // lm_head top-k: largest key per token
+#pragma unroll
+        for (int jt = 0; jt < NT8; ++jt) tk[jt][0] = tk[jt][1] = 0u;
 #pragma unroll
         for (int r = 0; r < RBW; ++r) {
           const int R = 16 * (RBW * wi + r) + g8;
@@ -504,12 +508,30 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
                 float v = acc[r][jt][e];
 #pragma unroll
                 for (int q = 0; q < TEAMS - 1; ++q) v += red[q * (BNX * S) + m * S + row];
-                if (part) part[m * kRows + row] = v;
-                else a.y[(size_t)m * P.N + t * kRows + row] = __half_as_ushort(__float2half_rn(
-                    QIN ? v * qsc[m] : ACT8 ? v * __ldg(a.xs + m) : v));
+                if (part) {
+                  part[m * kRows + row] = v;
+                } else {
+                  const __half hv = __float2half_rn(QIN ? v * qsc[m] : ACT8 ? v * __ldg(a.xs + m) : v);
+                  a.y[(size_t)m * P.N + t * kRows + row] = __half_as_ushort(hv);
+                  if constexpr (kTileMax) tk[jt][e & 1] = max(tk[jt][e & 1], order_key16(hv));
+                }
               }
             }
           }
+        }
+        if (kTileMax && a.tile_max && !part) {
+          // the eight lanes of a column (g8) hold the warp's rows of the same tokens
+#pragma unroll
+          for (int jt = 0; jt < NT8; ++jt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t k = tk[jt][h];
+              k = max(k, __shfl_xor_sync(0xffffffffu, k, 4));
+              k = max(k, __shfl_xor_sync(0xffffffffu, k, 8));
+              k = max(k, __shfl_xor_sync(0xffffffffu, k, 16));
+              const int m = 8 * jt + 2 * c4 + h;
+              if (g8 == 0 && m < P.M) atomicMax(a.tile_max + (size_t)m * P.T + t, k);
+            }
         }
       }
       // the buffer is free again, and every partial store precedes the publish below
@@ -554,8 +576,12 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
           for (int pp = 0; pp < 4; ++pp)
             if (p0 + pp <= pl) v += x[pp];
         }
-        a.y[(size_t)m * P.N + t * kRows + row] =
-            __half_as_ushort(__float2half_rn(QIN ? v * qsc[m] : ACT8 ? v * __ldg(a.xs + m) : v));
+        const __half hv = __float2half_rn(QIN ? v * qsc[m] : ACT8 ? v * __ldg(a.xs + m) : v);
+        a.y[(size_t)m * P.N + t * kRows + row] = __half_as_ushort(hv);
+        // a warp's 32 consecutive idx are 32 rows of one token (kCThreads and kRows are
+        // multiples of 32), and whole warps run this loop
+        if constexpr (kTileMax)
+          if (a.tile_max) tile_max_warp(a.tile_max + (size_t)m * P.T + t, order_key16(hv));
       }
     }
   }

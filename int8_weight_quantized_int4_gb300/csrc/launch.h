@@ -22,6 +22,9 @@ struct GemmArgs {
   int *err;                 // device error word
   int early_weights;        // weights may be streamed before the preceding kernel ends
   unsigned long long wait_ns;   // time limit of a pipeline wait (QW_OPT_WAIT_LIMIT_US)
+  uint32_t *tile_max;       // lm_head with top-k: [M][N/128] the largest order key of each
+                            // token's outputs in each 128-row tile (raised with atomicMax),
+                            // or nullptr
 };
 
 void count_launch();
@@ -72,6 +75,10 @@ cudaError_t launch_embed_gather(const int32_t *ids, int T, const void *packed, i
                                 uint16_t *out, int *err, cudaStream_t st);
 cudaError_t launch_topk(const uint16_t *logits, int M, int N, int k, uint16_t *vals, int32_t *idx,
                         void *ws, cudaStream_t st);
+// lm_head with top-k: the k best of each row of y [M, N] from the GEMM's tile maxima
+// (tile_max [M][N/128], cleared on the way)
+cudaError_t launch_topk_tiles(const uint16_t *y, int M, int N, int k, uint32_t *tile_max, uint16_t *vals,
+                              int32_t *idx, cudaStream_t st);
 
 cudaError_t launch_gemm_w4a16(const GemmArgs &a, cudaStream_t st);
 cudaError_t launch_gemm_w4a8(const GemmArgs &a, cudaStream_t st);

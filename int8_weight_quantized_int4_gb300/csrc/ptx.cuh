@@ -244,6 +244,29 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
+// ---------------------------------------------------------- top-k order --
+// Order key of an fp16 value: a 16-bit integer in the values' order, -0 taken as +0
+// (x + 0 is exact for every other value): a negative value's bits inverted, a
+// non-negative value's sign bit set.  No finite value maps to 0.
+__device__ __forceinline__ uint32_t order_key16(__half h) {
+  const uint32_t x = __half_as_ushort(__hadd(h, __ushort_as_half((unsigned short)0)));
+  return x ^ ((x & 0x8000u) ? 0xffffu : 0x8000u);
+}
+// The same for the two fp16 values of a word (low half = the lower position).
+__device__ __forceinline__ uint32_t order_keys2(uint32_t w) {
+  __half2 h = *reinterpret_cast<const __half2 *>(&w);
+  h = __hadd2(h, __float2half2_rn(0.0f));
+  const uint32_t x = *reinterpret_cast<const uint32_t *>(&h);
+  const uint32_t s = (x >> 15) & 0x00010001u;     // the two sign bits, at bits 0 and 16
+  return x ^ (s * 0x7fffu + 0x80008000u);         // 0xffff or 0x8000 per half
+}
+// Whole warp, one value per lane, all for the same (token, row tile): raise the tile's
+// recorded maximum to the warp's largest key.
+__device__ __forceinline__ void tile_max_warp(uint32_t *dst, uint32_t key) {
+  const uint32_t r = __reduce_max_sync(0xffffffffu, key);
+  if ((threadIdx.x & 31) == 0) atomicMax(dst, r);
+}
+
 // --------------------------------------------------------------- tcgen05 --
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),

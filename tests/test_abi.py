@@ -145,6 +145,27 @@ def test_no_device_reports_arch():
     assert L.qgemm_workspace_bytes(0, 4, 512, 256) == 0
 
 
+def test_lm_head_topk_argument_checks():
+    """Host-side rules of qgemm_lm_head_topk, checked before any device work."""
+    L = q.lib()
+    n = ctypes.c_void_p(0)
+    B = ctypes.c_size_t(1 << 30)
+
+    def call(mode, M, N, K, k, vals=FAKE, idx=FAKE):
+        return L.qgemm_lm_head_topk(mode, FAKE, FAKE, M, N, K, k, FAKE, vals, idx, FAKE, B, n)
+    assert call(q.MODE_W4A8, 4, 1024, 256, 8) == q.QW_ERR_INVALID_ARG       # modes W4A16, W8A16 only
+    assert call(q.MODE_W4A8_FUSED, 4, 1024, 256, 8) == q.QW_ERR_INVALID_ARG
+    assert call(q.MODE_W4A16, 4, 1024, 256, 0) == q.QW_ERR_INVALID_ARG
+    assert call(q.MODE_W4A16, 4, 1024, 256, 65) == q.QW_ERR_INVALID_ARG      # k <= 64
+    assert call(q.MODE_W4A16, 4, 262144 + 128, 256, 8) == q.QW_ERR_UNSUPPORTED_SHAPE
+    assert call(q.MODE_W4A16, 4, 1000, 256, 8) == q.QW_ERR_UNSUPPORTED_SHAPE  # N % 128
+    assert call(q.MODE_W4A16, 0, 1024, 256, 8) == q.QW_OK                      # empty
+    assert call(q.MODE_W4A16, 4, 1024, 256, 8, vals=n) == q.QW_ERR_INVALID_ARG
+    assert call(q.MODE_W4A16, 4, 1024, 256, 8, idx=ctypes.c_void_p((1 << 20) + 2)) == q.QW_ERR_ALIGNMENT
+    assert L.qgemm_lm_head_topk_workspace_bytes(q.MODE_W4A8, 4, 1024, 256, 8) == 0
+    assert L.qgemm_lm_head_topk_workspace_bytes(q.MODE_W4A16, 4, 1024, 256, 65) == 0
+
+
 SHAPES = [
     (0, 4, 512, 256, 152), (1, 1, 5120, 5120, 152), (0, 64, 5120, 5120, 152),
     (1, 64, 34816, 5120, 152), (1, 64, 5120, 17408, 152), (0, 8192, 34816, 5120, 152),
