@@ -211,14 +211,50 @@ int topk_logits(const uint16_t *logits, int M, int N, int k, uint16_t *vals, int
  *   ws: qgemm_lm_head_topk_workspace_bytes(mode, M, N, K, k) bytes, 256-byte
  *   aligned, zero-filled once; the first ..._workspace_zero_bytes stay zero
  *   after every call that returns QW_OK (zero-fill again after QW_ERR_TIMEOUT).
- * Two launches, async.  Returns as qgemm_w4a16, or QW_ERR_INVALID_ARG for another
- * mode or k.
+ * The GEMM runs on slices of at most 64 tokens (one launch each, the weights
+ * read once per slice), then the selection: async.  Returns as qgemm_w4a16, or
+ * QW_ERR_INVALID_ARG for another mode or k.
  * ------------------------------------------------------------------------ */
 size_t qgemm_lm_head_topk_workspace_bytes(int mode, int M, int N, int K, int k);
 size_t qgemm_lm_head_topk_workspace_zero_bytes(int mode, int M, int N, int K, int k);
 int qgemm_lm_head_topk(int mode, const uint16_t *x, const void *packed, int M, int N, int K, int k,
                        uint16_t *y, uint16_t *vals, int32_t *idx, void *ws, size_t ws_bytes,
                        qw_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * attn_int8qk_prefill -- causal prefill attention with the scores computed from
+ * int8 codes ("What this repo does that stock vLLM doesn't", paragraph "int8-QK
+ * prefill attention"):
+ *   1. K is smoothed by its per-head channel mean over the S keys (exact
+ *      binary64 sum / S, rounded to binary32; K' = fp32(k - mean));
+ *   2. every row of K' (one key of one KV head) and of Q (one query of one
+ *      head) becomes int8 codes and a binary32 scale: s = amax / 127 (IEEE
+ *      divide), code = round-half-to-even(x / s), s = 0 and codes 0 for a zero
+ *      row -- the activation quantizer's arithmetic;
+ *   3. score[i][j] = (sum_c qcode[i][c] kcode[j][c]) * sq[i] * sk[j] / sqrt(d),
+ *      the integer dot products exact on the tensor cores;
+ *   4. causal: the T queries are the last T positions of the S-token context
+ *      (query i at position S - T + i sees keys 0 .. S - T + i);
+ *   5. softmax, then P . V with P in fp16 and fp32 accumulation; out fp16.
+ * Query head h reads KV head h / (Hq / Hkv).
+ *   q [T][Hq][d], k and v [S][Hkv][d], out [T][Hq][d]: fp16, device, 16-byte
+ *   aligned.  d = 256 (the head dimension of the pages' model); T and S
+ *   multiples of 128 with T <= S <= 65536; Hkv divides Hq (<= 1024).  The
+ *   channel means are bit-exact for S <= 8192.
+ *   ws: attn_int8qk_workspace_bytes(...) bytes, 256-byte aligned, no zeroing
+ *   needed.  attn_int8qk_workspace_layout fills offsets[0..5] with the byte
+ *   offsets in ws of the query codes ([Hq][T][d] fp16 holding the int8 codes),
+ *   query scales ([Hq][T] binary32), key codes ([Hkv][S][d] fp16), key scales
+ *   ([Hkv][S] binary32), V^T ([Hkv][d][S] fp16) and the total size; they hold
+ *   the call's intermediate results afterwards.
+ * Three launches, async.  Returns QW_OK, QW_ERR_INVALID_ARG,
+ * QW_ERR_UNSUPPORTED_SHAPE, QW_ERR_ALIGNMENT, QW_ERR_WORKSPACE, QW_ERR_ARCH or
+ * QW_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+size_t attn_int8qk_workspace_bytes(int T, int S, int Hq, int Hkv, int d);
+int attn_int8qk_workspace_layout(int T, int S, int Hq, int Hkv, int d, size_t *offsets);
+int attn_int8qk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int T, int S, int Hq,
+                        int Hkv, int d, uint16_t *out, void *ws, size_t ws_bytes, qw_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * qgemm_w4a8_fused -- the W4A8 layer from fp16 activations: y is bit-identical

@@ -65,6 +65,9 @@ SIGNATURES = {
     "qgemm_lm_head_topk_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "qgemm_lm_head_topk_workspace_zero_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "qgemm_lm_head_topk": (_i, [_i, _p, _p, _i, _i, _i, _i, _p, _p, _p, _p, _sz, _p]),
+    "attn_int8qk_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "attn_int8qk_workspace_layout": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_size_t)]),
+    "attn_int8qk_prefill": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _sz, _p]),
     "qw_last_error_string": (ctypes.c_char_p, []),
     "qw_device_error": (_i, [_p]),
     "qw_num_kernel_launches": (_ll, []),
@@ -333,6 +336,45 @@ def embed_gather_w8(ids, packed, V: int, D: int, out=None):
     with torch.cuda.device(ids.device):
         _check(lib().embed_gather_w8(_ptr(ids), T, _ptr(packed), V, D, _ptr(out), _stream(ids)))
     return out
+
+
+def attn_int8qk_prefill(q, k, v, out=None, ws: Workspace | None = None):
+    """int8-QK causal prefill attention: q [T,Hq,d], k and v [S,Hkv,d] fp16 on the device
+    (the T queries are the context's last T positions) -> out [T,Hq,d] fp16."""
+    _need(q, torch.float16, "q", 3)
+    _need(k, torch.float16, "k", 3)
+    _need(v, torch.float16, "v", 3)
+    T, Hq, d = q.shape
+    S, Hkv, dk = k.shape
+    if dk != d or tuple(v.shape) != (S, Hkv, d):
+        raise ValueError("k and v must be [S, Hkv, d] with q's d")
+    if out is None:
+        out = torch.empty((T, Hq, d), dtype=torch.float16, device=q.device)
+    _need(out, torch.float16, "out", 3)
+    _need_shape(out, (T, Hq, d), "out")
+    if ws is None:
+        key = (q.device, torch.cuda.current_stream(q.device).cuda_stream, "attn")
+        ws = _default_ws.setdefault(key, Workspace(q.device))
+    with torch.cuda.device(q.device):
+        wbuf, wbytes = ws.get_bytes(int(lib().attn_int8qk_workspace_bytes(T, S, Hq, Hkv, d)))
+        _check(lib().attn_int8qk_prefill(_ptr(q), _ptr(k), _ptr(v), T, S, Hq, Hkv, d, _ptr(out), _ptr(wbuf),
+                                         wbytes, _stream(q)))
+    return out
+
+
+def attn_int8qk_intermediates(ws: Workspace, T: int, S: int, Hq: int, Hkv: int, d: int = 256):
+    """Views into the workspace of the last attn_int8qk_prefill call with these sizes:
+    (query codes [Hq,T,d], query scales [Hq,T], key codes [Hkv,S,d], key scales [Hkv,S],
+    V^T [Hkv,d,S]); codes as fp16 tensors holding the int8 values."""
+    off = (ctypes.c_size_t * 6)()
+    _check(lib().attn_int8qk_workspace_layout(T, S, Hq, Hkv, d, off))
+    b = ws.buf
+
+    def view(o, n, dt, shape):
+        return b[o:o + n * torch.tensor([], dtype=dt).element_size()].view(dt).view(shape)
+    return (view(off[0], Hq * T * d, torch.float16, (Hq, T, d)), view(off[1], Hq * T, torch.float32, (Hq, T)),
+            view(off[2], Hkv * S * d, torch.float16, (Hkv, S, d)), view(off[3], Hkv * S, torch.float32, (Hkv, S)),
+            view(off[4], Hkv * d * S, torch.float16, (Hkv, d, S)))
 
 
 _topk_ws = {}

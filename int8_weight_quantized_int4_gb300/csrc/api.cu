@@ -395,7 +395,8 @@ int qgemm_w8a16(const uint16_t *x, const void *packed_w8, int M, int N, int K, u
   return gemm_common(QW_MODE_W8A16, x, nullptr, packed_w8, M, N, K, y, ws, ws_bytes, stream);
 }
 
-// ---- lm_head with top-k: workspace = [tile maxima M x N/128 uint32, zero][GEMM workspace]
+// ---- lm_head with top-k: workspace = [tile maxima M x N/128 uint32 | row counters M]
+// (zero) [GEMM workspace] [selection pairs]
 static int lm_head_topk_shape(int mode, int M, int N, int K, int k) {
   if (mode != QW_MODE_W4A16 && mode != QW_MODE_W8A16)
     return fail(QW_ERR_INVALID_ARG, "mode %d: the lm_head with top-k takes QW_MODE_W4A16 or QW_MODE_W8A16", mode);
@@ -405,16 +406,23 @@ static int lm_head_topk_shape(int mode, int M, int N, int K, int k) {
   if (k < 1 || k > 64 || k > N) return fail(QW_ERR_INVALID_ARG, "k=%d outside 1..min(64, N)", k);
   return QW_OK;
 }
-static size_t lm_head_tile_bytes(int M, int N) { return qw::align_up((size_t)M * (N / 128) * 4, 256); }
+static size_t lm_head_tile_bytes(int M, int N) {
+  return qw::align_up((size_t)M * (N / 128) * 4, 256) + qw::align_up((size_t)M * 4, 256);
+}
+
+// the GEMM runs on slices of at most 64 tokens (token tiles the tile-maxima epilogue has)
+constexpr int kLmHeadSlice = 64;
 
 size_t qgemm_lm_head_topk_workspace_bytes(int mode, int M, int N, int K, int k) {
   if (lm_head_topk_shape(mode, M, N, K, k)) return 0;
-  return lm_head_tile_bytes(M, N) + qgemm_workspace_bytes(mode, M, N, K);
+  return lm_head_tile_bytes(M, N) +
+         qw::align_up(qgemm_workspace_bytes(mode, M < kLmHeadSlice ? M : kLmHeadSlice, N, K), 256) +
+         qw::topk_tiles_pair_bytes(M);
 }
 
 size_t qgemm_lm_head_topk_workspace_zero_bytes(int mode, int M, int N, int K, int k) {
   if (lm_head_topk_shape(mode, M, N, K, k)) return 0;
-  return lm_head_tile_bytes(M, N) + qgemm_workspace_zero_bytes(mode, M, N, K);
+  return lm_head_tile_bytes(M, N) + qgemm_workspace_zero_bytes(mode, M < kLmHeadSlice ? M : kLmHeadSlice, N, K);
 }
 
 int qgemm_lm_head_topk(int mode, const uint16_t *x, const void *packed, int M, int N, int K, int k, uint16_t *y,
@@ -426,15 +434,118 @@ int qgemm_lm_head_topk(int mode, const uint16_t *x, const void *packed, int M, i
   if (!aligned(vals, 2) || !aligned(idx, 4) || (ws && !aligned(ws, 256)))
     return fail(QW_ERR_ALIGNMENT, "vals 2-byte, idx 4-byte and the workspace 256-byte aligned");
   const size_t tb = lm_head_tile_bytes(M, N);
-  const size_t need = tb + qgemm_workspace_bytes(mode, M, N, K);
+  const size_t gb = qw::align_up(qgemm_workspace_bytes(mode, M < kLmHeadSlice ? M : kLmHeadSlice, N, K), 256);
+  const size_t need = tb + gb + qw::topk_tiles_pair_bytes(M);
   if (!ws || ws_bytes < need)
     return fail(QW_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws ? ws_bytes : (size_t)0);
-  uint32_t *tile_max = static_cast<uint32_t *>(ws);
-  rc = gemm_common(mode, x, nullptr, packed, M, N, K, y, static_cast<uint8_t *>(ws) + tb, ws_bytes - tb, stream,
-                   tile_max);
-  if (rc) return rc;
-  cudaError_t e = qw::launch_topk_tiles(y, M, N, k, tile_max, vals, idx, reinterpret_cast<cudaStream_t>(stream));
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  uint32_t *tile_max = reinterpret_cast<uint32_t *>(w);
+  int *counters = reinterpret_cast<int *>(w + qw::align_up((size_t)M * (N / 128) * 4, 256));
+  for (int m0 = 0; m0 < M; m0 += kLmHeadSlice) {
+    const int ms = M - m0 < kLmHeadSlice ? M - m0 : kLmHeadSlice;
+    rc = gemm_common(mode, x + (size_t)m0 * K, nullptr, packed, ms, N, K, y + (size_t)m0 * N, w + tb, gb, stream,
+                     tile_max + (size_t)m0 * (N / 128));
+    if (rc) return rc;
+  }
+  cudaError_t e = qw::launch_topk_tiles(y, M, N, k, tile_max, counters,
+                                        reinterpret_cast<unsigned long long *>(w + tb + gb), vals, idx,
+                                        reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "top-k kernel launch");
+  return QW_OK;
+}
+
+// ---- int8-QK causal prefill attention
+struct AttnWs {
+  size_t part, qc, qs, kc, ks, vt, total;
+};
+static AttnWs attn_ws(int T, int S, int Hq, int Hkv) {
+  AttnWs w{};
+  size_t o = 0;
+  auto take = [&](size_t n) {
+    const size_t r = o;
+    o += qw::align_up(n, 256);
+    return r;
+  };
+  const size_t d = qw::kAttnD;
+  w.part = take((size_t)(S / qw::kAttnBlk) * Hkv * d * 8);
+  w.qc = take((size_t)Hq * T * d * 2);
+  w.qs = take((size_t)Hq * T * 4);
+  w.kc = take((size_t)Hkv * S * d * 2);
+  w.ks = take((size_t)Hkv * S * 4);
+  w.vt = take((size_t)Hkv * d * S * 2);
+  w.total = o;
+  return w;
+}
+static int attn_shape(int T, int S, int Hq, int Hkv, int d) {
+  if (T < 0 || S < 0 || Hq < 1 || Hkv < 1) return fail(QW_ERR_INVALID_ARG, "bad size (T=%d S=%d Hq=%d Hkv=%d)", T, S, Hq, Hkv);
+  if (d != qw::kAttnD) return fail(QW_ERR_UNSUPPORTED_SHAPE, "head_dim %d: only %d", d, qw::kAttnD);
+  if (T % qw::kAttnBlk || S % qw::kAttnBlk || T > S || S > 65536 || Hq % Hkv || Hq > 1024)
+    return fail(QW_ERR_UNSUPPORTED_SHAPE,
+                "T and S must be multiples of %d with T <= S <= 65536, Hkv must divide Hq <= 1024 "
+                "(T=%d S=%d Hq=%d Hkv=%d)", qw::kAttnBlk, T, S, Hq, Hkv);
+  return QW_OK;
+}
+
+size_t attn_int8qk_workspace_bytes(int T, int S, int Hq, int Hkv, int d) {
+  if (attn_shape(T, S, Hq, Hkv, d) || T == 0) return 0;
+  return attn_ws(T, S, Hq, Hkv).total;
+}
+
+int attn_int8qk_workspace_layout(int T, int S, int Hq, int Hkv, int d, size_t *offsets) {
+  int rc = attn_shape(T, S, Hq, Hkv, d);
+  if (rc) return rc;
+  if (!offsets) return fail(QW_ERR_INVALID_ARG, "null output");
+  const AttnWs w = attn_ws(T, S, Hq, Hkv);
+  offsets[0] = w.qc;
+  offsets[1] = w.qs;
+  offsets[2] = w.kc;
+  offsets[3] = w.ks;
+  offsets[4] = w.vt;
+  offsets[5] = w.total;
+  return QW_OK;
+}
+
+int attn_int8qk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int T, int S, int Hq, int Hkv,
+                        int d, uint16_t *out, void *ws, size_t ws_bytes, qw_stream_t stream) {
+  int rc = attn_shape(T, S, Hq, Hkv, d);
+  if (rc) return rc;
+  if (T == 0) return QW_OK;
+  if (!q || !k || !v || !out) return fail(QW_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || (ws && !aligned(ws, 256)))
+    return fail(QW_ERR_ALIGNMENT, "q, k, v and out must be 16-byte aligned, the workspace 256-byte aligned");
+  const AttnWs w = attn_ws(T, S, Hq, Hkv);
+  if (!ws || ws_bytes < w.total)
+    return fail(QW_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", w.total, ws ? ws_bytes : (size_t)0);
+  DevInfo *dv = nullptr;
+  if ((rc = current_device(dv))) return rc;
+  if ((int)qw::attn_fwd_smem_bytes() > dv->smem_optin)
+    return fail(QW_ERR_UNSUPPORTED_SHAPE, "attention needs %zu B of shared memory, device has %d",
+                qw::attn_fwd_smem_bytes(), dv->smem_optin);
+  uint8_t *b = static_cast<uint8_t *>(ws);
+  qw::AttnLaunch L{};
+  L.q = q;
+  L.k = k;
+  L.v = v;
+  L.out = out;
+  L.T = T;
+  L.S = S;
+  L.Hq = Hq;
+  L.Hkv = Hkv;
+  L.part = reinterpret_cast<long long *>(b + w.part);
+  L.qc = reinterpret_cast<uint16_t *>(b + w.qc);
+  L.qs = reinterpret_cast<float *>(b + w.qs);
+  L.kc = reinterpret_cast<uint16_t *>(b + w.kc);
+  L.ks = reinterpret_cast<float *>(b + w.ks);
+  L.vt = reinterpret_cast<uint16_t *>(b + w.vt);
+  // 128-byte-swizzled boxes: Qc and Kc rows of 256 as four 64-wide slabs of 128 rows;
+  // V^T rows of S keys as two 64-key slabs of 256 rows
+  if ((rc = encode_act_map(&L.tq, L.qc, Hq * T, qw::kAttnD, qw::kAttnBlk, 2, false))) return rc;
+  if ((rc = encode_act_map(&L.tk, L.kc, Hkv * S, qw::kAttnD, qw::kAttnBlk, 2, false))) return rc;
+  if ((rc = encode_act_map(&L.tv, L.vt, Hkv * qw::kAttnD, S, qw::kAttnD, 1, false))) return rc;
+  L.err = dv->err;
+  L.wait_ns = 1000ull * (unsigned long long)g_opt_wait_limit_us.load(std::memory_order_relaxed);
+  cudaError_t e = qw::launch_attn(L, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "attention kernel launch");
   return QW_OK;
 }
 

@@ -335,149 +335,298 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const uint16_t *_
 // the logits, the largest order key among the tile's outputs (tile_max[m][t]).  With
 // t_k the k-th largest of those maxima, at least k logits are >= t_k (one per tile of
 // the k best), so every logit of the top k lies in a tile whose maximum is >= t_k: the
-// candidate tiles, exactly k of them unless maxima tie.  One CTA per token:
-//   1. the k largest tile maxima (radix selection over composites key << 16 | 0xffff - t)
-//      give t_k; with at most k tiles every tile is a candidate;
-//   2. the candidate tiles are listed in ascending order (per-warp ballots);
-//   3. the k largest logits of the candidate tiles are selected kTileBatch tiles at a
-//      time, the winners so far (all at smaller indices than the batch) listed first in
-//      index order, so that list positions follow the indices and the composites
-//      key << 16 | 0xffff - position order ties by the smaller index;
-//   4. the winners are written largest first.
-// The tile maxima are cleared on the way (zero again for the next call).
-constexpr int kTileBatch = 64;
-constexpr int kTileSel = (kTileBatch * kRows + kTopkMaxK + kTopkThreads - 1) / kTopkThreads;   // per thread
-constexpr int kMaxTiles = kTopkMaxN / kRows;
-constexpr int kTilesPer = kMaxTiles / kTopkThreads;                                           // 8
-static_assert(kTileSel * kTopkThreads <= 65536 && kMaxTiles <= 65536, "16-bit list positions");
+// candidate tiles, exactly k of them unless maxima tie.  kTopkSlices CTAs per token:
+//   1. every CTA finds t_k, the k-th largest 16-bit key among the tile maxima (every
+//      tile is a candidate when there are at most k), and lists the candidate tiles in
+//      ascending order (one block-wide scan);
+//   2. CTA s takes its share of the candidate tiles: the k largest of their logits
+//      (T, the k-th largest key, and r, how many keys equal to T are among the k; every
+//      logit above T and the first r equal to it, by warp ballots over consecutive
+//      positions), written to the workspace as (key, index) pairs;
+//   3. the last CTA of the token ranks the slices' pairs by (key descending, index
+//      ascending), writes the first k, and clears the tile maxima and its counter (zero
+//      again for the next call).
+// A k-th largest key is built two bits at a time from the top: the largest prefix with
+// at least k keys at or above it, by block-wide counts over keys held in registers two
+// to a word (SIMD compares; no atomics, which crowd onto a few addresses when the keys
+// of a row are close together).  A share with more logits than the registers hold (many
+// tied tile maxima) is read from global memory instead, in the same order.
+constexpr int kTileThreads = 256;
+constexpr int kTileWarps = kTileThreads / 32;
+constexpr int kMaxTiles = kTopkMaxN / kRows;                   // 2048
+constexpr int kTileWords = kMaxTiles / 2 / kTileThreads;       // 4: tile-maximum key pairs a thread
+constexpr int kStageWords = 8;                                 // logit key pairs a thread, registers
+constexpr int kStageKeys = 2 * kStageWords * kTileThreads;     // 4096 logits (32 tiles) a share
+constexpr int kMergeMax = kTopkSlices * kTopkMaxK;             // pairs the last CTA ranks
 
 struct TileTopkSmem {
-  TopkSmemT<kTileSel * kTopkThreads> s;
+  alignas(16) int cnt[2][4][kTileWarps];
+  int wsum[2][kTileWarps];
+  alignas(16) uint16_t tkey[kMaxTiles];
   uint16_t cand[kMaxTiles];
-  int wcount[kTopkThreads / 32];
-  uint32_t thr;
-  uint32_t run_key[kTopkMaxK], nxt_key[kTopkMaxK];   // winners so far, in index order
-  uint16_t run_val[kTopkMaxK], nxt_val[kTopkMaxK];
-  int run_idx[kTopkMaxK], nxt_idx[kTopkMaxK];
+  alignas(16) uint16_t lkey[kStageKeys];
+  unsigned long long mc[kMergeMax];               // merge: key << 32 | (2^32 - 1 - index)
+  int last;
 };
 
-__global__ void __launch_bounds__(kTopkThreads) topk_tiles_kernel(const uint16_t *__restrict__ y, int N, int k,
-                                                                  uint32_t *tile_max, uint16_t *vals,
+// Block-wide exclusive scan of a pair of counts; the totals in tot.  Two barriers.
+__device__ __forceinline__ int2 block_scan2(int a, int b, int (&wsum)[2][kTileWarps], int2 &tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int ia = a, ib = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ta = __shfl_up_sync(0xffffffffu, ia, o), tb = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) {
+      ia += ta;
+      ib += tb;
+    }
+  }
+  if (lane == 31) {
+    wsum[0][warp] = ia;
+    wsum[1][warp] = ib;
+  }
+  __syncthreads();
+  int pa = 0, pb = 0;
+  tot = make_int2(0, 0);
+#pragma unroll
+  for (int w = 0; w < kTileWarps; ++w) {
+    if (w < warp) {
+      pa += wsum[0][w];
+      pb += wsum[1][w];
+    }
+    tot.x += wsum[0][w];
+    tot.y += wsum[1][w];
+  }
+  __syncthreads();                                    // wsum free for the next scan
+  return make_int2(pa + ia - a, pb + ib - b);
+}
+
+// Block-wide sums of four per-thread counts (one barrier; buffer `buf` of two).
+__device__ __forceinline__ int4 block_sum4(int a, int b, int c, int d, TileTopkSmem &sm, int buf) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = __reduce_add_sync(0xffffffffu, a);
+  b = __reduce_add_sync(0xffffffffu, b);
+  c = __reduce_add_sync(0xffffffffu, c);
+  d = __reduce_add_sync(0xffffffffu, d);
+  if (lane == 0) {
+    sm.cnt[buf][0][warp] = a;
+    sm.cnt[buf][1][warp] = b;
+    sm.cnt[buf][2][warp] = c;
+    sm.cnt[buf][3][warp] = d;
+  }
+  __syncthreads();
+  int4 t = make_int4(0, 0, 0, 0);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int4 u = reinterpret_cast<const int4 *>(sm.cnt[buf][q])[0];
+    const int4 v = reinterpret_cast<const int4 *>(sm.cnt[buf][q])[1];
+    const int sum = u.x + u.y + u.z + u.w + v.x + v.y + v.z + v.w;
+    if (q == 0) t.x = sum;
+    else if (q == 1) t.y = sum;
+    else if (q == 2) t.z = sum;
+    else t.w = sum;
+  }
+  return t;
+}
+
+// How many of the two 16-bit keys of word x are >= c (1 <= c <= 0xffff).
+__device__ __forceinline__ int count_ge2(uint32_t x, uint32_t c) { return __popc(__vcmpgeu2(x, c | (c << 16))) >> 4; }
+
+// The k-th largest of the CTA's keys (k <= their number; padding keys are 0) and, in
+// *ties, how many keys equal to it are among the k largest.  each(f) calls f(word) for
+// every word of two keys this thread holds.  Nine barriers and one at the end.
+template <class Each>
+__device__ uint32_t kth_key16(Each each, int k, TileTopkSmem &sm, int *ties) {
+  uint32_t prefix = 0;
+  int round = 0;
+#pragma unroll 1
+  for (int b = 14; b >= 0; b -= 2, ++round) {
+    const uint32_t c1 = prefix | (1u << b), c2 = prefix | (2u << b), c3 = prefix | (3u << b);
+    int n1 = 0, n2 = 0, n3 = 0;
+    each([&](uint32_t x) {
+      n1 += count_ge2(x, c1);
+      n2 += count_ge2(x, c2);
+      n3 += count_ge2(x, c3);
+    });
+    const int4 t = block_sum4(n1, n2, n3, 0, sm, round & 1);
+    prefix = t.z >= k ? c3 : t.y >= k ? c2 : t.x >= k ? c1 : prefix;
+  }
+  int ngt = 0;
+  if (prefix < 0xffffu) each([&](uint32_t x) { ngt += count_ge2(x, prefix + 1); });
+  *ties = k - block_sum4(ngt, 0, 0, 0, sm, round & 1).x;
+  __syncthreads();                                    // cnt free for the next use
+  return prefix;
+}
+
+__global__ void __launch_bounds__(kTileThreads) topk_tiles_kernel(const uint16_t *__restrict__ y, int N, int k,
+                                                                  uint32_t *tile_max, int *counters,
+                                                                  unsigned long long *pairs, uint16_t *vals,
                                                                   int32_t *idx) {
   __shared__ TileTopkSmem sm;
   griddep_wait();
   griddep_launch_dependents();
-  const int m = blockIdx.x, T = N / kRows;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int sl = blockIdx.x, S = gridDim.x, m = blockIdx.y, T = N / kRows, tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const uint16_t *row = y + (size_t)m * N;
   uint32_t *tmx = tile_max + (size_t)m * T;
 
-  // ---- 1. the tile maxima (tile tid + 256 i in tk[i]), cleared for the next call
-  uint32_t tk[kTilesPer];
+  // ---- 1. the tile maxima (tiles 2 (tid + 256 i) and the next one in word i; loads from
+  // clamped addresses, issued together), t_k, the candidate tiles
+  uint32_t tw[kTileWords];
+  {
+    uint32_t v[2 * kTileWords];
 #pragma unroll
-  for (int i = 0; i < kTilesPer; ++i) {
-    const int t = tid + kTopkThreads * i;
-    tk[i] = t < T ? __ldcg(tmx + t) : 0u;
-  }
+    for (int i = 0; i < kTileWords; ++i) {
+      const int t = 2 * (tid + kTileThreads * i);
+      v[2 * i] = __ldcg(tmx + min(t, T - 1));
+      v[2 * i + 1] = __ldcg(tmx + min(t + 1, T - 1));
+    }
 #pragma unroll
-  for (int i = 0; i < kTilesPer; ++i) {
-    const int t = tid + kTopkThreads * i;
-    if (t < T) tmx[t] = 0u;
-  }
-  if (tid == 0) sm.thr = T > k ? 0xffffffffu : 0u;
-  if (T > k) {
-    uint32_t c[kTilesPer];
-#pragma unroll
-    for (int i = 0; i < kTilesPer; ++i) c[i] = (tk[i] << 16) | (0xffffu - (uint32_t)(tid + kTopkThreads * i));
-    select_regs(c, T > tid ? (T - 1 - tid) / kTopkThreads + 1 : 0, k, sm.s);
-    if (tid < k) atomicMin(&sm.thr, sm.s.sel[tid] >> 16);
+    for (int i = 0; i < kTileWords; ++i) {
+      const int t = 2 * (tid + kTileThreads * i);
+      const uint32_t lo = t < T ? v[2 * i] : 0u, hi = t + 1 < T ? v[2 * i + 1] : 0u;
+      tw[i] = lo | (hi << 16);
+      if (t < T) reinterpret_cast<uint32_t *>(sm.tkey)[t >> 1] = tw[i];
+    }
   }
   __syncthreads();
-  const uint32_t thr = sm.thr;
-
-  // ---- 2. candidate tiles, ascending
-  int ncand = 0;
+  int unused;
+  const uint32_t thr = T > k ? kth_key16([&](auto f) {
 #pragma unroll
-  for (int i = 0; i < kTilesPer; ++i) {
-    if (kTopkThreads * i >= T) break;                // uniform
-    const int t = tid + kTopkThreads * i;
-    const bool flag = t < T && tk[i] >= thr;
-    const unsigned bal = __ballot_sync(0xffffffffu, flag);
-    if (lane == 0) sm.wcount[warp] = __popc(bal);
-    __syncthreads();
-    int off = ncand, tot = 0;
-#pragma unroll
-    for (int w = 0; w < kTopkThreads / 32; ++w) {
-      off += w < warp ? sm.wcount[w] : 0;
-      tot += sm.wcount[w];
-    }
-    if (flag) sm.cand[off + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)t;
-    ncand += tot;
-    __syncthreads();
-  }
-
-  // ---- 3. the k best logits of the candidate tiles, a batch of tiles at a time
-  int nrun = 0;
-  for (int b0 = 0; b0 < ncand; b0 += kTileBatch) {
-    const int nb = ncand - b0 < kTileBatch ? ncand - b0 : kTileBatch;
-    const int total = nrun + nb * kRows;             // >= 128 > k
-    uint32_t c[kTileSel];
-#pragma unroll
-    for (int e = 0; e < kTileSel; ++e) {
-      const int j = tid + kTopkThreads * e;
-      uint32_t key = 0u;
-      if (j < nrun) {
-        key = sm.run_key[j];
-      } else if (j < total) {
-        const int q = j - nrun;
-        key = order_key16(__ushort_as_half(row[(int)sm.cand[b0 + (q >> 7)] * kRows + (q & (kRows - 1))]));
-      }
-      c[e] = (key << 16) | (0xffffu - (uint32_t)j);
-    }
-    select_regs(c, total > tid ? (total - 1 - tid) / kTopkThreads + 1 : 0, k, sm.s);
-    if (tid < k) {
-      const uint32_t comp = sm.s.sel[tid];
-      const int j = 0xffff - (int)(comp & 0xffffu);
-      uint16_t v;
-      int g;
-      if (j < nrun) {
-        v = sm.run_val[j];
-        g = sm.run_idx[j];
-      } else {
-        const int q = j - nrun;
-        g = (int)sm.cand[b0 + (q >> 7)] * kRows + (q & (kRows - 1));
-        v = row[g];
-      }
-      int r = 0;                                     // rank by list position = by index
-      for (int b = 0; b < k; ++b) r += (0xffff - (int)(sm.s.sel[b] & 0xffffu)) < j;
-      sm.nxt_key[r] = comp >> 16;
-      sm.nxt_val[r] = v;
-      sm.nxt_idx[r] = g;
-    }
-    __syncthreads();
-    if (tid < k) {
-      sm.run_key[tid] = sm.nxt_key[tid];
-      sm.run_val[tid] = sm.nxt_val[tid];
-      sm.run_idx[tid] = sm.nxt_idx[tid];
-    }
-    nrun = k;
-    __syncthreads();
-  }
-
-  // ---- 4. largest first (winners in index order: position breaks ties)
-  if (tid < k) sm.s.sel[tid] = (sm.run_key[tid] << 16) | (0xffffu - (uint32_t)tid);
+    for (int i = 0; i < kTileWords; ++i) f(tw[i]);
+  }, k, sm, &unused) : 1u;
+  const int tp = (T + kTileThreads - 1) / kTileThreads;
+  int nmine = 0;
+  for (int t = tp * tid; t < tp * tid + tp && t < T; ++t) nmine += sm.tkey[t] >= thr;
+  int2 tot;
+  int pos = block_scan2(nmine, 0, sm.wsum, tot).x;
+  for (int t = tp * tid; t < tp * tid + tp && t < T; ++t)
+    if (sm.tkey[t] >= thr) sm.cand[pos++] = (uint16_t)t;
+  const int ncand = tot.x;
   __syncthreads();
-  if (tid < k) {
-    const int r = rank_of(sm.s.sel, k, tid);
-    vals[(size_t)m * k + r] = sm.run_val[tid];
-    idx[(size_t)m * k + r] = sm.run_idx[tid];
+
+  // ---- 2. this slice's candidate tiles [c0, c1): position j = 128 (c - c0) + row
+  const int c0 = (int)((long long)ncand * sl / S), c1 = (int)((long long)ncand * (sl + 1) / S);
+  const int n = (c1 - c0) * kRows;                     // 0 or >= 128 > k
+  unsigned long long *out = pairs + ((size_t)m * S + sl) * kTopkMaxK;
+  if (n > 0) {
+    const bool staged = n <= kStageKeys;               // uniform
+    auto raw_at = [&](int j) { return row[(int)sm.cand[c0 + (j >> 7)] * kRows + (j & (kRows - 1))]; };
+    auto key_at = [&](int j) -> uint32_t { return order_key16(__ushort_as_half(raw_at(j))); };
+    uint32_t lw[kStageWords];                          // word i: positions 2 (tid + 256 i), + 1
+    if (staged) {
+      unsigned short v[2 * kStageWords];
+#pragma unroll
+      for (int i = 0; i < kStageWords; ++i) {
+        const int j = 2 * (tid + kTileThreads * i);
+        v[2 * i] = raw_at(min(j, n - 1));
+        v[2 * i + 1] = raw_at(min(j + 1, n - 1));
+      }
+#pragma unroll
+      for (int i = 0; i < kStageWords; ++i) {
+        const int j = 2 * (tid + kTileThreads * i);
+        lw[i] = (j < n ? order_key16(__ushort_as_half(v[2 * i])) : 0u) |
+                ((j + 1 < n ? order_key16(__ushort_as_half(v[2 * i + 1])) : 0u) << 16);
+        if (j < n) reinterpret_cast<uint32_t *>(sm.lkey)[j >> 1] = lw[i];
+      }
+    }
+    // the classification below reads the staged keys by position (each barrier of the
+    // selection orders these stores before it)
+    int r;
+    uint32_t tkey;
+    if (staged) {
+      tkey = kth_key16([&](auto f) {
+#pragma unroll
+        for (int i = 0; i < kStageWords; ++i) f(lw[i]);
+      }, k, sm, &r);
+    } else {
+      tkey = kth_key16([&](auto f) {
+        for (int j = 2 * tid; j < n; j += 2 * kTileThreads) f(key_at(j) | (j + 1 < n ? key_at(j + 1) << 16 : 0u));
+      }, k, sm, &r);
+    }
+    // the k best: every key above T and the first r equal to it; warp w takes positions
+    // [wc w, wc w + wc), lanes consecutive, so (warp, step, lane) is index order
+    auto skey = [&](int j) -> uint32_t { return staged ? (uint32_t)sm.lkey[j] : key_at(j); };
+    const int wc = ((n + kTileWarps - 1) / kTileWarps + 31) / 32 * 32;
+    const int jb = wc * warp, je = min(jb + wc, n);
+    const unsigned lt = (1u << lane) - 1u;
+    int cg = 0, ce = 0;
+    for (int j = jb + lane; j - lane < je; j += 32) {
+      const uint32_t x = j < je ? skey(j) : 0u;
+      cg += __popc(__ballot_sync(0xffffffffu, x > tkey));
+      ce += __popc(__ballot_sync(0xffffffffu, j < je && x == tkey));
+    }
+    if (lane == 0) {
+      sm.wsum[0][warp] = cg;
+      sm.wsum[1][warp] = ce;
+    }
+    __syncthreads();
+    int sg = 0, se = 0;
+#pragma unroll
+    for (int w = 0; w < kTileWarps; ++w)
+      if (w < warp) {
+        sg += sm.wsum[0][w];
+        se += sm.wsum[1][w];
+      }
+    for (int j = jb + lane; j - lane < je; j += 32) {
+      const uint32_t x = j < je ? skey(j) : 0u;
+      const unsigned bg = __ballot_sync(0xffffffffu, x > tkey);
+      const unsigned be = __ballot_sync(0xffffffffu, j < je && x == tkey);
+      int slot = -1;
+      if (x > tkey) slot = sg + __popc(bg & lt);
+      else if (j < je && x == tkey && se + __popc(be & lt) < r) slot = (k - r) + se + __popc(be & lt);
+      if (slot >= 0)
+        out[slot] = ((unsigned long long)x << 32) |
+                    (uint32_t)((int)sm.cand[c0 + (j >> 7)] * kRows + (j & (kRows - 1)));
+      sg += __popc(bg);
+      se += __popc(be);
+    }
+  } else {
+    for (int e = tid; e < k; e += kTileThreads) out[e] = 0ull;   // key 0: below every logit
   }
+
+  // ---- 3. publish; the last slice CTA of the token ranks the pairs and clears up
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int old = atomicAdd(counters + m, 1);
+    sm.last = old == S - 1;
+    if (sm.last) counters[m] = 0;
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();
+  const int total = S * k;
+  const unsigned long long *all = pairs + (size_t)m * S * kTopkMaxK;
+  for (int e = tid; e < total; e += kTileThreads) {
+    const unsigned long long p = __ldcg(all + (size_t)(e / k) * kTopkMaxK + e % k);
+    sm.mc[e] = (p & 0xffffffff00000000ull) | (0xffffffffull - (p & 0xffffffffull));
+  }
+  for (int t = tid; t < T; t += kTileThreads) tmx[t] = 0u;
+  __syncthreads();
+  // a pair's rank: how many pairs come before it (distinct composites; padding keys 0)
+  for (int e = tid; e < total; e += kTileThreads) {
+    const unsigned long long ce = sm.mc[e];
+    int rank = 0;
+#pragma unroll 16
+    for (int b = 0; b < total; ++b) rank += sm.mc[b] > ce;
+    if ((ce >> 32) != 0ull && rank < k) {
+      const int ie = (int)(0xffffffffull - (ce & 0xffffffffull));
+      vals[(size_t)m * k + rank] = row[ie];
+      idx[(size_t)m * k + rank] = ie;
+    }
+  }
+  __syncthreads();
 }
 
-cudaError_t launch_topk_tiles(const uint16_t *y, int M, int N, int k, uint32_t *tile_max, uint16_t *vals,
-                              int32_t *idx, cudaStream_t st) {
-  cudaError_t e = launch_pdl(reinterpret_cast<const void *>(topk_tiles_kernel), dim3(M), dim3(kTopkThreads), 0,
-                             st, y, N, k, tile_max, vals, idx);
+size_t topk_tiles_pair_bytes(int M) { return (size_t)M * kTopkSlices * kTopkMaxK * 8; }
+
+cudaError_t launch_topk_tiles(const uint16_t *y, int M, int N, int k, uint32_t *tile_max, int *counters,
+                              unsigned long long *pairs, uint16_t *vals, int32_t *idx, cudaStream_t st) {
+  // an ordinary launch: started early (programmatic dependent launch), the CTAs would be
+  // placed wherever the GEMM leaves room and share a few SMs after it ends
+  topk_tiles_kernel<<<dim3(kTopkSlices, M), kTileThreads, 0, st>>>(y, N, k, tile_max, counters, pairs, vals, idx);
+  cudaError_t e = cudaGetLastError();
   count_launch();
   return e;
 }

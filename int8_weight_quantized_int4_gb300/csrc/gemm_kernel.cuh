@@ -153,8 +153,10 @@ __device__ __forceinline__ int quant_code(float x, float s, float rs) {
   return max(-127, min(127, (int)qf));
 }
 
-template <int BN, int WBITS, bool TOKSCALE>
+// TMAX: the epilogue also raises the per-tile maxima of the lm_head's fused top-k
+template <int BN, int WBITS, bool TOKSCALE, bool TMAX>
 __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_constant__ GemmArgs a) {
+  static_assert(!TMAX || !TOKSCALE, "the lm_head's fused top-k is W4A16 or W8A16");
   constexpr uint32_t kChunk = WBITS == 8 ? kChunkW8 : kChunkW4;
   constexpr uint32_t kWStage = (kChunk + 127) / 128 * 128;
   static_assert(kChunk % 128 == 0, "weight slots stay 128-byte aligned");
@@ -554,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
               const __half hv = __float2half_rn(val);
               a.y[(size_t)m * P.N + n] = __half_as_ushort(hv);
               // the warp holds 32 rows of column m of tile t
-              if (a.tile_max) tile_max_warp(a.tile_max + (size_t)m * P.T + t, order_key16(hv));
+              if constexpr (TMAX) tile_max_warp(a.tile_max + (size_t)m * P.T + t, order_key16(hv));
             }
           }
         }
@@ -603,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         const float val = TOKSCALE ? acc * __ldg(a.xs + m) : acc;
         const __half hv = __float2half_rn(val);
         a.y[(size_t)m * P.N + n] = __half_as_ushort(hv);
-        if (a.tile_max) tile_max_warp(a.tile_max + (size_t)m * P.T + t, order_key16(hv));   // whole warps call
+        if constexpr (TMAX) tile_max_warp(a.tile_max + (size_t)m * P.T + t, order_key16(hv));   // whole warps call
       };
       if constexpr (TOKSCALE)  // warm L1 with this tile's token scales
         for (int m = m0 + row; m < m0 + mv; m += kRows) prefetch_l1(a.xs + m);

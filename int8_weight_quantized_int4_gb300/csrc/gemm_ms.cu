@@ -5,9 +5,9 @@
 
 namespace qw {
 
-template <int NT8, int AMODE, int RBW = 2>
+template <int NT8, int AMODE, int RBW = 2, bool TMAX = false>
 static cudaError_t run_ms(const GemmArgs &a, cudaStream_t st) {
-  auto *k = qgemm_ms_kernel<NT8, AMODE, RBW>;
+  auto *k = qgemm_ms_kernel<NT8, AMODE, RBW, TMAX>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(k), a.P.smem_bytes);
   if (e != cudaSuccess) return e;
   e = launch_pdl(reinterpret_cast<const void *>(k), dim3(a.P.grid), dim3(ms_threads()),
@@ -24,6 +24,11 @@ cudaError_t launch_gemm_ms(const GemmArgs &a, int act, cudaStream_t st) {
   // the in-kernel quantizer takes at most 4 tokens (the plan's fused rule)
   if (act == kActQuant) return a.P.M <= 4 ? run_ms<1, kActQuant>(a, st) : cudaErrorInvalidValue;
   if (act == kActI8) return one ? run_ms<1, kActI8>(a, st) : run_ms<2, kActI8>(a, st);
+  // the lm_head with top-k: the variant whose epilogue records the tile maxima
+  if (a.tile_max) {
+    if (four) return run_ms<1, kActF16, 4, true>(a, st);
+    return one ? run_ms<1, kActF16, 2, true>(a, st) : run_ms<2, kActF16, 2, true>(a, st);
+  }
   if (four) return run_ms<1, kActF16, 4>(a, st);
   return one ? run_ms<1, kActF16>(a, st) : run_ms<2, kActF16>(a, st);
 }

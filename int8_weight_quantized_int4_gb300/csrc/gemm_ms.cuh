@@ -114,11 +114,13 @@ __device__ __forceinline__ void frag_w4_zp(uint32_t w, uint32_t (&a)[4]) {
   a[3] = lop3_and_or(x, 0x00f000f0u, 0x64006400u);
 }
 
-template <int NT8, int AMODE, int RBW>
+// TMAX: the epilogue also raises the per-tile maxima of the lm_head's fused top-k
+template <int NT8, int AMODE, int RBW, bool TMAX>
 __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_constant__ GemmArgs a) {
   constexpr bool ACT8 = AMODE == kActI8;
   constexpr bool QIN = AMODE == kActQuant;
-  constexpr bool kTileMax = AMODE == kActF16;           // the lm_head's fused top-k is W4A16
+  constexpr bool kTileMax = TMAX;
+  static_assert(!TMAX || AMODE == kActF16, "the lm_head's fused top-k is W4A16");
   static_assert(RBW == 2 || RBW == 4, "16-row blocks per warp in a chunk");
   constexpr int KS = 1;                                 // accumulator sets per row block
   constexpr int TW = 8 / RBW;                           // warps per team (a chunk has 8 row blocks)
@@ -519,7 +521,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
             }
           }
         }
-        if (kTileMax && a.tile_max && !part) {
+        if (kTileMax && !part) {
           // the eight lanes of a column (g8) hold the warp's rows of the same tokens
 #pragma unroll
           for (int jt = 0; jt < NT8; ++jt)
@@ -580,8 +582,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
         a.y[(size_t)m * P.N + t * kRows + row] = __half_as_ushort(hv);
         // a warp's 32 consecutive idx are 32 rows of one token (kCThreads and kRows are
         // multiples of 32), and whole warps run this loop
-        if constexpr (kTileMax)
-          if (a.tile_max) tile_max_warp(a.tile_max + (size_t)m * P.T + t, order_key16(hv));
+        if constexpr (kTileMax) tile_max_warp(a.tile_max + (size_t)m * P.T + t, order_key16(hv));
       }
     }
   }

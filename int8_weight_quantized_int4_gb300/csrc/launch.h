@@ -76,9 +76,29 @@ cudaError_t launch_embed_gather(const int32_t *ids, int T, const void *packed, i
 cudaError_t launch_topk(const uint16_t *logits, int M, int N, int k, uint16_t *vals, int32_t *idx,
                         void *ws, cudaStream_t st);
 // lm_head with top-k: the k best of each row of y [M, N] from the GEMM's tile maxima
-// (tile_max [M][N/128], cleared on the way)
-cudaError_t launch_topk_tiles(const uint16_t *y, int M, int N, int k, uint32_t *tile_max, uint16_t *vals,
-                              int32_t *idx, cudaStream_t st);
+// (tile_max [M][N/128] and counters [M], zero, left zero), kTopkSlices CTAs a row whose
+// (key, index) pairs go through `pairs` (topk_tiles_pair_bytes(M) bytes)
+constexpr int kTopkSlices = 4;
+size_t topk_tiles_pair_bytes(int M);
+cudaError_t launch_topk_tiles(const uint16_t *y, int M, int N, int k, uint32_t *tile_max, int *counters,
+                              unsigned long long *pairs, uint16_t *vals, int32_t *idx, cudaStream_t st);
+
+// int8-QK causal prefill attention (attention.cu): head dimension and block sizes
+constexpr int kAttnD = 256;       // head_dim
+constexpr int kAttnBlk = 128;     // queries per block and keys per block
+struct AttnLaunch {
+  const uint16_t *q, *k, *v;      // [T][Hq][d], [S][Hkv][d], [S][Hkv][d] fp16
+  uint16_t *out;                  // [T][Hq][d] fp16
+  int T, S, Hq, Hkv;
+  long long *part;                // [S/128][Hkv][d] channel partial sums (workspace)
+  uint16_t *qc, *kc, *vt;         // [Hq][T][d], [Hkv][S][d] fp16 codes; [Hkv][d][S] fp16 V^T
+  float *qs, *ks;                 // [Hq][T], [Hkv][S] row scales
+  CUtensorMap tq, tk, tv;         // tensor maps of qc, kc, vt
+  int *err;
+  unsigned long long wait_ns;
+};
+size_t attn_fwd_smem_bytes();
+cudaError_t launch_attn(const AttnLaunch &L, cudaStream_t st);
 
 cudaError_t launch_gemm_w4a16(const GemmArgs &a, cudaStream_t st);
 cudaError_t launch_gemm_w4a8(const GemmArgs &a, cudaStream_t st);

@@ -150,3 +150,16 @@ def token_ids(T: int, V: int, seed: int) -> torch.Tensor:
     if T >= 3:
         ids[0], ids[1], ids[2] = 0, V - 1, ids[T - 1]
     return ids
+
+
+def attention(T: int, S: int, Hq: int, Hkv: int, d: int = 256, seed: int = 60,
+              k_offset_std: float = 4.0):
+    """Prefill attention inputs: q [T, Hq, d], k and v [S, Hkv, d] fp16.  q, v ~ N(0, 1);
+    k ~ N(0, 1) plus a per-(head, channel) offset ~ N(0, k_offset_std) shared by all keys
+    (the channel bias that mean-smoothing removes, "int8-QK prefill attention")."""
+    gen = generator(seed)
+    q = torch.randn((T, Hq, d), generator=gen, dtype=torch.float32)
+    off = k_offset_std * torch.randn((1, Hkv, d), generator=gen, dtype=torch.float32)
+    k = torch.randn((S, Hkv, d), generator=gen, dtype=torch.float32) + off
+    v = torch.randn((S, Hkv, d), generator=gen, dtype=torch.float32)
+    return q.to(torch.float16), k.to(torch.float16), v.to(torch.float16)
