@@ -15,9 +15,10 @@
 //   attn_fwd_kernel  : per (128-query block, query head), over the visible 128-key
 //                      blocks: S = Qc . Kc^T on tcgen05 (kind::f16; the integer dot
 //                      products are exact in fp32, |sum| < 2^24), the online softmax in
-//                      four softmax warps (one query row per thread, TMEM lane = row),
-//                      P as fp16 written into TMEM over S, O += P . V on tcgen05 with P
-//                      from TMEM, O / l at the end.
+//                      two groups of four warps (a query row per thread, TMEM lane =
+//                      row, each group half the keys of a block and half of O), P as
+//                      fp16 written into TMEM over S, O += P . V on tcgen05 with P from
+//                      TMEM, O / l at the end.
 #include <stdint.h>
 #include <cuda_fp16.h>
 #include "ptx.cuh"
@@ -151,14 +152,26 @@ __global__ void __launch_bounds__(kPrepThreads) attn_prep_kernel(const uint16_t 
 }
 
 // ----------------------------------------------------------------- forward --
-// Warps: 0 tensor copies, 1 MMA issue, 2-3 idle, 4-7 softmax (TMEM lanes 32 (w % 4) ..).
+// Warps: 0 Q and K copies, 1 MMA issue, 2 V copies, 3 idle, 4-11 softmax in two groups
+// (warp w reads TMEM lanes 32 (w % 4) ..; group g = (w - 4) / 4 takes keys 64 g .. 64 g + 63
+// of every block and O columns 128 g ..).
 // Shared memory (1024-byte aligned): Q tile, K tile, V^T tile (each 64 KB: 128-byte rows,
 // 128-byte swizzle, the K dimension split into 64-element halves), then the key scales
-// of two blocks and the barriers.  TMEM: O [0, 256), S/P buffers [256, 384) and [384, 512).
-constexpr int kFwdThreads = 256;
+// of two blocks, the groups' row maxima of two blocks and their row sums, the barriers.  TMEM: O [0, 256),
+// S/P buffers [256, 384) and [384, 512).
+constexpr int kFwdThreads = 384;
+constexpr int kSmGroups = 2;
 constexpr uint32_t kTileBytes = 65536;
 constexpr int kSoftmaxWarp0 = 4;
 constexpr uint32_t kOCol = 0, kSCol = 256;
+
+// 2^x (ex2.approx.ftz: relative error about 2^-22, 2^-inf = 0), for the softmax weights,
+// which are rounded to fp16 right after
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 struct AttnArgs {
   CUtensorMap tq, tk, tv;     // Qc [Hq*T][256], Kc [Hkv*S][256] (64 x 128 x 4 boxes), V^T [Hkv*256][S] (64 x 256 x 2)
@@ -176,16 +189,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_kernel(const __grid_c
   uint8_t *gbase = smem_raw + (sbase - raw);
   const uint32_t q_s = sbase, k_s = sbase + kTileBytes, v_s = sbase + 2 * kTileBytes;
   float *ksm = reinterpret_cast<float *>(gbase + 3 * kTileBytes);             // [2][128]
-  const uint32_t bars = sbase + 3 * kTileBytes + 1024;
-  uint8_t *gbars = gbase + 3 * kTileBytes + 1024;
-  // barriers: q_full, k_full, k_empty, v_full, v_empty, s_full[2], p_full[2], s_free[2], o_step, drain
+  float *xm = ksm + 2 * kAttnBlk;                                             // [2][2][128]
+  float *lx = xm + 4 * kAttnBlk;                                              // [2][128]
+  const uint32_t bars = sbase + 3 * kTileBytes + 4096;
+  uint8_t *gbars = gbase + 3 * kTileBytes + 4096;
+  // barriers: q_full, k_full, k_empty, v_full, v_empty, s_full[2], p_full[2], s_free[2], o_step
+  // (every P.V), drain, o_done (the last P.V; the output must not wait on o_step by parity,
+  // which may be two phases behind then)
   const uint32_t q_full = bars, k_full = bars + 8, k_empty = bars + 16, v_full = bars + 24, v_empty = bars + 32;
   auto s_full = [&](int b) { return bars + 40u + 8u * b; };
   auto p_full = [&](int b) { return bars + 56u + 8u * b; };
   auto s_free = [&](int b) { return bars + 72u + 8u * b; };
-  const uint32_t o_step = bars + 88, drain = bars + 96;
-  volatile WaitBlock *wctl = reinterpret_cast<volatile WaitBlock *>(gbars + 104);
-  volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbars + 104 + sizeof(WaitBlock));
+  const uint32_t o_step = bars + 88, drain = bars + 96, o_done = bars + 104;
+  volatile WaitBlock *wctl = reinterpret_cast<volatile WaitBlock *>(gbars + 112);
+  volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbars + 112 + sizeof(WaitBlock));
   auto pwait = [&](uint32_t bar, uint32_t parity) { return mbar_wait(bar, parity, wctl, a.wait_ns == 0); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -203,11 +220,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_kernel(const __grid_c
     mbar_init(v_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
-      mbar_init(p_full(b), 4);
+      mbar_init(p_full(b), 4 * kSmGroups);
       mbar_init(s_free(b), 1);
     }
     mbar_init(o_step, 1);
     mbar_init(drain, 1);
+    mbar_init(o_done, 1);
     wait_block_init(wctl, a.wait_ns, a.err);
     fence_mbar_init();
   }
@@ -228,25 +246,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_kernel(const __grid_c
   griddep_launch_dependents();
 
   if (warp == 0) {
-    // ------------------------------------------------------------ copies --
+    // ------------------------------------------------- Q and K copies --
+    // (K and V have their own copy threads, so that K of the next block is requested as
+    // soon as the scores of the current one are done, whatever P . V is doing)
     if (lane == 0) {
-      bool ok = true;
       mbar_arrive_expect_tx(q_full, kTileBytes);
       tma_load_3d(q_s, &a.tq, 0, h * a.T + qb * kAttnBlk, 0, q_full);
-      int nk = 0, nv = 0;
-      for (int j = 0; ok && j < nblk; ++j) {
-        if (j > 0 && !pwait(k_empty, (uint32_t)((j - 1) & 1))) { ok = false; break; }
+      int nk = 0;
+      for (int j = 0; j < nblk; ++j) {
+        if (j > 0 && !pwait(k_empty, (uint32_t)((j - 1) & 1))) break;
         mbar_arrive_expect_tx(k_full, kTileBytes);
         tma_load_3d(k_s, &a.tk, 0, g * a.S + j * kAttnBlk, 0, k_full);
         ++nk;
-        if (j > 0 && !pwait(v_empty, (uint32_t)((j - 1) & 1))) { ok = false; break; }
-        mbar_arrive_expect_tx(v_full, kTileBytes);
-        tma_load_3d(v_s, &a.tv, 0, g * kAttnD, 2 * j, v_full);
-        ++nv;
       }
       // every copy has landed before the CTA may exit
       mbar_drain(q_full, 0u, wctl);
       if (nk > 0) mbar_drain(k_full, (uint32_t)((nk - 1) & 1), wctl);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------- V copies --
+    if (lane == 0) {
+      int nv = 0;
+      for (int j = 0; j < nblk; ++j) {
+        if (j > 0 && !pwait(v_empty, (uint32_t)((j - 1) & 1))) break;
+        mbar_arrive_expect_tx(v_full, kTileBytes);
+        tma_load_3d(v_s, &a.tv, 0, g * kAttnD, 2 * j, v_full);
+        ++nv;
+      }
       if (nv > 0) mbar_drain(v_full, (uint32_t)((nv - 1) & 1), wctl);
     }
   } else if (warp == 1) {
@@ -283,6 +309,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_kernel(const __grid_c
           mma_commit(s_free(bp));
           mma_commit(v_empty);
           mma_commit(o_step);
+          if (jp == nblk - 1) mma_commit(o_done);
         }
       }
       // every MMA this thread issued has completed before the CTA may exit
@@ -291,44 +318,65 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_kernel(const __grid_c
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ----------------------------------------------------------- softmax --
-    const int st = threadIdx.x - kSoftmaxWarp0 * 32;            // 0..127: query row of the block
+    const int grp = (warp - kSoftmaxWarp0) >> 2;               // 0, 1: keys 64 grp .. of a block
+    const int row = ((warp - kSoftmaxWarp0) & 3) * 32 + lane;  // query row of the block (TMEM lane)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int qi = qb * kAttnBlk + st;                          // query index in the chunk
+    const int qi = qb * kAttnBlk + row;                         // query index in the chunk
     const int pos = a.S - a.T + qi;                             // its position in the context
+    const int c0 = 64 * grp;                                    // the group's first key of a block
+    constexpr int kSmThreads = 4 * kSmGroups * 32;
     // score in base 2: dot * ks * qs / sqrt(d) * log2(e)
     const float arow = __ldg(a.qs + (size_t)h * a.T + qi) * (1.4426950408889634f / 16.0f);
     float m_ref = -INFINITY, l = 0.0f;
     bool aborted = false;
+    // key scales of a block: thread row < 64 of group grp stages key 64 grp + row; block j + 1
+    // is staged during block j (visible after that block's barrier)
+    if (row < 64) ksm[c0 + row] = __ldg(a.ks + (size_t)g * a.S + c0 + row);
+    named_bar_sync(1, kSmThreads);
     for (int j = 0; j < nblk; ++j) {
       const int b = j & 1;
-      ksm[b * kAttnBlk + st] = __ldg(a.ks + (size_t)g * a.S + j * kAttnBlk + st);
+      if (row < 64 && j + 1 < nblk)
+        ksm[((j + 1) & 1) * kAttnBlk + c0 + row] = __ldg(a.ks + (size_t)g * a.S + (j + 1) * kAttnBlk + c0 + row);
       const bool got = pwait(s_full(b), (uint32_t)((j >> 1) & 1));
-      // all four warps decide together (and the key scales are in place)
-      if (named_bar_or(1, kAttnBlk, aborted || !got || wctl->abort)) { aborted = true; break; }
       tc_fence_after();
-      const float *kss = ksm + b * kAttnBlk;
       const uint32_t sadr = tmem + lane_base + kSCol + (uint32_t)(b * kAttnBlk);
       const bool masked = j * kAttnBlk + kAttnBlk - 1 > a.S - a.T + qb * kAttnBlk;   // block meets the diagonal
-      // pass 1: the block's row maximum
-      float mblk = -INFINITY;
-#pragma unroll
-      for (int c0 = 0; c0 < kAttnBlk; c0 += 32) {
+      // the group's 64 scores of the row, in registers
+      float x[64];
+      {
         uint32_t v[32];
-        tmem_ld32(sadr + (uint32_t)c0, v);
-        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float x = __uint_as_float(v[c]) * kss[c0 + c] * arow;
-          if (!masked || j * kAttnBlk + c0 + c <= pos) mblk = fmaxf(mblk, x);
+        for (int hh = 0; hh < 2; ++hh) {
+          tmem_ld32(sadr + (uint32_t)(c0 + 32 * hh), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) x[32 * hh + c] = __uint_as_float(v[c]);
         }
       }
-      // the reference maximum moves only when the new one is 2^8 above it (P stays
-      // below 256 in fp16); then O and l are rescaled, once the previous P.V is done
+      const float *kss = ksm + b * kAttnBlk + c0;
+      float mloc = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float t = x[c] * kss[c] * arow;
+        if (masked && j * kAttnBlk + c0 + c > pos) t = -INFINITY;
+        x[c] = t;
+        mloc = fmaxf(mloc, t);
+      }
+      xm[(b * kSmGroups + grp) * kAttnBlk + row] = mloc;
+      // both groups decide together; the row maxima and the next key scales are in place,
+      // and both groups' reads of S precede the P stores over it
+      tc_fence_before();
+      if (named_bar_or(1, kSmThreads, aborted || !got || wctl->abort)) { aborted = true; break; }
+      tc_fence_after();
+      const float mblk = fmaxf(mloc, xm[(b * kSmGroups + (grp ^ 1)) * kAttnBlk + row]);
+      // the reference maximum moves only when the new one is 2^8 above it (P stays below
+      // 256 in fp16); then O and l are rescaled, once the previous P.V is done (both
+      // groups take the same decision for a row)
       float factor = 1.0f;
       bool resc = false;
       if (mblk > m_ref + 8.0f) {
         if (m_ref != -INFINITY) {
-          factor = exp2f(m_ref - mblk);
+          factor = ex2_approx(m_ref - mblk);
           resc = true;
         }
         m_ref = mblk;
@@ -340,59 +388,47 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_kernel(const __grid_c
         } else {
           tc_fence_after();
 #pragma unroll 1
-          for (int c0 = 0; c0 < kAttnD; c0 += 32) {
+          for (int cc = 0; cc < kAttnD / kSmGroups; cc += 32) {
             uint32_t v[32];
-            tmem_ld32(tmem + lane_base + kOCol + (uint32_t)c0, v);
+            const uint32_t oadr = tmem + lane_base + kOCol + (uint32_t)(grp * (kAttnD / kSmGroups) + cc);
+            tmem_ld32(oadr, v);
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * factor);
-            tmem_st32(tmem + lane_base + kOCol + (uint32_t)c0, v);
+            tmem_st32(oadr, v);
           }
           tmem_wait_st();
         }
       }
       l *= factor;
       if (!aborted) {
-        // pass 2: P = 2^(x - m_ref) as fp16 pairs over the consumed S columns
+        // P = 2^(x - m_ref) as fp16 pairs, over S columns already read by both groups
+        uint32_t p[32];
 #pragma unroll
-        for (int c0 = 0; c0 < kAttnBlk; c0 += 64) {
-          uint32_t p[32];
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t v[32];
-            tmem_ld32(sadr + (uint32_t)(c0 + 32 * hh), v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const int key = j * kAttnBlk + c0 + 32 * hh + c;
-              float x0 = __uint_as_float(v[c]) * kss[c0 + 32 * hh + c] * arow;
-              float x1 = __uint_as_float(v[c + 1]) * kss[c0 + 32 * hh + c + 1] * arow;
-              if (masked && key > pos) x0 = -INFINITY;
-              if (masked && key + 1 > pos) x1 = -INFINITY;
-              const __half2 ph = __floats2half2_rn(exp2f(x0 - m_ref), exp2f(x1 - m_ref));
-              const float2 pf = __half22float2(ph);
-              l += pf.x + pf.y;
-              p[16 * hh + c / 2] = h2_as_u32(ph);
-            }
-          }
-          tmem_st32(sadr + (uint32_t)(c0 / 2), p);
+        for (int c = 0; c < 64; c += 2) {
+          const __half2 ph = __floats2half2_rn(ex2_approx(x[c] - m_ref), ex2_approx(x[c + 1] - m_ref));
+          const float2 pf = __half22float2(ph);
+          l += pf.x + pf.y;
+          p[c / 2] = h2_as_u32(ph);
         }
+        tmem_st32(sadr + (uint32_t)(c0 / 2), p);
         tmem_wait_st();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && !aborted) mbar_arrive(p_full(b));
     }
-    // ---- O / l into the output row
-    const bool got = !aborted && pwait(o_step, (uint32_t)((nblk - 1) & 1));
-    if (!named_bar_or(1, kAttnBlk, !got || wctl->abort)) {
+    // ---- O / l into the output row (group grp writes columns 128 grp ..)
+    const bool got = !aborted && pwait(o_done, 0u);
+    lx[grp * kAttnBlk + row] = l;
+    if (!named_bar_or(1, kSmThreads, !got || wctl->abort)) {
       tc_fence_after();
-      const float inv = 1.0f / l;
-      uint16_t *orow = a.out + ((size_t)qi * a.Hq + h) * kAttnD;
+      const float inv = 1.0f / (l + lx[(grp ^ 1) * kAttnBlk + row]);
+      uint16_t *orow = a.out + ((size_t)qi * a.Hq + h) * kAttnD + grp * (kAttnD / kSmGroups);
 #pragma unroll 1
-      for (int c0 = 0; c0 < kAttnD; c0 += 32) {
+      for (int cc = 0; cc < kAttnD / kSmGroups; cc += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kOCol + (uint32_t)c0, v);
+        tmem_ld32(tmem + lane_base + kOCol + (uint32_t)(grp * (kAttnD / kSmGroups) + cc), v);
         tmem_wait_ld();
         uint32_t o[16];
 #pragma unroll
@@ -400,7 +436,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_kernel(const __grid_c
           o[c] = h2_as_u32(__floats2half2_rn(__uint_as_float(v[2 * c]) * inv, __uint_as_float(v[2 * c + 1]) * inv));
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          reinterpret_cast<uint4 *>(orow + c0)[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+          reinterpret_cast<uint4 *>(orow + cc)[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
       }
     }
   }
@@ -415,7 +451,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_kernel(const __grid_c
   }
 }
 
-size_t attn_fwd_smem_bytes() { return 1024 + 3 * (size_t)kTileBytes + 1024 + 256; }
+size_t attn_fwd_smem_bytes() { return 1024 + 3 * (size_t)kTileBytes + 4096 + 256; }
 
 cudaError_t launch_attn(const AttnLaunch &L, cudaStream_t st) {
   cudaError_t e = launch_pdl(reinterpret_cast<const void *>(attn_ksum_kernel), dim3(L.S / kAttnBlk, L.Hkv),
