@@ -722,6 +722,29 @@ def extras(q, dev, stream, pk, pk_src):
     del pk4, l4
     torch.cuda.empty_cache()
 
+    # int8-QK causal prefill attention, head_dim 256, 24 query heads on 4 KV heads: a full
+    # 4k prefill and a 2k chunk at the end of a 16k context; parity on the last 128
+    # queries of one query head per KV head
+    import oracle.attention as attn_oracle
+    for T, S in ((4096, 4096), (2048, 16384)):
+        Hq, Hkv = 24, 4
+        qq, kk, vv = synth.attention(T, S, Hq, Hkv, seed=60 + T)
+        qd, kd, vd = qq.to(dev), kk.to(dev), vv.to(dev)
+        o = torch.empty((T, Hq, 256), dtype=torch.float16, device=dev)
+        wsa = q.Workspace(dev)
+        ms = timeit(lambda: q.attn_int8qk_prefill(qd, kd, vd, out=o, ws=wsa), 10)
+        pos = np.arange(T, dtype=np.float64) + (S - T)
+        flops = 4.0 * 256 * Hq * float((pos + 1).sum())      # QK^T and P.V over the causal triangle
+        heads = [h * (Hq // Hkv) for h in range(Hkv)]
+        ref = attn_oracle.attn_int8qk(qq[-128:, heads].numpy(), kk.numpy(), vv.numpy(), out_f64=True)
+        got = o[-128:, heads].float().cpu().numpy()
+        tf = flops / ms / 1e9
+        out[f"attn_int8qk_T{T}_S{S}_Hq{Hq}_Hkv{Hkv}"] = {
+            "us": round(ms * 1e3, 1), "TFLOPS": round(tf, 1), "frac_f16_peak": round(tf / peak16, 4),
+            "peak": "bf16_tflops burst", "parity": float(np.abs(got - ref).max() / np.abs(ref).max())}
+        del qd, kd, vd, o, wsa
+    torch.cuda.empty_cache()
+
     # top-k (k = 64) over synthetic logits of the lm_head's width
     for M in (1, 16, 64):
         lg = synth.logits(M, lh.N, seed=50 + M).to(dev)

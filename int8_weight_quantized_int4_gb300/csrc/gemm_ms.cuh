@@ -20,7 +20,8 @@
 //   warp 0, lane 0 : one bulk copy per packed chunk into the weight ring; the ring is
 //                    split into one part per team and a team's chunks fill its part
 //                    in order.  When the weights may be read ahead of the preceding
-//                    kernel, the chunks beyond the ring are first prefetched into L2.
+//                    kernel, the next chunks beyond the ring (kMsL2AheadChunks) are first
+//                    prefetched into L2.
 //   warp 1, lane 0 : one TMA tensor copy per block of four K groups of the
 //                    activations (8 or 16 token rows, 128-byte swizzle, zero fill past M)
 //   compute warps  : eight, in teams; team j takes the chunks with CTA-wide index = j

@@ -123,7 +123,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Wait for a phase that completes by itself (copies or MMAs this thread already
 // issued), whatever the abort flag says; after kWaitLimitNs record QW_ERR_TIMEOUT
 // and return.
-static __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity, volatile WaitBlock *w) {
+static __device__ __noinline__ void mbar_drain_slow(uint32_t bar, uint32_t parity, volatile WaitBlock *w) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait_sleep(bar, parity)) {
     if (globaltimer_ns() - t0 >= kWaitLimitNs) {
@@ -131,6 +131,10 @@ static __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity, vo
       return;
     }
   }
+}
+// (an already completed phase -- the usual case at the end of a kernel -- costs one test)
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, volatile WaitBlock *w) {
+  if (!mbar_test_wait(bar, parity)) mbar_drain_slow(bar, parity, w);
 }
 
 // ------------------------------------------------------------ bulk copies --

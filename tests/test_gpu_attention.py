@@ -59,6 +59,23 @@ def test_attention_matches_oracle(q, T, S, Hq, Hkv):
     assert cos > 0.99999, cos
 
 
+def test_attention_long_context_repeats_bitwise(q):
+    """A 2k chunk at the end of a 16k context (128 key blocks a query block, several
+    waves of CTAs), run 30 times: every run gives the same bits (the pipeline's waits
+    leave no window for a read before its producer)."""
+    T, S, Hq, Hkv = 2048, 16384, 24, 4
+    qq, kk, vv = synth.attention(T, S, Hq, Hkv, seed=11)
+    qd, kd, vd = qq.to(DEV), kk.to(DEV), vv.to(DEV)
+    ws = q.Workspace(DEV)
+    base = q.attn_int8qk_prefill(qd, kd, vd, ws=ws).clone()
+    out = torch.empty_like(base)
+    for _ in range(30):
+        q.attn_int8qk_prefill(qd, kd, vd, out=out, ws=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), base.view(torch.int16))
+    assert q.device_error() == 0
+
+
 def test_attention_repeat_is_bitwise_stable(q):
     T, S, Hq, Hkv = 256, 512, 4, 2
     qq, kk, vv = synth.attention(T, S, Hq, Hkv, seed=3)
