@@ -776,6 +776,10 @@ NCU_CASES = {
     "topk_m64": ("topk", 64, 248320, 64, 0),
     # dequant-on-gather of T rows from the int8 group-128 table: ("gather", T, V, D, 8)
     "embed_gather_t2048": ("gather", 2048, 248320, 5120, 8),
+    # int8-QK prefill attention: ("attn", T, S, Hq, Hkv)
+    "attn_t1024_s4096": ("attn", 1024, 4096, 24, 4),
+    # the lm_head with the fused top-k (k = 64): ("lmtopk", M, N, K, bits)
+    "lm_head_topk_w4a16_m16": ("lmtopk", 16, 248320, 5120, 4),
 }
 
 
@@ -797,6 +801,26 @@ def run_ncu_case(name):
         torch.cuda.synchronize()
         assert q.device_error() == 0
         print(json.dumps({"ncu_case": name, "T": M, "V": N, "D": K, "absmax": float(out.float().abs().max())}))
+        return
+    if mode == "attn":
+        T, S, Hq, Hkv = M, N, K, bits
+        qq, kk, vv = synth.attention(T, S, Hq, Hkv, seed=60 + T)
+        qd, kd, vd = qq.to(dev), kk.to(dev), vv.to(dev)
+        for _ in range(4):
+            o = q.attn_int8qk_prefill(qd, kd, vd)
+        torch.cuda.synchronize()
+        assert q.device_error() == 0
+        print(json.dumps({"ncu_case": name, "T": T, "S": S, "absmax": float(o.float().abs().max())}))
+        return
+    if mode == "lmtopk":
+        p = synth.lm_head_int4(M)
+        packed = q.qpack_w4(p.codes.to(dev), p.scales.to(dev))
+        x = p.x.to(dev)
+        for _ in range(4):
+            y, vals, idx = q.qgemm_lm_head_topk(q.MODE_W4A16, x, packed, N, K, 64)
+        torch.cuda.synchronize()
+        assert q.device_error() == 0
+        print(json.dumps({"ncu_case": name, "M": M, "idx0": int(idx[0, 0])}))
         return
     if mode == "topk":
         lg = synth.logits(M, N, seed=50 + M).to(dev)
