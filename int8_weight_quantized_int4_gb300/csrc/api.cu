@@ -175,35 +175,27 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
   a.tile_max = tile_max;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (mode == QW_MODE_W4A8_FUSED && P.fused) {
-    // the decode-batch kernel quantizes per token itself: fp16 tiles, as W4A16
-    a.xf16 = static_cast<const uint16_t *>(act);
-    if ((rc = encode_act_map(&a.tmap, act, M, K, qw::ms_rows(M), P.xblock, false))) return rc;
-    e = qw::launch_gemm_ms(a, 2, st);
-    if (e != cudaSuccess) return fail_cuda(e, "GEMM kernel launch");
-    return QW_OK;
-  }
-  if (mode == QW_MODE_W4A8_FUSED) {
-    // the standalone quantizer into the workspace, then the W4A8 GEMM (plan mode 1)
-    int8_t *q = reinterpret_cast<int8_t *>(w + P.ws_counters + P.ws_partials + P.ws_act);
-    float *s = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(q) + qw::align_up((size_t)M * K, 256));
-    e = qw::launch_quant_act(static_cast<const uint16_t *>(act), M, K, q, s, st);
-    if (e != cudaSuccess) return fail_cuda(e, "quant kernel launch");
-    act = q;
-    a.xs = s;
-    mode = QW_MODE_W4A8;
-  }
   // the decode-batch kernel's activation tiles hold 8 or 16 token rows
   const int box_rows = P.ms_teams ? qw::ms_rows(M) : P.bn;
-  if (mode == QW_MODE_W4A8 && qw::act8_in_kernel(mode, P.bn)) {
+  if (mode == QW_MODE_W4A8_FUSED) {
+    // the standalone quantizer writes fp16 codes and token scales into the workspace;
+    // the W4A8 GEMM reads the codes as fp16 tiles (plan mode kModeCodes16)
+    uint16_t *q = reinterpret_cast<uint16_t *>(w + P.ws_counters + P.ws_partials + P.ws_act);
+    float *s = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(q) + qw::align_up((size_t)M * K * 2, 256));
+    e = qw::launch_quant_act(static_cast<const uint16_t *>(act), M, K, q, true, s, st);
+    if (e != cudaSuccess) return fail_cuda(e, "quant kernel launch");
+    a.xs = s;
+    if ((rc = encode_act_map(&a.tmap, q, M, K, box_rows, P.xblock, false))) return rc;
+    e = P.ms_teams ? qw::launch_gemm_ms(a, 2, st) : qw::launch_gemm_w4a8(a, false, st);
+  } else if (mode == QW_MODE_W4A8 && qw::act8_in_kernel(mode, P.bn)) {
     if ((rc = encode_act_map(&a.tmap, act, M, K, box_rows, P.xblock, true))) return rc;
-    e = P.ms_teams ? qw::launch_gemm_ms(a, 1, st) : qw::launch_gemm_w4a8(a, st);
+    e = P.ms_teams ? qw::launch_gemm_ms(a, 1, st) : qw::launch_gemm_w4a8(a, true, st);
   } else if (mode == QW_MODE_W4A8) {
     uint16_t *wide = reinterpret_cast<uint16_t *>(w + P.ws_counters + P.ws_partials);
     if ((rc = encode_act_map(&a.tmap, wide, M, K, P.bn, P.xblock, false))) return rc;
     e = qw::launch_widen_i8(static_cast<const int8_t *>(act), wide, (size_t)M * K, d->sms, st);
     if (e != cudaSuccess) return fail_cuda(e, "widen kernel launch");
-    e = qw::launch_gemm_w4a8(a, st);
+    e = qw::launch_gemm_w4a8(a, false, st);
   } else {
     if ((rc = encode_act_map(&a.tmap, act, M, K, box_rows, P.xblock, false))) return rc;
     e = mode == QW_MODE_W8A16 ? qw::launch_gemm_w8a16(a, st)
@@ -299,7 +291,7 @@ int quant_act_int8(const uint16_t *x, int M, int K, int8_t *xq, float *xs, qw_st
   DevInfo *d = nullptr;
   int rc = current_device(d);
   if (rc) return rc;
-  cudaError_t e = qw::launch_quant_act(x, M, K, xq, xs, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = qw::launch_quant_act(x, M, K, xq, false, xs, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "quant kernel launch");
   return QW_OK;
 }

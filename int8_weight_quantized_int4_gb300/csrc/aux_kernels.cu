@@ -2,6 +2,7 @@
 // activation quantizer, weight packers, and the int8 -> fp16 code widening
 // used by the W4A8 GEMM.
 #include <stdint.h>
+#include <type_traits>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include "launch.h"
@@ -17,12 +18,17 @@ namespace qw {
 // s = amax / 127 with the IEEE divide, q = rne(x / s) clamped to [-127, 127].
 // The row is kept in registers (up to kQuantRegs 16-byte vectors per thread);
 // longer rows are re-read for the second pass.
+// CODES16: the codes are written as fp16 values (exact: |q| <= 127) for a GEMM that
+// reads them as fp16 tiles and applies the token scales in its epilogue, so that no
+// widening of int8 codes is needed there; otherwise as int8.
 constexpr int kQuantThreads = 256;
 constexpr int kQuantRegs = 12;
 
+template <bool CODES16>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const uint16_t *__restrict__ x, int K,
-                                                                  int8_t *__restrict__ q,
+                                                                  void *__restrict__ q,
                                                                   float *__restrict__ s) {
+  using Out = typename std::conditional<CODES16, uint4, uint2>::type;   // 8 codes
   __shared__ float red[kQuantThreads / 32];
   griddep_wait();
   griddep_launch_dependents();
@@ -63,11 +69,11 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const uint16_t
 
   const float sc = __fdiv_rn(amax, 127.0f);
   if (threadIdx.x == 0) s[row] = (amax == 0.0f) ? 0.0f : sc;
-  uint2 *qr = reinterpret_cast<uint2 *>(q + row * (size_t)K);
+  Out *qr = reinterpret_cast<Out *>(q) + row * (size_t)(K / 8);
 
-  auto quant8 = [&](const uint4 &v) -> uint2 {
+  auto quant8 = [&](const uint4 &v) -> Out {
     const __half2 *h = reinterpret_cast<const __half2 *>(&v);
-    uint32_t out[2] = {0u, 0u};
+    uint32_t out[4] = {0u, 0u, 0u, 0u};
     if (amax != 0.0f) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -76,11 +82,16 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const uint16_t
         int q1 = __float2int_rn(__fdiv_rn(f.y, sc));
         q0 = max(-127, min(127, q0));
         q1 = max(-127, min(127, q1));
-        const uint32_t pair = ((uint32_t)(q0 & 0xff)) | ((uint32_t)(q1 & 0xff) << 8);
-        out[e >> 1] |= pair << (16 * (e & 1));
+        if constexpr (CODES16) {
+          out[e] = h2_as_u32(__halves2half2(__int2half_rn(q0), __int2half_rn(q1)));
+        } else {
+          const uint32_t pair = ((uint32_t)(q0 & 0xff)) | ((uint32_t)(q1 & 0xff) << 8);
+          out[e >> 1] |= pair << (16 * (e & 1));
+        }
       }
     }
-    return make_uint2(out[0], out[1]);
+    if constexpr (CODES16) return make_uint4(out[0], out[1], out[2], out[3]);
+    else return make_uint2(out[0], out[1]);
   };
 #pragma unroll
   for (int r = 0; r < kQuantRegs; ++r) {
@@ -197,9 +208,11 @@ static int grid_for(size_t items, int threads, int sms) {
   return (int)(b < 1 ? 1 : b);
 }
 
-cudaError_t launch_quant_act(const uint16_t *x, int M, int K, int8_t *q, float *s, cudaStream_t st) {
-  cudaError_t e = launch_pdl(reinterpret_cast<const void *>(quant_act_kernel), dim3(M),
-                             dim3(kQuantThreads), 0, st, x, K, q, s);
+cudaError_t launch_quant_act(const uint16_t *x, int M, int K, void *q, bool codes16, float *s,
+                             cudaStream_t st) {
+  const void *k = codes16 ? reinterpret_cast<const void *>(quant_act_kernel<true>)
+                          : reinterpret_cast<const void *>(quant_act_kernel<false>);
+  cudaError_t e = launch_pdl(k, dim3(M), dim3(kQuantThreads), 0, st, x, K, q, s);
   count_launch();
   return e;
 }

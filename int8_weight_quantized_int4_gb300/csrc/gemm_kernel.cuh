@@ -138,29 +138,18 @@ __device__ __forceinline__ void widen_chunk(uint8_t *btile, const uint8_t *stg, 
   }
 }
 
-// q = clamp(rne(x / s), -127, 127) with x / s the IEEE binary32 quotient, as the
-// standalone quantizer computes it (used by the decode kernel's in-kernel quantizer), but without a divide per value: t = x * (1/s)
-// (correctly rounded reciprocal and product) is within 3 * 2^-24 * |x/s| <= 2.3e-5 of
-// the quotient, since |x/s| <= 127 (1 + 2^-24).  So rne(t) = rne(x / s) unless t lies
-// within 2^-14 of a half-integer; only those values take the IEEE divide, out of line
-// so that it is skipped rather than computed and discarded.
-static __device__ __noinline__ float quotient_rn(float x, float s) { return __fdiv_rn(x, s); }
-
-__device__ __forceinline__ int quant_code(float x, float s, float rs) {
-  const float t = __fmul_rn(x, rs);
-  float qf = rintf(t);
-  if (fabsf(t - floorf(t) - 0.5f) <= 6.103515625e-05f) qf = rintf(quotient_rn(x, s));
-  return max(-127, min(127, (int)qf));
-}
-
-// TMAX: the epilogue also raises the per-tile maxima of the lm_head's fused top-k
-template <int BN, int WBITS, bool TOKSCALE, bool TMAX>
+// TOKSCALE: W4A8, the epilogue multiplies by the token scales.  ACT8: the activations
+// are int8 codes, widened to fp16 in the kernel; otherwise fp16 tiles (fp16 x, or W4A8
+// codes already in fp16).  TMAX: the epilogue also raises the per-tile maxima of the
+// lm_head's fused top-k.
+template <int BN, int WBITS, bool TOKSCALE, bool TMAX, bool ACT8>
 __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_constant__ GemmArgs a) {
   static_assert(!TMAX || !TOKSCALE, "the lm_head's fused top-k is W4A16 or W8A16");
+  static_assert(!ACT8 || (TOKSCALE && BN <= kAct8InKernelMaxBn), "int8 codes are widened for small tiles");
   constexpr uint32_t kChunk = WBITS == 8 ? kChunkW8 : kChunkW4;
   constexpr uint32_t kWStage = (kChunk + 127) / 128 * 128;
   static_assert(kChunk % 128 == 0, "weight slots stay 128-byte aligned");
-  constexpr bool kAct8 = TOKSCALE && BN <= kAct8InKernelMaxBn;
+  constexpr bool kAct8 = ACT8;
   constexpr int kXBlock = act_block(BN);                 // chunks per activation copy
   constexpr uint32_t kXChunk = BN * kGroup * 2;          // one fp16 tile (two swizzled halves)
   constexpr uint32_t kXStage = kXBlock * (kXChunk + (kAct8 ? BN * kGroup : 0));

@@ -1,6 +1,6 @@
 // gemm_ms.cu -- instantiations of the decode-batch kernel (warp-level MMA): W4A16, W4A8
-// from int8 activations (widened in shared memory) and W4A8 from fp16 activations
-// (quantized per token in the kernel); one or two tiles of 8 tokens.
+// from int8 codes (widened in shared memory) and W4A8 from fp16 codes (written by the
+// standalone quantizer); one or two tiles of 8 tokens.
 #include "gemm_ms.cuh"
 
 namespace qw {
@@ -21,9 +21,8 @@ cudaError_t launch_gemm_ms(const GemmArgs &a, int act, cudaStream_t st) {
   if ((a.P.ms_teams != 2 && a.P.ms_teams != 4) || a.P.bn != kMsMaxTokens) return cudaErrorInvalidValue;
   const bool one = a.P.M <= 8, four = a.P.ms_teams == 4;
   if (four && !(one && act == kActF16)) return cudaErrorInvalidValue;
-  // the in-kernel quantizer takes at most 4 tokens (the plan's fused rule)
-  if (act == kActQuant) return a.P.M <= 4 ? run_ms<1, kActQuant>(a, st) : cudaErrorInvalidValue;
   if (act == kActI8) return one ? run_ms<1, kActI8>(a, st) : run_ms<2, kActI8>(a, st);
+  if (act == kActCodes16) return one ? run_ms<1, kActCodes16>(a, st) : run_ms<2, kActCodes16>(a, st);
   // the lm_head with top-k: the variant whose epilogue records the tile maxima
   if (a.tile_max) {
     if (four) return run_ms<1, kActF16, 4, true>(a, st);

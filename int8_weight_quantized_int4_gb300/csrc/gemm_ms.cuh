@@ -56,9 +56,10 @@ constexpr int kMsWarpW = 0;       // weight copies
 constexpr int kMsWarpX = 1;       // activation copies
 constexpr int kMsWarpC0 = 2;      // first compute warp
 
-// activation modes: fp16 x (W4A16), int8 codes + token scales (W4A8), fp16 x quantized
-// per token inside the kernel (W4A8 from fp16)
-enum { kActF16 = 0, kActI8 = 1, kActQuant = 2 };
+// activation modes: fp16 x (W4A16), int8 codes + token scales (W4A8), fp16 codes + token
+// scales (W4A8 from fp16 after the standalone quantizer: the W4A16 data path, the W4A8
+// epilogue)
+enum { kActF16 = 0, kActI8 = 1, kActCodes16 = 2 };
 
 __host__ __device__ constexpr int ms_threads() { return (kMsWarpC0 + kMsComputeWarps) * 32; }
 
@@ -119,7 +120,7 @@ __device__ __forceinline__ void frag_w4_zp(uint32_t w, uint32_t (&a)[4]) {
 template <int NT8, int AMODE, int RBW, bool TMAX>
 __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_constant__ GemmArgs a) {
   constexpr bool ACT8 = AMODE == kActI8;
-  constexpr bool QIN = AMODE == kActQuant;
+  constexpr bool TOKS = ACT8 || AMODE == kActCodes16;   // token scales in the epilogue
   constexpr bool kTileMax = TMAX;
   static_assert(!TMAX || AMODE == kActF16, "the lm_head's fused top-k is W4A16");
   static_assert(RBW == 2 || RBW == 4, "16-row blocks per warp in a chunk");
@@ -155,10 +156,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
   const uint32_t wbase = sbase + (uint32_t)SX * kXStage;
   const uint32_t rbase = wbase + (uint32_t)SW * kWStage;
   float *red = reinterpret_cast<float *>(gbase + (rbase - sbase));
-  // in-kernel quantizer: per-warp amax [8 warps][16 tokens], scales [16], reciprocals [16]
-  float *qamax = red + P.ms_red_bytes / 4;
-  float *qsc = qamax + 128, *qrc = qsc + 16;
-  const uint32_t bars = rbase + (uint32_t)P.ms_red_bytes + (uint32_t)kMsQuantFloats * 4;
+  const uint32_t bars = rbase + (uint32_t)P.ms_red_bytes;
   uint8_t *gbars = gbase + (bars - sbase);
   auto wfull_bar = [&](int s) { return bars + 8u * s; };
   auto wempty_bar = [&](int s) { return bars + 128u + 8u * s; };
@@ -199,51 +197,6 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
   const bool early = a.early_weights != 0;
   if (!(early && warp == kMsWarpW)) griddep_wait();
   griddep_launch_dependents();
-
-  if constexpr (QIN) {
-    // token scales, as the standalone quantizer: amax = max |x| over the whole row
-    // (binary32, exact), s = amax / 127 (IEEE divide); each compute warp takes a share
-    // of every row, then thread m combines the shares of row m
-    if (warp >= kMsWarpC0) {
-      const int cw = warp - kMsWarpC0, nv = P.K / 8;
-      constexpr int kBatch = 8;                     // loads in flight per thread
-      for (int m = 0; m < P.M; ++m) {
-        const uint4 *xr = reinterpret_cast<const uint4 *>(a.xf16 + (size_t)m * P.K);
-        float amax = 0.0f;
-        for (int v0 = cw * 32 + lane; v0 < nv; v0 += kBatch * kMsComputeWarps * 32) {
-          uint4 w[kBatch];
-#pragma unroll
-          for (int b = 0; b < kBatch; ++b) {
-            const int v = v0 + b * kMsComputeWarps * 32;
-            w[b] = v < nv ? __ldg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
-          }
-#pragma unroll
-          for (int b = 0; b < kBatch; ++b) {
-            const __half2 *h = reinterpret_cast<const __half2 *>(&w[b]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __half22float2(h[e]);
-              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-            }
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if (lane == 0) qamax[cw * 16 + m] = amax;
-      }
-      named_bar_sync(2, kMsComputeWarps * 32);
-      const int ct = threadIdx.x - kMsWarpC0 * 32;
-      if (ct < P.M) {
-        float amax = qamax[ct];
-#pragma unroll
-        for (int w = 1; w < kMsComputeWarps; ++w) amax = fmaxf(amax, qamax[w * 16 + ct]);
-        const float sc = amax == 0.0f ? 0.0f : __fdiv_rn(amax, 127.0f);
-        qsc[ct] = sc;
-        qrc[ct] = sc == 0.0f ? 0.0f : __frcp_rn(sc);
-      }
-      named_bar_sync(2, kMsComputeWarps * 32);
-    }
-  }
 
   Seg sg;
   if (warp == kMsWarpW) {
@@ -358,38 +311,12 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
         // every compute warp waits for every activation block and returns it once;
         // after an abort every wait gives up at once and the loops run out quickly
         pwait(xfull_bar(xs), xph);
-        if constexpr (ACT8 || QIN) {
-          // the compute warps together turn the block into fp16 codes, then all wait
+        if constexpr (ACT8) {
+          // the compute warps together widen the block's int8 codes, then all wait
           uint8_t *xb = gbase + (size_t)xs * kXStage;
-          for (int j = 0; j < nb; ++j) {
-            if constexpr (ACT8) {
-              widen_chunk<BNX, kCThreads>(xb + j * kXChunk, xb + kXBlock * kXChunk + j * (BNX * kGroup), ct,
-                                          P.M < BNX ? P.M : BNX);
-            } else {
-              // unit: four values 4 c .. 4 c + 3 of row r of group j
-              for (int un = ct; un < P.M * 32; un += kCThreads) {
-              const int r = un >> 5, c = un & 31;
-              {
-                uint8_t *q = xb + j * kXChunk + (c >> 4) * (BNX * 128) + r * 128 +
-                             ((((c >> 1) & 7) ^ (r & 7)) << 4) + ((c & 1) << 3);
-                const uint2 v = *reinterpret_cast<const uint2 *>(q);
-                const float sc = qsc[r], rs = qrc[r];
-                uint32_t o[2] = {v.x, v.y};
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const float2 f = __half22float2(u32_as_h2(o[e]));
-                  int q0 = 0, q1 = 0;
-                  if (sc != 0.0f) {
-                    q0 = quant_code(f.x, sc, rs);
-                    q1 = quant_code(f.y, sc, rs);
-                  }
-                  o[e] = h2_as_u32(__halves2half2(__int2half_rn(q0), __int2half_rn(q1)));
-                }
-                *reinterpret_cast<uint2 *>(q) = make_uint2(o[0], o[1]);
-              }
-              }
-            }
-          }
+          for (int j = 0; j < nb; ++j)
+            widen_chunk<BNX, kCThreads>(xb + j * kXChunk, xb + kXBlock * kXChunk + j * (BNX * kGroup), ct,
+                                        P.M < BNX ? P.M : BNX);
           named_bar_sync(3, kCThreads);
         }
         for (int j = (tm - cidx) & (TEAMS - 1); j < nb; j += TEAMS) {
@@ -514,7 +441,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
                 if (part) {
                   part[m * kRows + row] = v;
                 } else {
-                  const __half hv = __float2half_rn(QIN ? v * qsc[m] : ACT8 ? v * __ldg(a.xs + m) : v);
+                  const __half hv = __float2half_rn(TOKS ? v * __ldg(a.xs + m) : v);
                   a.y[(size_t)m * P.N + t * kRows + row] = __half_as_ushort(hv);
                   if constexpr (kTileMax) tk[jt][e & 1] = max(tk[jt][e & 1], order_key16(hv));
                 }
@@ -579,7 +506,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
           for (int pp = 0; pp < 4; ++pp)
             if (p0 + pp <= pl) v += x[pp];
         }
-        const __half hv = __float2half_rn(QIN ? v * qsc[m] : ACT8 ? v * __ldg(a.xs + m) : v);
+        const __half hv = __float2half_rn(TOKS ? v * __ldg(a.xs + m) : v);
         a.y[(size_t)m * P.N + t * kRows + row] = __half_as_ushort(hv);
         // a warp's 32 consecutive idx are 32 rows of one token (kCThreads and kRows are
         // multiples of 32), and whole warps run this loop

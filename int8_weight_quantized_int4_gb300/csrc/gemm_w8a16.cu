@@ -5,7 +5,7 @@ namespace qw {
 
 template <int BN, bool TMAX = false>
 static cudaError_t run_w8a16(const GemmArgs &a, cudaStream_t st) {
-  auto *k = qgemm_tc_kernel<BN, 8, false, TMAX>;
+  auto *k = qgemm_tc_kernel<BN, 8, false, TMAX, false>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(k), a.P.smem_bytes);
   if (e != cudaSuccess) return e;
   e = launch_pdl(reinterpret_cast<const void *>(k), dim3(a.P.grid), dim3(kThreads),

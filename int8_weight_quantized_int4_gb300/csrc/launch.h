@@ -14,7 +14,6 @@ struct GemmArgs {
                             // int8 [M,K] (128 x bn boxes) for W4A8 at decode sizes
   Plan P;
   const float *xs;          // token scales [M] (W4A8) or nullptr
-  const uint16_t *xf16;     // fused W4A8: fp16 activations [M,K], quantized in the kernel
   const uint8_t *wpack;     // packed weights
   uint16_t *y;              // fp16 [M,N]
   int *counters;            // [tiles] arrival counters (stream-K)
@@ -57,7 +56,9 @@ cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cud
 // Raise the dynamic shared-memory limit of `func` on the current device (once).
 cudaError_t ensure_smem_attr(const void *func, int bytes);
 
-cudaError_t launch_quant_act(const uint16_t *x, int M, int K, int8_t *q, float *s, cudaStream_t st);
+// per-token quantizer: codes to q (int8 [M,K], or fp16 [M,K] when codes16), scales to s [M]
+cudaError_t launch_quant_act(const uint16_t *x, int M, int K, void *q, bool codes16, float *s,
+                             cudaStream_t st);
 cudaError_t launch_widen_i8(const int8_t *src, uint16_t *dst, size_t n, int sms, cudaStream_t st);
 cudaError_t launch_pack_w4(const int8_t *codes, const uint16_t *scales, int N, int K, void *packed,
                            int *err, int sms, cudaStream_t st);
@@ -101,10 +102,12 @@ size_t attn_fwd_smem_bytes();
 cudaError_t launch_attn(const AttnLaunch &L, cudaStream_t st);
 
 cudaError_t launch_gemm_w4a16(const GemmArgs &a, cudaStream_t st);
-cudaError_t launch_gemm_w4a8(const GemmArgs &a, cudaStream_t st);
+// W4A8 (token scales in the epilogue): act8, int8 codes widened in the kernel (token
+// tiles up to kAct8InKernelMaxBn); otherwise fp16 codes read as fp16 tiles
+cudaError_t launch_gemm_w4a8(const GemmArgs &a, bool act8, cudaStream_t st);
 cudaError_t launch_gemm_w8a16(const GemmArgs &a, cudaStream_t st);
 // decode batches (plan.ms_teams > 0); act: 0 fp16 activations (W4A16), 1 int8 codes and
-// token scales (W4A8), 2 fp16 activations quantized per token in the kernel (W4A8)
+// token scales (W4A8), 2 fp16 codes and token scales (W4A8 after the quantizer)
 cudaError_t launch_gemm_ms(const GemmArgs &a, int act, cudaStream_t st);
 
 }  // namespace qw

@@ -43,7 +43,7 @@ struct Plan {
   int xstages;                   // activation ring depth (blocks of xblock chunks)
   int xblock;                    // chunks per activation block (one tensor copy)
   int smem_bytes;
-  int fused;                     // W4A8 with the per-token quantizer inside the GEMM
+  int fused;                     // W4A8 with the per-token quantizer inside the GEMM (none now)
   int ms_teams;                  // > 0: the warp-level MMA kernel for decode batches (M <= 16),
                                  // with this many teams of warps (one chunk per team at a time)
   int ms_red_bytes;              // its shared-memory buffer for the teams' partial sums
@@ -150,18 +150,12 @@ constexpr int kStreamKMaxTilesPerSm = 32;  // stream-K only below this many tile
 QW_HD int chunk_bytes(int mode) { return mode == 2 ? kChunkW8 : kChunkW4; }
 
 // Modes (as in the C ABI): 0 W4A16, 1 W4A8, 2 W8A16, 3 W4A8 from fp16 activations
-// (quantized per token by the library).  Mode 3 quantizes inside the GEMM when the
-// fp16 rows fit in shared memory next to the pipeline (at most kFusedRowsMax bytes,
-// token tiles of 16); otherwise it runs the standalone quantizer into the workspace
-// and then the mode-1 GEMM.
-// Mode 3 quantizes inside the decode-batch kernel for up to 4 tokens whose fp16 rows
-// take at most kFusedRowsMax bytes (every CTA reads them all from L2 to find the token
-// scales, which costs more than a separate quantizer launch for larger batches);
-// otherwise it runs the standalone quantizer into the workspace and then the mode-1 GEMM.
-constexpr int kFusedRowsMax = 48 * 1024;
-QW_HD bool quant_in_kernel(int mode, int M, int K) {
-  return mode == 3 && M >= 1 && M <= 4 && (long long)M * K * 2 <= kFusedRowsMax;
-}
+// (quantized per token by the library).
+// Mode 3 runs the standalone quantizer, which writes the codes into the workspace as
+// fp16 values, with the token scales; the GEMM runs on them as plan mode kModeCodes16:
+// int4 weights, fp16 activation tiles as in W4A16, token scales in the epilogue as in
+// W4A8 (the products and sums are those of the int8 path: the codes are exact in fp16).
+constexpr int kModeCodes16 = 4;
 
 // W4A8 widens int8 activation codes to fp16 inside the GEMM (through a staging
 // slot) for token tiles up to this size; larger tiles use a separate widening pass.
@@ -199,14 +193,15 @@ constexpr int kMsLongChunksPerSm = 32;
 // = 41 MB, well inside the 129 MB L2).
 constexpr int kMsL2AheadChunks = 16;
 QW_HD bool ms_kernel(int mode, int M) {
-  return (mode == 0 || mode == 1 || mode == 3) && M >= 1 && M <= kMsMaxTokens;
+  return (mode == 0 || mode == 1 || mode == kModeCodes16) && M >= 1 && M <= kMsMaxTokens;
 }
 // token rows of its activation tiles: 8 (one tile of eight tokens) or 16
 QW_HD int ms_rows(int M) { return M <= 8 ? 8 : 16; }
 // 16-row blocks of a chunk per warp: 4 for long launches of up to 8 tokens from fp16
-// activations (more independent MMA chains per warp), else 2.  A team computes one chunk
-// at a time with 8 / (row blocks per warp) warps, so there are as many teams as row blocks
-// per warp.
+// activations (more independent MMA chains per warp), else 2 (W4A8 always: the fp16-code
+// plan sums in the order of the int8 one, which makes the two paths bit-identical).  A
+// team computes one chunk at a time with 8 / (row blocks per warp) warps, so there are as
+// many teams as row blocks per warp.
 QW_HD int ms_row_blocks(int mode, int M, bool long_launch) { return long_launch && mode == 0 && M <= 8 ? 4 : 2; }
 // the teams other than the first leave their sums here at the end of a tile segment
 QW_HD int ms_red_bytes(int M, int teams) { return (teams - 1) * ms_rows(M) * kMsRedStride * 4; }
@@ -214,15 +209,12 @@ QW_HD int ms_red_bytes(int M, int teams) { return (teams - 1) * ms_rows(M) * kMs
 QW_HD int ms_xstage_bytes(int mode, int M) {
   return 4 * ms_rows(M) * kGroup * (mode == 1 ? 3 : 2);
 }
-// shared-memory floats of the in-kernel quantizer: per-warp amax [8][16], scales [16] and
-// reciprocals [16]
-constexpr int kMsQuantFloats = 8 * 16 + 16 + 16;
 // ring depths: three activation blocks when that leaves eight weight slots, else two;
 // the weight slots (at most kMaxWStages) split evenly between the teams
 QW_HD bool ms_ring_depths(int mode, int M, int teams, int &xst, int &wst) {
   const int xb = ms_xstage_bytes(mode, M), wb = (int)align_up((size_t)kChunkW4, 128);
   for (int x = 3; x >= 2; --x) {
-    int w = (kMsSmemLimit - kSmemReserve - ms_red_bytes(M, teams) - kMsQuantFloats * 4 - x * xb) / wb;
+    int w = (kMsSmemLimit - kSmemReserve - ms_red_bytes(M, teams) - x * xb) / wb;
     if (w > kMaxWStages) w = kMaxWStages;
     w -= w % teams;
     if (w >= 8 || (x == 2 && w >= 2 * teams)) { xst = x; wst = w; return true; }
@@ -299,10 +291,10 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   if (mode < 0 || mode > 3 || M < 0 || N < 0 || K < 0 || num_sms < 1) return -1;
   if (N % kRows || K % kGroup) return -2;
   if (num_sms > kMaxGrid / 2) num_sms = kMaxGrid / 2;
-  P.fused = quant_in_kernel(mode, M, K) ? 1 : 0;
-  // mode 3 outside the fused range is the quantizer followed by a mode-1 plan
-  const bool quant_first = mode == 3 && !P.fused;
-  if (quant_first) mode = 1;
+  P.fused = 0;
+  // mode 3 is the quantizer (fp16 codes) followed by a kModeCodes16 plan
+  const bool quant_first = mode == 3;
+  if (quant_first) mode = kModeCodes16;
   P.mode = mode; P.M = M; P.N = N; P.K = K;
   P.bn = pick_bn(M);
   P.U = (M + P.bn - 1) / P.bn;
@@ -329,7 +321,7 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
     P.ms_red_bytes = ms_red_bytes(M, P.ms_teams);
     if (!ms_ring_depths(mode, M, P.ms_teams, P.xstages, P.stages)) return -2;
     P.smem_bytes = P.xstages * ms_xstage_bytes(mode, M) + P.stages * wstage_bytes(mode) + P.ms_red_bytes +
-                   kMsQuantFloats * 4 + kSmemReserve;
+                   kSmemReserve;
   } else {
     P.ms_red_bytes = 0;
     if (!ring_depths(mode, P.bn, P.xstages, P.stages)) return -2;
@@ -342,8 +334,8 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   P.ws_counters = align_up((size_t)kStreamKMaxTilesPerSm * num_sms * 4, 256);
   P.ws_partials = P.stream_k ? (size_t)2 * P.grid * P.bn * kRows * 4 : 0;
   P.ws_act = (mode == 1 && !act8_in_kernel(mode, P.bn)) ? align_up((size_t)M * K * 2, 256) : 0;
-  // quantizer output (int8 codes, then binary32 token scales) when it runs first
-  P.ws_quant = quant_first ? align_up((size_t)M * K, 256) + align_up((size_t)M * 4, 256) : 0;
+  // quantizer output (fp16 codes, then binary32 token scales) when it runs first
+  P.ws_quant = quant_first ? align_up((size_t)M * K * 2, 256) + align_up((size_t)M * 4, 256) : 0;
   P.ws_zero = P.ws_counters;
   P.ws_bytes = P.ws_counters + P.ws_partials + P.ws_act + P.ws_quant;
   return 0;

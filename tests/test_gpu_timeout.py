@@ -46,9 +46,7 @@ CASES = [
     ("w4a16", 1, 256, 256),        # decode kernel, one 8-token tile, stream-K split
     ("w4a16", 16, 256, 512),       # decode kernel, 16 tokens
     ("w4a8", 16, 256, 512),        # decode kernel widening int8 codes
-    ("w4a8_fused", 4, 4096, 6144), # decode kernel quantizing fp16 rows itself (more chunks
-                                   # than ring slots: with every row read before the first
-                                   # wait, only the copy threads' second-lap waits can pend)
+    ("w4a8_fused", 4, 4096, 6144), # the quantizer, then the decode kernel on fp16 codes
     ("w4a16", 64, 256, 512),       # tcgen05 GEMM, 64-token tile, two MMA issuers
     ("w4a8", 64, 384, 512),        # tcgen05 GEMM, int8 widened in the kernel
     ("w8a16", 16, 256, 512),       # tcgen05 GEMM, int8 weights, four issuers
