@@ -55,12 +55,12 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "qgemm_ms_kernel_proj_w4a16_m16.md")
-KERNEL_SOURCES = ("gemm_ms.cuh", "gemm_kernel.cuh", "ptx.cuh", "schedule.h")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "qgemm_rb_kernel_proj_w4a16_m16.md")
+KERNEL_SOURCES = ("gemm_rb.cuh", "gemm_ms.cuh", "gemm_kernel.cuh", "ptx.cuh", "schedule.h")
 
 
 def profiled_traffic():
-    """DRAM bytes (read + write) of one M = 16 projection launch of the decode-batch
+    """DRAM bytes (read + write) of one M = 16 projection launch of the row-block decode
     kernel, from the committed ncu summary, provided the kernel sources still hash to
     what was profiled; else None."""
     try:
@@ -84,6 +84,13 @@ def w4a8_kernels(M, N, K):
     import int8_weight_quantized_int4_gb300 as q
     p = q.plan(q.MODE_W4A8_FUSED, M, N, K, torch.cuda.get_device_properties(0).multi_processor_count)
     return 1 if p.fused else 2
+
+
+def gemm_kernel_name(M, N, K):
+    """The GEMM kernel a W4A16 call of this shape runs on (from the library's plan)."""
+    import int8_weight_quantized_int4_gb300 as q
+    p = q.plan(q.MODE_W4A16, M, N, K, torch.cuda.get_device_properties(0).multi_processor_count)
+    return "qgemm_rb_kernel" if p.decode_row_blocks else "qgemm_ms_kernel" if p.decode_teams else "qgemm_tc_kernel"
 
 
 def w4_bytes(n, k):
@@ -388,13 +395,13 @@ def run_ours(args):
                 "TFLOPS": round(flops / us / 1e6, 2), "alg_GBps": round(alg / us / 1e3, 1),
                 "frac_hbm": round(alg / us / 1e3 / hbm, 4),
                 "kernels_per_layer": 1 if mode == "w4a16" else w4a8_kernels(M, N, K),
-                "kernel": "qgemm_ms_kernel" if M <= 16 else "qgemm_tc_kernel"}
+                "kernel": gemm_kernel_name(M, N, K)}
         return per, table
 
     per, per_m = per_m_table(blocks)
     _, per_m_default = per_m_table(blocks_default)
-    # roofline of the dominant kernel: the decode-batch kernel (M <= 16, both modes, about
-    # two thirds of the step's device time), W4A16 launches at M = 1, 4, 16
+    # roofline of the dominant kernel: the decode kernel (M <= 16, both modes), W4A16
+    # launches at M = 1, 4, 16
     roof_bytes = roof_ms = 0.0
     for (mode, M), v in per.items():
         if mode == "w4a16" and M <= 16:
@@ -402,7 +409,7 @@ def run_ours(args):
             roof_ms += sum(v)
     achieved = roof_bytes / (roof_ms / 1e3) / 1e9
     traffic = profiled_traffic()
-    roofline = {"bound": "hbm", "kernel": "qgemm_ms_kernel (W4A16, M = 1, 4, 16, K = N = 5120)",
+    roofline = {"bound": "hbm", "kernel": gemm_kernel_name(1, N, K) + " (W4A16, M = 1, 4, 16, K = N = 5120)",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "peak_source": pk_src + " (hbm_gbs)",
                 "traffic": traffic,

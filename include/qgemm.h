@@ -405,14 +405,24 @@ typedef struct {
     int fused;              /* 1 when W4A8's quantizer runs inside the GEMM (0: no plan does) */
     int decode_teams;       /* > 0: int4 weights and M <= 16 run on the decode-batch kernel
                                (warp-level MMA), with this many teams of four warps */
+    int decode_row_blocks;  /* > 0: int4 weights and M <= 16 on a layer of at most 3 x
+                               num_sms 16-row blocks run on the row-block decode kernel:
+                               every CTA owns at most this many whole row blocks (all of K),
+                               no stream-K split (stream_k = 0, no segments) */
 } qw_plan_t;
 
 int qw_plan(int mode, int M, int N, int K, int num_sms, qw_plan_t *out);
 
 /* The segments (tile, first group, end group, partial slot or -1) CTA `cta`
- * processes under `plan`, in order; returns how many, writing at most `cap`. */
+ * processes under `plan`, in order; returns how many, writing at most `cap`
+ * (0 under a row-block plan: see qw_plan_row_blocks). */
 int qw_plan_segments(const qw_plan_t *plan, int cta, int cap, long long *tile, int *g0,
                      int *g1, int *slot);
+
+/* Under a row-block plan (decode_row_blocks > 0): the 16-row blocks [*rb_begin, *rb_end)
+ * CTA `cta` computes over all of K (rows 16 * rb_begin .. 16 * rb_end - 1 of y).  Returns
+ * QW_OK, or QW_ERR_INVALID_ARG for another plan or a CTA outside the grid. */
+int qw_plan_row_blocks(const qw_plan_t *plan, int cta, int *rb_begin, int *rb_end);
 
 #ifdef __cplusplus
 }

@@ -42,7 +42,8 @@ class Plan(ctypes.Structure):
     _fields_ = [("bn", _i), ("token_tiles", _i), ("row_tiles", _i), ("groups", _i),
                 ("tiles", _ll), ("chunks", _ll), ("grid", _i), ("stream_k", _i), ("stages", _i),
                 ("smem_bytes", _i), ("ws_bytes", _sz), ("ws_zero_bytes", _sz),
-                ("act_stages", _i), ("act_block", _i), ("fused", _i), ("decode_teams", _i)]
+                ("act_stages", _i), ("act_block", _i), ("fused", _i), ("decode_teams", _i),
+                ("decode_row_blocks", _i)]
 
 
 SIGNATURES = {
@@ -78,6 +79,7 @@ SIGNATURES = {
     "qw_diag_f8f6f4_gemm": (_i, [_p, _p, _i, _i, _p, _p]),
     "qw_plan": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(Plan)]),
     "qw_plan_segments": (_i, [ctypes.POINTER(Plan), _i, _i, _p, _p, _p, _p]),
+    "qw_plan_row_blocks": (_i, [ctypes.POINTER(Plan), _i, _p, _p]),
 }
 
 _lib = None
@@ -537,3 +539,10 @@ def plan_segments(p: Plan, cta: int):
     slot = (ctypes.c_int * max(n, 1))()
     lib().qw_plan_segments(ctypes.byref(p), cta, n, tile, g0, g1, slot)
     return [(tile[i], g0[i], g1[i], slot[i]) for i in range(n)]
+
+
+def plan_row_blocks(p: Plan, cta: int):
+    """Under a row-block plan: the 16-row blocks (begin, end) CTA `cta` computes."""
+    b, e = ctypes.c_int(), ctypes.c_int()
+    _check(lib().qw_plan_row_blocks(ctypes.byref(p), cta, ctypes.byref(b), ctypes.byref(e)))
+    return b.value, e.value

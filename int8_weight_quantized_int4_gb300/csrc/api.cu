@@ -88,8 +88,7 @@ int current_device(DevInfo *&out) {
 // cuTensorMapEncodeTiled, fetched once through the runtime's driver entry point
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
-
-int encode_act_map(CUtensorMap *map, const void *ptr, int M, int K, int bn, int block, bool int8) {
+bool load_encoder() {
   std::call_once(g_encode_once, [] {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -99,7 +98,11 @@ int encode_act_map(CUtensorMap *map, const void *ptr, int M, int K, int bn, int 
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     cudaGetLastError();
   });
-  if (!g_encode) return fail(QW_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  return g_encode != nullptr;
+}
+
+int encode_act_map(CUtensorMap *map, const void *ptr, int M, int K, int bn, int block, bool int8) {
+  if (!load_encoder()) return fail(QW_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   const cuuint32_t estride[3] = {1, 1, 1};
   CUresult r;
   if (int8) {
@@ -123,6 +126,28 @@ int encode_act_map(CUtensorMap *map, const void *ptr, int M, int K, int bn, int 
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
   if (r != CUDA_SUCCESS) return fail(QW_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return QW_OK;
+}
+
+// The packed int4 weights [N/128 row tiles][K/128 groups][8448 B] seen as 8-byte words
+// [T][G][1056] for the row-block decode kernel: `codes` boxes are one row block's 1 KB of
+// codes (128 words from word 128 b) over kRbXBlock groups; scale boxes its 32 B of scales
+// (4 words from word 1024 + 4 b).  Unswizzled, zero fill past the last group.
+int encode_weight_maps(CUtensorMap *codes, CUtensorMap *scales, const void *packed, int N, int K) {
+  if (!load_encoder()) return fail(QW_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const cuuint64_t gdim[3] = {qw::kChunkW4 / 8, (cuuint64_t)K / 128, (cuuint64_t)N / 128};
+  const cuuint64_t gstride[2] = {(cuuint64_t)qw::kChunkW4, (cuuint64_t)qw::kChunkW4 * (K / 128)};
+  const cuuint32_t cbox[3] = {128u, (cuuint32_t)qw::kRbXBlock, 1u};
+  const cuuint32_t sbox[3] = {4u, (cuuint32_t)qw::kRbXBlock, 1u};
+  CUresult r = g_encode(codes, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void *>(packed), gdim, gstride,
+                        cbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS)
+    r = g_encode(scales, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void *>(packed), gdim, gstride, sbox,
+                 estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(QW_ERR_CUDA, "cuTensorMapEncodeTiled (weights) failed (%d)", (int)r);
   return QW_OK;
 }
 
@@ -175,8 +200,13 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
   a.tile_max = tile_max;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  // the decode-batch kernel's activation tiles hold 8 or 16 token rows
-  const int box_rows = P.ms_teams ? qw::ms_rows(M) : P.bn;
+  // the decode-batch kernels' activation tiles hold 8 or 16 token rows
+  const bool decode = P.ms_teams > 0 || P.rb_max > 0;
+  const int box_rows = decode ? qw::ms_rows(M) : P.bn;
+  if (P.rb_max && (rc = encode_weight_maps(&a.wmap, &a.smap, packed, N, K))) return rc;
+  auto launch_decode = [&](int act) {
+    return P.rb_max ? qw::launch_gemm_rb(a, act, st) : qw::launch_gemm_ms(a, act, st);
+  };
   if (mode == QW_MODE_W4A8_FUSED) {
     // the standalone quantizer writes fp16 codes and token scales into the workspace;
     // the W4A8 GEMM reads the codes as fp16 tiles (plan mode kModeCodes16)
@@ -186,10 +216,10 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
     if (e != cudaSuccess) return fail_cuda(e, "quant kernel launch");
     a.xs = s;
     if ((rc = encode_act_map(&a.tmap, q, M, K, box_rows, P.xblock, false))) return rc;
-    e = P.ms_teams ? qw::launch_gemm_ms(a, 2, st) : qw::launch_gemm_w4a8(a, false, st);
+    e = decode ? launch_decode(2) : qw::launch_gemm_w4a8(a, false, st);
   } else if (mode == QW_MODE_W4A8 && qw::act8_in_kernel(mode, P.bn)) {
     if ((rc = encode_act_map(&a.tmap, act, M, K, box_rows, P.xblock, true))) return rc;
-    e = P.ms_teams ? qw::launch_gemm_ms(a, 1, st) : qw::launch_gemm_w4a8(a, true, st);
+    e = decode ? launch_decode(1) : qw::launch_gemm_w4a8(a, true, st);
   } else if (mode == QW_MODE_W4A8) {
     uint16_t *wide = reinterpret_cast<uint16_t *>(w + P.ws_counters + P.ws_partials);
     if ((rc = encode_act_map(&a.tmap, wide, M, K, P.bn, P.xblock, false))) return rc;
@@ -199,7 +229,7 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
   } else {
     if ((rc = encode_act_map(&a.tmap, act, M, K, box_rows, P.xblock, false))) return rc;
     e = mode == QW_MODE_W8A16 ? qw::launch_gemm_w8a16(a, st)
-        : P.ms_teams          ? qw::launch_gemm_ms(a, 0, st)
+        : decode              ? launch_decode(0)
                               : qw::launch_gemm_w4a16(a, st);
   }
   if (e != cudaSuccess) return fail_cuda(e, "GEMM kernel launch");
@@ -603,12 +633,24 @@ int qw_plan(int mode, int M, int N, int K, int num_sms, qw_plan_t *out) {
   out->act_block = P.xblock;
   out->fused = P.fused;
   out->decode_teams = P.ms_teams;
+  out->decode_row_blocks = P.rb_max;
+  return QW_OK;
+}
+
+int qw_plan_row_blocks(const qw_plan_t *plan, int cta, int *rb_begin, int *rb_end) {
+  if (!plan || plan->decode_row_blocks < 1 || cta < 0 || cta >= plan->grid || !rb_begin || !rb_end)
+    return fail(QW_ERR_INVALID_ARG, "bad query");
+  // the planner's balanced split of the N / 16 row blocks over the grid
+  const long long RB = (long long)plan->row_tiles * 8;
+  *rb_begin = (int)(cta * RB / plan->grid);
+  *rb_end = (int)((cta + 1) * RB / plan->grid);
   return QW_OK;
 }
 
 int qw_plan_segments(const qw_plan_t *plan, int cta, int cap, long long *tile, int *g0, int *g1,
                      int *slot) {
   if (!plan || cta < 0 || cta >= plan->grid || cap < 0) return fail(QW_ERR_INVALID_ARG, "bad query");
+  if (plan->decode_row_blocks > 0) return 0;
   qw::Plan P{};
   P.bn = plan->bn;
   P.U = plan->token_tiles;

@@ -12,6 +12,9 @@ namespace qw {
 struct GemmArgs {
   CUtensorMap tmap;         // activations: fp16 [M,K] (64 x bn boxes, 128-byte swizzle) or
                             // int8 [M,K] (128 x bn boxes) for W4A8 at decode sizes
+  CUtensorMap wmap, smap;   // row-block decode kernel: the packed int4 weights seen as
+                            // [row tiles][groups][1056 x 8 B]: boxes of one row block's codes
+                            // (1 KB) and scales (32 B) over 8 consecutive groups
   Plan P;
   const float *xs;          // token scales [M] (W4A8) or nullptr
   const uint8_t *wpack;     // packed weights
@@ -109,5 +112,7 @@ cudaError_t launch_gemm_w8a16(const GemmArgs &a, cudaStream_t st);
 // decode batches (plan.ms_teams > 0); act: 0 fp16 activations (W4A16), 1 int8 codes and
 // token scales (W4A8), 2 fp16 codes and token scales (W4A8 after the quantizer)
 cudaError_t launch_gemm_ms(const GemmArgs &a, int act, cudaStream_t st);
+// decode batches on layers of few rows (plan.rb_max > 0): the row-block kernel, act as above
+cudaError_t launch_gemm_rb(const GemmArgs &a, int act, cudaStream_t st);
 
 }  // namespace qw

@@ -47,6 +47,8 @@ struct Plan {
   int ms_teams;                  // > 0: the warp-level MMA kernel for decode batches (M <= 16),
                                  // with this many teams of warps (one chunk per team at a time)
   int ms_red_bytes;              // its shared-memory buffer for the teams' partial sums
+  int rb_max;                    // > 0: the row-block decode kernel, at most this many 16-row
+                                 // blocks per CTA (begin[p]: first row block of CTA p)
   float grid_per_chunk;          // grid / chunks, to estimate a chunk's owner
   size_t ws_counters, ws_partials, ws_act, ws_quant, ws_bytes, ws_zero;
   int begin[kMaxGrid + 1];       // stream-K: first chunk of each CTA (begin[grid] = chunks)
@@ -222,6 +224,37 @@ QW_HD bool ms_ring_depths(int mode, int M, int teams, int &xst, int &wst) {
   return false;
 }
 
+// Decode batches on layers of few rows: the row-block kernel.  When the layer's 16-row
+// blocks (N / 16) number at most kRbMax per SM, every CTA takes a contiguous range of 1 to
+// kRbMax row blocks over the whole K and its compute warps split the K groups, adding their
+// sums in shared memory at the end: no tile is cut between CTAs, so there are no partial
+// sums, no tile counters and no last-arriver reduction.  Up to 8 tokens a launch long
+// enough for two tile-kernel CTAs per SM (kMsLongChunksPerSm) stays on the tile kernel,
+// which measured faster there (a 5120 x 17408 layer: 15.1 against 17.6 us at one token).
+constexpr int kRbMax = 3;                 // row blocks per CTA at most
+constexpr int kRbXBlock = 8;              // K groups per ring stage: one per compute warp
+constexpr int kRbMaxStages = 6;
+QW_HD bool rb_kernel(int mode, int M, int N, int K, int num_sms) {
+  if (!ms_kernel(mode, M) || (long long)(N / 16) > (long long)kRbMax * num_sms) return false;
+  return ms_rows(M) > 8 || (long long)(N / kRows) * (K / kGroup) < (long long)kMsLongChunksPerSm * num_sms;
+}
+// one ring stage holds the data of kRbXBlock consecutive K groups: the activation tiles
+// (8 groups of ms_rows(M) x 128 fp16, + the int8 staging tiles for W4A8 from int8 codes),
+// then per row block the 8 groups' codes (8 x 1 KB) and scales (8 x 32 B); a multiple of
+// 1 KB (the activation tiles' 128-byte swizzle)
+QW_HD int rb_x_bytes(int mode, int M) { return kRbXBlock * ms_rows(M) * kGroup * (mode == 1 ? 3 : 2); }
+constexpr int kRbWBytes = kRbMax * kRbXBlock * 1024;     // codes of a stage
+constexpr int kRbSBytes = kRbMax * kRbXBlock * 32;       // scales of a stage
+QW_HD int rb_stage_bytes(int mode, int M) {
+  return (int)align_up((size_t)(rb_x_bytes(mode, M) + kRbWBytes + kRbSBytes), 1024);
+}
+// one CTA per SM, as many stages as fit (at most kRbMaxStages, at least 2)
+QW_HD bool rb_ring_depths(int mode, int M, int &st) {
+  st = (kSmemLimit - kSmemReserve) / rb_stage_bytes(mode, M);
+  if (st > kRbMaxStages) st = kRbMaxStages;
+  return st >= 2;
+}
+
 // Ring depths: the deepest activation ring (at most kMaxXStages, or 3 for token
 // tiles up to 64 whose blocks already span several groups, at least 2) that still
 // leaves four weight slots; the weight ring takes the rest (at most kMaxWStages),
@@ -317,7 +350,23 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   fill_begin(P);
   P.xblock = act_block(P.bn);
   P.ms_teams = ms_kernel(mode, M) ? ms_row_blocks(mode, M, ctas > num_sms) : 0;
-  if (P.ms_teams) {
+  P.rb_max = 0;
+  if (P.chunks > 0 && rb_kernel(mode, M, N, K, num_sms)) {
+    // the row-block kernel: CTA p takes row blocks [begin[p], begin[p + 1])
+    const int RB = N / 16;
+    P.ms_teams = 0;
+    P.stream_k = 0;
+    P.grid = RB < num_sms ? RB : num_sms;
+    for (int p = 0; p <= kMaxGrid; ++p)
+      P.begin[p] = p <= P.grid ? (int)((long long)p * RB / P.grid) : RB;
+    P.rb_max = (RB + P.grid - 1) / P.grid;
+    for (int p = 0; p < kMaxGrid; ++p) P.cut[p][0] = P.cut[p][1] = 0;
+    P.xblock = kRbXBlock;
+    P.ms_red_bytes = 0;
+    if (!rb_ring_depths(mode, M, P.stages)) return -2;
+    P.xstages = P.stages;
+    P.smem_bytes = P.stages * rb_stage_bytes(mode, M) + kSmemReserve;
+  } else if (P.ms_teams) {
     P.ms_red_bytes = ms_red_bytes(M, P.ms_teams);
     if (!ms_ring_depths(mode, M, P.ms_teams, P.xstages, P.stages)) return -2;
     P.smem_bytes = P.xstages * ms_xstage_bytes(mode, M) + P.stages * wstage_bytes(mode) + P.ms_red_bytes +
@@ -332,7 +381,7 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   // that no plan's partials or widened activations ever overlap another plan's
   // counters: a workspace zeroed once stays valid for calls of any shape.
   P.ws_counters = align_up((size_t)kStreamKMaxTilesPerSm * num_sms * 4, 256);
-  P.ws_partials = P.stream_k ? (size_t)2 * P.grid * P.bn * kRows * 4 : 0;
+  P.ws_partials = P.stream_k ? (size_t)2 * P.grid * P.bn * kRows * 4 : 0;   // (row-block plans: 0)
   P.ws_act = (mode == 1 && !act8_in_kernel(mode, P.bn)) ? align_up((size_t)M * K * 2, 256) : 0;
   // quantizer output (fp16 codes, then binary32 token scales) when it runs first
   P.ws_quant = quant_first ? align_up((size_t)M * K * 2, 256) + align_up((size_t)M * 4, 256) : 0;

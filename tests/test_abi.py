@@ -174,12 +174,35 @@ SHAPES = [
 ]
 
 
+def _check_row_blocks(p, M, N, sms):
+    """Row-block plan: the N / 16 row blocks split into consecutive ranges of 1..rb_max
+    (balanced within one) over min(N / 16, sms) CTAs, no stream-K, no segments."""
+    RB = N // 16
+    assert M <= 16 and RB <= 3 * sms and p.stream_k == 0 and p.decode_teams == 0
+    assert p.grid == min(RB, sms) and 1 <= p.decode_row_blocks <= 3
+    assert p.decode_row_blocks == -(-RB // p.grid)
+    # one ring of stages of 8 K groups (activations and weights), 2 to 6 deep, one CTA per SM
+    assert p.act_block == 8 and p.act_stages == p.stages and 2 <= p.stages <= 6
+    assert p.smem_bytes <= 232448
+    nxt, sizes = 0, []
+    for cta in range(p.grid):
+        assert q.plan_segments(p, cta) == []
+        b, e = q.plan_row_blocks(p, cta)
+        assert b == nxt and e > b
+        nxt = e
+        sizes.append(e - b)
+    assert nxt == RB and max(sizes) - min(sizes) <= 1 and max(sizes) == p.decode_row_blocks
+
+
 @pytest.mark.parametrize("mode,M,N,K,sms", SHAPES)
 def test_schedule_covers_every_chunk_once(mode, M, N, K, sms):
     p = q.plan(mode, M, N, K, sms)
     assert p.bn in (16, 32, 64, 128, 256) and p.bn >= min(M, 256)
     assert p.token_tiles == -(-M // p.bn) and p.row_tiles == N // 128 and p.groups == K // 128
     assert 1 <= p.grid <= sms and p.stages >= 2 and p.smem_bytes <= 232448
+    if p.decode_row_blocks:
+        _check_row_blocks(p, M, N, sms)
+        return
     seen = {}
     slots = set()
     pieces = {}
@@ -217,10 +240,34 @@ def test_schedule_covers_every_chunk_once(mode, M, N, K, sms):
         assert max(load.values()) <= -(-p.groups // b) and min(load.values()) >= p.groups // (b + 1)
 
 
+def test_schedule_row_blocks_for_decode_projections():
+    """Decode batches (M <= 16, int4 weights) on a 5120-row layer: the row-block kernel,
+    320 row blocks over 152 CTAs (2 or 3 each); a layer of more than 3 x 152 row blocks,
+    or up to 8 tokens over at least 32 chunks per SM, keeps the tile-based decode kernel."""
+    for mode in (0, 1, 3):
+        for M in (1, 4, 8, 9, 16):
+            for K in (5120, 17408):
+                p = q.plan(mode, M, 5120, K, 152)
+                if K == 17408 and M <= 8:              # 5440 chunks: 35.8 per SM
+                    assert p.decode_row_blocks == 0 and p.decode_teams > 0 and p.grid == 304
+                    continue
+                assert p.decode_row_blocks == 3 and p.grid == 152
+                _check_row_blocks(p, M, 5120, 152)
+    assert q.plan(0, 1, 7296, 5120, 152).decode_row_blocks == 3
+    p = q.plan(0, 1, 7424, 5120, 152)
+    assert p.decode_row_blocks == 0 and p.decode_teams > 0
+    assert q.plan(0, 1, 248320, 5120, 152).decode_row_blocks == 0
+    assert q.plan(0, 17, 5120, 5120, 152).decode_row_blocks == 0        # the tcgen05 GEMM
+    assert q.plan(2, 16, 5120, 5120, 152).decode_row_blocks == 0        # int8 weights
+    p = q.plan(0, 2, 256, 1024, 152)                                      # fewer row blocks than SMs
+    assert p.grid == 16 and p.decode_row_blocks == 1
+    _check_row_blocks(p, 2, 256, 152)
+
+
 def test_schedule_tile_aligned_split_for_short_launches():
     """Projection-sized stream-K launches (>= 3 CTAs per tile, <= 16 chunks per CTA) cut
     every tile into b or b+1 equal pieces, one piece per CTA, larger pieces first."""
-    for mode, M in ((0, 1), (1, 16), (0, 64)):
+    for mode, M in ((0, 32), (1, 64), (0, 64)):
         p = q.plan(mode, M, 5120, 5120, 152)
         assert p.stream_k == 1 and p.tiles == 40 and p.grid == 152
         pieces = {}
@@ -371,6 +418,9 @@ def test_schedule_partition_random_shapes():
             continue
         # one CTA per SM; the decode-batch kernel (half an SM each) runs two for long launches
         assert 1 <= p.grid <= (2 * sms if p.decode_teams else sms) and p.smem_bytes <= 232448 and p.stages >= 2
+        if p.decode_row_blocks:
+            _check_row_blocks(p, M, N, sms)
+            continue
         if p.decode_teams:
             assert p.smem_bytes <= 113 * 1024 and M <= 16 and mode in (0, 1, 3)
         assert p.bn >= min(M, 256) and p.token_tiles == -(-M // p.bn)

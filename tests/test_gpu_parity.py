@@ -228,6 +228,35 @@ def test_ffn_pair_m64_w4a8(q):
     assert max(e_up.values()) <= TOL and max(e_dn.values()) <= TOL, (e_up, e_dn)
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 5120, 5120), (3, 7296, 1152), (8, 2048, 640), (9, 5120, 2944),
+                                   (16, 256, 128), (16, 4864, 17408), (5, 384, 8192), (2, 4096, 3072)])
+def test_row_block_kernel(q, M, N, K):
+    """Decode batches on layers of at most 3 x SMs 16-row blocks run on the row-block
+    kernel: row blocks straddling 128-row tiles, K not a multiple of the 8-group stage
+    (ragged last stage), fewer row blocks than SMs, one and two tiles of 8 tokens.  Every
+    output (or a column sample of the widest) against the oracle in both modes, W4A8 from
+    fp16 bit-identical to the two-step path, repeated calls bit-identical."""
+    p = synth.make_problem(M, N, K, seed=5100 + M + N // 128 + K // 128, outlier_frac=0.01)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    pl = q.plan(q.MODE_W4A16, M, N, K, sms)
+    if N // 16 > 3 * sms:
+        pytest.skip("more row blocks than this device's row-block plans take")
+    assert pl.decode_row_blocks > 0 and pl.stream_k == 0, (pl.decode_row_blocks, pl.decode_teams)
+    cols = None if N * K <= 5120 * 5120 else torch.arange(0, N, 3)
+    e = run_modes(q, p, ("w4a16", "w4a8"), cols=cols)
+    assert max(e.values()) <= TOL, e
+    xd = p.x.to(DEV)
+    packed = q.qpack_w4(p.codes.to(DEV), p.scales.to(DEV))
+    y1 = q.qgemm_w4a16(xd, packed, N, K)
+    y2 = q.qgemm_w4a16(xd, packed, N, K)
+    xq, xs = q.quant_act_int8(xd)
+    z1 = q.qgemm_w4a8(xq, xs, packed, N, K)
+    z2 = q.qgemm_w4a8_fused(xd, packed, N, K)
+    torch.cuda.synchronize()
+    assert q.device_error() == 0
+    assert np.array_equal(bits(y1), bits(y2)) and np.array_equal(bits(z1), bits(z2))
+
+
 @pytest.mark.parametrize("M", [1, 5, 16])
 def test_decode_long_launch_two_ctas_per_sm(q, M):
     """A decode-sized batch over enough chunks that the schedule runs two CTAs per SM
