@@ -94,8 +94,10 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
   // named barrier, so that all of them pass the same barriers
   volatile int *decide = reinterpret_cast<volatile int *>(gbars + 192);
   volatile WaitBlock *wctl = reinterpret_cast<volatile WaitBlock *>(gbars + 200);
-  // the compute warps' sums at the end: [warp][row block][token][16 rows] binary32, over
-  // the ring (every copy into it has been waited for by then)
+  // the compute warps' sums at the end: [warp][row block][token][16 rows, padded to kRS]
+  // binary32 (the padding spreads a warp's stores over the banks), over the ring (every
+  // copy into it has been waited for by then)
+  constexpr int kRS = 17;
   float *red = reinterpret_cast<float *>(gbase);
   auto pwait = [&](uint32_t bar, uint32_t parity) { return mbar_wait(bar, parity, wctl, a.wait_ns == 0); };
   auto stage = [&](int s) { return sbase + (uint32_t)s * kStage; };
@@ -297,7 +299,7 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int m = 8 * jt + 2 * c4 + (e & 1), row = g8 + 8 * (e >> 1);
-            red[((cw * RBM + r) * BNX + m) * 16 + row] = acc[r][jt][e];
+            red[((cw * RBM + r) * BNX + m) * kRS + row] = acc[r][jt][e];
           }
     }
     named_bar_sync(1, kCThreads);
@@ -307,7 +309,7 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
         const int r = idx / (mv * 16), m = (idx >> 4) % mv, row = idx & 15;
         float v = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kCompute; ++w) v += red[((w * RBM + r) * BNX + m) * 16 + row];
+        for (int w = 0; w < kCompute; ++w) v += red[((w * RBM + r) * BNX + m) * kRS + row];
         const __half hv = __float2half_rn(TOKS ? v * __ldg(a.xs + m) : v);
         const int n = (rb0 + r) * 16 + row;
         a.y[(size_t)m * P.N + n] = __half_as_ushort(hv);
