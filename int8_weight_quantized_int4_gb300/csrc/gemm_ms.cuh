@@ -233,7 +233,9 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
 #pragma unroll
           for (int j = 0; j < TEAMS; ++j)
             if (j == tm) { slot = j * SWT + s[j]; par = ph[j]; }
-          if (!pwait(wempty_bar(slot), par ^ 1u)) { ok = false; break; }
+          // never a copy after an abort: the compute warps then release slots whose
+          // copies may still be in flight, and a refill would arm the same phase twice
+          if (!pwait(wempty_bar(slot), par ^ 1u) || wctl->abort) { ok = false; break; }
           mbar_arrive_expect_tx(wfull_bar(slot), kChunkW4);
           bulk_g2s(w_smem(slot), src, kChunkW4, wfull_bar(slot), pol);
 #pragma unroll
@@ -258,7 +260,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         for (int g = sg.g0; g < sg.g1; g += kXBlock) {
-          if (!pwait(xempty_bar(s), ph ^ 1u)) { ok = false; break; }
+          if (!pwait(xempty_bar(s), ph ^ 1u) || wctl->abort) { ok = false; break; }
           mbar_arrive_expect_tx(xfull_bar(s), kXBytes);
           ++nfill;
           if constexpr (ACT8) tma_load_3d(x_smem(s) + kXBlock * kXChunk, &a.tmap, 0, 0, g, xfull_bar(s));

@@ -147,7 +147,9 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
       int s = 0, nfill = 0;
       uint32_t ph = 0;
       for (int i = 0; i < nst; ++i) {
-        if (!pwait(empty_bar(s), ph ^ 1u)) break;
+        // never a copy after an abort: the compute warps then release stages whose copies
+        // may still be in flight, and a refill would arm the same phase twice
+        if (!pwait(empty_bar(s), ph ^ 1u) || wctl->abort) break;
         mbar_arrive_expect_tx(wfull_bar(s), (uint32_t)nrb * (kXB * (1024u + 32u)));
         for (int r = 0; r < nrb; ++r) {
           const int rb = rb0 + r;
@@ -168,7 +170,9 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
       int s = 0, nfill = 0;
       uint32_t ph = 0;
       for (int i = 0; i < nst; ++i) {
-        if (!pwait(empty_bar(s), ph ^ 1u)) break;
+        // never a copy after an abort: the compute warps then release stages whose copies
+        // may still be in flight, and a refill would arm the same phase twice
+        if (!pwait(empty_bar(s), ph ^ 1u) || wctl->abort) break;
         mbar_arrive_expect_tx(xfull_bar(s), kXBytes);
         ++nfill;
         if constexpr (ACT8) tma_load_3d(stage(s) + kXB * kXChunk, &a.tmap, 0, 0, i * kXB, xfull_bar(s));
@@ -287,8 +291,11 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
       if (lane == 0) mbar_arrive(empty_bar(s));
       if (++s == SS) { s = 0; ph ^= 1u; }
     }
-    // ---- the eight warps' sums meet in shared memory (over the ring: every copy into it
-    // has been waited for by every compute warp), added in warp order
+    // ---- the warps' sums meet in shared memory (over the ring: every copy into it has
+    // been waited for by every compute warp), added in warp order.  The abort flag is read
+    // once every compute warp has left its loop (no wait of theirs can fail after that):
+    // after an abort a copy may still be landing in the ring, so nothing is written.
+    named_bar_sync(1, kCThreads);
     if (ct == 0) *decide = wctl->abort;
     named_bar_sync(1, kCThreads);
     if (!*decide) {
