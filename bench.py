@@ -80,7 +80,7 @@ def profiled_traffic():
 
 def w4a8_kernels(M, N, K):
     """Kernels one qgemm_w4a8_fused call launches: 1 when the quantizer runs inside
-    the GEMM (no plan does so now), else the quantizer (fp16 codes) + the GEMM."""
+    the GEMM, else the quantizer (fp16 codes) + the GEMM."""
     import int8_weight_quantized_int4_gb300 as q
     p = q.plan(q.MODE_W4A8_FUSED, M, N, K, torch.cuda.get_device_properties(0).multi_processor_count)
     return 1 if p.fused else 2

@@ -262,10 +262,14 @@ int attn_int8qk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
  * item 4: activations quantized to int8 per token, int4 weights).
  *   x [M, K] fp16, device, 16-byte aligned.  Other arguments as qgemm_w4a16;
  *   the workspace is qgemm_workspace_bytes(QW_MODE_W4A8_FUSED, M, N, K).
- * Two launches: the quantizer writes its codes, as fp16 values (exact,
- * |q| <= 127), and the token scales into the workspace; the W4A8 GEMM reads the
- * codes as fp16 tiles (no widening of int8 codes) in the same order of summation
- * as qgemm_w4a8, and multiplies by the token scales in its epilogue.  Async.
+ * When the layer runs on the row-block decode kernel (N / 16 <= 3 x SMs), M <= 2
+ * and the M fp16 rows take at most 48 KB (M*K*2 bytes), one launch: every CTA finds
+ * the token scales (amax over the whole rows, from L2, while its first weights load)
+ * and turns each activation tile into codes in shared memory with the quantizer's
+ * exact arithmetic.  Otherwise two launches: the quantizer writes its codes, as fp16
+ * values (exact, |q| <= 127), and the token scales into the workspace; the W4A8 GEMM
+ * reads the codes as fp16 tiles (no widening of int8 codes) in the same order of
+ * summation as qgemm_w4a8, and multiplies by the token scales in its epilogue.  Async.
  * Returns as qgemm_w4a8.
  * ------------------------------------------------------------------------ */
 int qgemm_w4a8_fused(const uint16_t *x, const void *packed_w4, int M, int N, int K, uint16_t *y,
@@ -402,7 +406,7 @@ typedef struct {
     size_t ws_zero_bytes;   /* leading workspace bytes that must be zero */
     int act_stages;         /* activation ring depth in shared memory (blocks) */
     int act_block;          /* K groups per activation block (one tensor copy) */
-    int fused;              /* 1 when W4A8's quantizer runs inside the GEMM (0: no plan does) */
+    int fused;              /* QW_MODE_W4A8_FUSED: 1 when the quantizer runs inside the GEMM */
     int decode_teams;       /* > 0: int4 weights and M <= 16 run on the decode-batch kernel
                                (warp-level MMA), with this many teams of four warps */
     int decode_row_blocks;  /* > 0: int4 weights and M <= 16 on a layer of at most 3 x

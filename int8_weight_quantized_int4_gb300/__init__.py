@@ -293,7 +293,8 @@ def qgemm_w4a8(xq, xs, packed, N: int, K: int, y=None, ws: Workspace | None = No
 
 def qgemm_w4a8_fused(x, packed, N: int, K: int, y=None, ws: Workspace | None = None):
     """The W4A8 layer from fp16 activations: bit-identical to qgemm_w4a8 applied to
-    quant_act_int8(x).  The quantizer writes fp16 codes that the GEMM reads as fp16 tiles."""
+    quant_act_int8(x).  Small decode batches quantize inside the row-block GEMM; otherwise
+    the quantizer writes fp16 codes that the GEMM reads as fp16 tiles."""
     _need(x, torch.float16, "x", 2)
     M = x.shape[0]
     if x.shape[1] != K:

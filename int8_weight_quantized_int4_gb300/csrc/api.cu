@@ -207,7 +207,12 @@ int gemm_common(int mode, const void *act, const float *xs, const void *packed, 
   auto launch_decode = [&](int act) {
     return P.rb_max ? qw::launch_gemm_rb(a, act, st) : qw::launch_gemm_ms(a, act, st);
   };
-  if (mode == QW_MODE_W4A8_FUSED) {
+  if (mode == QW_MODE_W4A8_FUSED && P.fused) {
+    // the row-block kernel quantizes per token itself: fp16 tiles, as W4A16
+    a.xf16 = static_cast<const uint16_t *>(act);
+    if ((rc = encode_act_map(&a.tmap, act, M, K, box_rows, P.xblock, false))) return rc;
+    e = launch_decode(3);
+  } else if (mode == QW_MODE_W4A8_FUSED) {
     // the standalone quantizer writes fp16 codes and token scales into the workspace;
     // the W4A8 GEMM reads the codes as fp16 tiles (plan mode kModeCodes16)
     uint16_t *q = reinterpret_cast<uint16_t *>(w + P.ws_counters + P.ws_partials + P.ws_act);

@@ -58,8 +58,9 @@ constexpr int kMsWarpC0 = 2;      // first compute warp
 
 // activation modes: fp16 x (W4A16), int8 codes + token scales (W4A8), fp16 codes + token
 // scales (W4A8 from fp16 after the standalone quantizer: the W4A16 data path, the W4A8
-// epilogue)
-enum { kActF16 = 0, kActI8 = 1, kActCodes16 = 2 };
+// epilogue), fp16 x quantized per token inside the kernel (W4A8 from fp16; row-block
+// kernel only)
+enum { kActF16 = 0, kActI8 = 1, kActCodes16 = 2, kActQuant = 3 };
 
 __host__ __device__ constexpr int ms_threads() { return (kMsWarpC0 + kMsComputeWarps) * 32; }
 

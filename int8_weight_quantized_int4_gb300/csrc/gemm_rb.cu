@@ -1,6 +1,6 @@
 // gemm_rb.cu -- instantiations of the row-block decode kernel: W4A16 (with and without
-// the lm_head's tile maxima), W4A8 from int8 codes and W4A8 from fp16 codes; one or two
-// tiles of 8 tokens.
+// the lm_head's tile maxima), W4A8 from int8 codes, from fp16 codes, and from fp16
+// activations quantized in the kernel; one or two tiles of 8 tokens.
 #include "gemm_rb.cuh"
 
 namespace qw {
@@ -21,6 +21,7 @@ cudaError_t launch_gemm_rb(const GemmArgs &a, int act, cudaStream_t st) {
   const bool one = a.P.M <= 8;
   if (act == kActI8) return one ? run_rb<1, kActI8>(a, st) : run_rb<2, kActI8>(a, st);
   if (act == kActCodes16) return one ? run_rb<1, kActCodes16>(a, st) : run_rb<2, kActCodes16>(a, st);
+  if (act == kActQuant) return one ? run_rb<1, kActQuant>(a, st) : cudaErrorInvalidValue;
   if (a.tile_max) return one ? run_rb<1, kActF16, true>(a, st) : run_rb<2, kActF16, true>(a, st);
   return one ? run_rb<1, kActF16>(a, st) : run_rb<2, kActF16>(a, st);
 }

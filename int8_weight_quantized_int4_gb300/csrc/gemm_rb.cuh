@@ -28,7 +28,8 @@
 //                    the weights become MMA fragments (mma.sync m16n8k16, weights as the A
 //                    operand in registers) and accumulate into a per-group fp32 sum per row
 //                    block, scaled by the signed group scale into the running sum.  int8
-//                    activations are first widened to fp16 in the tile by all the warps.
+//                    activations are first widened to fp16 in the tile, and fp16 ones to
+//                    be quantized in the kernel turned into codes, each warp its own half.
 //                    At the end the sixteen sums of every output are added in warp order in
 //                    shared memory (deterministic) and written as fp16 y.
 #pragma once
@@ -46,6 +47,27 @@ namespace qw {
 constexpr int kRbCompute = 16;                        // compute warps
 __host__ __device__ constexpr int rb_threads() { return (kMsWarpC0 + kRbCompute) * 32; }
 
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// q = clamp(rne(x / s), -127, 127) with x / s the IEEE binary32 quotient, as the standalone
+// quantizer computes it, without a divide per value: t = x * (1/s) (correctly rounded
+// reciprocal and product) is within 3 * 2^-24 * |x/s| <= 2.3e-5 of the quotient, since
+// |x/s| <= 127 (1 + 2^-24).  So rne(t) = rne(x / s) unless t lies within 2^-14 of a
+// half-integer, i.e. unless |t - rne(t)| >= 0.5 - 2^-14 (t - rne(t) is exact); only those
+// values take the IEEE divide, out of line so that it is skipped rather than computed and
+// discarded.  s = 0 (an all-zero row) has 1/s = 0, so t = 0 and q = 0, as the quantizer.
+static __device__ __noinline__ int rb_quant_slow(float x, float s) {
+  return max(-127, min(127, __float2int_rn(__fdiv_rn(x, s))));
+}
+__device__ __forceinline__ int rb_quant_code(float x, float s, float rs) {
+  const float t = __fmul_rn(x, rs);
+  const int q = __float2int_rn(t);
+  if (fabsf(t - (float)q) >= 0.5f - 6.103515625e-05f) return rb_quant_slow(x, s);
+  return max(-127, min(127, q));
+}
+
 __device__ __forceinline__ void rb_x_offsets(int lane, int bnx, uint32_t (&xoff)[4]) {
   const int mi = lane >> 3, lrow = lane & 7;
 #pragma unroll
@@ -58,8 +80,10 @@ __device__ __forceinline__ void rb_x_offsets(int lane, int bnx, uint32_t (&xoff)
 template <int NT8, int AMODE, bool TMAX>
 __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_constant__ GemmArgs a) {
   constexpr bool ACT8 = AMODE == kActI8;
-  constexpr bool TOKS = ACT8 || AMODE == kActCodes16;   // token scales in the epilogue
+  constexpr bool QIN = AMODE == kActQuant;                 // fp16 x quantized per token here
+  constexpr bool TOKS = ACT8 || QIN || AMODE == kActCodes16;   // token scales in the epilogue
   static_assert(!TMAX || AMODE == kActF16, "the lm_head's fused top-k is W4A16");
+  static_assert(!QIN || NT8 == 1, "the in-kernel quantizer serves up to 8 tokens");
   static_assert(NT8 == 1 || NT8 == 2, "one or two tiles of 8 tokens");
   constexpr int kCompute = kRbCompute;
   constexpr int kCThreads = kCompute * 32;
@@ -94,6 +118,10 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
   // named barrier, so that all of them pass the same barriers
   volatile int *decide = reinterpret_cast<volatile int *>(gbars + 192);
   volatile WaitBlock *wctl = reinterpret_cast<volatile WaitBlock *>(gbars + 200);
+  // in-kernel quantizer: per-warp row maxima [16 warps][16 tokens], token scales s and 1/s
+  float *qamax = reinterpret_cast<float *>(gbars + 256);
+  float *qsc = qamax + kRbCompute * 16, *qrc = qsc + 16;
+  static_assert(256 + (kRbCompute * 16 + 32) * 4 <= kRbReserve - 1024, "quantizer data in the reserve");
   // the compute warps' sums at the end: [warp][row block][token][16 rows, padded to kRS]
   // binary32 (the padding spreads a warp's stores over the banks), over the ring (every
   // copy into it has been waited for by then)
@@ -187,6 +215,46 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
     const int gj = cw & (kXB - 1), hh = cw / kXB;    // group of the stage, half of its K steps
     const int g8 = lane >> 2, c4 = lane & 3;
     const int ct = threadIdx.x - kMsWarpC0 * 32;     // 0 .. kCThreads - 1
+    const int mv = P.M < BNX ? P.M : BNX;
+    if constexpr (QIN) {
+      // token scales, as the standalone quantizer: amax = max |x| over the whole row
+      // (binary32, exact in any order), s = amax / 127 (IEEE divide); the rows come from
+      // L2 while the first weights are in flight
+      const int nv = G * 16;                        // 16-byte vectors of a row
+      for (int m = 0; m < mv; ++m) {
+        const uint4 *xr = reinterpret_cast<const uint4 *>(a.xf16 + (size_t)m * P.K);
+        float amax = 0.0f;
+        for (int v0 = ct; v0 < nv; v0 += 4 * kCThreads) {
+          uint4 w[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int v = v0 + b * kCThreads;
+            w[b] = v < nv ? __ldg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const __half2 *hv = reinterpret_cast<const __half2 *>(&w[b]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __half22float2(hv[e]);
+              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) qamax[cw * 16 + m] = amax;
+      }
+      named_bar_sync(2, kCThreads);
+      if (ct < mv) {
+        float amax = qamax[ct];
+        for (int w = 1; w < kCompute; ++w) amax = fmaxf(amax, qamax[w * 16 + ct]);
+        const float sc = amax == 0.0f ? 0.0f : __fdiv_rn(amax, 127.0f);
+        qsc[ct] = sc;
+        qrc[ct] = sc == 0.0f ? 0.0f : __frcp_rn(sc);
+      }
+      named_bar_sync(2, kCThreads);
+    }
     uint32_t xoff[4];
     rb_x_offsets(lane, BNX, xoff);
     // the two pairs of K steps of this warp's half
@@ -210,18 +278,47 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
       // every compute warp waits for every stage and returns it once; after an abort every
       // wait gives up at once and the loop runs out quickly
       pwait(xfull_bar(s), ph);
-      if constexpr (ACT8) {
-        // the compute warps together widen the stage's int8 codes, then all wait
-        const int nb = G - i * kXB < kXB ? G - i * kXB : kXB;
-        uint8_t *xb = gbase + (size_t)s * kStage;
-        for (int j = 0; j < nb; ++j)
-          widen_chunk<BNX, kCThreads>(xb + j * kXChunk, xb + kXB * kXChunk + j * (BNX * kGroup), ct,
-                                      P.M < BNX ? P.M : BNX);
-        named_bar_sync(3, kCThreads);
-      }
       pwait(wfull_bar(s), ph);
       if (i * kXB + gj < G) {
         const uint32_t xt = stage(s) + (uint32_t)gj * kXChunk;
+        if constexpr (QIN) {
+          // this warp's 64-wide half of the group's tile becomes codes, in place (the other
+          // half is the other warp's): rows below M, one pair of K values per lane and step
+          // (pair j of row r: 8-value piece j / 4 of the half, swizzled by r % 8)
+          const uint32_t half = xt + (uint32_t)hh * (BNX * 128);
+          for (int pr = lane; pr < mv * 32; pr += 32) {
+            const int r = pr >> 5, j = pr & 31;
+            const uint32_t addr = half + (uint32_t)(r * 128 + (((j >> 2) ^ (r & 7)) << 4) + (j & 3) * 4);
+            const float sc = qsc[r], rs = qrc[r];
+            const float2 f = __half22float2(u32_as_h2(lds32(addr)));
+            const int q0 = rb_quant_code(f.x, sc, rs), q1 = rb_quant_code(f.y, sc, rs);
+            sts32(addr, h2_as_u32(__halves2half2(__int2half_rn(q0), __int2half_rn(q1))));
+          }
+          __syncwarp();
+        }
+        if constexpr (ACT8) {
+          // this warp's half of the group's int8 codes (unswizzled staging rows) widened to
+          // fp16 in its half of the tile: rows below M, 16 codes per lane and step
+          const uint8_t *stg = gbase + (size_t)s * kStage + kXB * kXChunk + gj * (BNX * kGroup) + hh * 64;
+          uint8_t *row0 = gbase + (size_t)s * kStage + gj * kXChunk + hh * (BNX * 128);
+          const __half2 k1152 = __float2half2_rn(1152.0f);
+          for (int pc = lane; pc < mv * 4; pc += 32) {
+            const int r = pc >> 2, c = pc & 3;                // 16 codes: pieces 2c, 2c + 1
+            const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * kGroup + c * 16);
+            const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
+                                   v.w ^ 0x80808080u};
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              o[2 * i] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w[i], 0x64646464u, 0x4140)), k1152));
+              o[2 * i + 1] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w[i], 0x64646464u, 0x4342)), k1152));
+            }
+            uint8_t *row = row0 + r * 128;
+            *reinterpret_cast<uint4 *>(row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          __syncwarp();
+        }
         const uint32_t wc = stage(s) + kWOff + (uint32_t)gj * 1024u;
         const uint32_t sc = stage(s) + kSOff + (uint32_t)gj * 32u + (uint32_t)g8 * 4u;
         uint32_t sc2[RBM];
@@ -311,13 +408,12 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
     }
     named_bar_sync(1, kCThreads);
     if (!*decide) {
-      const int mv = P.M < BNX ? P.M : BNX;
       for (int idx = ct; idx < nrb * mv * 16; idx += kCThreads) {
         const int r = idx / (mv * 16), m = (idx >> 4) % mv, row = idx & 15;
         float v = 0.0f;
 #pragma unroll
         for (int w = 0; w < kCompute; ++w) v += red[((w * RBM + r) * BNX + m) * kRS + row];
-        const __half hv = __float2half_rn(TOKS ? v * __ldg(a.xs + m) : v);
+        const __half hv = __float2half_rn(QIN ? v * qsc[m] : TOKS ? v * __ldg(a.xs + m) : v);
         const int n = (rb0 + r) * 16 + row;
         a.y[(size_t)m * P.N + n] = __half_as_ushort(hv);
         if constexpr (TMAX) atomicMax(a.tile_max + (size_t)m * P.T + (n >> 7), order_key16(hv));

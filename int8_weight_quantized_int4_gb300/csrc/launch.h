@@ -17,6 +17,7 @@ struct GemmArgs {
                             // (1 KB) and scales (32 B) over 8 consecutive groups
   Plan P;
   const float *xs;          // token scales [M] (W4A8) or nullptr
+  const uint16_t *xf16;     // W4A8 quantized in the kernel: the fp16 activations [M,K]
   const uint8_t *wpack;     // packed weights
   uint16_t *y;              // fp16 [M,N]
   int *counters;            // [tiles] arrival counters (stream-K)
@@ -113,6 +114,7 @@ cudaError_t launch_gemm_w8a16(const GemmArgs &a, cudaStream_t st);
 // token scales (W4A8), 2 fp16 codes and token scales (W4A8 after the quantizer)
 cudaError_t launch_gemm_ms(const GemmArgs &a, int act, cudaStream_t st);
 // decode batches on layers of few rows (plan.rb_max > 0): the row-block kernel, act as above
+// or 3: fp16 activations quantized per token in the kernel (plan.fused)
 cudaError_t launch_gemm_rb(const GemmArgs &a, int act, cudaStream_t st);
 
 }  // namespace qw

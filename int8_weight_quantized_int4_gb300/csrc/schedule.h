@@ -43,7 +43,7 @@ struct Plan {
   int xstages;                   // activation ring depth (blocks of xblock chunks)
   int xblock;                    // chunks per activation block (one tensor copy)
   int smem_bytes;
-  int fused;                     // W4A8 with the per-token quantizer inside the GEMM (none now)
+  int fused;                     // W4A8 with the per-token quantizer inside the GEMM (row-block plans)
   int ms_teams;                  // > 0: the warp-level MMA kernel for decode batches (M <= 16),
                                  // with this many teams of warps (one chunk per team at a time)
   int ms_red_bytes;              // its shared-memory buffer for the teams' partial sums
@@ -157,7 +157,13 @@ QW_HD int chunk_bytes(int mode) { return mode == 2 ? kChunkW8 : kChunkW4; }
 // fp16 values, with the token scales; the GEMM runs on them as plan mode kModeCodes16:
 // int4 weights, fp16 activation tiles as in W4A16, token scales in the epilogue as in
 // W4A8 (the products and sums are those of the int8 path: the codes are exact in fp16).
+// On the row-block kernel, up to kFusedMaxTokens tokens whose fp16 rows take at most
+// kFusedRowsMax bytes, the kernel quantizes instead (plan.fused, mode 3): every CTA reads
+// the whole rows anyway, and quantizes all of them (each CTA needs every code), so the
+// quantizer's arithmetic is paid once per CTA -- worth it only for a few tokens.
 constexpr int kModeCodes16 = 4;
+constexpr int kFusedRowsMax = 48 * 1024;
+constexpr int kFusedMaxTokens = 2;   // measured: 1-2 tokens faster than quantizer + GEMM, 4 not
 
 // W4A8 widens int8 activation codes to fp16 inside the GEMM (through a staging
 // slot) for token tiles up to this size; larger tiles use a separate widening pass.
@@ -195,7 +201,7 @@ constexpr int kMsLongChunksPerSm = 32;
 // = 41 MB, well inside the 129 MB L2).
 constexpr int kMsL2AheadChunks = 16;
 QW_HD bool ms_kernel(int mode, int M) {
-  return (mode == 0 || mode == 1 || mode == kModeCodes16) && M >= 1 && M <= kMsMaxTokens;
+  return (mode == 0 || mode == 1 || mode == 3 || mode == kModeCodes16) && M >= 1 && M <= kMsMaxTokens;
 }
 // token rows of its activation tiles: 8 (one tile of eight tokens) or 16
 QW_HD int ms_rows(int M) { return M <= 8 ? 8 : 16; }
@@ -232,6 +238,7 @@ QW_HD bool ms_ring_depths(int mode, int M, int teams, int &xst, int &wst) {
 // enough for two tile-kernel CTAs per SM (kMsLongChunksPerSm) stays on the tile kernel,
 // which measured faster there (a 5120 x 17408 layer: 15.1 against 17.6 us at one token).
 constexpr int kRbMax = 3;                 // row blocks per CTA at most
+constexpr int kRbReserve = 4096;          // barriers, the in-kernel quantizer's amax and scales
 constexpr int kRbXBlock = 8;              // K groups per ring stage: one per compute warp
 constexpr int kRbMaxStages = 6;
 QW_HD bool rb_kernel(int mode, int M, int N, int K, int num_sms) {
@@ -250,7 +257,7 @@ QW_HD int rb_stage_bytes(int mode, int M) {
 }
 // one CTA per SM, as many stages as fit (at most kRbMaxStages, at least 2)
 QW_HD bool rb_ring_depths(int mode, int M, int &st) {
-  st = (kSmemLimit - kSmemReserve) / rb_stage_bytes(mode, M);
+  st = (kSmemLimit - kRbReserve) / rb_stage_bytes(mode, M);
   if (st > kRbMaxStages) st = kRbMaxStages;
   return st >= 2;
 }
@@ -324,9 +331,10 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
   if (mode < 0 || mode > 3 || M < 0 || N < 0 || K < 0 || num_sms < 1) return -1;
   if (N % kRows || K % kGroup) return -2;
   if (num_sms > kMaxGrid / 2) num_sms = kMaxGrid / 2;
-  P.fused = 0;
-  // mode 3 is the quantizer (fp16 codes) followed by a kModeCodes16 plan
-  const bool quant_first = mode == 3;
+  P.fused = (mode == 3 && M <= kFusedMaxTokens && (long long)M * K * 2 <= kFusedRowsMax &&
+             rb_kernel(kModeCodes16, M, N, K, num_sms)) ? 1 : 0;
+  // mode 3 outside that is the quantizer (fp16 codes) followed by a kModeCodes16 plan
+  const bool quant_first = mode == 3 && !P.fused;
   if (quant_first) mode = kModeCodes16;
   P.mode = mode; P.M = M; P.N = N; P.K = K;
   P.bn = pick_bn(M);
@@ -365,7 +373,7 @@ inline int make_plan(int mode, int M, int N, int K, int num_sms, Plan &P) {
     P.ms_red_bytes = 0;
     if (!rb_ring_depths(mode, M, P.stages)) return -2;
     P.xstages = P.stages;
-    P.smem_bytes = P.stages * rb_stage_bytes(mode, M) + kSmemReserve;
+    P.smem_bytes = P.stages * rb_stage_bytes(mode, M) + kRbReserve;
   } else if (P.ms_teams) {
     P.ms_red_bytes = ms_red_bytes(M, P.ms_teams);
     if (!ms_ring_depths(mode, M, P.ms_teams, P.xstages, P.stages)) return -2;

@@ -350,10 +350,11 @@ def test_signed_scales_sign_fold_equivalence(q):
                                    (17, 640, 640), (64, 640, 1024), (8, 27648, 5120), (48, 1280, 2048),
                                    (200, 1280, 2048)])
 def test_w4a8_fused_bit_identical_to_two_step(q, M, N, K):
-    """qgemm_w4a8_fused(x) equals qgemm_w4a8(quant_act_int8(x)) bit for bit -- its
-    GEMM reads the quantizer's fp16 codes where qgemm_w4a8 widens int8 ones (decode
-    kernel at 1..16 tokens, a long two-CTAs-per-SM decode launch, tensor-core tiles
-    of 32, 64 and 256) -- and meets the tolerance against the oracle."""
+    """qgemm_w4a8_fused(x) equals qgemm_w4a8(quant_act_int8(x)) bit for bit -- in one
+    row-block kernel that quantizes per token itself (M*K*2 <= 48 KB on a layer of few
+    rows), or through the quantizer's fp16 codes where qgemm_w4a8 widens int8 ones
+    (decode kernels at 1..16 tokens, a long two-CTAs-per-SM decode launch, tensor-core
+    tiles of 32, 64 and 256) -- and meets the tolerance against the oracle."""
     p = synth.make_problem(M, N, K, seed=11 + M, outlier_frac=0.01)
     x = _special_rows(p.x) if M >= 4 else p.x
     xd = x.to(DEV)
@@ -364,20 +365,27 @@ def test_w4a8_fused_bit_identical_to_two_step(q, M, N, K):
     torch.cuda.synchronize()
     assert q.device_error() == 0
     pl = q.plan(q.MODE_W4A8_FUSED, M, N, K, torch.cuda.get_device_properties(DEV).multi_processor_count)
-    assert pl.fused == 0
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    rb = M <= 16 and N // 16 <= 3 * sms and (M > 8 or (N // 128) * (K // 128) < 32 * sms)
+    assert pl.fused == (1 if (rb and M <= 2 and M * K * 2 <= 48 * 1024) else 0)
     assert np.array_equal(bits(y1), bits(y2))
     oq, os_ = oracle.quant_act_int8(x.numpy())
     assert nerr(y1, oracle.w4a8(oq, os_, p.codes, p.scales)) <= TOL
 
 
-def test_w4a8_fused_quantizer_near_ties(q):
+@pytest.mark.parametrize("amaxes", [(100.0, 3.3), (0.0173, 55.5), (100.0, 3.3, 0.0173, 55.5)])
+def test_w4a8_fused_quantizer_near_ties(q, amaxes):
     """Quotients x / s a few 2^-12 from half-integers, with scales that are not powers of
-    two: through identity weights (y[m,n] = s_m * q[m,n]) every code the fp16-code
-    quantizer produces shows in y, which must equal the two-step path bit for bit."""
-    M, N, K = 4, 1280, 1280
-    rng = np.random.default_rng(5)
+    two: through identity weights (y[m,n] = s_m * q[m,n]) every code shows in y, which must
+    equal the two-step path bit for bit -- the codes of the row-block kernel's in-kernel
+    quantizer (2 tokens: reciprocal product, IEEE quotient near ties) and of the standalone
+    quantizer (4 tokens)."""
+    M, N, K = len(amaxes), 1280, 1280
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert q.plan(q.MODE_W4A8_FUSED, M, N, K, sms).fused == (1 if M <= 2 else 0)
+    rng = np.random.default_rng(5 + M)
     x = np.zeros((M, K), np.float16)
-    for m, amax in enumerate((100.0, 3.3, 0.0173, 55.5)):
+    for m, amax in enumerate(amaxes):
         s = np.float64(np.float16(amax)) / 127.0
         n = rng.integers(-127, 127, K)
         delta = rng.integers(-3, 4, K) * 2.0 ** -12
