@@ -234,9 +234,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
 #pragma unroll
           for (int j = 0; j < TEAMS; ++j)
             if (j == tm) { slot = j * SWT + s[j]; par = ph[j]; }
-          // never a copy after an abort: the compute warps then release slots whose
-          // copies may still be in flight, and a refill would arm the same phase twice
-          if (!pwait(wempty_bar(slot), par ^ 1u) || wctl->abort) { ok = false; break; }
+          if (!pwait(wempty_bar(slot), par ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(wfull_bar(slot), kChunkW4);
           bulk_g2s(w_smem(slot), src, kChunkW4, wfull_bar(slot), pol);
 #pragma unroll
@@ -261,7 +259,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         for (int g = sg.g0; g < sg.g1; g += kXBlock) {
-          if (!pwait(xempty_bar(s), ph ^ 1u) || wctl->abort) { ok = false; break; }
+          if (!pwait(xempty_bar(s), ph ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(xfull_bar(s), kXBytes);
           ++nfill;
           if constexpr (ACT8) tma_load_3d(x_smem(s) + kXBlock * kXChunk, &a.tmap, 0, 0, g, xfull_bar(s));
@@ -301,6 +299,9 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
     int npend = 0, pend_tile[2] = {0, 0}, pend_cut[2] = {0, 0};
     const int cut_first = P.cut[cta][0], cut_last = P.cut[cta][1];
     bool aborted = false;
+    // a warp that saw a wait give up releases no slot again: the copy it gave up on may
+    // still be landing, and a producer released now would arm that slot's phase twice
+    bool live = true;
     for (int i = 0; segment(P, cta, i, sg); ++i) {
       float acc[RBW][NT8][4];
 #pragma unroll
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
         const int nb = sg.g1 - gb < kXBlock ? sg.g1 - gb : kXBlock;
         // every compute warp waits for every activation block and returns it once;
         // after an abort every wait gives up at once and the loops run out quickly
-        pwait(xfull_bar(xs), xph);
+        live = pwait(xfull_bar(xs), xph) && live;
         if constexpr (ACT8) {
           // the compute warps together widen the block's int8 codes, then all wait
           uint8_t *xb = gbase + (size_t)xs * kXStage;
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
         }
         for (int j = (tm - cidx) & (TEAMS - 1); j < nb; j += TEAMS) {
           const int slot = tm * SWT + s;
-          pwait(wfull_bar(slot), ph);
+          live = pwait(wfull_bar(slot), ph) && live;
           const uint32_t xt = x_smem(xs) + (uint32_t)j * kXChunk;
           const uint32_t wc = w_smem(slot);
           uint32_t sc2[RBW];
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
             }
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(wempty_bar(slot));
+          if (lane == 0 && live) mbar_arrive(wempty_bar(slot));
           if (++s == SWT) { s = 0; ph ^= 1u; }
 #pragma unroll
           for (int r = 0; r < RBW; ++r) {
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(xempty_bar(xs));
+        if (lane == 0 && live) mbar_arrive(xempty_bar(xs));
         if (++xs == SX) { xs = 0; xph ^= 1u; }
         cidx += nb;
       }

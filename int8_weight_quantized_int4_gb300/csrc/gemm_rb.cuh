@@ -175,9 +175,7 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
       int s = 0, nfill = 0;
       uint32_t ph = 0;
       for (int i = 0; i < nst; ++i) {
-        // never a copy after an abort: the compute warps then release stages whose copies
-        // may still be in flight, and a refill would arm the same phase twice
-        if (!pwait(empty_bar(s), ph ^ 1u) || wctl->abort) break;
+        if (!pwait(empty_bar(s), ph ^ 1u)) break;
         mbar_arrive_expect_tx(wfull_bar(s), (uint32_t)nrb * (kXB * (1024u + 32u)));
         for (int r = 0; r < nrb; ++r) {
           const int rb = rb0 + r;
@@ -198,9 +196,7 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
       int s = 0, nfill = 0;
       uint32_t ph = 0;
       for (int i = 0; i < nst; ++i) {
-        // never a copy after an abort: the compute warps then release stages whose copies
-        // may still be in flight, and a refill would arm the same phase twice
-        if (!pwait(empty_bar(s), ph ^ 1u) || wctl->abort) break;
+        if (!pwait(empty_bar(s), ph ^ 1u)) break;
         mbar_arrive_expect_tx(xfull_bar(s), kXBytes);
         ++nfill;
         if constexpr (ACT8) tma_load_3d(stage(s) + kXB * kXChunk, &a.tmap, 0, 0, i * kXB, xfull_bar(s));
@@ -274,11 +270,14 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
         for (int e = 0; e < 4; ++e) acc[r][jt][e] = 0.0f;
     int s = 0;
     uint32_t ph = 0;
+    // a warp that saw a wait give up releases no stage again: a copy it gave up on may
+    // still be landing, and a producer released now would arm that stage's phase twice
+    bool live = true;
     for (int i = 0; i < nst; ++i) {
       // every compute warp waits for every stage and returns it once; after an abort every
       // wait gives up at once and the loop runs out quickly
-      pwait(xfull_bar(s), ph);
-      pwait(wfull_bar(s), ph);
+      live = pwait(xfull_bar(s), ph) && live;
+      live = pwait(wfull_bar(s), ph) && live;
       if (i * kXB + gj < G) {
         const uint32_t xt = stage(s) + (uint32_t)gj * kXChunk;
         if constexpr (QIN) {
@@ -385,7 +384,7 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(s));
+      if (lane == 0 && live) mbar_arrive(empty_bar(s));
       if (++s == SS) { s = 0; ph ^= 1u; }
     }
     // ---- the warps' sums meet in shared memory (over the ring: every copy into it has
