@@ -281,7 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   if (warp == kWarpTma) {
     // ------------------------------------------------------ weight copies --
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
+      // a chunk read by one token tile streams through L2 (evict first); with several
+      // token tiles the CTAs of a supergroup read it within a short time, so it stays
+      const uint64_t pol = P.U > 1 ? policy_evict_normal() : policy_evict_first();
       int s[2] = {0, 0}, nfill[2] = {0, 0}, cidx = 0;
       uint32_t ph[2] = {0, 0};
       bool ok = true;
