@@ -905,13 +905,23 @@ def run_diag(args):
                 if ops / ms / 1e9 > best:
                     best, per_iter = ops / ms / 1e9, ms * 1e6 / iters
             out["mma_sync"][f"{kind}_chains{chains}"] = {"TOPS": round(best, 1), "ns_per_iteration": round(per_iter, 2)}
+    # kind + 2: the warp-collective issue form (the library's kernels); without it lane 0
+    # issues alone inside a divergent branch
     for name, kind, a_tmem, n, issuers, chunks, window in (
             ("f16_A_tmem_n16_1issuer_wait_each", 0, 1, 16, 1, 64, 1),
             ("f16_A_tmem_n16_4issuers_no_wait", 0, 1, 16, 4, 256, 0),
             ("f16_A_smem_n16_1issuer_wait_each", 0, 0, 16, 1, 64, 1),
             ("f8f6f4_A_tmem_n16_1issuer_wait_each", 1, 1, 16, 1, 64, 1),
             ("f16_A_tmem_n256_dense", 0, 1, 256, 1, 2048, 0),
-            ("f8f6f4_A_tmem_n256_dense", 1, 1, 256, 1, 2048, 0)):
+            ("f8f6f4_A_tmem_n256_dense", 1, 1, 256, 1, 2048, 0),
+            ("warp_f16_A_tmem_n16_1issuer_wait_each", 2, 1, 16, 1, 64, 1),
+            ("warp_f16_A_tmem_n16_1issuer_window4", 2, 1, 16, 1, 2048, 4),
+            ("warp_f16_A_tmem_n64_1issuer_window4", 2, 1, 64, 1, 2048, 4),
+            ("warp_f16_A_smem_n64_1issuer_window4", 2, 0, 64, 1, 2048, 4),
+            ("warp_f16_A_tmem_n128_1issuer_window4", 2, 1, 128, 1, 2048, 4),
+            ("warp_f16_A_tmem_n256_dense", 2, 1, 256, 1, 2048, 0),
+            ("warp_f8f6f4_A_tmem_n256_dense", 3, 1, 256, 1, 2048, 0),
+            ("f16_A_tmem_n64_1issuer_window4", 0, 1, 64, 1, 2048, 4)):
         q.diag_tc_probe(kind, a_tmem, n, issuers, chunks, window, sms)
         torch.cuda.synchronize()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -922,7 +932,7 @@ def run_diag(args):
         ms = s.elapsed_time(e)
         a = o.cpu().numpy().astype(np.float64)[:, :issuers, :]
         done = a[..., 3].sum()
-        nmma = 8 if kind == 0 else 4
+        nmma = 8 if kind % 2 == 0 else 4
         out["tcgen05"][name] = {
             "issue_ns_per_mma": round(float(a[..., 0].sum() / done / nmma), 1),
             "wait_ns_per_chunk": round(float(a[..., 1].sum() / done), 1),

@@ -363,10 +363,13 @@ long long qw_num_kernel_launches(void);
  *       *ops (host) = 2*m*n*k per MMA x the MMAs of the launch; the caller times
  *       the launch.  Async.
  *   qw_diag_tc_probe  tcgen05.mma timing at the GEMM's shapes: `grid` CTAs (<= SMs,
- *       one per SM); lane 0 of warps 0..issuers-1 each stream `chunks` chunks of a
+ *       one per SM); warps 0..issuers-1 each stream `chunks` chunks of a
  *       128 x n x 128 product (kind 0: kind::f16, 8 MMAs of K = 16; kind 1:
- *       kind::f8f6f4 with e4m3 operands, 4 MMAs of K = 32) into its own
- *       accumulator, A from TMEM (a_tmem = 1) or shared memory.  window 0: one
+ *       kind::f8f6f4 with e4m3 operands, 4 MMAs of K = 32) into their own
+ *       accumulator, A from TMEM (a_tmem = 1) or shared memory.  kind + 2 selects
+ *       the warp-collective issue (the whole warp runs the loop, an elected lane
+ *       issues: the form of the library's kernels) instead of lane 0 issuing alone
+ *       inside a divergent branch.  window 0: one
  *       commit at the end; w >= 1: a commit per chunk, chunk c first waiting for
  *       chunk c - w's commit (a ring of w operand slots).  n*issuers <= 256,
  *       window <= 8.  out: device, grid*4*4 uint64; per (CTA, issuer): issue ns,

@@ -277,45 +277,47 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_kernel(const __grid_c
     }
   } else if (warp == 1) {
     // --------------------------------------------------------------- MMA --
-    if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_f16_f32(128, kAttnBlk), kIdO = idesc_f16_f32(128, kAttnD);
-      bool ok = pwait(q_full, 0u);
-      for (int j = 0; ok && j <= nblk; ++j) {
-        if (j < nblk) {
-          const int b = j & 1;
-          if (j >= 2 && !pwait(s_free(b), (uint32_t)(((j >> 1) - 1) & 1))) { ok = false; break; }
-          if (!pwait(k_full, (uint32_t)(j & 1))) { ok = false; break; }
-          tc_fence_after();
+    // The whole warp runs the loop (waits are warp votes) and the leader lane issues:
+    // see mma_f16_ts_w.
+    const uint32_t leader = elect_leader();
+    auto wwait = [&](uint32_t bar, uint32_t parity) { return __all_sync(0xffffffffu, pwait(bar, parity)); };
+    constexpr uint32_t kIdS = idesc_f16_f32(128, kAttnBlk), kIdO = idesc_f16_f32(128, kAttnD);
+    bool ok = wwait(q_full, 0u);
+    for (int j = 0; ok && j <= nblk; ++j) {
+      if (j < nblk) {
+        const int b = j & 1;
+        if (j >= 2 && !wwait(s_free(b), (uint32_t)(((j >> 1) - 1) & 1))) { ok = false; break; }
+        if (!wwait(k_full, (uint32_t)(j & 1))) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kAttnD / 16; ++kk) {
-            const uint32_t off = (uint32_t)((kk >> 2) * (kAttnBlk * 128) + (kk & 3) * 32);
-            mma_f16_ss(tmem + kSCol + (uint32_t)(b * kAttnBlk), smem_desc_sw128(q_s + off),
+        for (int kk = 0; kk < kAttnD / 16; ++kk) {
+          const uint32_t off = (uint32_t)((kk >> 2) * (kAttnBlk * 128) + (kk & 3) * 32);
+          mma_f16_ss_w(leader, tmem + kSCol + (uint32_t)(b * kAttnBlk), smem_desc_sw128(q_s + off),
                        smem_desc_sw128(k_s + off), kIdS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(s_full(b));
-          mma_commit(k_empty);
         }
-        if (j >= 1) {
-          const int jp = j - 1, bp = jp & 1;
-          if (!pwait(p_full(bp), (uint32_t)((jp >> 1) & 1))) { ok = false; break; }
-          if (!pwait(v_full, (uint32_t)(jp & 1))) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kAttnBlk / 16; ++kk) {
-            const uint32_t off = (uint32_t)((kk >> 2) * (kAttnD * 128) + (kk & 3) * 32);
-            mma_f16_ts(tmem + kOCol, tmem + kSCol + (uint32_t)(bp * kAttnBlk + 8 * kk), smem_desc_sw128(v_s + off),
-                       kIdO, (jp > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(s_free(bp));
-          mma_commit(v_empty);
-          mma_commit(o_step);
-          if (jp == nblk - 1) mma_commit(o_done);
-        }
+        mma_commit_w(leader, s_full(b));
+        mma_commit_w(leader, k_empty);
       }
-      // every MMA this thread issued has completed before the CTA may exit
-      mma_commit(drain);
-      mbar_drain(drain, 0u, wctl);
+      if (j >= 1) {
+        const int jp = j - 1, bp = jp & 1;
+        if (!wwait(p_full(bp), (uint32_t)((jp >> 1) & 1))) { ok = false; break; }
+        if (!wwait(v_full, (uint32_t)(jp & 1))) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kAttnBlk / 16; ++kk) {
+          const uint32_t off = (uint32_t)((kk >> 2) * (kAttnD * 128) + (kk & 3) * 32);
+          mma_f16_ts_w(leader, tmem + kOCol, tmem + kSCol + (uint32_t)(bp * kAttnBlk + 8 * kk),
+                       smem_desc_sw128(v_s + off), kIdO, (jp > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit_w(leader, s_free(bp));
+        mma_commit_w(leader, v_empty);
+        mma_commit_w(leader, o_step);
+        if (jp == nblk - 1) mma_commit_w(leader, o_done);
+      }
     }
+    // every MMA the leader issued has completed before the CTA may exit
+    mma_commit_w(leader, drain);
+    mbar_drain(drain, 0u, wctl);
   } else if (warp >= kSoftmaxWarp0) {
     // ----------------------------------------------------------- softmax --
     const int grp = (warp - kSoftmaxWarp0) >> 2;               // 0, 1: keys 64 grp .. of a block

@@ -113,9 +113,11 @@ __global__ void __launch_bounds__(kPeakThreads) mma_peak_kernel(int iters, float
 // -------------------------------------------------------- tcgen05 probe ----
 struct TcProbe {
   int kind;       // 0: kind::f16 (8 MMAs of K = 16 per chunk), 1: kind::f8f6f4 e4m3 (4 of K = 32)
+  int warp_form;  // 0: lane 0 issues inside a divergent branch; 1: the whole warp runs the
+                  // loop and an elected lane issues (the form of the library's kernels)
   int a_tmem;     // 1: A from TMEM (a ring of 4 slots), 0: A from shared memory
   int n;          // MMA N
-  int issuers;    // issuing threads (lane 0 of warps 0..issuers-1), one accumulator each
+  int issuers;    // issuing warps 0..issuers-1, one accumulator each
   int chunks;     // chunks per issuer
   int window;     // 0: one commit at the end; w >= 1: a commit per chunk into a ring of w
                   // barriers, chunk c waiting for chunk c - w's commit first
@@ -124,14 +126,36 @@ struct TcProbe {
 };
 
 constexpr int kProbeThreads = 128;
+
+// warp-collective kind::f8f6f4 issue (as mma_f16_ts_w / mma_f16_ss_w)
+__device__ __forceinline__ void mma_f8_ts_w(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 e, %5, 0;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f8_ss_w(uint32_t leader, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 e, %5, 0;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
 constexpr int kProbeMaxWindow = 8;
 
+// F8: kind::f8f6f4 (else kind::f16); A_TMEM: A from TMEM (else shared memory); WARP: the
+// warp-collective issue (else lane 0 alone).  The K loop of a chunk is unrolled with no
+// branch inside, as in the GEMM.
+template <bool F8, bool A_TMEM, bool WARP>
 __global__ void __launch_bounds__(kProbeThreads, 1) tc_probe_kernel(const TcProbe p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (base - raw);
-  const bool f8 = p.kind == 1;
+  constexpr bool f8 = F8;
   const uint32_t row_bytes = f8 ? 128u : 256u;            // one 128-wide K group
   const uint32_t btile = base;                             // n rows
   const uint32_t atile = base + (uint32_t)p.n * row_bytes; // 128 rows (shared-memory A)
@@ -168,10 +192,11 @@ __global__ void __launch_bounds__(kProbeThreads, 1) tc_probe_kernel(const TcProb
   tc_fence_after();
 
   const int q = warp;
-  if (lane == 0 && q < p.issuers) {
+  if (q < p.issuers && (WARP || lane == 0)) {
+    const uint32_t leader = WARP ? elect_leader() : 1u;
     const uint32_t idesc = idesc_f16_f32(128, p.n);
     const uint32_t d = tmem + (uint32_t)(q * p.n);
-    const int nk = f8 ? 4 : 8;
+    constexpr int nk = f8 ? 4 : 8;
     const uint64_t bdesc0 = smem_desc_sw128(btile), adesc0 = smem_desc_sw128(atile);
     uint64_t t_issue = 0, t_wait = 0;
     uint32_t phase = 0;   // bit w: parity of ring barrier w
@@ -184,26 +209,31 @@ __global__ void __launch_bounds__(kProbeThreads, 1) tc_probe_kernel(const TcProb
       const uint64_t t0 = globaltimer_ns();
       if (p.window > 0 && c >= p.window) {
         ok = diag_wait(bar, (phase >> w) & 1u, p.err);
+        if (WARP) ok = __all_sync(0xffffffffu, ok);
         phase ^= 1u << w;
       }
       const uint64_t t1 = globaltimer_ns();
       const uint32_t a0 = tmem + 256u + (uint32_t)((c & 3) * 64);
-#pragma unroll 1
+#pragma unroll
       for (int k = 0; k < nk; ++k) {
         // K step k: f16 -> 64-wide half k / 4, 32 bytes (16 values) into it; f8 -> 32 bytes
         const uint32_t boff = f8 ? (uint32_t)k * 32u : (uint32_t)((k >> 2) * p.n * 128 + (k & 3) * 32);
         const uint32_t aoff = f8 ? (uint32_t)k * 32u : (uint32_t)((k >> 2) * 128 * 128 + (k & 3) * 32);
         const uint64_t bd = bdesc0 + (uint64_t)(boff >> 4);
         const uint32_t acc = (c > 0 || k > 0) ? 1u : 0u;
-        if (f8) {
-          if (p.a_tmem) mma_f8_ts(d, a0 + (uint32_t)(k * 8), bd, idesc, acc);
-          else mma_f8_ss(d, adesc0 + (uint64_t)(aoff >> 4), bd, idesc, acc);
-        } else {
-          if (p.a_tmem) mma_f16_ts(d, a0 + (uint32_t)(k * 8), bd, idesc, acc);
-          else mma_f16_ss(d, adesc0 + (uint64_t)(aoff >> 4), bd, idesc, acc);
-        }
+        if constexpr (WARP && F8 && A_TMEM) mma_f8_ts_w(leader, d, a0 + (uint32_t)(k * 8), bd, idesc, acc);
+        else if constexpr (WARP && F8) mma_f8_ss_w(leader, d, adesc0 + (uint64_t)(aoff >> 4), bd, idesc, acc);
+        else if constexpr (WARP && A_TMEM) mma_f16_ts_w(leader, d, a0 + (uint32_t)(k * 8), bd, idesc, acc);
+        else if constexpr (WARP) mma_f16_ss_w(leader, d, adesc0 + (uint64_t)(aoff >> 4), bd, idesc, acc);
+        else if constexpr (F8 && A_TMEM) mma_f8_ts(d, a0 + (uint32_t)(k * 8), bd, idesc, acc);
+        else if constexpr (F8) mma_f8_ss(d, adesc0 + (uint64_t)(aoff >> 4), bd, idesc, acc);
+        else if constexpr (A_TMEM) mma_f16_ts(d, a0 + (uint32_t)(k * 8), bd, idesc, acc);
+        else mma_f16_ss(d, adesc0 + (uint64_t)(aoff >> 4), bd, idesc, acc);
       }
-      if (p.window > 0) mma_commit(bar);
+      if (p.window > 0) {
+        if constexpr (WARP) mma_commit_w(leader, bar);
+        else mma_commit(bar);
+      }
       const uint64_t t2 = globaltimer_ns();
       t_wait += t1 - t0;
       t_issue += t2 - t1;
@@ -214,25 +244,30 @@ __global__ void __launch_bounds__(kProbeThreads, 1) tc_probe_kernel(const TcProb
       const uint64_t t0 = globaltimer_ns();
       if (p.window == 0) {
         const uint32_t bar = bars + 8u * (uint32_t)(q * kProbeMaxWindow);
-        mma_commit(bar);
+        if constexpr (WARP) mma_commit_w(leader, bar);
+        else mma_commit(bar);
         ok = diag_wait(bar, 0u, p.err);
+        if (WARP) ok = __all_sync(0xffffffffu, ok);
       } else {
         const int pend = p.chunks < p.window ? p.chunks : p.window;
         for (int j = 0; j < pend && ok; ++j) {
           const int c = p.chunks - pend + j;
           const int w = c % p.window;
           ok = diag_wait(bars + 8u * (uint32_t)(q * kProbeMaxWindow + w), (phase >> w) & 1u, p.err);
+          if (WARP) ok = __all_sync(0xffffffffu, ok);
           phase ^= 1u << w;
         }
       }
       t_wait += globaltimer_ns() - t0;
     }
     const uint64_t total = globaltimer_ns() - T0;
-    unsigned long long *o = p.out + ((size_t)blockIdx.x * 4 + q) * 4;
-    o[0] = t_issue;
-    o[1] = t_wait;
-    o[2] = total;
-    o[3] = (unsigned long long)done;
+    if (lane == 0) {
+      unsigned long long *o = p.out + ((size_t)blockIdx.x * 4 + q) * 4;
+      o[0] = t_issue;
+      o[1] = t_wait;
+      o[2] = total;
+      o[3] = (unsigned long long)done;
+    }
     if (!ok) {
       // let anything still in flight finish before the TMEM goes away
       const uint64_t t0 = globaltimer_ns();
@@ -374,21 +409,27 @@ int qw_diag_mma_peak(int kind, int ctas, int iters, int chains, float *sink, dou
 
 int qw_diag_tc_probe(int kind, int a_tmem, int n, int issuers, int chunks, int window,
                      unsigned long long *out, int grid, qw_stream_t stream) {
-  if (kind < 0 || kind > 1 || n < 16 || n > 256 || n % 16 || issuers < 1 || issuers > 4 ||
+  if (kind < 0 || kind > 3 || n < 16 || n > 256 || n % 16 || issuers < 1 || issuers > 4 ||
       n * issuers > 256 || chunks < 1 || window < 0 || window > qw::kProbeMaxWindow || !out || grid < 1)
     return qw::set_last_error(QW_ERR_INVALID_ARG, "qw_diag_tc_probe: bad argument");
   int sms = 0, *err = nullptr;
   int rc = qw::device_info(&sms, &err);
   if (rc) return rc;
   if (grid > sms) return qw::set_last_error(QW_ERR_INVALID_ARG, "qw_diag_tc_probe: at most one CTA per SM");
-  const int row_bytes = kind == 1 ? 128 : 256;
+  const int row_bytes = (kind & 1) ? 128 : 256;
   // tiles + barriers; at least 120 KB so that one CTA holds an SM (one TMEM allocation each)
   int smem = 1024 + (n + 128) * row_bytes + 1024;
   if (smem < 120 * 1024) smem = 120 * 1024;
-  qw::TcProbe p{kind, a_tmem ? 1 : 0, n, issuers, chunks, window, out, err};
-  cudaError_t e = qw::ensure_smem_attr(reinterpret_cast<const void *>(qw::tc_probe_kernel), smem);
+  qw::TcProbe p{kind & 1, kind >> 1, a_tmem ? 1 : 0, n, issuers, chunks, window, out, err};
+  void (*const kernels[8])(const qw::TcProbe) = {
+      qw::tc_probe_kernel<false, false, false>, qw::tc_probe_kernel<false, true, false>,
+      qw::tc_probe_kernel<true, false, false>,  qw::tc_probe_kernel<true, true, false>,
+      qw::tc_probe_kernel<false, false, true>,  qw::tc_probe_kernel<false, true, true>,
+      qw::tc_probe_kernel<true, false, true>,   qw::tc_probe_kernel<true, true, true>};
+  const auto kern = kernels[(kind >> 1) * 4 + (kind & 1) * 2 + (a_tmem ? 1 : 0)];
+  cudaError_t e = qw::ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
   if (e == cudaSuccess) {
-    qw::tc_probe_kernel<<<grid, qw::kProbeThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    kern<<<grid, qw::kProbeThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
     qw::count_launch();
     e = cudaGetLastError();
   }

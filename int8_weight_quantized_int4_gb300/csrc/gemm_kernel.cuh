@@ -161,6 +161,12 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   constexpr int kNAcc = BN <= 128 ? 2 : 1;             // accumulator sets (double buffer)
   constexpr int kIssuers = BN <= 32 ? 4 : BN <= 64 ? 2 : 1;
   static_assert(kIssuers <= kMaxIssuers && (kIssuers & (kIssuers - 1)) == 0, "issuers");
+  // The single-thread roles (copies, MMA issue) run as whole warps, the leader lane
+  // issuing (see mma_f16_ts_w), on token tiles of 64 and more: a tcgen05.mma issued
+  // that way costs a third of one issued by a lone lane.  On narrower tiles (four
+  // issuers, the weight stream the limit) lane 0 runs them alone: every lane of six
+  // warps polling the barriers measured 3 % slower there.
+  constexpr bool kWarpIssue = kIssuers <= 2;
   // W4A8 widening: the two widen warps, plus the two issuer warps left idle when a
   // token tile needs at most two issuers
   constexpr int kWidenW = kIssuers <= 2 ? kWidenWarps + 2 : kWidenWarps;
@@ -199,6 +205,13 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   volatile int *bcast = reinterpret_cast<volatile int *>(gbars + kBcastSlot);
   // a pipeline wait: bounded by the launch's limit, gives up once the CTA aborts
   auto pwait = [&](uint32_t bar, uint32_t parity) { return mbar_wait(bar, parity, wctl, a.wait_ns == 0); };
+  // the same in a single-thread role: run as a whole warp, every lane waits and the warp
+  // goes on only if all saw the phase (their waits may end differently after an abort)
+  auto vwait = [&](uint32_t bar, uint32_t parity) {
+    const bool got = pwait(bar, parity);
+    if constexpr (kWarpIssue) return __all_sync(0xffffffffu, got) != 0;
+    else return got;
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -280,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------ weight copies --
-    if (lane == 0) {
+    if (kWarpIssue || lane == 0) {
+      const uint32_t leader = kWarpIssue ? elect_leader() : 1u;
       // a chunk read by one token tile streams through L2 (evict first); with several
       // token tiles the CTAs of a supergroup read it within a short time, so it stays
       const uint64_t pol = P.U > 1 ? policy_evict_normal() : policy_evict_first();
@@ -293,9 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         const uint8_t *src = a.wpack + ((size_t)t * P.G + sg.g0) * kChunk;
         for (int g = sg.g0; g < sg.g1; ++g, ++cidx, src += kChunk) {
           const int p = cidx & 1, slot = p * SWH + s[p];
-          if (!pwait(wempty_bar(slot), ph[p] ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(wfull_bar(slot), kChunk);
-          bulk_g2s(w_smem(slot), src, kChunk, wfull_bar(slot), pol);
+          if (!vwait(wempty_bar(slot), ph[p] ^ 1u)) { ok = false; break; }
+          mbar_arrive_expect_tx_w(leader, wfull_bar(slot), kChunk);
+          bulk_g2s_w(leader, w_smem(slot), src, kChunk, wfull_bar(slot), pol);
           ++nfill[p];
           if (++s[p] == SWH) { s[p] = 0; ph[p] ^= 1u; }
         }
@@ -309,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     // -------------------------------------------------- activation copies --
     // one tensor copy per block of up to kXBlock consecutive groups of a segment;
     // a block that runs past the segment (or past K) brings data nobody reads
-    if (lane == 0) {
+    if (kWarpIssue || lane == 0) {
+      const uint32_t leader = kWarpIssue ? elect_leader() : 1u;
       if (early) griddep_wait();
       int s = 0, nfill = 0;
       uint32_t ph = 0;
@@ -318,16 +333,16 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
         int u, t;
         tile_coords(P, sg.tile, u, t);
         for (int g = sg.g0; g < sg.g1; g += kXBlock) {
-          if (!pwait(xempty_bar(s), ph ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(xfull_bar(s), kXBytes);
+          if (!vwait(xempty_bar(s), ph ^ 1u)) { ok = false; break; }
+          mbar_arrive_expect_tx_w(leader, xfull_bar(s), kXBytes);
           ++nfill;
           if constexpr (kAct8) {
             // int8 codes: a 128 x BN x kXBlock box into the staging tiles (unswizzled)
-            tma_load_3d(x_smem(s) + kXBlock * kXChunk, &a.tmap, 0, u * BN, g, xfull_bar(s));
+            tma_load_3d_w(leader, x_smem(s) + kXBlock * kXChunk, &a.tmap, 0, u * BN, g, xfull_bar(s));
           } else {
             // fp16: a 64 x BN x (2 kXBlock) box, both 64-wide halves of every group,
             // 128-byte swizzle
-            tma_load_3d(x_smem(s), &a.tmap, 0, u * BN, 2 * g, xfull_bar(s));
+            tma_load_3d_w(leader, x_smem(s), &a.tmap, 0, u * BN, 2 * g, xfull_bar(s));
           }
           if (++s == SX) { s = 0; ph ^= 1u; }
         }
@@ -423,53 +438,54 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
     // waits for every activation block and hands it back exactly once: by a commit
     // (completes when its MMAs on the block are done) if it used the block, else by
     // a plain arrive.
-    if (lane == 0) {
+    if (kWarpIssue || lane == 0) {
+      const uint32_t leader = kWarpIssue ? elect_leader() : 1u;
       const int q = warp - kWarpMma0;
       int xs = 0, cidx = 0;
       uint32_t xph = 0;
       bool ok = true;
       for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
         const int b = i % kNAcc;
-        if (!pwait(accempty_bar(b), ((i / kNAcc) & 1) ^ 1)) { ok = false; break; }
+        if (!vwait(accempty_bar(b), ((i / kNAcc) & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(kAccCol0 + (b * kIssuers + q) * BN);
         bool first = true, xready = false, used = false;
         int j = 0;                                     // chunk within the activation block
         for (int g = sg.g0; g < sg.g1; ++g, ++cidx) {
           if (!xready) {
-            if (!pwait(kAct8 ? bfull_bar(xs) : xfull_bar(xs), xph)) { ok = false; break; }
+            if (!vwait(kAct8 ? bfull_bar(xs) : xfull_bar(xs), xph)) { ok = false; break; }
             xready = true;
           }
           if ((cidx & (kIssuers - 1)) == q) {
             const int h = cidx >> 1;                   // position in the parity's half
             const int aslot = (cidx & 1) * kAHalf + h % kAHalf;
-            if (!pwait(afull_bar(aslot), (uint32_t)(h / kAHalf) & 1u)) { ok = false; break; }
+            if (!vwait(afull_bar(aslot), (uint32_t)(h / kAHalf) & 1u)) { ok = false; break; }
             tc_fence_after();
             // descriptor start addresses advance by (offset >> 4); no carry out of the
             // 14-bit field since shared-memory addresses stay below 256 KB
             const uint64_t bdesc0 = smem_desc_sw128(x_smem(xs) + (uint32_t)j * kXChunk);
             const uint32_t a0 = tmem + (uint32_t)(aslot * 64);
-#pragma unroll
+  #pragma unroll
             for (int k = 0; k < 8; ++k)
-              mma_f16_ts(d, a0 + (uint32_t)(k * 8),
-                         bdesc0 + (uint64_t)(((k >> 2) * BN * 128 + (k & 3) * 32) >> 4), kIdesc,
-                         (!first || k > 0) ? 1u : 0u);
+              mma_f16_ts_w(leader, d, a0 + (uint32_t)(k * 8),
+                           bdesc0 + (uint64_t)(((k >> 2) * BN * 128 + (k & 3) * 32) >> 4), kIdesc,
+                           (!first || k > 0) ? 1u : 0u);
             first = false;
             used = true;
-            mma_commit(aempty_bar(aslot));
+            mma_commit_w(leader, aempty_bar(aslot));
           }
           if (++j == kXBlock || g + 1 == sg.g1) {
-            if (used) mma_commit(xempty_bar(xs));
-            else mbar_arrive(xempty_bar(xs));
+            if (used) mma_commit_w(leader, xempty_bar(xs));
+            else mbar_arrive_w(leader, xempty_bar(xs));
             if (++xs == SX) { xs = 0; xph ^= 1u; }
             j = 0;
             xready = used = false;
           }
         }
-        if (ok) mma_commit(accfull_bar(b));
+        if (ok) mma_commit_w(leader, accfull_bar(b));
       }
-      // every MMA this thread issued has completed before the CTA may exit
-      mma_commit(bars + kBarDrain);
+      // every MMA the leader issued has completed before the CTA may exit
+      mma_commit_w(leader, bars + kBarDrain);
       mbar_drain(bars + kBarDrain, 0, wctl);
     }
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {

@@ -202,73 +202,73 @@ __global__ void __launch_bounds__(ms_threads(), 2) qgemm_ms_kernel(const __grid_
   Seg sg;
   if (warp == kMsWarpW) {
     // ------------------------------------------------------ weight copies --
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      if (early) {
-        // ahead of the preceding kernel: the next kMsL2AheadChunks chunks that will not
-        // fit the ring now are pulled into L2, so that their copies after the wait come
-        // from L2, not HBM (a bounded number: a long launch pulling all of its chunks
-        // would push its own earlier ones out of L2 before they are copied)
-        int c = 0;
-        for (int i = 0; c < SW + kMsL2AheadChunks && segment(P, cta, i, sg); ++i) {
-          int u, t;
-          tile_coords(P, sg.tile, u, t);
-          const uint8_t *src = a.wpack + ((size_t)t * P.G + sg.g0) * kChunkW4;
-          for (int g = sg.g0; g < sg.g1 && c < SW + kMsL2AheadChunks; ++g, ++c, src += kChunkW4)
-            if (c >= SW) prefetch_l2(src, kChunkW4);
-        }
-      }
-      int s[TEAMS], nfill[TEAMS], cidx = 0;
-      uint32_t ph[TEAMS];
-#pragma unroll
-      for (int j = 0; j < TEAMS; ++j) s[j] = 0, nfill[j] = 0, ph[j] = 0;
-      bool ok = true;
-      for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
+    // (the whole warp runs the producer loops, waits are warp votes and the leader lane
+    // issues: a copy issued by a lone lane in a divergent branch costs several times more)
+    const uint32_t leader = elect_leader();
+    const uint64_t pol = policy_evict_first();
+    if (early) {
+      // ahead of the preceding kernel: the next kMsL2AheadChunks chunks that will not
+      // fit the ring now are pulled into L2, so that their copies after the wait come
+      // from L2, not HBM (a bounded number: a long launch pulling all of its chunks
+      // would push its own earlier ones out of L2 before they are copied)
+      int c = 0;
+      for (int i = 0; c < SW + kMsL2AheadChunks && segment(P, cta, i, sg); ++i) {
         int u, t;
         tile_coords(P, sg.tile, u, t);
         const uint8_t *src = a.wpack + ((size_t)t * P.G + sg.g0) * kChunkW4;
-        for (int g = sg.g0; g < sg.g1; ++g, ++cidx, src += kChunkW4) {
-          const int tm = cidx & (TEAMS - 1);
-          int slot = 0;
-          uint32_t par = 0;
-#pragma unroll
-          for (int j = 0; j < TEAMS; ++j)
-            if (j == tm) { slot = j * SWT + s[j]; par = ph[j]; }
-          if (!pwait(wempty_bar(slot), par ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(wfull_bar(slot), kChunkW4);
-          bulk_g2s(w_smem(slot), src, kChunkW4, wfull_bar(slot), pol);
-#pragma unroll
-          for (int j = 0; j < TEAMS; ++j)
-            if (j == tm) {
-              ++nfill[j];
-              if (++s[j] == SWT) { s[j] = 0; ph[j] ^= 1u; }
-            }
-        }
+        for (int g = sg.g0; g < sg.g1 && c < SW + kMsL2AheadChunks; ++g, ++c, src += kChunkW4)
+          if (c >= SW) prefetch_l2_w(leader, src, kChunkW4);
       }
-      // the last fill of every slot has landed before the CTA may exit
-#pragma unroll
-      for (int j = 0; j < TEAMS; ++j)
-        for (int k = 0; k < SWT && k < nfill[j]; ++k)
-          mbar_drain(wfull_bar(j * SWT + k), k < s[j] ? ph[j] : ph[j] ^ 1u, wctl);
     }
+    int s[TEAMS], nfill[TEAMS], cidx = 0;
+    uint32_t ph[TEAMS];
+#pragma unroll
+    for (int j = 0; j < TEAMS; ++j) s[j] = 0, nfill[j] = 0, ph[j] = 0;
+    bool ok = true;
+    for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
+      int u, t;
+      tile_coords(P, sg.tile, u, t);
+      const uint8_t *src = a.wpack + ((size_t)t * P.G + sg.g0) * kChunkW4;
+      for (int g = sg.g0; g < sg.g1; ++g, ++cidx, src += kChunkW4) {
+        const int tm = cidx & (TEAMS - 1);
+        int slot = 0;
+        uint32_t par = 0;
+#pragma unroll
+        for (int j = 0; j < TEAMS; ++j)
+          if (j == tm) { slot = j * SWT + s[j]; par = ph[j]; }
+        if (!__all_sync(0xffffffffu, pwait(wempty_bar(slot), par ^ 1u))) { ok = false; break; }
+        mbar_arrive_expect_tx_w(leader, wfull_bar(slot), kChunkW4);
+        bulk_g2s_w(leader, w_smem(slot), src, kChunkW4, wfull_bar(slot), pol);
+#pragma unroll
+        for (int j = 0; j < TEAMS; ++j)
+          if (j == tm) {
+            ++nfill[j];
+            if (++s[j] == SWT) { s[j] = 0; ph[j] ^= 1u; }
+          }
+      }
+    }
+    // the last fill of every slot has landed before the CTA may exit
+#pragma unroll
+    for (int j = 0; j < TEAMS; ++j)
+      for (int k = 0; k < SWT && k < nfill[j]; ++k)
+        mbar_drain(wfull_bar(j * SWT + k), k < s[j] ? ph[j] : ph[j] ^ 1u, wctl);
   } else if (warp == kMsWarpX) {
     // -------------------------------------------------- activation copies --
-    if (lane == 0) {
-      int s = 0, nfill = 0;
-      uint32_t ph = 0;
-      bool ok = true;
-      for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
-        for (int g = sg.g0; g < sg.g1; g += kXBlock) {
-          if (!pwait(xempty_bar(s), ph ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(xfull_bar(s), kXBytes);
-          ++nfill;
-          if constexpr (ACT8) tma_load_3d(x_smem(s) + kXBlock * kXChunk, &a.tmap, 0, 0, g, xfull_bar(s));
-          else tma_load_3d(x_smem(s), &a.tmap, 0, 0, 2 * g, xfull_bar(s));
-          if (++s == SX) { s = 0; ph ^= 1u; }
-        }
+    const uint32_t leader = elect_leader();
+    int s = 0, nfill = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int i = 0; ok && segment(P, cta, i, sg); ++i) {
+      for (int g = sg.g0; g < sg.g1; g += kXBlock) {
+        if (!__all_sync(0xffffffffu, pwait(xempty_bar(s), ph ^ 1u))) { ok = false; break; }
+        mbar_arrive_expect_tx_w(leader, xfull_bar(s), kXBytes);
+        ++nfill;
+        if constexpr (ACT8) tma_load_3d_w(leader, x_smem(s) + kXBlock * kXChunk, &a.tmap, 0, 0, g, xfull_bar(s));
+        else tma_load_3d_w(leader, x_smem(s), &a.tmap, 0, 0, 2 * g, xfull_bar(s));
+        if (++s == SX) { s = 0; ph ^= 1u; }
       }
-      for (int k = 0; k < SX && k < nfill; ++k) mbar_drain(xfull_bar(k), k < s ? ph : ph ^ 1u, wctl);
     }
+    for (int k = 0; k < SX && k < nfill; ++k) mbar_drain(xfull_bar(k), k < s ? ph : ph ^ 1u, wctl);
   } else if (warp >= kMsWarpC0) {
     // ------------------------------------------------------------ compute --
     const int cw = warp - kMsWarpC0, tm = cw / TW, wi = cw % TW;

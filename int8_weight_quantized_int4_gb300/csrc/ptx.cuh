@@ -147,6 +147,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ void bulk_g2s_w(uint32_t leader, uint32_t dst, const void *src, uint32_t bytes,
+                                           uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %5, 0;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;\n\t}" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy), "r"(leader)
+      : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -195,6 +204,41 @@ __device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, 
                "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// Warp-collective forms of the above (every lane calls with the same operands, the
+// leader lane -- elect_leader() -- issues; see the note on warp-collective issue below).
+__device__ __forceinline__ void tma_load_3d_w(uint32_t leader, uint32_t dst, const void *tmap, int x, int y, int z,
+                                              uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %6, 0;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_hint_w(uint32_t leader, uint32_t dst, const void *tmap, int x, int y,
+                                                   int z, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %7, 0;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4}], [%5], %6;\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_3d_w(uint32_t leader, const void *tmap, int x, int y, int z) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %4, 0;\n\t"
+      "@e cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n\t}" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(x), "r"(y), "r"(z), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_w(uint32_t leader, uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b64 st;\n\tsetp.ne.b32 e, %2, 0;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(bytes), "r"(leader)
+      : "memory");
+}
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
@@ -208,6 +252,14 @@ __device__ __forceinline__ void prefetch_l1(const void *p) {
 
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2_w(uint32_t leader, const void *src, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %2, 0;\n\t@e cp.async.bulk.prefetch.L2.global [%0], %1;\n\t}" ::"l"(
+          src),
+      "r"(bytes), "r"(leader)
+      : "memory");
 }
 
 // Programmatic dependent launch: wait until the preceding kernel of the stream has
@@ -358,6 +410,48 @@ __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+
+// ---- warp-collective issue ----
+// Issued by one lane inside a divergent branch, a tcgen05.mma holds that warp for ~115
+// cycles whatever its shape; issued from a converged warp, every lane holding the same
+// operands and one lane predicated on, ~19 cycles (GB300, `bench.py --diag`).  The
+// leader is elected once per role and passed to every call, so the commits come from
+// the thread whose MMAs they track.  All lanes of the warp make every call.
+__device__ __forceinline__ uint32_t elect_leader() {
+  uint32_t p;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+  return p;
+}
+__device__ __forceinline__ void mma_f16_ts_w(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 e, %5, 0;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f16_ss_w(uint32_t leader, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 e, %5, 0;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint32_t leader, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %1, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+      "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_w(uint32_t leader, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b64 st;\n\tsetp.ne.b32 e, %1, 0;\n\t"
+      "@e mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar),
+      "r"(leader)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
