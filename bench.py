@@ -71,11 +71,25 @@ def profiled_traffic():
     nbytes = re.search(r"^dram_bytes_per_launch: (\d+)", text, re.M)
     if not (sha and nbytes):
         return None
+    return int(nbytes.group(1)) if sources_sha256(KERNEL_SOURCES) == sha.group(1) else None
+
+
+def code_only(text: bytes) -> bytes:
+    """C/C++/CUDA source without its comments and blank lines (trailing blanks dropped):
+    what the compiler sees, so that a comment edit leaves a profile's link intact."""
+    s = re.sub(r"/\*.*?\*/", "", text.decode(), flags=re.S)
+    s = re.sub(r"//[^\n]*", "", s)
+    return "\n".join(ln.rstrip() for ln in s.split("\n") if ln.strip()).encode()
+
+
+def sources_sha256(files) -> str:
+    """sha256 over the code (code_only) of the given csrc/ files, in that order: the
+    kernel_sources_sha256 line of the summaries under profiles/."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in files:
         with open(os.path.join(ROOT, "int8_weight_quantized_int4_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return int(nbytes.group(1)) if h.hexdigest() == sha.group(1) else None
+            h.update(code_only(fh.read()))
+    return h.hexdigest()
 
 
 def w4a8_kernels(M, N, K):

@@ -17,8 +17,9 @@
 //                    scale's sign, stored into TMEM as the A operand
 //   MMA warps      : 8 x tcgen05.mma kind::f16 (K = 16 each) per chunk, fp32
 //                    accumulator in TMEM; tcgen05.commit frees the operands.  An
-//                    MMA holds its issuing thread for about 50 ns whatever its N, so
-//                    one thread cannot keep up with HBM on small token tiles: up to
+//                    MMA holds a lone issuing lane ~34 ns whatever its N (a converged
+//                    warp ~9 ns: the form used on tiles of 64 tokens and more), so
+//                    one issuer cannot keep up with HBM on small token tiles: up to
 //                    four warps issue chunks round-robin into their own accumulators
 //                    (4 for token tiles <= 32, 2 for 64, as TMEM allows), and the
 //                    epilogue adds them in a fixed order
@@ -154,9 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1) qgemm_tc_kernel(const __grid_cons
   constexpr uint32_t kXChunk = BN * kGroup * 2;          // one fp16 tile (two swizzled halves)
   constexpr uint32_t kXStage = kXBlock * (kXChunk + (kAct8 ? BN * kGroup : 0));
   constexpr uint32_t kXBytes = kXBlock * (kAct8 ? BN * kGroup : kXChunk);   // per copy
-  // MMA issuers, one accumulator each: a tcgen05.mma holds its issuing thread ~73 ns
-  // whatever its N, so a chunk's 8 MMAs take one thread ~0.6 us -- several issuers keep
-  // the weight stream going; TMEM holds issuers x accumulator sets x BN columns plus the
+  // MMA issuers, one accumulator each: a chunk's 8 MMAs hold a lone issuing lane
+  // ~0.3 us (a converged warp ~0.1 us) and complete ~0.1 us after their commit --
+  // several issuers keep the weight stream going (one measured 17 % slower at 64 tokens
+  // even in the warp form); TMEM holds issuers x accumulator sets x BN columns plus the
   // A ring.
   constexpr int kNAcc = BN <= 128 ? 2 : 1;             // accumulator sets (double buffer)
   constexpr int kIssuers = BN <= 32 ? 4 : BN <= 64 ? 2 : 1;

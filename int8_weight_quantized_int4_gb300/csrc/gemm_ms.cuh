@@ -7,13 +7,14 @@
 // per-token int8 activations).
 //
 // At these batch sizes the layer is bound by streaming the packed weights from HBM: a
-// 128 x 128 chunk (8,448 bytes) must be consumed every ~0.19 us per SM.  On this part a
-// tcgen05.mma holds its issuing thread ~73 ns whatever its N, and a chunk needs eight of
-// them (K = 16 each), so a 5th-generation MMA pipeline tops out near that rate and sits
-// behind a dequant -> TMEM -> MMA -> commit chain.  Here the weights are the MMA's A
-// operand (16 weight rows x 16 K per instruction, in registers), the tokens its B
-// operand (8 per instruction: one n8 tile for M <= 8, two for M <= 16): 64 or 128 MMAs
-// of 2k MACs per chunk, issued like any other instruction, with no asynchronous chain.
+// 128 x 128 chunk (8,448 bytes) must be consumed every ~0.19 us per SM.  A 5th-generation
+// MMA pipeline needs every chunk dequantized into TMEM before its eight tcgen05.mma
+// (K = 16 each, ~34 ns apiece from a lone issuing lane, ~9 ns from a converged warp) and
+// frees it ~0.1 us after their commit: a dequant -> TMEM -> MMA -> commit chain per chunk.
+// Here the weights are the MMA's A operand (16 weight rows x 16 K per instruction, in
+// registers), the tokens its B operand (8 per instruction: one n8 tile for M <= 8, two
+// for M <= 16): 64 or 128 MMAs of 2k MACs per chunk, issued like any other instruction,
+// with no asynchronous chain.
 //
 // Roles (persistent CTAs, the stream-K schedule of schedule.h; a CTA takes at most half
 // an SM, so the next layer's CTAs start while this layer's finish):

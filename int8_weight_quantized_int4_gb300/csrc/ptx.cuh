@@ -413,11 +413,13 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 }
 
 // ---- warp-collective issue ----
-// Issued by one lane inside a divergent branch, a tcgen05.mma holds that warp for ~115
-// cycles whatever its shape; issued from a converged warp, every lane holding the same
-// operands and one lane predicated on, ~19 cycles (GB300, `bench.py --diag`).  The
-// leader is elected once per role and passed to every call, so the commits come from
-// the thread whose MMAs they track.  All lanes of the warp make every call.
+// Issued by one lane inside a divergent branch, a tcgen05.mma holds that warp ~34 ns
+// whatever its shape; issued from a converged warp, every lane holding the same operands
+// and one lane predicated on, ~9 ns (GB300, `bench.py --diag`: the tcgen05 probe, kind +
+// 2).  The leader is elected once per role and passed to every call, so the commits come
+// from the thread whose MMAs they track.  All lanes of the warp make every call; a wait
+// in such a role is taken by every lane and voted (__all_sync), which measured faster
+// than the leader waiting alone and handing its answer on.
 __device__ __forceinline__ uint32_t elect_leader() {
   uint32_t p;
   asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
