@@ -215,16 +215,17 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
     if constexpr (QIN) {
       // token scales, as the standalone quantizer: amax = max |x| over the whole row
       // (binary32, exact in any order), s = amax / 127 (IEEE divide); the rows come from
-      // L2 while the first weights are in flight
+      // L2 while the first weights are in flight.  One token: the whole CTA on its row;
+      // several: warps cw = m, m + mv, ... take token m, so that every row is requested
+      // at once (four 16-byte loads a lane in flight: two rows of K <= 8192 in one trip)
       const int nv = G * 16;                        // 16-byte vectors of a row
-      for (int m = 0; m < mv; ++m) {
-        const uint4 *xr = reinterpret_cast<const uint4 *>(a.xf16 + (size_t)m * P.K);
-        float amax = 0.0f;
-        for (int v0 = ct; v0 < nv; v0 += 4 * kCThreads) {
+      auto row_amax = [&](const uint4 *xr, int t0, int step) {
+        float am = 0.0f;
+        for (int v0 = t0; v0 < nv; v0 += 4 * step) {
           uint4 w[4];
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
-            const int v = v0 + b * kCThreads;
+            const int v = v0 + b * step;
             w[b] = v < nv ? __ldg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
           }
 #pragma unroll
@@ -233,19 +234,32 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 f = __half22float2(hv[e]);
-              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+              am = fmaxf(am, fmaxf(fabsf(f.x), fabsf(f.y)));
             }
           }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if (lane == 0) qamax[cw * 16 + m] = amax;
+        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        return am;
+      };
+      float amax;
+      if (mv == 1) {
+        amax = row_amax(reinterpret_cast<const uint4 *>(a.xf16), ct, kCThreads);
+      } else {
+        const int m = cw % mv, nw = (kCompute - 1 - m) / mv + 1;   // token, its warps
+        amax = row_amax(reinterpret_cast<const uint4 *>(a.xf16 + (size_t)m * P.K), (cw / mv) * 32 + lane,
+                        nw * 32);
       }
+      if (lane == 0) qamax[cw] = amax;
       named_bar_sync(2, kCThreads);
       if (ct < mv) {
-        float amax = qamax[ct];
-        for (int w = 1; w < kCompute; ++w) amax = fmaxf(amax, qamax[w * 16 + ct]);
-        const float sc = amax == 0.0f ? 0.0f : __fdiv_rn(amax, 127.0f);
+        float am = 0.0f;
+#pragma unroll
+        for (int r = 0; r < kCompute; ++r) {        // the warps of token ct, loads independent
+          const int w = ct + r * mv;
+          if (w < kCompute) am = fmaxf(am, qamax[w]);
+        }
+        const float sc = am == 0.0f ? 0.0f : __fdiv_rn(am, 127.0f);
         qsc[ct] = sc;
         qrc[ct] = sc == 0.0f ? 0.0f : __frcp_rn(sc);
       }

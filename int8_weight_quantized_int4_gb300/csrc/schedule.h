@@ -163,7 +163,11 @@ QW_HD int chunk_bytes(int mode) { return mode == 2 ? kChunkW8 : kChunkW4; }
 // quantizer's arithmetic is paid once per CTA -- worth it only for a few tokens.
 constexpr int kModeCodes16 = 4;
 constexpr int kFusedRowsMax = 48 * 1024;
-constexpr int kFusedMaxTokens = 2;   // measured: 1-2 tokens faster than quantizer + GEMM, 4 not
+// Measured on the 5120 x 5120 layer (weights-immutable option): 8.1 / 9.1 us at 1 / 2
+// tokens against ~9.8 / 10.4 for quantizer + GEMM; at 4 and 8 tokens 10.6 / 13.9 against
+// 10.4 / 10.7 -- there the per-stage quantization in every CTA, not the scale pass (one
+// round trip for all tokens), costs.
+constexpr int kFusedMaxTokens = 2;
 
 // W4A8 widens int8 activation codes to fp16 inside the GEMM (through a staging
 // slot) for token tiles up to this size; larger tiles use a separate widening pass.
