@@ -56,7 +56,7 @@ def peaks():
 
 
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "qgemm_rb_kernel_proj_w4a16_m16.md")
-KERNEL_SOURCES = ("gemm_rb.cuh", "gemm_ms.cuh", "gemm_kernel.cuh", "ptx.cuh", "schedule.h")
+KERNEL_SOURCES = ("gemm_rb.cuh", "quant_code.cuh", "gemm_ms.cuh", "gemm_kernel.cuh", "ptx.cuh", "schedule.h")
 
 
 def profiled_traffic():

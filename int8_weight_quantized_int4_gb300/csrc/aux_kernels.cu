@@ -8,6 +8,7 @@
 #include "launch.h"
 #include "ptx.cuh"
 #include "schedule.h"
+#include "quant_code.cuh"
 
 namespace qw {
 
@@ -15,7 +16,9 @@ namespace qw {
 // Per-token int8 quantization ("In full" item 4 of "What this repo does that
 // stock vLLM doesn't": activations quantized to int8 per token).
 // One CTA per row.  amax over the row (warp shuffles, then shared memory),
-// s = amax / 127 with the IEEE divide, q = rne(x / s) clamped to [-127, 127].
+// s = amax / 127 with the IEEE divide, q = rne(x / s) clamped to [-127, 127] -- the IEEE
+// quotient's code, found from the reciprocal product except within 2^-14 of a tie
+// (quant_code.cuh).
 // The row is kept in registers (up to kQuantRegs 16-byte vectors per thread);
 // longer rows are re-read for the second pass.
 // CODES16: the codes are written as fp16 values (exact: |q| <= 127) for a GEMM that
@@ -23,9 +26,12 @@ namespace qw {
 // widening of int8 codes is needed there; otherwise as int8.
 constexpr int kQuantThreads = 256;
 constexpr int kQuantRegs = 12;
+// (one CTA per SM stated in the launch bounds: the default register target spilled the
+// row and the codes, which cost ~1 us a decode layer; at ~100 registers two CTAs of a long
+// prefill still share an SM, measured no slower)
 
 template <bool CODES16>
-__global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const uint16_t *__restrict__ x, int K,
+__global__ void __launch_bounds__(kQuantThreads, 1) quant_act_kernel(const uint16_t *__restrict__ x, int K,
                                                                   void *__restrict__ q,
                                                                   float *__restrict__ s) {
   using Out = typename std::conditional<CODES16, uint4, uint2>::type;   // 8 codes
@@ -71,17 +77,34 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const uint16_t
   if (threadIdx.x == 0) s[row] = (amax == 0.0f) ? 0.0f : sc;
   Out *qr = reinterpret_cast<Out *>(q) + row * (size_t)(K / 8);
 
+  const float rs = amax == 0.0f ? 0.0f : __frcp_rn(sc);
   auto quant8 = [&](const uint4 &v) -> Out {
     const __half2 *h = reinterpret_cast<const __half2 *>(&v);
     uint32_t out[4] = {0u, 0u, 0u, 0u};
     if (amax != 0.0f) {
+      // the eight codes from the reciprocal product; near a tie all eight again from the
+      // divide (a rare branch, kept out of the common path's registers)
+      int qc[8];
+      bool near_tie = false;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 f = __half22float2(h[e]);
-        int q0 = __float2int_rn(__fdiv_rn(f.x, sc));
-        int q1 = __float2int_rn(__fdiv_rn(f.y, sc));
-        q0 = max(-127, min(127, q0));
-        q1 = max(-127, min(127, q1));
+        bool t0, t1;
+        qc[2 * e] = quant_code_fast(f.x, rs, t0);
+        qc[2 * e + 1] = quant_code_fast(f.y, rs, t1);
+        near_tie = near_tie || t0 || t1;
+      }
+      if (near_tie) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(h[e]);
+          qc[2 * e] = quant_code_div(f.x, sc);
+          qc[2 * e + 1] = quant_code_div(f.y, sc);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int q0 = qc[2 * e], q1 = qc[2 * e + 1];
         if constexpr (CODES16) {
           out[e] = h2_as_u32(__halves2half2(__int2half_rn(q0), __int2half_rn(q1)));
         } else {

@@ -36,6 +36,7 @@
 #include <stdint.h>
 #include <cuda_fp16.h>
 #include "gemm_ms.cuh"   // mma_16816, ldsm_x4, lds128, lds32, frag_w4, frag_w4_zp, ms_threads
+#include "quant_code.cuh"
 
 namespace qw {
 
@@ -49,23 +50,6 @@ __host__ __device__ constexpr int rb_threads() { return (kMsWarpC0 + kRbCompute)
 
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// q = clamp(rne(x / s), -127, 127) with x / s the IEEE binary32 quotient, as the standalone
-// quantizer computes it, without a divide per value: t = x * (1/s) (correctly rounded
-// reciprocal and product) is within 3 * 2^-24 * |x/s| <= 2.3e-5 of the quotient, since
-// |x/s| <= 127 (1 + 2^-24).  So rne(t) = rne(x / s) unless t lies within 2^-14 of a
-// half-integer, i.e. unless |t - rne(t)| >= 0.5 - 2^-14 (t - rne(t) is exact); only those
-// values take the IEEE divide, out of line so that it is skipped rather than computed and
-// discarded.  s = 0 (an all-zero row) has 1/s = 0, so t = 0 and q = 0, as the quantizer.
-static __device__ __noinline__ int rb_quant_slow(float x, float s) {
-  return max(-127, min(127, __float2int_rn(__fdiv_rn(x, s))));
-}
-__device__ __forceinline__ int rb_quant_code(float x, float s, float rs) {
-  const float t = __fmul_rn(x, rs);
-  const int q = __float2int_rn(t);
-  if (fabsf(t - (float)q) >= 0.5f - 6.103515625e-05f) return rb_quant_slow(x, s);
-  return max(-127, min(127, q));
 }
 
 __device__ __forceinline__ void rb_x_offsets(int lane, int bnx, uint32_t (&xoff)[4]) {
@@ -304,7 +288,7 @@ __global__ void __launch_bounds__(rb_threads(), 1) qgemm_rb_kernel(const __grid_
             const uint32_t addr = half + (uint32_t)(r * 128 + (((j >> 2) ^ (r & 7)) << 4) + (j & 3) * 4);
             const float sc = qsc[r], rs = qrc[r];
             const float2 f = __half22float2(u32_as_h2(lds32(addr)));
-            const int q0 = rb_quant_code(f.x, sc, rs), q1 = rb_quant_code(f.y, sc, rs);
+            const int q0 = quant_code(f.x, sc, rs), q1 = quant_code(f.y, sc, rs);
             sts32(addr, h2_as_u32(__halves2half2(__int2half_rn(q0), __int2half_rn(q1))));
           }
           __syncwarp();
