@@ -429,3 +429,19 @@ def test_schedule_partition_random_shapes():
         assert p.stages % 2 == 0 and 4 <= p.stages <= 16, p.stages
         assert 2 <= p.act_stages <= 4 and p.act_block in (1, 2, 4)
         _check_partition(p)
+
+
+def test_profile_link_hash_ignores_comments_only():
+    """The hash that ties a profile summary to its kernel sources covers the code with
+    comments and blank lines removed: a comment edit keeps it, any change the compiler
+    sees breaks it."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    src = b"// header\nint f(int x) {  // trailing\n  /* block\n     comment */return x + 1;\n}\n\n"
+    same = b"// another header\n\nint f(int x) {\n  return x + 1;   // reworded\n}\n"
+    other = b"int f(int x) {\n  return x + 2;\n}\n"
+    assert bench.code_only(src) == bench.code_only(same)
+    assert bench.code_only(src) != bench.code_only(other)
+    h = bench.sources_sha256(bench.KERNEL_SOURCES)
+    assert len(h) == 64 and h == bench.sources_sha256(bench.KERNEL_SOURCES)

@@ -67,6 +67,44 @@ def test_quant_act_bitexact(q, M, K):
     assert np.array_equal(xq.cpu().numpy(), oq)
 
 
+@pytest.mark.parametrize("codes16", [False, True])
+def test_quant_act_near_ties(q, codes16):
+    """Every quotient x / s within a few 2^-12 of a half-integer, on 64 rows of 5120 with
+    scales that are not powers of two: the quantizer's reciprocal product leaves most of
+    these to its IEEE-divide branch (a group of eight holding one near-tie is redone).
+    Codes and scales bit-exact against the oracle; the fp16-code output (W4A8 from fp16,
+    read through identity weights) carries the same codes."""
+    M, K = 64, 5120
+    rng = np.random.default_rng(11)
+    x = np.zeros((M, K), np.float16)
+    for m in range(M):
+        amax = float(np.float16(rng.uniform(0.01, 200.0)))
+        s = np.float64(amax) / 127.0
+        n = rng.integers(-127, 127, K)
+        delta = rng.integers(-3, 4, K) * 2.0 ** -12
+        x[m] = ((n + 0.5 + delta) * s).astype(np.float16)
+        x[m, rng.integers(0, K)] = np.float16(amax)
+    oq, os_ = oracle.quant_act_int8(x)
+    xd = torch.from_numpy(x).to(DEV)
+    if not codes16:
+        xq, xs = q.quant_act_int8(xd)
+        assert np.array_equal(xs.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+        assert np.array_equal(xq.cpu().numpy(), oq)
+        return
+    # through the fused entry at 64 tokens (quantizer with fp16 codes, then the GEMM): with
+    # identity weights y[m, n] = fp16(s_m * q[m, n]) for n < N
+    N = 1280
+    codes = torch.zeros((N, K), dtype=torch.int8)
+    codes[torch.arange(N), torch.arange(N)] = 1
+    scales = torch.ones((N, K // 128), dtype=torch.float16)
+    packed = q.qpack_w4(codes.to(DEV), scales.to(DEV))
+    y = q.qgemm_w4a8_fused(xd, packed, N, K)
+    torch.cuda.synchronize()
+    assert q.device_error() == 0
+    expect = (oq[:, :N].astype(np.float32) * os_[:, None].astype(np.float32)).astype(np.float16)
+    assert np.array_equal(bits(y), expect.view(np.int16))
+
+
 def test_quant_act_prefill_size(q):
     x = synth.activations(8192, 5120, synth.generator(4))
     xq, xs = q.quant_act_int8(x.to(DEV))
