@@ -87,7 +87,9 @@ def _tie_problem(M, N, K, seed):
 
 
 @pytest.mark.parametrize("M,N,K,k", [(1, 16384, 256, 64), (5, 16384, 256, 1), (16, 32768, 128, 64),
-                                     (64, 8192, 256, 33), (3, 1024, 256, 64), (2, 256, 128, 7)])
+                                     (64, 8192, 256, 33), (3, 1024, 256, 64), (2, 256, 128, 7),
+                                     # row-block kernel with two 8-token tiles, 2 and 3 row blocks a CTA
+                                     (12, 4096, 512, 64), (16, 7168, 1024, 40)])
 def test_lm_head_topk_ties(q, M, N, K, k):
     codes, scales, x = _tie_problem(M, N, K, seed=M * 131 + N + k)
     packed = q.qpack_w4(codes.to(DEV), scales.to(DEV))
