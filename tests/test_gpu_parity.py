@@ -630,3 +630,34 @@ def test_binding_rejects_short_or_misshapen_buffers(q):
     assert q.device_error() == 0
     y = q.qgemm_w4a16(x, packed, 256, 256)                  # the right sizes still run
     assert y.shape == (2, 256)
+
+
+@pytest.mark.parametrize("imm", [False, True])
+@pytest.mark.parametrize("M,N,K", [(64, 5120, 5120), (64, 34816, 5120), (256, 34816, 5120), (128, 5120, 17408)])
+def test_tc_warp_issue_repeat_bitwise(q, imm, M, N, K):
+    """The tcgen05 GEMM on token tiles of 64 and more issues from whole warps (warp-voted
+    waits, one elected lane issuing every MMA, commit and copy): repeated launches, with and
+    without the weights-immutable overlap, give bit-identical results and no device error,
+    and the first matches the oracle."""
+    gen = synth.generator(900 + M + N // 128)
+    codes = torch.randint(-8, 8, (N, K), generator=gen, dtype=torch.int8)
+    scales = ((torch.rand((N, K // 128), generator=gen) - 0.3) * 0.02).to(torch.float16)
+    x = (torch.randn((M, K), generator=gen) * 0.5).to(torch.float16)
+    packed = q.qpack_w4(codes.to(DEV), scales.to(DEV))
+    xd = x.to(DEV)
+    ws = q.Workspace(DEV)
+    y = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    q.set_weights_immutable(imm)
+    try:
+        q.qgemm_w4a16(xd, packed, N, K, y=y, ws=ws)
+        ref = y.clone()
+        for _ in range(30):
+            q.qgemm_w4a16(xd, packed, N, K, y=y, ws=ws)
+            assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+        torch.cuda.synchronize()
+        assert q.device_error() == 0
+    finally:
+        q.set_weights_immutable(False)
+    cols = np.arange(0, N, 97)
+    expect = oracle.w4a16(x, codes.numpy()[cols], scales.numpy()[cols])
+    assert nerr(ref.cpu()[:, cols], expect) <= TOL
