@@ -19,22 +19,31 @@ namespace qw {
 // s = amax / 127 with the IEEE divide, q = rne(x / s) clamped to [-127, 127] -- the IEEE
 // quotient's code, found from the reciprocal product except within 2^-14 of a tie
 // (quant_code.cuh).
-// The row is kept in registers (up to kQuantRegs 16-byte vectors per thread);
-// longer rows are re-read for the second pass.
+// The row is kept in registers (up to quant_regs(WIDE) 16-byte vectors per thread);
+// longer rows are re-read (from L2) for the second pass.
 // CODES16: the codes are written as fp16 values (exact: |q| <= 127) for a GEMM that
 // reads them as fp16 tiles and applies the token scales in its epilogue, so that no
 // widening of int8 codes is needed there; otherwise as int8.
+// Two forms, by how the CTAs should share SMs (measured on the 5120 x 5120 W4A8 layer and
+// the W4A8 prefill, same box):
+//   narrow (WIDE false): 4 vectors a thread, ~48 registers.  Up to 8 tokens its CTAs fit
+//     beside the row-block GEMM CTAs still on the SMs and start at once (4 tokens 9.26 ->
+//     8.64 us a layer); from 256 tokens several share an SM and the stream runs faster
+//     (2048-token prefill projection 136.0 -> 127.8 us).
+//   wide (WIDE true): 12 vectors a thread, one CTA per SM stated in the launch bounds
+//     (~100 registers; at the default register target this form spilled).  For 16-255
+//     tokens, whose CTAs cannot fit beside the GEMM's: the narrow form's CTAs then crowd
+//     onto the first SMs to free up (16 tokens 11.44 -> 12.01 us).
 constexpr int kQuantThreads = 256;
-constexpr int kQuantRegs = 12;
-// (one CTA per SM stated in the launch bounds: the default register target spilled the
-// row and the codes, which cost ~1 us a decode layer; at ~100 registers two CTAs of a long
-// prefill still share an SM, measured no slower)
+constexpr int kQuantNarrowMaxTokens = 8, kQuantNarrowMinTokens = 256;
+__host__ __device__ constexpr int quant_regs(bool wide) { return wide ? 12 : 4; }
 
-template <bool CODES16>
-__global__ void __launch_bounds__(kQuantThreads, 1) quant_act_kernel(const uint16_t *__restrict__ x, int K,
+template <bool CODES16, bool WIDE>
+__global__ void __launch_bounds__(kQuantThreads, WIDE ? 1 : 0) quant_act_kernel(const uint16_t *__restrict__ x, int K,
                                                                   void *__restrict__ q,
                                                                   float *__restrict__ s) {
   using Out = typename std::conditional<CODES16, uint4, uint2>::type;   // 8 codes
+  constexpr int kQuantRegs = quant_regs(WIDE);
   __shared__ float red[kQuantThreads / 32];
   griddep_wait();
   griddep_launch_dependents();
@@ -233,8 +242,11 @@ static int grid_for(size_t items, int threads, int sms) {
 
 cudaError_t launch_quant_act(const uint16_t *x, int M, int K, void *q, bool codes16, float *s,
                              cudaStream_t st) {
-  const void *k = codes16 ? reinterpret_cast<const void *>(quant_act_kernel<true>)
-                          : reinterpret_cast<const void *>(quant_act_kernel<false>);
+  const bool wide = M > kQuantNarrowMaxTokens && M < kQuantNarrowMinTokens;
+  const void *k = codes16 ? (wide ? reinterpret_cast<const void *>(quant_act_kernel<true, true>)
+                                  : reinterpret_cast<const void *>(quant_act_kernel<true, false>))
+                          : (wide ? reinterpret_cast<const void *>(quant_act_kernel<false, true>)
+                                  : reinterpret_cast<const void *>(quant_act_kernel<false, false>));
   cudaError_t e = launch_pdl(k, dim3(M), dim3(kQuantThreads), 0, st, x, K, q, s);
   count_launch();
   return e;
