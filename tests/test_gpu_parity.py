@@ -57,7 +57,9 @@ def _special_rows(x):
 
 
 @pytest.mark.parametrize("M,K", [(1, 5120), (4, 5120), (16, 5120), (64, 5120), (64, 17408),
-                                 (7, 136), (5, 8), (33, 24576 + 64)])
+                                 (7, 136), (5, 8), (33, 24576 + 64),
+                                 # the narrow form (up to 8 tokens, from 256) on rows it re-reads
+                                 (3, 17408), (256, 9216)])
 def test_quant_act_bitexact(q, M, K):
     x = synth.activations(M, K, synth.generator(100 + M + K), outlier_frac=0.01)
     x = _special_rows(x)
